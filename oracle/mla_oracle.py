@@ -1,0 +1,409 @@
+"""Float64 CPU oracle for absorbed MLA decode over a paged latent cache.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports, calls or
+executes this module: only the tests, ``__graft_entry__.smoke()`` and the
+bench's CPU-baseline / reference arm use it.  It shares no code with the CUDA
+path.  Every function is the plain definition (or, for the split planner, the
+rule written out step by step) in float64 NumPy, with no blocking, fusion or
+reordering beyond what the definition states.
+
+Sources (web pages, cited by title and section):
+  [MLA-in-depth]  "MLA in full detail" (mlinterviewnotes, ch. 7.2): Step 2 "fold
+                  W_UK into the query", Step 3 "attend against the latent
+                  directly", Step 4 "fold W_UV into the output", "What it costs",
+                  and the closing float64 single-head parity reference.
+  [zdszero]       "MLA" (zdszero.github.io): "Normal 与 Absorb" (the Normal and
+                  Absorb forms), "计算量分析" (the MAC table), "谁更省" (the T~170
+                  crossover), the decoupled-RoPE note that the scale stays sqrt(192).
+  [mlxcel]        "mlxcel: MLA absorbed decode": the bytes/token table and the
+                  Stage-2 split-KV merge contract (partials normalised by their own
+                  denominator, grouped by an indptr).
+  [M5.8]          "M5.8 - Multi-Head Latent Attention: Latent KV State, Weight
+                  Absorption, and FlashMLA": 0x04 "Batched absorption trace"
+                  (canonical einsum shapes), 0x05 "Paged and ragged address
+                  translation", 0x06 "Numeric Cache Ledger", 0x09 (decode
+                  intensity), 0x0C (exact merge of sequence-split state).
+
+Parity status: every function below is pinned by a CPU test (closed forms,
+printed values, brute force, a library routine or an invariant) except
+``plan_ref``, whose rule the pages leave open; it is pinned by brute-force
+coverage/balance properties and is bit-exact-compared with the device planner.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+D_C = 512      # kv_lora_rank
+D_R = 64       # qk_rope_head_dim
+D_N = 128      # qk_nope_head_dim
+D_V = 128      # v_head_dim
+D_K = D_C + D_R
+PAGE = 64
+ROWS_PER_BLOCK = 128   # flattened (t, h) query rows handled together
+MIN_SPLIT_PAGES = 4
+
+SCALE = 1.0 / math.sqrt(D_N + D_R)   # 1/sqrt(192): [zdszero] decoupled-RoPE note; [MLA-in-depth] parity reference
+
+
+# ---------------------------------------------------------------------------
+# Paged address translation  ([M5.8] 0x05 "Paged and ragged address translation")
+# ---------------------------------------------------------------------------
+def physical_row(block_table_row: np.ndarray, j: int, page: int = PAGE) -> int:
+    """physical(j) = block_table[page(j)] * P + offset(j), page(j) = j // P, offset(j) = j mod P."""
+    logical_page, offset = divmod(int(j), page)
+    phys_page = int(block_table_row[logical_page])
+    if phys_page < 0:
+        raise IndexError(f"logical row {j} maps to an unassigned page")
+    return phys_page * page + offset
+
+
+def gather_rows(pool: np.ndarray, block_table_row: np.ndarray, n_rows: int) -> np.ndarray:
+    """Logical rows 0..n_rows-1 of one sequence, in order, as [n_rows, 576] (same dtype as pool).
+
+    ``pool`` is [num_blocks, P, 576]; rows are resolved one logical page at a time.
+    """
+    page = pool.shape[1]
+    flat = pool.reshape(-1, pool.shape[-1])
+    out = np.empty((n_rows, pool.shape[-1]), dtype=pool.dtype)
+    for j in range(n_rows):
+        out[j] = flat[physical_row(block_table_row, j, page)]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Absorption GEMMs  ([M5.8] 0x04 "Batched absorption trace"; [MLA-in-depth] Steps 2 and 4)
+# ---------------------------------------------------------------------------
+def absorb_ref(q_nope: np.ndarray, w_uk: np.ndarray) -> np.ndarray:
+    """q_lat[b,t,h,c] = sum_n q_nope[b,t,h,n] * W_UK[h,n,c]   (W_UK is [H, d_N, d_c])."""
+    return np.einsum("bthn,hnc->bthc", q_nope, w_uk)
+
+
+def unabsorb_ref(o_lat: np.ndarray, w_uv: np.ndarray) -> np.ndarray:
+    """o[b,t,h,v] = sum_c o_lat[b,t,h,c] * W_UV[h,v,c]   (W_UV is [H, d_V, d_c])."""
+    return np.einsum("bthc,hvc->bthv", o_lat, w_uv)
+
+
+# ---------------------------------------------------------------------------
+# Causal visibility for T new rows already in the cache
+# ---------------------------------------------------------------------------
+def visible_limit(S: int, T: int, t: int, causal: bool) -> int:
+    """Number of cache rows query token t (0..T-1) attends to.
+
+    The T new rows are the last T of the S visible rows (they were appended
+    before the step); with causal masking token t sees rows 0..S-T+t, i.e. the
+    prefix plus new rows up to and including itself (bottom-right alignment;
+    [MLA-in-depth] "prefix P=5, Q=3" gives P*Q + Q(Q+1)/2 visible pairs).
+    """
+    if not causal:
+        return S
+    return max(0, min(S, S - T + t + 1))
+
+
+def causal_mask(S: int, T: int, causal: bool) -> np.ndarray:
+    """Boolean [T, S]: True where token t may attend to cache row j."""
+    m = np.zeros((T, S), dtype=bool)
+    for t in range(T):
+        m[t, :visible_limit(S, T, t, causal)] = True
+    return m
+
+
+# ---------------------------------------------------------------------------
+# Absorbed decode  ([M5.8] 0x04 absorbed reference; [MLA-in-depth] Step 3)
+# ---------------------------------------------------------------------------
+def softmax_rows(s: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Softmax over the last (key) axis with max subtraction; returns (p, lse).
+
+    Rows whose entries are all -inf give p = 0 and lse = -inf.
+    """
+    m = np.max(s, axis=-1, keepdims=True)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    e = np.exp(s - m_safe)
+    l = np.sum(e, axis=-1, keepdims=True)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        p = np.where(l > 0, e / np.where(l > 0, l, 1.0), 0.0)
+        lse = np.where(l[..., 0] > 0, m_safe[..., 0] + np.log(np.where(l[..., 0] > 0, l[..., 0], 1.0)), -np.inf)
+    return p, lse
+
+
+def attend_latent(q_lat: np.ndarray, q_pe: np.ndarray, rows: np.ndarray, mask: np.ndarray,
+                  scale: float = SCALE) -> tuple[np.ndarray, np.ndarray]:
+    """One sequence: q_lat [T,H,512], q_pe [T,H,64], rows [S,576], mask [T,S].
+
+    s[t,h,j] = (q_lat[t,h] . c_j + q_pe[t,h] . k_pe_j) * scale, softmax over j
+    (the key axis only), o_lat[t,h] = sum_j p[t,h,j] c_j, lse = log sum_j e^{s}.
+    Returns (o_lat [T,H,512], lse [T,H]).
+    """
+    d_c = q_lat.shape[-1]
+    c = rows[:, :d_c]
+    kpe = rows[:, d_c:]
+    s = (np.einsum("thc,jc->thj", q_lat, c) + np.einsum("thr,jr->thj", q_pe, kpe)) * scale
+    s = np.where(mask[:, None, :], s, -np.inf)
+    p, lse = softmax_rows(s)
+    o = np.einsum("thj,jc->thc", p, c)
+    return o, lse
+
+
+def decode_ref(q_lat: np.ndarray, q_pe: np.ndarray, pool: np.ndarray, block_table: np.ndarray,
+               seq_lens: np.ndarray, causal: bool, scale: float = SCALE, batches=None):
+    """Absorbed attention over the paged latent cache for every (or the listed) sequence.
+
+    q_lat [B,T,H,512], q_pe [B,T,H,64] (float64), pool [num_blocks,64,576] (float64),
+    block_table [B,max_pages], seq_lens [B] (visible rows including the T new ones).
+    Returns o_lat [B,T,H,512] and lse [B,T,H] (natural log; -inf, o=0 for S_b=0).
+    """
+    B, T, H, d_c = q_lat.shape
+    o_lat = np.zeros((B, T, H, d_c))
+    lse = np.full((B, T, H), -np.inf)
+    for b in (range(B) if batches is None else batches):
+        S = int(seq_lens[b])
+        if S == 0:
+            continue
+        rows = gather_rows(pool, block_table[b], S)
+        o_lat[b], lse[b] = attend_latent(q_lat[b], q_pe[b], rows, causal_mask(S, T, causal), scale)
+    return o_lat, lse
+
+
+def absorbed_layer_ref(q_nope, q_pe, pool, block_table, seq_lens, w_uk, w_uv, causal, scale=SCALE):
+    """The whole absorbed chain: absorb, latent attention, un-absorb.  Returns (o, o_lat, lse, q_lat)."""
+    q_lat = absorb_ref(q_nope, w_uk)
+    o_lat, lse = decode_ref(q_lat, q_pe, pool, block_table, seq_lens, causal, scale)
+    return unabsorb_ref(o_lat, w_uv), o_lat, lse, q_lat
+
+
+# ---------------------------------------------------------------------------
+# Normal (decompressed) path  ([zdszero] Normal mode; [MLA-in-depth] Step 1 "what the naive path does")
+# ---------------------------------------------------------------------------
+def normal_ref(q_nope, q_pe, pool, block_table, seq_lens, w_uk, w_uv, causal, scale=SCALE, batches=None):
+    """Up-project every cached latent into per-head keys/values, then ordinary MHA.
+
+    k_nope[j,h,n] = sum_c W_UK[h,n,c] c_j[c];  v[j,h,v] = sum_c W_UV[h,v,c] c_j[c];
+    k[j,h] = [k_nope[j,h] ; k_pe_j] (192 wide, k_pe broadcast over heads);
+    q[t,h] = [q_nope ; q_pe];  o = softmax(q k^T * scale) v.
+    Returns o [B,T,H,128] and lse [B,T,H].
+    """
+    B, T, H, _ = q_nope.shape
+    d_c = w_uk.shape[-1]
+    d_r = q_pe.shape[-1]
+    o = np.zeros((B, T, H, w_uv.shape[1]))
+    lse = np.full((B, T, H), -np.inf)
+    for b in (range(B) if batches is None else batches):
+        S = int(seq_lens[b])
+        if S == 0:
+            continue
+        rows = gather_rows(pool, block_table[b], S)
+        c = rows[:, :d_c]
+        kpe = rows[:, d_c:]
+        k_nope = np.einsum("hnc,jc->jhn", w_uk, c)
+        v = np.einsum("hvc,jc->jhv", w_uv, c)
+        k = np.concatenate([k_nope, np.broadcast_to(kpe[:, None, :], (S, H, d_r))], axis=-1)
+        q = np.concatenate([q_nope[b], q_pe[b]], axis=-1)
+        s = np.einsum("thd,jhd->thj", q, k) * scale
+        s = np.where(causal_mask(S, T, causal)[:, None, :], s, -np.inf)
+        p, lse[b] = softmax_rows(s)
+        o[b] = np.einsum("thj,jhv->thv", p, v)
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# Split-KV partial state and its exact merge
+# ([M5.8] 0x0C exact merge; [mlxcel] Stage 2 merge contract)
+# ---------------------------------------------------------------------------
+def partial_ref(q_lat_b, q_pe_b, pool, block_table_row, S, T, causal, page_begin, page_end, scale=SCALE):
+    """Attention of one sequence restricted to the keys in logical pages [page_begin, page_end).
+
+    Returns the partial output normalised by its own denominator, o_r [T,H,512],
+    and its log-sum-exp lse_r [T,H] (natural log; -inf where no key is visible).
+    """
+    T_, H, d_c = q_lat_b.shape
+    page = pool.shape[1]
+    j0 = page_begin * page
+    j1 = min(S, page_end * page)
+    if j1 <= j0:
+        return np.zeros((T_, H, d_c)), np.full((T_, H), -np.inf)
+    rows_all = gather_rows(pool, block_table_row, j1)
+    mask = causal_mask(S, T, causal)[:, j0:j1]
+    return attend_latent(q_lat_b, q_pe_b, rows_all[j0:j1], mask, scale)
+
+
+def merge_ref(part_o: np.ndarray, part_lse: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Exact merge of R partial states: part_o [R,...,D] (each normalised), part_lse [R,...].
+
+    m = max_r lse_r; w_r = e^{lse_r - m}; o = sum_r w_r o_r / sum_r w_r; lse = m + ln sum_r w_r.
+    (Equivalent to m = max m_r, l = sum e^{m_r-m} l_r, o = sum e^{m_r-m} o_r, O = o/l.)
+    If every partial is empty (lse = -inf) the result is o = 0, lse = -inf.
+    """
+    part_o = np.asarray(part_o, dtype=np.float64)
+    part_lse = np.asarray(part_lse, dtype=np.float64)
+    if part_o.shape[0] == 0:
+        return np.zeros(part_o.shape[1:]), np.full(part_lse.shape[1:], -np.inf)
+    m = np.max(part_lse, axis=0)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    w = np.exp(part_lse - m_safe)
+    w = np.where(np.isfinite(part_lse), w, 0.0)
+    l = np.sum(w, axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        o = np.where(l[..., None] > 0, np.sum(w[..., None] * part_o, axis=0) / np.where(l > 0, l, 1.0)[..., None], 0.0)
+        lse = np.where(l > 0, m_safe + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# Split planner.  The pages leave the rule open (FlashMLA's scheduler metadata
+# is opaque; [M5.8] 0x08 only says it must be rebuilt when geometry or lengths
+# change).  This is the rule both the device planner and this restatement follow.
+# ---------------------------------------------------------------------------
+def group_pages(seq_lens, T: int, H: int, causal: bool) -> list[tuple[int, int, int]]:
+    """Work groups (b, rb, n_pages) in b-major order.
+
+    Query rows of a sequence are flattened as r = t*H + h and cut into row
+    blocks of 128; row block rb needs the pages visible to its last token.
+    """
+    R = T * H
+    RB = (R + ROWS_PER_BLOCK - 1) // ROWS_PER_BLOCK
+    out = []
+    for b, S in enumerate(seq_lens):
+        S = int(S)
+        for rb in range(RB):
+            r_last = min(R, (rb + 1) * ROWS_PER_BLOCK) - 1
+            t_last = r_last // H
+            vis = visible_limit(S, T, t_last, causal)
+            out.append((b, rb, (vis + PAGE - 1) // PAGE))
+    return out
+
+
+def plan_ref(seq_lens, T: int, H: int, causal: bool, num_slots: int, num_splits_override: int = 0):
+    """Deterministic split plan.
+
+    Returns dict with
+      segments : list of (b, rb, page_begin, page_end, range_id, slot)  slot=-1 => final output
+      num_ranges, num_partials,
+      range_ptr: [num_ranges+1] segment offsets of each work range,
+      merge    : list of (b, rb, slot_begin, count) for every group not finished by a
+                 single final segment (count 0 => the group is empty: o=0, lse=-inf).
+    Rule:
+      1. groups (b, rb, n) as in group_pages; W = sum n.
+      2. override N>0: a group with n>0 is cut into k=min(n,N) segments,
+         segment s = [floor(s n/k), floor((s+1) n/k)); each segment is its own range.
+      3. auto: q = max(4, ceil(W/G)).  If the non-empty groups number at most G
+         and none has more than ceil(5q/4) pages, every non-empty group is one
+         segment and one range.  Otherwise range r covers global pages
+         [r q, min(W,(r+1) q)) of the concatenated groups, and each group is cut
+         where the range boundaries fall.
+      4. a segment that covers its whole group is final (slot -1); the other
+         segments get partial slots numbered in segment order.
+    """
+    groups = group_pages(seq_lens, T, H, causal)
+    G = max(1, int(num_slots))
+    raw = []  # (b, rb, p0, p1, range)
+    n_ranges = 0
+    if num_splits_override > 0:
+        for (b, rb, n) in groups:
+            if n == 0:
+                continue
+            k = min(n, int(num_splits_override))
+            for s in range(k):
+                raw.append((b, rb, (s * n) // k, ((s + 1) * n) // k, n_ranges))
+                n_ranges += 1
+    else:
+        W = sum(n for (_, _, n) in groups)
+        q = max(MIN_SPLIT_PAGES, -(-W // G)) if W > 0 else MIN_SPLIT_PAGES
+        nonempty = [g for g in groups if g[2] > 0]
+        max_n = max((g[2] for g in nonempty), default=0)
+        if len(nonempty) <= G and max_n <= -(-5 * q // 4):
+            for (b, rb, n) in nonempty:
+                raw.append((b, rb, 0, n, n_ranges))
+                n_ranges += 1
+        else:
+            off = 0
+            for (b, rb, n) in groups:
+                p = 0
+                while p < n:
+                    r = (off + p) // q
+                    end_in_group = min(n, (r + 1) * q - off)
+                    raw.append((b, rb, p, end_in_group, r))
+                    p = end_in_group
+                off += n
+            n_ranges = -(-W // q) if W > 0 else 0
+    n_of = {(b, rb): n for (b, rb, n) in groups}
+    segments = []
+    slot = 0
+    for (b, rb, p0, p1, r) in raw:
+        if p0 == 0 and p1 == n_of[(b, rb)]:
+            segments.append((b, rb, p0, p1, r, -1))
+        else:
+            segments.append((b, rb, p0, p1, r, slot))
+            slot += 1
+    range_ptr = [0] * (n_ranges + 1)
+    for s in segments:
+        range_ptr[s[4] + 1] += 1
+    for r in range(n_ranges):
+        range_ptr[r + 1] += range_ptr[r]
+    merge = []
+    for (b, rb, n) in groups:
+        segs = [s for s in segments if s[0] == b and s[1] == rb]
+        if n == 0:
+            merge.append((b, rb, 0, 0))
+        elif segs[0][5] >= 0:
+            merge.append((b, rb, segs[0][5], len(segs)))
+    return {"segments": segments, "num_ranges": n_ranges, "num_partials": slot,
+            "range_ptr": range_ptr, "merge": merge}
+
+
+# ---------------------------------------------------------------------------
+# Byte and operation ledgers
+# ([mlxcel] bytes/token table; [M5.8] 0x02 and 0x06 ledgers; [zdszero] 计算量分析;
+#  [MLA-in-depth] "What it costs")
+# ---------------------------------------------------------------------------
+def latent_bytes_per_token(d_c=D_C, d_r=D_R, elem=2) -> int:
+    """One cached row per token per layer: (d_c + d_R) values."""
+    return (d_c + d_r) * elem
+
+
+def decompressed_bytes_per_token(H, d_n=D_N, d_r=D_R, d_v=D_V, elem=2) -> int:
+    """Per-head keys (d_N + d_R wide) and values (d_V wide) for every head."""
+    return H * ((d_n + d_r) + d_v) * elem
+
+
+def normal_upproj_macs(S, d_c=D_C, H=128, d_n=D_N, d_v=D_V) -> int:
+    """kv_b up-projection of S cached latents into keys and values: S*d_c*H*d_N + S*d_c*H*d_V."""
+    return S * d_c * H * d_n + S * d_c * H * d_v
+
+
+def absorb_upproj_macs(T, d_c=D_C, H=128, d_n=D_N, d_v=D_V) -> int:
+    """Absorbing W_UK into T queries and applying W_UV to T outputs."""
+    return T * H * d_n * d_c + T * H * d_c * d_v
+
+
+def normal_attention_macs(T, S, H=128, d_n=D_N, d_r=D_R, d_v=D_V) -> int:
+    return H * (T * S * (d_n + d_r) + T * S * d_v)
+
+
+def absorb_attention_macs(T, S, H=128, d_c=D_C, d_r=D_R) -> int:
+    return H * (T * S * (d_c + d_r) + T * S * d_c)
+
+
+def visible_pairs(S, T, causal) -> int:
+    """Number of (query token, cache row) pairs that attend (from the mask)."""
+    return int(causal_mask(S, T, causal).sum())
+
+
+def decode_core_flops(H, pairs, d_c=D_C, d_r=D_R) -> int:
+    """2 flops per MAC of q.k (d_c+d_R wide) and p.v (d_c wide) per head per visible pair."""
+    return 2 * H * pairs * ((d_c + d_r) + d_c)
+
+
+def crossover_T(S, H=128) -> float:
+    """Query-block length T at which Absorb and Normal cost the same MACs for context S.
+
+    Solves absorb_upproj(T) + absorb_attention(T,S) = normal_upproj(S) + normal_attention(T,S)
+    for T (both sides linear in T).
+    """
+    a = absorb_upproj_macs(1, H=H) + absorb_attention_macs(1, S, H=H) - normal_attention_macs(1, S, H=H)
+    return normal_upproj_macs(S, H=H) / a
+
+
+def decode_intensity(H, d_c=D_C, d_r=D_R, elem=2) -> float:
+    """Core FLOPs per cache byte at T=1 (query/output traffic excluded)."""
+    return decode_core_flops(H, 1, d_c, d_r) / ((d_c + d_r) * elem)
