@@ -1,0 +1,360 @@
+"""Benchmark: absorbed MLA decode at V3 geometry (H=128, B=64, S=4096, T=1).
+
+One step = one pass of the whole hot path through libmla.so: split plan,
+absorption (q_nope @ W_UK), split-KV latent attention (+ LSE merge when the
+plan splits), un-absorption (o_lat @ W_UV).  The step is captured into CUDA
+graphs (pre: plan + absorb; decode; post: un-absorb) so that host launch cost
+does not pace the GPU; the decode graph is bracketed by CUDA events on the
+launching stream to time the dominant kernel.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU runs are replicas: each rank runs the same independent batch (the
+path shards by request and needs no collective); ``value`` is the tokens of
+all ranks divided by the slowest rank's time.  ``--impl reference`` times the
+float64 CPU oracle on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD_INDEX = 2
+METRIC = "MLA decode tokens/s and achieved HBM GB/s (% of roofline) at V3 geometry"
+L2_BYTES = 129 * 2**20
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes each kernel of the step must move at minimum (inputs read once, outputs written once)."""
+    H, B, T = w.H, w.B, w.T
+    rows = int(w.seq_lens.astype(np.int64).sum())
+    BT = B * T
+    decode = rows * 1152 + BT * H * (512 + 64) * 2 + BT * H * 512 * 2 + BT * H * 4 + w.block_table.size * 4 + B * 4
+    absorb = BT * H * 128 * 2 + H * 128 * 512 * 2 + BT * H * 512 * 2
+    unabsorb = BT * H * 512 * 2 + H * 128 * 512 * 2 + BT * H * 128 * 2
+    return {"decode": decode, "absorb": absorb, "unabsorb": unabsorb, "step": decode + absorb + unabsorb}
+
+
+def algorithmic_flops(w) -> dict:
+    H = w.H
+    from_pairs = 0
+    for S in w.seq_lens:
+        S = int(S)
+        for t in range(w.T):
+            lim = S if not w.causal else max(0, min(S, S - w.T + t + 1))
+            from_pairs += lim
+    decode = 2 * H * from_pairs * (576 + 512)
+    bmm = 2 * 2 * w.B * w.T * H * 128 * 512
+    return {"decode": decode, "bmm": bmm, "step": decode + bmm}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling in the background during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(w, budget_s: float = 15.0):
+    """Time the float64 oracle (absorb + latent attention + un-absorb) on whole sequences of the
+    workload until ~budget_s of CPU work; returns (tokens/s, sequences done, seconds, cores)."""
+    from mla_latent_cache_gb300 import workloads as W
+    from oracle import mla_oracle as O
+    pool, bt = w.compact_view()
+    f = W.bf16_bits_to_f64
+    q_nope, q_pe, w_uk, w_uv = f(w.q_nope), f(w.q_pe), f(w.w_uk), f(w.w_uv)
+    done = 0
+    t0 = time.perf_counter()
+    while done < w.B:
+        b = done
+        n = (int(w.seq_lens[b]) + 63) // 64
+        local_pool = f(pool[bt[b, :n]])          # this sequence's blocks, widened to float64
+        local_bt = np.arange(n, dtype=np.int64)[None]
+        O.absorbed_layer_ref(q_nope[[b]], q_pe[[b]], local_pool, local_bt, w.seq_lens[[b]], w_uk, w_uv, w.causal)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    except Exception:
+        threads = cores
+    return done * w.T / dt, done, dt, min(cores, threads) if threads else cores
+
+
+def _emit(line: dict):
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from mla_latent_cache_gb300 import workloads as W
+    w = W.config_workload(WORKLOAD_INDEX)
+    per_step = []
+    samples = []
+    for _ in range(args.warmup):
+        cpu_oracle_sample(_one_seq(w), budget_s=0.0)
+    budget = min(args.ref_budget, 120.0 / max(1, args.steps))   # whole run stays within a few minutes
+    for _ in range(args.steps):
+        tps, done, dt, cores = cpu_oracle_sample(w, budget_s=budget)
+        per_step.append(dt)
+        samples.append((tps, done, dt, cores))
+    tps = sum(s[1] for s in samples) * w.T / sum(per_step)
+    cores = samples[-1][3]
+    ms = 1000.0 * w.B * w.T / tps
+    _emit({"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": w.name, "H": w.H, "B": w.B, "T": w.T, "S": int(w.seq_lens[0]), "page": 64},
+           "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                            "sample": f"whole sequences of the workload, {samples[-1][1]} per step "
+                                      f"(~{budget:.1f} s budget); ms_per_step extrapolates to B={w.B}"},
+           "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
+    return 0
+
+
+def _one_seq(w):
+    from mla_latent_cache_gb300 import workloads as W
+    return W.custom_workload(w.H, [64], T=1, seed=1)
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from mla_latent_cache_gb300 import binding as L
+    from mla_latent_cache_gb300 import workloads as W
+    from mla_latent_cache_gb300.runtime import DecodeStep
+
+    w = W.config_workload(WORKLOAD_INDEX)
+    st = DecodeStep(w, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    hbm_peak, tc_peak, peak_kind = _peaks()
+    ab = algorithmic_bytes(w)
+    fl = algorithmic_flops(w)
+
+    # warm up eagerly once (sets kernel attributes), then capture
+    with torch.cuda.stream(stream):
+        st.step(stream)
+    stream.synchronize()
+    g_pre, g_dec, g_post = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_pre, stream=stream):
+        st.plan(stream)
+        st.absorb(stream)
+    with torch.cuda.graph(g_dec, stream=stream):
+        st.decode(stream)
+    with torch.cuda.graph(g_post, stream=stream):
+        st.unabsorb(stream)
+    launches_per_step = 5  # plan, absorb, decode, merge, un-absorb
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            g_pre.replay(); g_dec.replay(); g_post.replay()
+    stream.synchronize()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            for i in range(args.steps):
+                g_pre.replay()
+                evs[i][0].record(stream)
+                g_dec.replay()
+                evs[i][1].record(stream)
+                g_post.replay()
+            t_end.record(stream)
+        stream.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens_per_step = w.B * w.T * world
+    value = tokens_per_step / (ms / 1000.0)
+    status, info = L.mla_read_device_status(st.workspace, stream)
+    if status != L.MLA_OK:
+        raise RuntimeError(f"device status after timing: {L.mla_status_string(status)} ({info})")
+
+    # end to end through the C ABI with host buffers: per step, copy the step's inputs
+    # (q_nope, q_pe, seq_lens, block table) from pinned host memory, run, read o back.
+    h_qn = torch.empty_like(st.q_nope, device="cpu").pin_memory(); h_qn.copy_(st.q_nope)
+    h_qp = torch.empty_like(st.q_pe, device="cpu").pin_memory(); h_qp.copy_(st.q_pe)
+    h_sl = torch.empty_like(st.seq_lens, device="cpu").pin_memory(); h_sl.copy_(st.seq_lens)
+    h_bt = torch.empty_like(st.block_table, device="cpu").pin_memory(); h_bt.copy_(st.block_table)
+    h_o = torch.empty_like(st.o, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_qn, h_qp, h_sl, h_bt))
+    d2h = h_o.numel() * h_o.element_size()
+    e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        st.q_nope.copy_(h_qn, non_blocking=True)
+        st.q_pe.copy_(h_qp, non_blocking=True)
+        st.seq_lens.copy_(h_sl, non_blocking=True)
+        st.block_table.copy_(h_bt, non_blocking=True)
+        g_pre.replay(); g_dec.replay(); g_post.replay()
+        h_o.copy_(st.o, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = tokens_per_step / (e2e_ms / 1000.0)
+
+    achieved = ab["decode"] / (dec_ms / 1000.0) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "H": w.H, "B": w.B, "T": w.T, "S": int(w.seq_lens[0]), "page": 64,
+                   "pool_blocks": w.num_blocks, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2: 302 MB latent pool streamed per step vs 129 MB L2",
+                   "step": "plan + absorb + decode(+merge) + unabsorb, CUDA graphs"},
+        "roofline": {"bound": "hbm", "kernel": "mla_decode (split-KV decode + merge)", "achieved": achieved,
+                     "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": None, "algorithmic_bytes": ab["decode"], "decode_ms": dec_ms,
+                     "decode_tflops": fl["decode"] / (dec_ms / 1000.0) / 1e12},
+        "step_hbm_gbs": ab["step"] / (ms / 1000.0) / 1e9,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, done, dt, cores = cpu_oracle_sample(w, budget_s=args.ref_budget)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{done} whole sequences of the workload (absorb + attention + "
+                                          f"un-absorb, float64) in {dt:.1f} s"}
+    if rank == 0:
+        _emit(line)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of CPU oracle work per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,205 @@
+/*
+ * mla.h — C ABI of libmla.so: absorbed Multi-head Latent Attention (MLA) decode
+ * over a paged latent KV cache, for GB300 (sm_103a).
+ *
+ * The operation (sources cited by page title and section):
+ *   - "MLA in full detail" (mlinterviewnotes ch. 7.2), Step 2 "fold W_UK into
+ *     the query", Step 3 "attend against the latent directly", Step 4 "fold
+ *     W_UV into the output";
+ *   - "M5.8 - Multi-Head Latent Attention ..." 0x04 "Batched absorption trace"
+ *     (canonical shapes), 0x05 "Paged and ragged address translation", 0x08
+ *     "FlashMLA Runtime ABI" (scheduler metadata that must be rebuilt when the
+ *     batch geometry or the lengths change; a returned LSE), 0x0C (exact merge
+ *     of split softmax state);
+ *   - "mlxcel: MLA absorbed decode", Stage 2 (split-KV partials normalised by
+ *     their own denominator, merged by log-sum-exp through an indptr).
+ *
+ * Geometry: kv_lora_rank d_c = 512, RoPE width d_R = 64, nope width d_N = 128,
+ * value width d_V = 128, page (block) size P = 64, softmax scale 1/sqrt(192).
+ * One cached row is 576 bf16 values: [c_KV (512) | k_pe (64)], shared by all
+ * H query heads (one latent KV head).
+ *
+ * Tensor layouts (row-major, contiguous unless a stride is given; bf16 unless noted):
+ *   q_nope [B,T,H,128]   q_pe [B,T,H,64]   q_lat [B,T,H,512]
+ *   W_UK, W_UV [H,128,512]   (W_UK[h,n,c] contracted over n with q_nope;
+ *                             W_UV[h,v,c] contracted over c with o_lat)
+ *   cache: latent row j of block k at ckv + k*ckv_block_stride + j*ckv_row_stride
+ *          (elements), its RoPE values at kpe + k*kpe_block_stride + j*kpe_row_stride;
+ *          one combined [num_blocks, 64, 576] buffer or two separate ones
+ *   block_table int32 [B, bt_stride]; seq_lens int32 [B] (visible rows,
+ *          including the T new rows, which are the last T of them)
+ *   o_lat [B,T,H,512]   lse float32 [B,T,H] (natural log)   o [B,T,H,128]
+ *
+ * Conventions.
+ *   Ownership: the caller allocates every device buffer, the workspace
+ *     included.  The library never allocates or frees device memory and never
+ *     synchronises, except mla_read_device_status.
+ *   Asynchrony: every call enqueues work on `stream` and returns at once.  The
+ *     returned status covers host-side validation and launch errors only;
+ *     errors seen by kernels are recorded in the workspace's status word and
+ *     read back with mla_read_device_status.
+ *   Alignment: every device pointer must be 16-byte aligned, and strides must
+ *     keep rows 16-byte aligned (MLA_ERR_ALIGN otherwise).
+ *   Causality: with causal != 0, query token t of sequence b sees cache rows
+ *     0 .. S_b - T + t (bottom-right aligned); otherwise all S_b rows.
+ *   Empty sequences: S_b = 0 gives o_lat = 0 and lse = -inf.
+ *   Errors never trap: a kernel that meets a bad block id, a length beyond the
+ *     block table, a stale plan or a wait that runs out records an error code
+ *     in the workspace and skips the access.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* mla_stream_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_ARG = -1,          /* null pointer, negative size, unsupported flag */
+  MLA_ERR_SHAPE = -2,        /* geometry not supported (d_* must be 512/64/128/128, P = 64, 1 <= H <= 128, 128 % H == 0) */
+  MLA_ERR_ALIGN = -3,        /* pointer or stride not 16-byte aligned */
+  MLA_ERR_WORKSPACE = -4,    /* workspace smaller than mla_workspace_size() */
+  MLA_ERR_PLAN_STALE = -5,   /* (device) plan built for other lengths/geometry */
+  MLA_ERR_CUDA = -6,         /* a CUDA runtime call or launch failed */
+  MLA_ERR_DEVICE_CHECK = -7, /* (device) bad block id, or seq_len beyond the block table, or T > seq_len */
+  MLA_ERR_TIMEOUT = -8       /* (device) a bounded wait ran out */
+} mla_status;
+
+typedef struct {
+  int H;               /* query heads (DeepSeek-V2-Lite 16, V3 128) */
+  int d_lat;           /* kv_lora_rank, must be 512 */
+  int d_rope;          /* qk_rope_head_dim, must be 64 */
+  int d_nope;          /* qk_nope_head_dim, must be 128 */
+  int d_v;             /* v_head_dim, must be 128 */
+  int block_size;      /* rows per cache page, must be 64 */
+  float softmax_scale; /* 1/sqrt(d_nope + d_rope) = 1/sqrt(192) */
+} mla_geom;
+
+typedef struct {
+  const void* ckv;          /* bf16 latent part of the pool (512 values per row) */
+  const void* kpe;          /* bf16 RoPE part (64 values per row); for the combined 576-wide row, (bf16*)ckv + 512 */
+  int64_t ckv_row_stride;   /* elements between consecutive latent rows of a block (576 combined, 512 split) */
+  int64_t ckv_block_stride; /* elements between consecutive latent blocks (64*576 combined) */
+  int64_t kpe_row_stride;   /* elements between consecutive RoPE rows (576 combined, 64 split) */
+  int64_t kpe_block_stride; /* elements between consecutive RoPE blocks */
+  int num_blocks;           /* blocks in the pool; valid block ids are 0 .. num_blocks-1 */
+} mla_cache;
+
+typedef struct {
+  int B;                   /* sequences in the batch (>= 0) */
+  int T;                   /* new query tokens per sequence (>= 1) */
+  int causal;              /* 1: causal within the new tokens */
+  int max_pages;           /* width of a block-table row, in pages (>= 1) */
+  int num_slots;           /* work ranges run concurrently by the decode kernel; 0 = library default for the device */
+  int num_splits_override; /* 0: automatic split rule; N > 0: every query-row group is cut into min(pages, N) chunks */
+} mla_batch;
+
+/*
+ * Scheduler plan stored at the start of the workspace (all int32; written by
+ * mla_plan, read by mla_decode).  Offsets are in bytes from the workspace base.
+ * The split rule (the pages leave it open; FlashMLA's metadata is opaque):
+ *   query rows of a sequence are flattened r = t*H + h and cut into row blocks
+ *   of 128 (a "group" (b, rb)); a group needs the pages visible to its last
+ *   token.  Let W be the total pages over all groups and q = max(4, ceil(W/G)),
+ *   G = num_slots.  With an override N, each group is cut into min(n, N) even
+ *   chunks, one range each.  Otherwise, if at most G groups are non-empty and
+ *   none exceeds ceil(5q/4) pages, each group is one segment and one range;
+ *   else range r covers global pages [r q, (r+1) q) of the concatenated groups.
+ *   A segment covering its whole group writes final outputs; the others write
+ *   partial state to numbered slots, merged afterwards.
+ */
+enum {
+  MLA_HDR_MAGIC = 0, MLA_HDR_B, MLA_HDR_T, MLA_HDR_H, MLA_HDR_CAUSAL, MLA_HDR_NUM_GROUPS,
+  MLA_HDR_NUM_SEGMENTS, MLA_HDR_NUM_RANGES, MLA_HDR_NUM_PARTIALS, MLA_HDR_NUM_MERGE,
+  MLA_HDR_SEQ_HASH, MLA_HDR_ERROR, MLA_HDR_ERROR_INFO, MLA_HDR_PAGES_PER_RANGE,
+  MLA_HDR_NUM_SLOTS, MLA_HDR_OVERRIDE, MLA_HDR_MAX_PAGES,
+  MLA_HDR_OFF_SEGMENTS, MLA_HDR_OFF_RANGE_PTR, MLA_HDR_OFF_MERGE, MLA_HDR_OFF_PART_LSE, MLA_HDR_OFF_PART_O,
+  MLA_HDR_CAP_SEGMENTS, MLA_HDR_CAP_PARTIALS, MLA_HDR_CAP_RANGES, MLA_HDR_CAP_GROUPS,
+  MLA_HDR_WORDS = 64
+};
+#define MLA_PLAN_MAGIC 0x4d4c4131 /* "MLA1" */
+/* segment record: int32[8] = {b, rb, page_begin, page_end, range, slot (-1 = final), 0, 0}
+ * merge record:   int32[4] = {b, rb, slot_begin, count} (count 0 = empty group)
+ * part_lse float32 [cap_partials, 128]; part_o float32 [cap_partials, 128, 512] (normalised) */
+
+/* Bytes of workspace needed for this geometry and batch shape. 0 on invalid arguments. */
+size_t mla_workspace_size(const mla_geom* geom, const mla_batch* batch);
+
+/*
+ * Build the split plan on the device from seq_lens (device int32 [B]) into the
+ * workspace.  Must be re-run whenever B, T, causal, the lengths or num_slots
+ * change (the plan is stamped with them; mla_decode with checked != 0 flags a
+ * stale plan).  Also clears the workspace status word.
+ */
+mla_status mla_plan(const mla_geom* geom, const mla_batch* batch, const int32_t* seq_lens,
+                    void* workspace, size_t ws_bytes, mla_stream_t stream);
+
+/*
+ * q_lat[b,t,h,:] = q_nope[b,t,h,:] @ W_UK[h]   over BT = B*T query tokens.
+ * q_nope [BT,H,128], w_uk [H,128,512], q_lat [BT,H,512] (all bf16, device).
+ * fp32 accumulation, bf16 output (round to nearest even).
+ */
+mla_status mla_absorb_q(const mla_geom* geom, const void* q_nope, const void* w_uk, void* q_lat,
+                        int BT, mla_stream_t stream);
+
+/*
+ * o[b,t,h,v] = sum_c o_lat[b,t,h,c] * W_UV[h,v,c]   over BT query tokens.
+ * o_lat [BT,H,512], w_uv [H,128,512], o [BT,H,128] (bf16, device); fp32 accumulation.
+ */
+mla_status mla_unabsorb_o(const mla_geom* geom, const void* o_lat, const void* w_uv, void* o,
+                          int BT, mla_stream_t stream);
+
+/*
+ * Absorbed attention over the paged latent cache, using the plan in the
+ * workspace: scores s = (q_lat . c_j + q_pe . k_pe_j) * scale, softmax over the
+ * visible rows j, o_lat = sum_j p_j c_j, lse = log sum_j e^{s_j}.  Launches the
+ * split-KV decode kernel and, when the plan has partial segments, the merge.
+ * q_lat [B,T,H,512], q_pe [B,T,H,64] bf16; o_lat [B,T,H,512] bf16; lse [B,T,H] float32.
+ * checked != 0 validates every block id read, the plan stamp and T <= S_b on the
+ * device (errors go to the status word; invalid pages are skipped).
+ */
+mla_status mla_decode(const mla_geom* geom, const mla_batch* batch, const void* q_lat, const void* q_pe,
+                      const mla_cache* cache, const int32_t* block_table, int bt_stride,
+                      const int32_t* seq_lens, int checked, void* o_lat, float* lse,
+                      void* workspace, size_t ws_bytes, mla_stream_t stream);
+
+/*
+ * Exact merge of split partial states (mlxcel Stage-2 contract, natural-log LSE):
+ * part_o float32 [N, rows, D] (each normalised by its own denominator),
+ * part_lse float32 [N, rows] (natural log, -inf = empty), indptr int32 [M+1]
+ * (partials indptr[m] .. indptr[m+1]-1 form output m).  Writes o bf16 [M, rows, D]
+ * and lse float32 [M, rows]: m* = max lse_r, w_r = e^{lse_r - m*},
+ * o = sum w_r o_r / sum w_r, lse = m* + ln sum w_r; an output with no
+ * non-empty partial gets o = 0, lse = -inf.  D must be a multiple of 8.
+ */
+mla_status mla_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M,
+                           int rows, int D, void* o, float* lse, mla_stream_t stream);
+
+/*
+ * Test export: copy the S_b logical rows of sequence b, in order, through the
+ * decode kernel's own address path, into out bf16 [S_b, 576] (latent | RoPE).
+ */
+mla_status mla_debug_gather(const mla_cache* cache, const int32_t* block_table, int bt_stride,
+                            const int32_t* seq_lens, int b, void* out, mla_stream_t stream);
+
+/* Synchronise `stream`, then return the status word a kernel recorded in the
+ * workspace (MLA_OK if none) and, if info != NULL, its detail word. */
+mla_status mla_read_device_status(const void* workspace, int* info, mla_stream_t stream);
+
+/* Static description of a status code. */
+const char* mla_status_string(mla_status status);
+
+/* SMs of the current device (the default for num_slots). */
+int mla_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_H_ */

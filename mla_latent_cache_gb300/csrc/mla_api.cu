@@ -1,0 +1,229 @@
+// The C ABI of libmla.so (declared in include/mla.h): host-side validation,
+// workspace layout and kernel launches.  No allocation, no synchronisation
+// (except mla_read_device_status).
+#include <string.h>
+
+#include "mla_internal.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mla_status check_geom(const mla_geom* g) {
+  if (!g) return MLA_ERR_ARG;
+  if (g->d_lat != kDLat || g->d_rope != kDRope || g->d_nope != kDNope || g->d_v != kDV || g->block_size != kPage)
+    return MLA_ERR_SHAPE;
+  if (g->H < 1 || g->H > kRowsPerBlock || (kRowsPerBlock % g->H) != 0) return MLA_ERR_SHAPE;
+  if (!(g->softmax_scale > 0.f)) return MLA_ERR_ARG;
+  return MLA_OK;
+}
+
+mla_status check_batch(const mla_batch* b) {
+  if (!b) return MLA_ERR_ARG;
+  if (b->B < 0 || b->T < 1 || b->max_pages < 1 || b->num_slots < 0 || b->num_splits_override < 0)
+    return MLA_ERR_ARG;
+  if ((long long)b->T * kRowsPerBlock > (1LL << 24)) return MLA_ERR_SHAPE;
+  return MLA_OK;
+}
+
+mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+}  // namespace
+
+int resolve_slots(const mla_batch* b) {
+  if (b->num_slots > 0) return b->num_slots;
+  const int sms = mla_device_sm_count();
+  return sms > 0 ? sms : 1;
+}
+
+bool compute_layout(const mla_geom* g, const mla_batch* b, WsLayout* L) {
+  const long long RB = ((long long)b->T * g->H + kRowsPerBlock - 1) / kRowsPerBlock;
+  const long long groups = (long long)b->B * RB;
+  const int G = resolve_slots(b);
+  long long cap_ranges, cap_segments, cap_partials;
+  if (b->num_splits_override > 0) {
+    const long long k = b->num_splits_override < b->max_pages ? b->num_splits_override : b->max_pages;
+    cap_ranges = cap_segments = cap_partials = groups * k;
+  } else {
+    cap_ranges = G;
+    cap_segments = groups + G;
+    cap_partials = 2LL * G;
+  }
+  if (groups > (1 << 26) || cap_segments > (1 << 26)) return false;
+  size_t off = align_up(MLA_HDR_WORDS * sizeof(int));
+  L->off_groups = off;     off = align_up(off + (size_t)groups * kGroupWords * sizeof(int));
+  L->off_segments = off;   off = align_up(off + (size_t)cap_segments * kSegWords * sizeof(int));
+  L->off_range_ptr = off;  off = align_up(off + (size_t)(cap_ranges + 1) * sizeof(int));
+  L->off_merge = off;      off = align_up(off + (size_t)groups * kMergeWords * sizeof(int));
+  L->off_part_lse = off;   off = align_up(off + (size_t)cap_partials * kRowsPerBlock * sizeof(float));
+  L->off_part_o = off;     off = align_up(off + (size_t)cap_partials * kRowsPerBlock * kDLat * sizeof(float));
+  L->total = off;
+  L->cap_groups = (int)groups;
+  L->cap_segments = (int)cap_segments;
+  L->cap_ranges = (int)cap_ranges;
+  L->cap_partials = (int)cap_partials;
+  L->num_slots = G;
+  return true;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int mla_device_sm_count(void) {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_ARG: return "invalid argument";
+    case MLA_ERR_SHAPE: return "unsupported geometry or shape";
+    case MLA_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case MLA_ERR_WORKSPACE: return "workspace too small";
+    case MLA_ERR_PLAN_STALE: return "plan built for other lengths or geometry";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_DEVICE_CHECK: return "device check failed (block id, length or T)";
+    case MLA_ERR_TIMEOUT: return "bounded wait ran out";
+  }
+  return "unknown status";
+}
+
+size_t mla_workspace_size(const mla_geom* geom, const mla_batch* batch) {
+  if (check_geom(geom) != MLA_OK || check_batch(batch) != MLA_OK) return 0;
+  WsLayout L;
+  if (!compute_layout(geom, batch, &L)) return 0;
+  return L.total;
+}
+
+mla_status mla_plan(const mla_geom* geom, const mla_batch* batch, const int32_t* seq_lens, void* workspace,
+                    size_t ws_bytes, mla_stream_t stream) {
+  mla_status s = check_geom(geom);
+  if (s != MLA_OK) return s;
+  if ((s = check_batch(batch)) != MLA_OK) return s;
+  if (!workspace || (batch->B > 0 && !seq_lens)) return MLA_ERR_ARG;
+  if (!aligned16(workspace) || !aligned16(seq_lens)) return MLA_ERR_ALIGN;
+  WsLayout L;
+  if (!compute_layout(geom, batch, &L)) return MLA_ERR_SHAPE;
+  if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
+  return cuda_status(launch_plan(seq_lens, geom, batch, L, workspace, (cudaStream_t)stream));
+}
+
+mla_status mla_absorb_q(const mla_geom* geom, const void* q_nope, const void* w_uk, void* q_lat, int BT,
+                        mla_stream_t stream) {
+  mla_status s = check_geom(geom);
+  if (s != MLA_OK) return s;
+  if (BT < 0) return MLA_ERR_ARG;
+  if (BT == 0) return MLA_OK;
+  if (!q_nope || !w_uk || !q_lat) return MLA_ERR_ARG;
+  if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_lat)) return MLA_ERR_ALIGN;
+  return cuda_status(launch_absorb(static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(w_uk),
+                                   static_cast<__nv_bfloat16*>(q_lat), BT, geom->H, (cudaStream_t)stream));
+}
+
+mla_status mla_unabsorb_o(const mla_geom* geom, const void* o_lat, const void* w_uv, void* o, int BT,
+                          mla_stream_t stream) {
+  mla_status s = check_geom(geom);
+  if (s != MLA_OK) return s;
+  if (BT < 0) return MLA_ERR_ARG;
+  if (BT == 0) return MLA_OK;
+  if (!o_lat || !w_uv || !o) return MLA_ERR_ARG;
+  if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(o)) return MLA_ERR_ALIGN;
+  return cuda_status(launch_unabsorb(static_cast<const __nv_bfloat16*>(o_lat), static_cast<const __nv_bfloat16*>(w_uv),
+                                     static_cast<__nv_bfloat16*>(o), BT, geom->H, (cudaStream_t)stream));
+}
+
+static mla_status check_cache(const mla_cache* cache, CacheView* cv) {
+  if (!cache || !cache->ckv || !cache->kpe || cache->num_blocks < 1) return MLA_ERR_ARG;
+  if (cache->ckv_row_stride < 1 || cache->kpe_row_stride < 1 || cache->ckv_block_stride < 1 ||
+      cache->kpe_block_stride < 1)
+    return MLA_ERR_ARG;
+  if (!aligned16(cache->ckv) || !aligned16(cache->kpe)) return MLA_ERR_ALIGN;
+  if ((cache->ckv_row_stride * 2) % 16 != 0 || (cache->ckv_block_stride * 2) % 16 != 0 ||
+      (cache->kpe_row_stride * 2) % 16 != 0 || (cache->kpe_block_stride * 2) % 16 != 0)
+    return MLA_ERR_ALIGN;
+  cv->ckv = static_cast<const __nv_bfloat16*>(cache->ckv);
+  cv->kpe = static_cast<const __nv_bfloat16*>(cache->kpe);
+  cv->ckv_row = cache->ckv_row_stride;
+  cv->ckv_block = cache->ckv_block_stride;
+  cv->kpe_row = cache->kpe_row_stride;
+  cv->kpe_block = cache->kpe_block_stride;
+  cv->num_blocks = cache->num_blocks;
+  return MLA_OK;
+}
+
+mla_status mla_decode(const mla_geom* geom, const mla_batch* batch, const void* q_lat, const void* q_pe,
+                      const mla_cache* cache, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                      int checked, void* o_lat, float* lse, void* workspace, size_t ws_bytes, mla_stream_t stream) {
+  mla_status s = check_geom(geom);
+  if (s != MLA_OK) return s;
+  if ((s = check_batch(batch)) != MLA_OK) return s;
+  if (batch->B == 0) return MLA_OK;
+  if (!q_lat || !q_pe || !block_table || !seq_lens || !o_lat || !lse || !workspace) return MLA_ERR_ARG;
+  if (bt_stride < batch->max_pages) return MLA_ERR_ARG;
+  if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned16(o_lat) || !aligned16(lse) || !aligned16(workspace) ||
+      !aligned16(block_table) || !aligned16(seq_lens))
+    return MLA_ERR_ALIGN;
+  CacheView cv;
+  if ((s = check_cache(cache, &cv)) != MLA_OK) return s;
+  WsLayout L;
+  if (!compute_layout(geom, batch, &L)) return MLA_ERR_SHAPE;
+  if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = launch_decode_simple(geom, batch, L, static_cast<const __nv_bfloat16*>(q_lat),
+                                       static_cast<const __nv_bfloat16*>(q_pe), cv, block_table, bt_stride, seq_lens,
+                                       checked, static_cast<__nv_bfloat16*>(o_lat), lse, workspace, st);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  e = launch_plan_merge(geom, batch, L, static_cast<__nv_bfloat16*>(o_lat), lse, workspace, st);
+  return cuda_status(e);
+}
+
+mla_status mla_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M, int rows, int D,
+                           void* o, float* lse, mla_stream_t stream) {
+  if (M < 0 || rows < 0 || D <= 0 || (D % 8) != 0) return MLA_ERR_ARG;
+  if (M == 0 || rows == 0) return MLA_OK;
+  if (!part_o || !part_lse || !indptr || !o || !lse) return MLA_ERR_ARG;
+  if (!aligned16(part_o) || !aligned16(o) || !aligned16(indptr)) return MLA_ERR_ALIGN;
+  if (((size_t)rows * D * sizeof(float)) % 16 != 0) return MLA_ERR_ALIGN;
+  return cuda_status(launch_split_merge(part_o, part_lse, indptr, M, rows, D, static_cast<__nv_bfloat16*>(o), lse,
+                                        (cudaStream_t)stream));
+}
+
+mla_status mla_debug_gather(const mla_cache* cache, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                            int b, void* out, mla_stream_t stream) {
+  if (!block_table || !seq_lens || !out || b < 0 || bt_stride < 1) return MLA_ERR_ARG;
+  if (!aligned16(out)) return MLA_ERR_ALIGN;
+  CacheView cv;
+  mla_status s = check_cache(cache, &cv);
+  if (s != MLA_OK) return s;
+  return cuda_status(launch_debug_gather(cv, block_table, bt_stride, seq_lens, b, static_cast<__nv_bfloat16*>(out),
+                                         (cudaStream_t)stream));
+}
+
+mla_status mla_read_device_status(const void* workspace, int* info, mla_stream_t stream) {
+  if (!workspace) return MLA_ERR_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MLA_ERR_CUDA;
+  int words[2] = {0, 0};
+  const char* base = static_cast<const char*>(workspace) + MLA_HDR_ERROR * sizeof(int);
+  if (cudaMemcpy(words, base, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  if (info) *info = words[1];
+  return (mla_status)words[0];
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// Internal declarations shared by the libmla translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int kDLat = 512;
+constexpr int kDRope = 64;
+constexpr int kDK = kDLat + kDRope;  // 576
+constexpr int kDNope = 128;
+constexpr int kDV = 128;
+constexpr int kPage = 64;
+constexpr int kRowsPerBlock = 128;   // flattened (t, h) query rows per group
+constexpr int kMinSplitPages = 4;
+constexpr int kSegWords = 8;
+constexpr int kMergeWords = 4;
+constexpr int kGroupWords = 8;
+
+// Workspace layout, computed on the host from (geometry, batch shape, slots).
+struct WsLayout {
+  size_t off_groups, off_segments, off_range_ptr, off_merge, off_part_lse, off_part_o, total;
+  int cap_groups, cap_segments, cap_ranges, cap_partials;
+  int num_slots;
+};
+
+bool compute_layout(const mla_geom* g, const mla_batch* b, WsLayout* L);
+int resolve_slots(const mla_batch* b);
+
+// Status word helpers (device): first error wins.
+__device__ __forceinline__ void record_error(int* hdr, int code, int info) {
+  if (atomicCAS(&hdr[MLA_HDR_ERROR], 0, code) == 0) {
+    atomicExch(&hdr[MLA_HDR_ERROR_INFO], info);
+  }
+}
+
+// Paged address translation ("M5.8", 0x05): physical row of logical row j of
+// sequence b is block_table[b, j / 64] * 64 + j % 64; the element offset of
+// that row is block * block_stride + (j % 64) * row_stride.
+struct CacheView {
+  const __nv_bfloat16* ckv;
+  const __nv_bfloat16* kpe;
+  int64_t ckv_row, ckv_block, kpe_row, kpe_block;
+  int num_blocks;
+};
+
+__device__ __forceinline__ const __nv_bfloat16* ckv_row_ptr(const CacheView& c, int block, int j_in_page) {
+  return c.ckv + (int64_t)block * c.ckv_block + (int64_t)j_in_page * c.ckv_row;
+}
+__device__ __forceinline__ const __nv_bfloat16* kpe_row_ptr(const CacheView& c, int block, int j_in_page) {
+  return c.kpe + (int64_t)block * c.kpe_block + (int64_t)j_in_page * c.kpe_row;
+}
+
+// Visible rows of query token t (bottom-right causal alignment).
+__host__ __device__ __forceinline__ int visible_limit(int S, int T, int t, int causal) {
+  if (!causal) return S;
+  int v = S - T + t + 1;
+  return v < 0 ? 0 : (v > S ? S : v);
+}
+
+// Launchers (one per translation unit); all return cudaError_t of the launch.
+cudaError_t launch_plan(const int32_t* seq_lens, const mla_geom* g, const mla_batch* b,
+                        const WsLayout& L, void* ws, cudaStream_t st);
+cudaError_t launch_decode_simple(const mla_geom* g, const mla_batch* b, const WsLayout& L,
+                                 const __nv_bfloat16* q_lat, const __nv_bfloat16* q_pe, const CacheView& cv,
+                                 const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                                 int checked, __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st);
+cudaError_t launch_plan_merge(const mla_geom* g, const mla_batch* b, const WsLayout& L,
+                              __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st);
+cudaError_t launch_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M,
+                               int rows, int D, __nv_bfloat16* o, float* lse, cudaStream_t st);
+cudaError_t launch_absorb(const __nv_bfloat16* q_nope, const __nv_bfloat16* w_uk, __nv_bfloat16* q_lat,
+                          int BT, int H, cudaStream_t st);
+cudaError_t launch_unabsorb(const __nv_bfloat16* o_lat, const __nv_bfloat16* w_uv, __nv_bfloat16* o,
+                            int BT, int H, cudaStream_t st);
+cudaError_t launch_debug_gather(const CacheView& cv, const int32_t* block_table, int bt_stride,
+                                const int32_t* seq_lens, int b, __nv_bfloat16* out, cudaStream_t st);
+
+}  // namespace mla

@@ -1,0 +1,110 @@
+"""Device-side state for one decode step, built on the C ABI.
+
+``DecodeStep`` owns the device buffers (PyTorch allocations) for one batch
+shape and runs the hot path through libmla.so:
+plan -> absorb (q_nope @ W_UK) -> split-KV latent attention (+ merge) ->
+un-absorb (o_lat @ W_UV).  Nothing here computes: it allocates and marshals.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import binding as L
+from .workloads import Workload
+
+
+def _u16_to_bf16(torch, a: np.ndarray, device):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def pool_to_device(torch, w: Workload, device):
+    """Materialise the [num_blocks, 64, 576] pool on the device (NaN outside the referenced blocks)."""
+    pool = torch.full((w.num_blocks, 64, 576), float("nan"), dtype=torch.bfloat16, device=device)
+    data = _u16_to_bf16(torch, w.pool_data, device)
+    ids = torch.from_numpy(w.pool_ids).to(device)
+    pool.index_copy_(0, ids, data)
+    return pool
+
+
+class DecodeStep:
+    def __init__(self, w: Workload, device="cuda", num_slots: int = 0, num_splits_override: int = 0,
+                 checked: bool = False, with_absorb: bool = True):
+        import torch
+        self.torch = torch
+        self.w = w
+        self.device = torch.device(device)
+        self.geom = L.make_geom(w.H)
+        self.batch = L.make_batch(w.B, w.T, w.causal, w.max_pages, num_slots, num_splits_override)
+        self.checked = 1 if checked else 0
+        dev = self.device
+        self.pool = pool_to_device(torch, w, dev)
+        self.cache = L.cache_from_pool(self.pool)
+        self.block_table = torch.from_numpy(w.block_table).to(dev)
+        self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
+        self.q_pe = _u16_to_bf16(torch, w.q_pe, dev)
+        if with_absorb:
+            self.q_nope = _u16_to_bf16(torch, w.q_nope, dev)
+            self.w_uk = _u16_to_bf16(torch, w.w_uk, dev)
+            self.w_uv = _u16_to_bf16(torch, w.w_uv, dev)
+            self.q_lat = torch.empty((w.B, w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+            self.o = torch.empty((w.B, w.T, w.H, 128), dtype=torch.bfloat16, device=dev)
+        else:
+            self.q_lat = _u16_to_bf16(torch, w.q_lat, dev)
+        self.o_lat = torch.empty((w.B, w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.B, w.T, w.H), dtype=torch.float32, device=dev)
+        self.ws_bytes = L.mla_workspace_size(self.geom, self.batch)
+        if self.ws_bytes == 0:
+            raise L.MlaError(L.MLA_ERR_ARG, "mla_workspace_size")
+        self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
+
+    @property
+    def BT(self) -> int:
+        return self.w.B * self.w.T
+
+    def plan(self, stream=None):
+        L.check(L.mla_plan(self.geom, self.batch, self.seq_lens, self.workspace, self.ws_bytes, stream), "mla_plan")
+
+    def absorb(self, stream=None):
+        L.check(L.mla_absorb_q(self.geom, self.q_nope, self.w_uk, self.q_lat, self.BT, stream), "mla_absorb_q")
+
+    def decode(self, stream=None):
+        L.check(L.mla_decode(self.geom, self.batch, self.q_lat, self.q_pe, self.cache, self.block_table,
+                             self.block_table.shape[1], self.seq_lens, self.checked, self.o_lat, self.lse,
+                             self.workspace, self.ws_bytes, stream), "mla_decode")
+
+    def unabsorb(self, stream=None):
+        L.check(L.mla_unabsorb_o(self.geom, self.o_lat, self.w_uv, self.o, self.BT, stream), "mla_unabsorb_o")
+
+    def step(self, stream=None):
+        """One pass of the whole hot path (plan, absorb, decode + merge, un-absorb)."""
+        self.plan(stream)
+        self.absorb(stream)
+        self.decode(stream)
+        self.unabsorb(stream)
+
+    def plan_header(self):
+        return read_plan_header(self.torch, self.workspace)
+
+    def plan_tables(self):
+        return read_plan_tables(self.torch, self.workspace)
+
+
+def read_plan_header(torch, workspace):
+    """The plan header words (include/mla.h) copied to the host."""
+    return workspace[: L.HDR_WORDS * 4].view(torch.int32).cpu().numpy()
+
+
+def read_plan_tables(torch, workspace):
+    """(segments [n,8], range_ptr [n_ranges+1], merge [m,4]) copied from the workspace."""
+    hdr = read_plan_header(torch, workspace)
+
+    def words(off, n):
+        return workspace[off: off + 4 * n].view(torch.int32).cpu().numpy()
+
+    nseg = int(hdr[L.HDR["NUM_SEGMENTS"]])
+    nr = int(hdr[L.HDR["NUM_RANGES"]])
+    nm = int(hdr[L.HDR["NUM_MERGE"]])
+    seg = words(int(hdr[L.HDR["OFF_SEGMENTS"]]), nseg * 8).reshape(nseg, 8)
+    rp = words(int(hdr[L.HDR["OFF_RANGE_PTR"]]), nr + 1)
+    mg = words(int(hdr[L.HDR["OFF_MERGE"]]), nm * 4).reshape(nm, 4)
+    return seg, rp, mg

@@ -1,0 +1,66 @@
+"""The C ABI loads and exports every symbol include/mla.h declares; host-side validation (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "mla.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(mla):
+    names = _declared()
+    assert "mla_decode" in names and "mla_absorb_q" in names and "mla_split_merge" in names
+    lib = ctypes.CDLL(mla.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"libmla.so does not export {n}"
+    assert set(mla.EXPORTED) >= set(names)
+
+
+def test_status_strings(mla):
+    for code in range(-8, 1):
+        s = mla.mla_status_string(code)
+        assert s and s != "unknown status"
+    assert mla.mla_status_string(17) == "unknown status"
+
+
+def test_workspace_size_host_only(mla):
+    g = mla.make_geom(128)
+    b = mla.make_batch(64, 1, False, 64, num_slots=152)
+    ws = mla.mla_workspace_size(g, b)
+    # 2*G partial slots of 128 x 512 fp32 dominate
+    assert ws >= 2 * 152 * 128 * 512 * 4
+    assert ws % 256 == 0
+    b2 = mla.make_batch(1, 1, False, 2048, num_slots=152, num_splits_override=256)
+    assert mla.mla_workspace_size(g, b2) >= 256 * 128 * 512 * 4
+    # invalid geometry / batch -> 0
+    assert mla.mla_workspace_size(mla.make_geom(96), b) == 0
+    bad = mla.make_batch(4, 0, False, 8, num_slots=4)
+    assert mla.mla_workspace_size(g, bad) == 0
+
+
+def test_host_validation_rejects_before_launch(mla):
+    g = mla.make_geom(16)
+    # null pointers are rejected on the host before any CUDA call
+    assert mla.mla_absorb_q(g, None, None, None, 4, 0) == mla.MLA_ERR_ARG
+    assert mla.mla_unabsorb_o(g, None, None, None, 4, 0) == mla.MLA_ERR_ARG
+    assert mla.mla_absorb_q(g, 0x1000, 0x2000, 0x3008, 4, 0) == mla.MLA_ERR_ALIGN
+    assert mla.mla_absorb_q(mla.make_geom(24), 0x1000, 0x2000, 0x3000, 4, 0) == mla.MLA_ERR_SHAPE
+    assert mla.mla_absorb_q(g, 0x1000, 0x2000, 0x3000, 0, 0) == mla.MLA_OK  # nothing to do
+    b = mla.make_batch(2, 1, False, 8, num_slots=4)
+    assert mla.mla_plan(g, b, None, None, 0, 0) == mla.MLA_ERR_ARG
+    assert mla.mla_plan(g, b, 0x1000, 0x2000, 16, 0) == mla.MLA_ERR_WORKSPACE
+    cache = mla.mla_cache(0x1000, 0x1400, 576, 64 * 576, 576, 64 * 576, 8)
+    assert mla.mla_decode(g, b, None, None, cache, None, 8, None, 0, None, None, None, 0, 0) == mla.MLA_ERR_ARG
+    bad_cache = mla.mla_cache(0x1000, 0x1402, 576, 64 * 576, 576, 64 * 576, 8)
+    assert mla.mla_decode(g, b, 0x1000, 0x2000, bad_cache, 0x3000, 8, 0x4000, 0, 0x5000, 0x6000, 0x7000,
+                          1 << 30, 0) == mla.MLA_ERR_ALIGN
+    assert mla.mla_split_merge(None, None, None, 2, 4, 12, None, None, 0) == mla.MLA_ERR_ARG
+    assert mla.mla_split_merge(0x1000, 0x2000, 0x3000, 0, 4, 16, 0x4000, 0x5000, 0) == mla.MLA_OK
