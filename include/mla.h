@@ -189,6 +189,30 @@ mla_status mla_split_merge(const float* part_o, const float* part_lse, const int
 mla_status mla_debug_gather(const mla_cache* cache, const int32_t* block_table, int bt_stride,
                             const int32_t* seq_lens, int b, void* out, mla_stream_t stream);
 
+/*
+ * Decode for callers that cannot allocate device memory (no counterpart on the
+ * source pages; this is a deployment convenience).  Code running inside an
+ * allocator or memory-pool callback, or a serving loop that must keep device
+ * memory fixed once it starts, can still run a step: this call plans and
+ * decodes (plus the split merge) using a fixed scratch array of
+ * MLA_NOALLOC_SCRATCH_BYTES held in the library's device image, so the caller
+ * passes only inputs and outputs (same meaning as mla_plan + mla_decode with
+ * checked = 0).  It calls no allocator.
+ *   Limit: returns MLA_ERR_WORKSPACE, before launching anything, when
+ *     mla_workspace_size(geom, batch) exceeds MLA_NOALLOC_SCRATCH_BYTES; a
+ *     smaller num_slots (or num_splits_override) shrinks the need.
+ *   Set-up: the first call on a device looks up the scratch address with that
+ *     device current; make that first call before any stream capture.
+ *   Sharing: all calls on a device share the one array (every GPU that loads
+ *     the library holds it until exit).  Calls that overlap on the GPU race;
+ *     order them on one stream.  Nothing in the array needs clearing between
+ *     calls: the planning step rewrites all the state the kernels read.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+mla_status mla_decode_noalloc(const mla_geom* geom, const mla_batch* batch, const void* q_lat, const void* q_pe,
+                              const mla_cache* cache, const int32_t* block_table, int bt_stride,
+                              const int32_t* seq_lens, void* o_lat, float* lse, mla_stream_t stream);
+
 /* Synchronise `stream`, then return the status word a kernel recorded in the
  * workspace (MLA_OK if none) and, if info != NULL, its detail word. */
 mla_status mla_read_device_status(const void* workspace, int* info, mla_stream_t stream);

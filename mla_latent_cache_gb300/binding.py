@@ -71,6 +71,7 @@ def _load() -> ctypes.CDLL:
         "mla_absorb_q": (I, [G, P, P, P, I, P]),
         "mla_unabsorb_o": (I, [G, P, P, P, I, P]),
         "mla_decode": (I, [G, Bt, P, P, C, P, I, P, I, P, P, P, ctypes.c_size_t, P]),
+        "mla_decode_noalloc": (I, [G, Bt, P, P, C, P, I, P, P, P, P]),
         "mla_split_merge": (I, [P, P, P, I, I, I, P, P, P]),
         "mla_debug_gather": (I, [C, P, I, P, I, P, P]),
         "mla_read_device_status": (I, [P, ctypes.POINTER(ctypes.c_int), P]),
@@ -85,7 +86,8 @@ def _load() -> ctypes.CDLL:
 
 
 _lib = _load()
-EXPORTED = ("mla_workspace_size", "mla_plan", "mla_absorb_q", "mla_unabsorb_o", "mla_decode", "mla_split_merge",
+EXPORTED = ("mla_workspace_size", "mla_plan", "mla_absorb_q", "mla_unabsorb_o", "mla_decode", "mla_decode_noalloc",
+            "mla_split_merge",
             "mla_debug_gather", "mla_read_device_status", "mla_status_string", "mla_device_sm_count")
 
 
@@ -172,6 +174,17 @@ def mla_decode(geom, batch, q_lat, q_pe, cache: mla_cache, block_table, bt_strid
     return _lib.mla_decode(ctypes.byref(geom), ctypes.byref(batch), _ptr(q_lat), _ptr(q_pe), ctypes.byref(cache),
                            _ptr(block_table), bt_stride, _ptr(seq_lens), int(checked), _ptr(o_lat), _ptr(lse),
                            _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def mla_decode_noalloc(geom, batch, q_lat, q_pe, cache: mla_cache, block_table, bt_stride: int, seq_lens, o_lat, lse,
+                       stream=None) -> int:
+    """Plan + decode in the library's fixed device scratch (for callers that cannot allocate)."""
+    return _lib.mla_decode_noalloc(ctypes.byref(geom), ctypes.byref(batch), _ptr(q_lat), _ptr(q_pe),
+                                   ctypes.byref(cache), _ptr(block_table), bt_stride, _ptr(seq_lens), _ptr(o_lat),
+                                   _ptr(lse), _stream(stream))
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def mla_split_merge(part_o, part_lse, indptr, M: int, rows: int, D: int, o, lse, stream=None) -> int:
