@@ -97,7 +97,7 @@ typedef struct {
   int T;                   /* new query tokens per sequence (>= 1) */
   int causal;              /* 1: causal within the new tokens */
   int max_pages;           /* width of a block-table row, in pages (>= 1) */
-  int num_slots;           /* work ranges run concurrently by the decode kernel; 0 = library default for the device */
+  int num_slots;           /* work ranges run concurrently (one per CTA pair); 0 = half the device's SM count */
   int num_splits_override; /* 0: automatic split rule; N > 0: every query-row group is cut into min(pages, N) chunks */
 } mla_batch;
 

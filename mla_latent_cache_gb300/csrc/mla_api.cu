@@ -36,10 +36,10 @@ mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_E
 
 }  // namespace
 
+// Default work-range count: one per CTA pair of the decode kernel (half the SMs).
 int resolve_slots(const mla_batch* b) {
   if (b->num_slots > 0) return b->num_slots;
-  const int sms = mla_device_sm_count();
-  return sms > 0 ? sms : 1;
+  return decode_sm103_pairs_per_device();
 }
 
 bool compute_layout(const mla_geom* g, const mla_batch* b, WsLayout* L) {
@@ -186,7 +186,7 @@ mla_status mla_decode(const mla_geom* geom, const mla_batch* batch, const void* 
   if (!compute_layout(geom, batch, &L)) return MLA_ERR_SHAPE;
   if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = launch_decode_simple(geom, batch, L, static_cast<const __nv_bfloat16*>(q_lat),
+  cudaError_t e = launch_decode_sm103(geom, batch, L, static_cast<const __nv_bfloat16*>(q_lat),
                                        static_cast<const __nv_bfloat16*>(q_pe), cv, block_table, bt_stride, seq_lens,
                                        checked, static_cast<__nv_bfloat16*>(o_lat), lse, workspace, st);
   if (e != cudaSuccess) return MLA_ERR_CUDA;

@@ -1,0 +1,548 @@
+// Split-KV absorbed-MLA decode on the sm_103a tensor cores (TMA + tcgen05/TMEM).
+//
+// What it computes ("MLA in full detail", Step 3; "M5.8" 0x04 absorbed
+// reference): for every query row (b, t, h) of a plan segment,
+//   s_j = (q_lat . c_j + q_pe . k_pe_j) * scale   over the visible cache rows j,
+//   o_lat = sum_j softmax(s)_j c_j,  lse = log sum_j e^{s_j},
+// where row j of the paged cache is [c_j (512) | k_pe_j (64)] and page
+// j / 64 is found through the block table ("M5.8" 0x05).
+//
+// Work decomposition.  A query-row group is 128 flattened (t, h) rows of one
+// sequence (one token's 128 heads at V3 geometry).  The fp32 accumulator of a
+// full group, 128 x 512, would fill all 512 TMEM columns of an SM and leave no
+// room for the score tile, so each group is processed by a PAIR of CTAs: CTA
+// half h owns output columns [256 h, 256 h + 256).  Both CTAs of a pair form
+// the full 128 x 32 score tile S = Q K^T over all 576 columns for each
+// 32-row half page (the pair reads the same rows, the second read usually
+// hitting L2) and each accumulates P V for its 256 columns.  TMEM per CTA: O
+// half at columns 0..255, a double-buffered S tile at 256..319.
+//
+// Per CTA: warp 0 lane 0 issues TMA loads (the query tile, 9 boxes of
+// 128 x 64, kept for the whole segment; cache tiles as 32 x 64 boxes through
+// a 16-slot ring), warp 1 lane 0 issues tcgen05 MMAs, and warps 4..7 (one
+// thread per query row, matching TMEM lanes) run the online softmax, write P
+// (bf16, 128-byte swizzled, the A operand of P V) and the epilogue.  The
+// softmax keeps a per-row reference max and rescales the TMEM accumulator only
+// when the running max grows past it by more than 2^8 (exact for any
+// reference; only the rounding differs), with scores in log2 units.  Rows of
+// the last page past the sequence end are zeroed in shared memory before P V
+// so that stale or NaN cache contents never reach the accumulator.
+//
+// Every mbarrier wait is bounded; a wait that runs out records MLA_ERR_TIMEOUT
+// in the workspace, raises a CTA-wide abort flag, drains the TMA loads and
+// MMAs already issued, frees TMEM and returns.
+#include <math.h>
+
+#include "mla_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace mla {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 256;
+constexpr int kQBoxBytes = 128 * 64 * 2;   // 16 KB: 128 query rows x 64 bf16
+constexpr int kTileRows = 32;              // cache rows per tile (half a page)
+constexpr int kBoxBytes = kTileRows * 64 * 2;  // 4 KB: 32 cache rows x 64 bf16
+constexpr int kBoxes = 9;                  // 8 latent boxes + 1 RoPE box per row
+constexpr int kSlots = 16;
+constexpr int kSmemQ = 0;
+constexpr int kSmemRing = kSmemQ + kBoxes * kQBoxBytes;   // 147456
+constexpr int kSmemP = kSmemRing + kSlots * kBoxBytes;    // 212992
+constexpr int kSmemBar = kSmemP + 128 * 64 * 2;           // 229376
+constexpr int kSmemBytes = kSmemBar + 512;
+constexpr int kSmemAlloc = kSmemBytes + 1024;             // slack to align the base to 1024 B
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0;
+constexpr uint32_t kTmemS = 256;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+
+enum {
+  BAR_KV_FULL = 0,
+  BAR_KV_EMPTY = BAR_KV_FULL + kSlots,
+  BAR_Q_FULL = BAR_KV_EMPTY + kSlots,
+  BAR_Q_EMPTY,
+  BAR_S_FULL,  // two
+  BAR_S_EMPTY = BAR_S_FULL + 2,  // two
+  BAR_P_FULL = BAR_S_EMPTY + 2,
+  BAR_P_EMPTY,
+  BAR_O_EMPTY,
+  BAR_FINAL,
+  kNumBars
+};
+static_assert(kNumBars * 8 + 16 <= 512, "barrier area");
+
+struct FastArgs {
+  const int32_t* block_table;
+  int bt_stride;
+  const int32_t* seq_lens;
+  int B, T, H, causal, checked, max_pages, num_blocks;
+  float scale_log2;  // softmax scale times log2(e)
+  __nv_bfloat16* o_lat;
+  float* lse;
+  WsLayout L;
+};
+
+// Box order within one tile: the five boxes this half only needs for Q K^T
+// come first (their slots are released right after the MMAs), then the four
+// latent boxes whose columns this half accumulates in P V (held until P V).
+// With 9 boxes per tile and 16 ring slots, box k of tile i reuses the slot of
+// box k+7 of tile i-2 or k-7... of tile i-1 (k >= 7): always a box whose
+// release precedes Q K^T of tile i in the MMA issue order (Q K^T(i-1), then
+// P V(i-2), then Q K^T(i)), so the ring never waits on P V(i-1).
+__device__ __forceinline__ int box_order(int half, int k) {
+  if (k == 4) return 8;
+  if (half == 0) return k < 4 ? 4 + k : k - 5;
+  return k < 4 ? k : k - 1;
+}
+
+struct Shared {
+  uint32_t base;  // shared-window address of the 1024-aligned base
+  __device__ uint32_t q(int box) const { return base + kSmemQ + box * kQBoxBytes; }
+  __device__ uint32_t slot(int s) const { return base + kSmemRing + s * kBoxBytes; }
+  __device__ uint32_t p() const { return base + kSmemP; }
+  __device__ uint32_t bar(int i) const { return base + kSmemBar + i * 8; }
+};
+
+__device__ __forceinline__ void fail(int* hdr, volatile int* abort_flag, int where) {
+  *abort_flag = 1;
+  record_error(hdr, MLA_ERR_TIMEOUT, where);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_sm103_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_constant__ CUtensorMap tm_qpe,
+                        const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
+                        FastArgs a, char* ws) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Shared sh{smem_addr(smem)};
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + kSmemBar + kNumBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemBar + kNumBars * 8 + 4);
+
+  int* hdr = reinterpret_cast<int*>(ws);
+  const int* seg = reinterpret_cast<const int*>(ws + a.L.off_segments);
+  const int* rptr = reinterpret_cast<const int*>(ws + a.L.off_range_ptr);
+  float* part_lse = reinterpret_cast<float*>(ws + a.L.off_part_lse);
+  float* part_o = reinterpret_cast<float*>(ws + a.L.off_part_o);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int half = blockIdx.x & 1;
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+  const int num_ranges = hdr[MLA_HDR_NUM_RANGES];
+  const int R = a.T * a.H;
+
+  if (tid == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(sh.bar(BAR_KV_FULL + i), 1);
+      mbar_init(sh.bar(BAR_KV_EMPTY + i), 1);
+    }
+    mbar_init(sh.bar(BAR_Q_FULL), 1);
+    mbar_init(sh.bar(BAR_Q_EMPTY), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sh.bar(BAR_S_FULL + i), 1);
+      mbar_init(sh.bar(BAR_S_EMPTY + i), 128);
+    }
+    mbar_init(sh.bar(BAR_P_FULL), 128);
+    mbar_init(sh.bar(BAR_P_EMPTY), 1);
+    mbar_init(sh.bar(BAR_O_EMPTY), 128);
+    mbar_init(sh.bar(BAR_FINAL), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_qlat);
+    prefetch_tmap(&tm_qpe);
+    prefetch_tmap(&tm_ckv);
+    prefetch_tmap(&tm_kpe);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_base_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_slot;
+
+  if (a.checked && blockIdx.x == 0 && tid == 0) {
+    if (hdr[MLA_HDR_MAGIC] != MLA_PLAN_MAGIC || hdr[MLA_HDR_B] != a.B || hdr[MLA_HDR_T] != a.T ||
+        hdr[MLA_HDR_H] != a.H || hdr[MLA_HDR_CAUSAL] != a.causal) {
+      record_error(hdr, MLA_ERR_PLAN_STALE, 0);
+    } else {
+      unsigned h = 0;
+      for (int b = 0; b < a.B; ++b) {
+        unsigned S = (unsigned)a.seq_lens[b];
+        unsigned x = (unsigned)b + 0x632BE5ABu;
+        x ^= x >> 16; x *= 0x7feb352dU; x ^= x >> 15; x *= 0x846ca68bU; x ^= x >> 16;
+        unsigned y = S * 0x9E3779B1u + x;
+        y ^= y >> 16; y *= 0x7feb352dU; y ^= y >> 15; y *= 0x846ca68bU; y ^= y >> 16;
+        h += y;
+      }
+      if ((int)h != hdr[MLA_HDR_SEQ_HASH]) record_error(hdr, MLA_ERR_PLAN_STALE, 1);
+    }
+  }
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int gbox = 0, sc = 0;
+      bool q_in_flight = false;
+      bool ok = true;
+      for (int r = pair; ok && r < num_ranges; r += num_pairs) {
+        for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
+          const int* rec = seg + (size_t)si * kSegWords;
+          const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3];
+          if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
+          const int row0 = b * R + rb * kRowsPerBlock;
+          mbar_arrive_expect_tx(sh.bar(BAR_Q_FULL), kBoxes * kQBoxBytes);
+          for (int box = 0; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_FULL), 64 * box, row0);
+          tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_FULL), 0, row0);
+          q_in_flight = true;
+          for (int tt = 2 * p0; ok && tt < 2 * p1; ++tt) {
+            const int p = tt >> 1, r0 = (tt & 1) * kTileRows;
+            int blk = a.block_table[(size_t)b * a.bt_stride + p];
+            if (blk < 0 || blk >= a.num_blocks) {
+              // An out-of-pool id reads as zeros through the tensor map; report it when checking.
+              if (a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | p);
+              blk = -1;
+            }
+            for (int k = 0; k < kBoxes; ++k, ++gbox) {
+              const int s = gbox % kSlots;
+              if (!mbar_wait(sh.bar(BAR_KV_EMPTY + s), ((gbox / kSlots) & 1) ^ 1, abort_flag)) {
+                fail(hdr, abort_flag, 11); ok = false; break;
+              }
+              mbar_arrive_expect_tx(sh.bar(BAR_KV_FULL + s), kBoxBytes);
+              const int box = box_order(half, k);
+              if (box < 8) tma_load_3d(sh.slot(s), &tm_ckv, sh.bar(BAR_KV_FULL + s), 64 * box, r0, blk);
+              else tma_load_3d(sh.slot(s), &tm_kpe, sh.bar(BAR_KV_FULL + s), 0, r0, blk);
+            }
+          }
+          ++sc;
+        }
+      }
+      // Drain: every load issued must have landed before the CTA may exit.
+      const int first = gbox > kSlots ? gbox - kSlots : 0;
+      for (int g = first; g < gbox; ++g) {
+        volatile int never = 0;
+        mbar_wait(sh.bar(BAR_KV_FULL + g % kSlots), (g / kSlots) & 1, &never);
+      }
+      if (q_in_flight) {
+        volatile int never = 0;
+        mbar_wait(sh.bar(BAR_Q_FULL), (sc - 1) & 1, &never);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_bf16_f32(128, kTileRows, 0);
+      const uint32_t id_pv = idesc_bf16_f32(128, 64, 1);
+      int gbox = 0, ti = 0, sc = 0;
+      bool ok = true;
+      int own[4] = {0, 0, 0, 0}, own_prev[4] = {0, 0, 0, 0};
+      auto issue_pv = [&](int t, const int (&slots)[4], bool first_of_seg) -> bool {
+        if (first_of_seg && sc > 0) {
+          if (!mbar_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 20); return false; }
+        }
+        if (!mbar_wait(sh.bar(BAR_P_FULL), t & 1, abort_flag)) { fail(hdr, abort_flag, 21); return false; }
+        tc_fence_after();
+        for (int c = 0; c < 4; ++c) {
+          for (int kk = 0; kk < kTileRows / 16; ++kk) {
+            const uint64_t ad = sw128_desc(sh.p() + 32 * kk, 16, 1024);
+            const uint64_t bd = sw128_desc(sh.slot(slots[c]) + 2048 * kk, kBoxBytes, 1024);
+            mma_bf16(tmem + kTmemO + 64 * c, ad, bd, id_pv, (first_of_seg && kk == 0) ? 0u : 1u);
+          }
+          mma_commit(sh.bar(BAR_KV_EMPTY + slots[c]));
+        }
+        mma_commit(sh.bar(BAR_P_EMPTY));
+        return true;
+      };
+      for (int r = pair; ok && r < num_ranges; r += num_pairs) {
+        for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
+          const int* rec = seg + (size_t)si * kSegWords;
+          const int n_tiles = 2 * (rec[3] - rec[2]);
+          if (!mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag)) { fail(hdr, abort_flag, 22); ok = false; break; }
+          tc_fence_after();
+          for (int i = 0; ok && i < n_tiles; ++i, ++ti) {
+            const int buf = ti & 1;
+            if (!mbar_wait(sh.bar(BAR_S_EMPTY + buf), ((ti >> 1) & 1) ^ 1, abort_flag)) {
+              fail(hdr, abort_flag, 23); ok = false; break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + kTmemS + kTileRows * buf;
+            for (int k = 0; k < kBoxes; ++k, ++gbox) {
+              const int s = gbox % kSlots;
+              if (!mbar_wait(sh.bar(BAR_KV_FULL + s), (gbox / kSlots) & 1, abort_flag)) {
+                fail(hdr, abort_flag, 24); ok = false; break;
+              }
+              tc_fence_after();
+              const int box = box_order(half, k);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = sw128_desc(sh.q(box) + 32 * kk, 16, 1024);
+                const uint64_t bd = sw128_desc(sh.slot(s) + 32 * kk, 16, 1024);
+                mma_bf16(d, ad, bd, id_qk, (k | kk) ? 1u : 0u);
+              }
+              if (k < 5) mma_commit(sh.bar(BAR_KV_EMPTY + s));
+              else own[k - 5] = s;
+            }
+            if (!ok) break;
+            mma_commit(sh.bar(BAR_S_FULL + buf));
+            if (i == n_tiles - 1) mma_commit(sh.bar(BAR_Q_EMPTY));
+            if (i > 0 && !issue_pv(ti - 1, own_prev, i == 1)) { ok = false; break; }
+            for (int c = 0; c < 4; ++c) own_prev[c] = own[c];
+          }
+          if (ok && n_tiles > 0 && !issue_pv(ti - 1, own_prev, n_tiles == 1)) ok = false;
+          ++sc;
+        }
+      }
+      // Wait for every MMA issued so far before TMEM is released.
+      mma_commit(sh.bar(BAR_FINAL));
+      volatile int never = 0;
+      mbar_wait(sh.bar(BAR_FINAL), 0, &never);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int row = tid - 128;            // query row within the group == TMEM lane
+    const int q4 = warp - 4;
+    const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
+    int ti = 0, sc = 0;
+    bool ok = true;
+    for (int r = pair; ok && r < num_ranges; r += num_pairs) {
+      for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
+        const int* rec = seg + (size_t)si * kSegWords;
+        const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3], slot_out = rec[5];
+        int S = a.seq_lens[b];
+        S = S < 0 ? 0 : min(S, a.max_pages * kPage);
+        const int fr = rb * kRowsPerBlock + row;
+        const bool row_valid = fr < R;
+        const int limit = row_valid ? visible_limit(S, a.T, fr / a.H, a.causal) : 0;
+        float m_ref = -INFINITY, l = 0.f;
+        const int n_tiles = 2 * (p1 - p0);
+        for (int i = 0; i < n_tiles; ++i, ++ti) {
+          const int buf = ti & 1;
+          bool w_ok = mbar_wait(sh.bar(BAR_S_FULL + buf), (ti >> 1) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 30); ok = false; break; }
+          tc_fence_after();
+          uint32_t sr[kTileRows];
+          tmem_ld32(t_lane + kTmemS + kTileRows * buf, sr);
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(sh.bar(BAR_S_EMPTY + buf));
+          const int jbase = (2 * p0 + i) * kTileRows;   // first cache row of this tile
+          float s[kTileRows];
+          float tmax = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < kTileRows; ++j) {
+            float v = __uint_as_float(sr[j]) * a.scale_log2;
+            v = (jbase + j < limit) ? v : -INFINITY;
+            s[j] = v;
+            tmax = fmaxf(tmax, v);
+          }
+          if (i > 0) {
+            w_ok = mbar_wait(sh.bar(BAR_P_EMPTY), (ti - 1) & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 31); ok = false; break; }
+            tc_fence_after();
+          }
+          // Lazy rescale of the running state (per row; TMEM access per warp).
+          const bool grow = tmax > m_ref + kRescaleThreshold;
+          const float new_ref = grow ? tmax : m_ref;
+          const float factor = (grow && m_ref != -INFINITY) ? ex2(m_ref - new_ref) : 1.f;
+          if (i > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              uint32_t o[32];
+              tmem_ld32(t_lane + kTmemO + 32 * c, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+              tmem_st32(t_lane + kTmemO + 32 * c, o);
+            }
+            tmem_wait_st();
+          }
+          l *= factor;
+          m_ref = new_ref;
+          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          // P row (bf16) into the 128-byte-swizzled A tile of P V.
+          float psum = 0.f;
+          const uint32_t prow = sh.p() + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < kTileRows / 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 8 * c + 2 * e;
+              const float x0 = s[j] == -INFINITY ? 0.f : ex2(s[j] - m_use);
+              const float x1 = s[j + 1] == -INFINITY ? 0.f : ex2(s[j + 1] - m_use);
+              psum += x0 + x1;
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            const uint32_t dst = prow + ((c ^ (row & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                         "r"(w[3])
+                         : "memory");
+          }
+          l += psum;
+          // Cache rows past the sequence end (last page only) are zeroed in the
+          // four value boxes before P V reads them.
+          const int valid = S - jbase;
+          if (valid < kTileRows) {
+            for (int idx = row; idx < 4 * kTileRows; idx += 128) {
+              const int c = idx / kTileRows, rr = idx % kTileRows;
+              if (rr >= valid) {
+                const uint32_t dst = sh.slot((9 * ti + 5 + c) % kSlots) + rr * 128;
+#pragma unroll
+                for (int z = 0; z < 8; ++z)
+                  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst + 16 * z), "r"(0) : "memory");
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(sh.bar(BAR_P_FULL));
+        }
+        if (!ok) break;
+        // Epilogue: wait for the last P V, then normalise and store this half's columns.
+        {
+          const bool w_ok = mbar_wait(sh.bar(BAR_P_EMPTY), (ti - 1) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 32); ok = false; break; }
+          tc_fence_after();
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const float lse_v = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[32];
+          tmem_ld32(t_lane + kTmemO + 32 * c, o);
+          tmem_wait_ld();
+          if (row_valid) {
+            if (slot_out < 0) {
+              __nv_bfloat16* dst = a.o_lat + ((size_t)b * R + fr) * kDLat + 256 * half + 32 * c;
+#pragma unroll
+              for (int e = 0; e < 32; e += 8) {
+                uint4 v;
+                __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                __nv_bfloat162 h3 = __floats2bfloat162_rn(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                v.x = *reinterpret_cast<uint32_t*>(&h0); v.y = *reinterpret_cast<uint32_t*>(&h1);
+                v.z = *reinterpret_cast<uint32_t*>(&h2); v.w = *reinterpret_cast<uint32_t*>(&h3);
+                *reinterpret_cast<uint4*>(dst + e) = v;
+              }
+            } else {
+              float* dst = part_o + ((size_t)slot_out * kRowsPerBlock + row) * kDLat + 256 * half + 32 * c;
+#pragma unroll
+              for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4*>(dst + e) =
+                    make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                                __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            }
+          }
+        }
+        if (row_valid && half == 0) {
+          if (slot_out < 0) a.lse[(size_t)b * R + fr] = lse_v;
+          else part_lse[(size_t)slot_out * kRowsPerBlock + row] = lse_v;
+        }
+        tc_fence_before();
+        mbar_arrive(sh.bar(BAR_O_EMPTY));
+        ++sc;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// --------------------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+              const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides_bytes, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int decode_sm103_pairs_per_device() {
+  const int sms = mla_device_sm_count();
+  return sms >= 2 ? sms / 2 : 1;
+}
+
+cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsLayout& L,
+                                const __nv_bfloat16* q_lat, const __nv_bfloat16* q_pe, const CacheView& cv,
+                                const int32_t* block_table, int bt_stride, const int32_t* seq_lens, int checked,
+                                __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st) {
+  const long long rows_total = (long long)b->B * b->T * g->H;
+  CUtensorMap m_qlat, m_qpe, m_ckv, m_kpe;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)kDLat, (cuuint64_t)rows_total};
+    const cuuint64_t str[1] = {(cuuint64_t)kDLat * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!make_map(&m_qlat, q_lat, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)kDRope, (cuuint64_t)rows_total};
+    const cuuint64_t str[1] = {(cuuint64_t)kDRope * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!make_map(&m_qpe, q_pe, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)kDLat, (cuuint64_t)kPage, (cuuint64_t)cv.num_blocks};
+    const cuuint64_t str[2] = {(cuuint64_t)cv.ckv_row * 2, (cuuint64_t)cv.ckv_block * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kTileRows, 1};
+    if (!make_map(&m_ckv, cv.ckv, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)kDRope, (cuuint64_t)kPage, (cuuint64_t)cv.num_blocks};
+    const cuuint64_t str[2] = {(cuuint64_t)cv.kpe_row * 2, (cuuint64_t)cv.kpe_block * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kTileRows, 1};
+    if (!make_map(&m_kpe, cv.kpe, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  FastArgs a;
+  a.block_table = block_table; a.bt_stride = bt_stride; a.seq_lens = seq_lens;
+  a.B = b->B; a.T = b->T; a.H = g->H; a.causal = b->causal ? 1 : 0; a.checked = checked;
+  a.max_pages = b->max_pages; a.num_blocks = cv.num_blocks;
+  a.scale_log2 = g->softmax_scale * 1.4426950408889634f;
+  a.o_lat = o_lat; a.lse = lse; a.L = L;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int pairs = L.cap_ranges;
+  const int max_pairs = decode_sm103_pairs_per_device();
+  if (pairs > max_pairs) pairs = max_pairs;
+  if (pairs <= 0) return cudaSuccess;
+  decode_sm103_kernel<<<2 * pairs, kThreads, kSmemAlloc, st>>>(m_qlat, m_qpe, m_ckv, m_kpe, a,
+                                                              reinterpret_cast<char*>(ws));
+  return cudaGetLastError();
+}
+
+}  // namespace mla

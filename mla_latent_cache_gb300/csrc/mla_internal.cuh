@@ -69,6 +69,11 @@ cudaError_t launch_decode_simple(const mla_geom* g, const mla_batch* b, const Ws
                                  const __nv_bfloat16* q_lat, const __nv_bfloat16* q_pe, const CacheView& cv,
                                  const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                                  int checked, __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st);
+cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsLayout& L,
+                                const __nv_bfloat16* q_lat, const __nv_bfloat16* q_pe, const CacheView& cv,
+                                const int32_t* block_table, int bt_stride, const int32_t* seq_lens, int checked,
+                                __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st);
+int decode_sm103_pairs_per_device();
 cudaError_t launch_plan_merge(const mla_geom* g, const mla_batch* b, const WsLayout& L,
                               __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st);
 cudaError_t launch_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M,
