@@ -133,7 +133,7 @@ mla_status mla_absorb_q(const mla_geom* geom, const void* q_nope, const void* w_
   if (BT == 0) return MLA_OK;
   if (!q_nope || !w_uk || !q_lat) return MLA_ERR_ARG;
   if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_lat)) return MLA_ERR_ALIGN;
-  return cuda_status(launch_absorb(static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(w_uk),
+  return cuda_status(launch_absorb_sm103(static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(w_uk),
                                    static_cast<__nv_bfloat16*>(q_lat), BT, geom->H, (cudaStream_t)stream));
 }
 
@@ -145,7 +145,7 @@ mla_status mla_unabsorb_o(const mla_geom* geom, const void* o_lat, const void* w
   if (BT == 0) return MLA_OK;
   if (!o_lat || !w_uv || !o) return MLA_ERR_ARG;
   if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(o)) return MLA_ERR_ALIGN;
-  return cuda_status(launch_unabsorb(static_cast<const __nv_bfloat16*>(o_lat), static_cast<const __nv_bfloat16*>(w_uv),
+  return cuda_status(launch_unabsorb_sm103(static_cast<const __nv_bfloat16*>(o_lat), static_cast<const __nv_bfloat16*>(w_uv),
                                      static_cast<__nv_bfloat16*>(o), BT, geom->H, (cudaStream_t)stream));
 }
 
@@ -223,7 +223,20 @@ mla_status mla_read_device_status(const void* workspace, int* info, mla_stream_t
   const char* base = static_cast<const char*>(workspace) + MLA_HDR_ERROR * sizeof(int);
   if (cudaMemcpy(words, base, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
   if (info) *info = words[1];
-  return (mla_status)words[0];
+  if (words[0] != 0) return (mla_status)words[0];
+  // The absorption kernels have no workspace; their (rare) timeout is kept per device.
+  int* bmm = bmm_status_ptr();
+  if (bmm) {
+    int v = 0;
+    if (cudaMemcpy(&v, bmm, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+    if (v != 0) {
+      const int zero = 0;
+      cudaMemcpy(bmm, &zero, sizeof(int), cudaMemcpyHostToDevice);
+      if (info) *info = -1;
+      return (mla_status)v;
+    }
+  }
+  return MLA_OK;
 }
 
 }  // extern "C"

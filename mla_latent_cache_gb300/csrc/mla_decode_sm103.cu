@@ -57,6 +57,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemS = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+constexpr int kPrefetchPages = 3;          // L2 prefetch distance ahead of the page being loaded
 
 enum {
   BAR_KV_FULL = 0,
@@ -78,6 +79,9 @@ struct FastArgs {
   int bt_stride;
   const int32_t* seq_lens;
   int B, T, H, causal, checked, max_pages, num_blocks;
+  const __nv_bfloat16* ckv;  // pool base, for the L2 prefetch of whole pages
+  int64_t ckv_block;         // elements between blocks
+  int page_contiguous;       // 1 when a block's 64 rows x 576 values are one contiguous range
   float scale_log2;  // softmax scale times log2(e)
   __nv_bfloat16* o_lat;
   float* lse;
@@ -198,8 +202,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int box = 0; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_FULL), 64 * box, row0);
           tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_FULL), 0, row0);
           q_in_flight = true;
+          // The page loads below are issued only a ring's depth ahead of use, so pages
+          // further ahead are pulled into L2 first; the CTA of half 0 does it for the pair.
+          auto prefetch_page = [&](int pp) {
+            if (half != 0 || pp >= p1) return;
+            const int pb = a.block_table[(size_t)b * a.bt_stride + pp];
+            if (pb < 0 || pb >= a.num_blocks) return;
+            if (a.page_contiguous) {
+              prefetch_l2_bulk(a.ckv + (int64_t)pb * a.ckv_block, kPage * kDK * 2);
+            } else {
+              for (int rr = 0; rr < kPage; rr += kTileRows) {
+                for (int box = 0; box < 8; ++box) prefetch_l2_tile_3d(&tm_ckv, 64 * box, rr, pb);
+                prefetch_l2_tile_3d(&tm_kpe, 0, rr, pb);
+              }
+            }
+          };
+          for (int pp = p0; pp < p0 + kPrefetchPages; ++pp) prefetch_page(pp);
           for (int tt = 2 * p0; ok && tt < 2 * p1; ++tt) {
             const int p = tt >> 1, r0 = (tt & 1) * kTileRows;
+            if ((tt & 1) == 0) prefetch_page(p + kPrefetchPages);
             int blk = a.block_table[(size_t)b * a.bt_stride + p];
             if (blk < 0 || blk >= a.num_blocks) {
               // An out-of-pool id reads as zeros through the tensor map; report it when checking.
@@ -237,6 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(128, kTileRows, 0);
       const uint32_t id_pv = idesc_bf16_f32(128, 64, 1);
+      // Descriptors are built once; k-steps and slots only move the start-address field
+      // (16-byte units): +2 per 32-byte K step of a K-major tile, +128 per 16-row K step
+      // of an MN-major tile, +kBoxBytes/16 per ring slot.
+      uint64_t qdesc[kBoxes];
+#pragma unroll
+      for (int bx = 0; bx < kBoxes; ++bx) qdesc[bx] = sw128_desc(sh.q(bx), 16, 1024);
+      const uint64_t kdesc0 = sw128_desc(sh.slot(0), 16, 1024);
+      const uint64_t vdesc0 = sw128_desc(sh.slot(0), kBoxBytes, 1024);
+      const uint64_t pdesc = sw128_desc(sh.p(), 16, 1024);
       int gbox = 0, ti = 0, sc = 0;
       bool ok = true;
       int own[4] = {0, 0, 0, 0}, own_prev[4] = {0, 0, 0, 0};
@@ -247,11 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(sh.bar(BAR_P_FULL), t & 1, abort_flag)) { fail(hdr, abort_flag, 21); return false; }
         tc_fence_after();
         for (int c = 0; c < 4; ++c) {
-          for (int kk = 0; kk < kTileRows / 16; ++kk) {
-            const uint64_t ad = sw128_desc(sh.p() + 32 * kk, 16, 1024);
-            const uint64_t bd = sw128_desc(sh.slot(slots[c]) + 2048 * kk, kBoxBytes, 1024);
-            mma_bf16(tmem + kTmemO + 64 * c, ad, bd, id_pv, (first_of_seg && kk == 0) ? 0u : 1u);
-          }
+          const uint64_t vd = vdesc0 + (uint64_t)(slots[c] * (kBoxBytes >> 4));
+#pragma unroll
+          for (int kk = 0; kk < kTileRows / 16; ++kk)
+            mma_bf16(tmem + kTmemO + 64 * c, pdesc + 2 * kk, vd + 128 * kk, id_pv, (first_of_seg && kk == 0) ? 0u : 1u);
           mma_commit(sh.bar(BAR_KV_EMPTY + slots[c]));
         }
         mma_commit(sh.bar(BAR_P_EMPTY));
@@ -276,12 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fail(hdr, abort_flag, 24); ok = false; break;
               }
               tc_fence_after();
-              const int box = box_order(half, k);
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = sw128_desc(sh.q(box) + 32 * kk, 16, 1024);
-                const uint64_t bd = sw128_desc(sh.slot(s) + 32 * kk, 16, 1024);
-                mma_bf16(d, ad, bd, id_qk, (k | kk) ? 1u : 0u);
-              }
+              const uint64_t ad = qdesc[box_order(half, k)];
+              const uint64_t bd = kdesc0 + (uint64_t)(s * (kBoxBytes >> 4));
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id_qk, (k | kk) ? 1u : 0u);
               if (k < 5) mma_commit(sh.bar(BAR_KV_EMPTY + s));
               else own[k - 5] = s;
             }
@@ -528,6 +555,9 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
   a.block_table = block_table; a.bt_stride = bt_stride; a.seq_lens = seq_lens;
   a.B = b->B; a.T = b->T; a.H = g->H; a.causal = b->causal ? 1 : 0; a.checked = checked;
   a.max_pages = b->max_pages; a.num_blocks = cv.num_blocks;
+  a.ckv = cv.ckv; a.ckv_block = cv.ckv_block;
+  a.page_contiguous = (cv.ckv_row == kDK && cv.ckv_block == (int64_t)kPage * kDK && cv.kpe == cv.ckv + kDLat &&
+                       cv.kpe_row == kDK && cv.kpe_block == cv.ckv_block) ? 1 : 0;
   a.scale_log2 = g->softmax_scale * 1.4426950408889634f;
   a.o_lat = o_lat; a.lse = lse; a.L = L;
   static bool attr_set = false;

@@ -65,10 +65,6 @@ __host__ __device__ __forceinline__ int visible_limit(int S, int T, int t, int c
 // Launchers (one per translation unit); all return cudaError_t of the launch.
 cudaError_t launch_plan(const int32_t* seq_lens, const mla_geom* g, const mla_batch* b,
                         const WsLayout& L, void* ws, cudaStream_t st);
-cudaError_t launch_decode_simple(const mla_geom* g, const mla_batch* b, const WsLayout& L,
-                                 const __nv_bfloat16* q_lat, const __nv_bfloat16* q_pe, const CacheView& cv,
-                                 const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
-                                 int checked, __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st);
 cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsLayout& L,
                                 const __nv_bfloat16* q_lat, const __nv_bfloat16* q_pe, const CacheView& cv,
                                 const int32_t* block_table, int bt_stride, const int32_t* seq_lens, int checked,
@@ -78,10 +74,11 @@ cudaError_t launch_plan_merge(const mla_geom* g, const mla_batch* b, const WsLay
                               __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st);
 cudaError_t launch_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M,
                                int rows, int D, __nv_bfloat16* o, float* lse, cudaStream_t st);
-cudaError_t launch_absorb(const __nv_bfloat16* q_nope, const __nv_bfloat16* w_uk, __nv_bfloat16* q_lat,
-                          int BT, int H, cudaStream_t st);
-cudaError_t launch_unabsorb(const __nv_bfloat16* o_lat, const __nv_bfloat16* w_uv, __nv_bfloat16* o,
-                            int BT, int H, cudaStream_t st);
+cudaError_t launch_absorb_sm103(const __nv_bfloat16* q_nope, const __nv_bfloat16* w_uk, __nv_bfloat16* q_lat,
+                                int BT, int H, cudaStream_t st);
+cudaError_t launch_unabsorb_sm103(const __nv_bfloat16* o_lat, const __nv_bfloat16* w_uv, __nv_bfloat16* o,
+                                  int BT, int H, cudaStream_t st);
+int* bmm_status_ptr();
 cudaError_t launch_debug_gather(const CacheView& cv, const int32_t* block_table, int bt_stride,
                                 const int32_t* seq_lens, int b, __nv_bfloat16* out, cudaStream_t st);
 
