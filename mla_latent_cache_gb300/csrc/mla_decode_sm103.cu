@@ -15,11 +15,15 @@
 // the full 128 x 32 score tile S = Q K^T over all 576 columns for each
 // 32-row half page (the pair reads the same rows, the second read usually
 // hitting L2) and each accumulates P V for its 256 columns.  TMEM per CTA: O
-// half at columns 0..255, a double-buffered S tile at 256..319.
+// half at columns 0..255, a double-buffered S tile at 256..319, and query
+// columns 0..383 (packed bf16 pairs, the TMEM A operand of Q K^T) at
+// 320..511.  The rest of the query tile (latent 384..511 and RoPE) stays in
+// shared memory, which leaves room for a 40-slot ring of cache boxes (about
+// four tiles of lookahead).
 //
-// Per CTA: warp 0 lane 0 issues TMA loads (the query tile, 9 boxes of
-// 128 x 64, kept for the whole segment; cache tiles as 32 x 64 boxes through
-// a 16-slot ring), warp 1 lane 0 issues tcgen05 MMAs, and warps 4..7 (one
+// Per CTA: warp 0 lane 0 issues TMA loads (three 128 x 64 query boxes kept
+// for the whole segment; cache tiles as 32 x 64 boxes through the ring),
+// warp 1 lane 0 issues tcgen05 MMAs, and warps 4..7 (one
 // thread per query row, matching TMEM lanes) run the online softmax, write P
 // (bf16, 128-byte swizzled, the A operand of P V) and the epilogue.  The
 // softmax keeps a per-row reference max and rescales the TMEM accumulator only
@@ -46,16 +50,19 @@ constexpr int kQBoxBytes = 128 * 64 * 2;   // 16 KB: 128 query rows x 64 bf16
 constexpr int kTileRows = 32;              // cache rows per tile (half a page)
 constexpr int kBoxBytes = kTileRows * 64 * 2;  // 4 KB: 32 cache rows x 64 bf16
 constexpr int kBoxes = 9;                  // 8 latent boxes + 1 RoPE box per row
-constexpr int kSlots = 16;
+constexpr int kQTmemBoxes = 6;             // query column boxes 0..5 are held in TMEM
+constexpr int kQSmemBoxes = kBoxes - kQTmemBoxes;  // boxes 6, 7 (latent) and 8 (RoPE) in shared memory
+constexpr int kSlots = 40;
 constexpr int kSmemQ = 0;
-constexpr int kSmemRing = kSmemQ + kBoxes * kQBoxBytes;   // 147456
-constexpr int kSmemP = kSmemRing + kSlots * kBoxBytes;    // 212992
-constexpr int kSmemBar = kSmemP + 128 * 64 * 2;           // 229376
-constexpr int kSmemBytes = kSmemBar + 512;
-constexpr int kSmemAlloc = kSmemBytes + 1024;             // slack to align the base to 1024 B
+constexpr int kSmemRing = kSmemQ + kQSmemBoxes * kQBoxBytes;  // 49152
+constexpr int kSmemP = kSmemRing + kSlots * kBoxBytes;        // 212992
+constexpr int kSmemBar = kSmemP + 128 * 64 * 2;               // 229376
+constexpr int kSmemBytes = kSmemBar + 1024;
+constexpr int kSmemAlloc = kSmemBytes + 1024;                 // slack to align the base to 1024 B
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;
-constexpr uint32_t kTmemS = 256;
+constexpr uint32_t kTmemO = 0;     // O half: 256 fp32 columns
+constexpr uint32_t kTmemS = 256;   // S: 2 x 32 fp32 columns
+constexpr uint32_t kTmemQ = 320;   // Q boxes 0..5: 6 x 32 columns of packed bf16 pairs
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 constexpr int kPrefetchPages = 3;          // L2 prefetch distance ahead of the page being loaded
 
@@ -70,11 +77,13 @@ enum {
   BAR_P_EMPTY,
   BAR_O_EMPTY,
   BAR_FINAL,
+  BAR_QT_FULL,
   kNumBars
 };
-static_assert(kNumBars * 8 + 16 <= 512, "barrier area");
+static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
 
 struct FastArgs {
+  const __nv_bfloat16* q_lat;
   const int32_t* block_table;
   int bt_stride;
   const int32_t* seq_lens;
@@ -103,7 +112,7 @@ __device__ __forceinline__ int box_order(int half, int k) {
 
 struct Shared {
   uint32_t base;  // shared-window address of the 1024-aligned base
-  __device__ uint32_t q(int box) const { return base + kSmemQ + box * kQBoxBytes; }
+  __device__ uint32_t q(int box) const { return base + kSmemQ + (box - kQTmemBoxes) * kQBoxBytes; }
   __device__ uint32_t slot(int s) const { return base + kSmemRing + s * kBoxBytes; }
   __device__ uint32_t p() const { return base + kSmemP; }
   __device__ uint32_t bar(int i) const { return base + kSmemBar + i * 8; }
@@ -152,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sh.bar(BAR_P_EMPTY), 1);
     mbar_init(sh.bar(BAR_O_EMPTY), 128);
     mbar_init(sh.bar(BAR_FINAL), 1);
+    mbar_init(sh.bar(BAR_QT_FULL), 128);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_qlat);
@@ -198,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3];
           if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
           const int row0 = b * R + rb * kRowsPerBlock;
-          mbar_arrive_expect_tx(sh.bar(BAR_Q_FULL), kBoxes * kQBoxBytes);
-          for (int box = 0; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_FULL), 64 * box, row0);
+          mbar_arrive_expect_tx(sh.bar(BAR_Q_FULL), kQSmemBoxes * kQBoxBytes);
+          for (int box = kQTmemBoxes; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_FULL), 64 * box, row0);
           tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_FULL), 0, row0);
           q_in_flight = true;
           // The page loads below are issued only a ring's depth ahead of use, so pages
@@ -261,9 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Descriptors are built once; k-steps and slots only move the start-address field
       // (16-byte units): +2 per 32-byte K step of a K-major tile, +128 per 16-row K step
       // of an MN-major tile, +kBoxBytes/16 per ring slot.
-      uint64_t qdesc[kBoxes];
+      uint64_t qdesc[kQSmemBoxes];
 #pragma unroll
-      for (int bx = 0; bx < kBoxes; ++bx) qdesc[bx] = sw128_desc(sh.q(bx), 16, 1024);
+      for (int bx = 0; bx < kQSmemBoxes; ++bx) qdesc[bx] = sw128_desc(sh.q(kQTmemBoxes + bx), 16, 1024);
       const uint64_t kdesc0 = sw128_desc(sh.slot(0), 16, 1024);
       const uint64_t vdesc0 = sw128_desc(sh.slot(0), kBoxBytes, 1024);
       const uint64_t pdesc = sw128_desc(sh.p(), 16, 1024);
@@ -290,7 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
           const int* rec = seg + (size_t)si * kSegWords;
           const int n_tiles = 2 * (rec[3] - rec[2]);
-          if (!mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag)) { fail(hdr, abort_flag, 22); ok = false; break; }
+          if (!mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag) ||
+              !mbar_wait(sh.bar(BAR_QT_FULL), sc & 1, abort_flag)) {
+            fail(hdr, abort_flag, 22); ok = false; break;
+          }
           tc_fence_after();
           for (int i = 0; ok && i < n_tiles; ++i, ++ti) {
             const int buf = ti & 1;
@@ -305,10 +318,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fail(hdr, abort_flag, 24); ok = false; break;
               }
               tc_fence_after();
-              const uint64_t ad = qdesc[box_order(half, k)];
+              const int box = box_order(half, k);
               const uint64_t bd = kdesc0 + (uint64_t)(s * (kBoxBytes >> 4));
+              if (box < kQTmemBoxes) {
+                const uint32_t at = tmem + kTmemQ + 32 * box;   // 16 bf16 of K = 8 TMEM columns per step
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id_qk, (k | kk) ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(d, at + 8 * kk, bd + 2 * kk, id_qk, (k | kk) ? 1u : 0u);
+              } else {
+                const uint64_t ad = qdesc[box - kQTmemBoxes];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id_qk, (k | kk) ? 1u : 0u);
+              }
               if (k < 5) mma_commit(sh.bar(BAR_KV_EMPTY + s));
               else own[k - 5] = s;
             }
@@ -344,6 +364,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int fr = rb * kRowsPerBlock + row;
         const bool row_valid = fr < R;
         const int limit = row_valid ? visible_limit(S, a.T, fr / a.H, a.causal) : 0;
+        // Query columns 0..383 of this row go to TMEM (the A operand of Q K^T for
+        // boxes 0..5), once the previous segment's Q K^T MMAs have finished with it.
+        {
+          bool w_ok = sc == 0 || mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 33); ok = false; break; }
+          tc_fence_after();
+          const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)b * R + fr) * kDLat);
+#pragma unroll 1
+          for (int bx = 0; bx < kQTmemBoxes; ++bx) {
+            uint32_t qv[32];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const uint4 v = row_valid ? __ldg(src + 8 * bx + e) : make_uint4(0, 0, 0, 0);
+              qv[4 * e] = v.x; qv[4 * e + 1] = v.y; qv[4 * e + 2] = v.z; qv[4 * e + 3] = v.w;
+            }
+            tmem_st32(t_lane + kTmemQ + 32 * bx, qv);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(sh.bar(BAR_QT_FULL));
+        }
         float m_ref = -INFINITY, l = 0.f;
         const int n_tiles = 2 * (p1 - p0);
         for (int i = 0; i < n_tiles; ++i, ++ti) {
@@ -552,6 +593,7 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
     if (!make_map(&m_kpe, cv.kpe, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   FastArgs a;
+  a.q_lat = q_lat;
   a.block_table = block_table; a.bt_stride = bt_stride; a.seq_lens = seq_lens;
   a.B = b->B; a.T = b->T; a.H = g->H; a.causal = b->causal ? 1 : 0; a.checked = checked;
   a.max_pages = b->max_pages; a.num_blocks = cv.num_blocks;
