@@ -1,4 +1,5 @@
-// Split-KV absorbed-MLA decode on the sm_103a tensor cores (TMA + tcgen05/TMEM).
+// Split-KV absorbed-MLA decode on the sm_103a tensor cores (TMA + tcgen05/TMEM,
+// 2-CTA clusters exchanging partial scores through distributed shared memory).
 //
 // What it computes ("MLA in full detail", Step 3; "M5.8" 0x04 absorbed
 // reference): for every query row (b, t, h) of a plan segment,
@@ -8,33 +9,42 @@
 // j / 64 is found through the block table ("M5.8" 0x05).
 //
 // Work decomposition.  A query-row group is 128 flattened (t, h) rows of one
-// sequence (one token's 128 heads at V3 geometry).  The fp32 accumulator of a
-// full group, 128 x 512, would fill all 512 TMEM columns of an SM and leave no
-// room for the score tile, so each group is processed by a PAIR of CTAs: CTA
-// half h owns output columns [256 h, 256 h + 256).  Both CTAs of a pair form
-// the full 128 x 32 score tile S = Q K^T over all 576 columns for each
-// 32-row half page (the pair reads the same rows, the second read usually
-// hitting L2) and each accumulates P V for its 256 columns.  TMEM per CTA: O
-// half at columns 0..255, a double-buffered S tile at 256..319, and query
-// columns 0..383 (packed bf16 pairs, the TMEM A operand of Q K^T) at
-// 320..511.  The rest of the query tile (latent 384..511 and RoPE) stays in
-// shared memory, which leaves room for a 40-slot ring of cache boxes (about
-// four tiles of lookahead).
+// sequence (one token's 128 heads at V3 geometry).  Its fp32 accumulator,
+// 128 x 512, would take all 512 TMEM columns of an SM, so each group is
+// handled by a CLUSTER of two CTAs, and each CTA owns half of the latent
+// columns: CTA 0 latent 0..255 plus the 64 RoPE columns, CTA 1 latent
+// 256..511.  For each 64-row cache page:
+//   - each CTA loads only its own column boxes (the pair reads every cache
+//     byte exactly once) and forms a PARTIAL score tile over its columns,
+//     S_h = Q[:, cols_h] K[:, cols_h]^T (128 x 64, fp32, in TMEM);
+//   - the two partial tiles are swapped through distributed shared memory and
+//     both CTAs form S = S_0 + S_1 in the same order, so both hold bit-identical
+//     scores, maxima and P;
+//   - each CTA accumulates O[:, cols_h] += P V[:, cols_h] with the latent boxes
+//     it already holds (V is the leading 512 columns of the cached row).
+// Tensor-core shapes: Q K^T partials are M=128 x N=64 per K=16 step; P V is
+// M=128 x N=256 x K=16 (four steps per page).
 //
-// Per CTA: warp 0 lane 0 issues TMA loads (three 128 x 64 query boxes kept
-// for the whole segment; cache tiles as 32 x 64 boxes through the ring),
-// warp 1 lane 0 issues tcgen05 MMAs, and warps 4..7 (one
-// thread per query row, matching TMEM lanes) run the online softmax, write P
-// (bf16, 128-byte swizzled, the A operand of P V) and the epilogue.  The
-// softmax keeps a per-row reference max and rescales the TMEM accumulator only
-// when the running max grows past it by more than 2^8 (exact for any
-// reference; only the rounding differs), with scores in log2 units.  Rows of
-// the last page past the sequence end are zeroed in shared memory before P V
-// so that stale or NaN cache contents never reach the accumulator.
+// TMEM per CTA: O half at columns 0..255, a double-buffered 64-column S
+// partial at 256..383, and the CTA's 256 latent query columns (packed bf16
+// pairs, the TMEM A operand of Q K^T) at 384..511.  CTA 0 keeps the RoPE
+// query box in shared memory.
 //
-// Every mbarrier wait is bounded; a wait that runs out records MLA_ERR_TIMEOUT
-// in the workspace, raises a CTA-wide abort flag, drains the TMA loads and
-// MMAs already issued, frees TMEM and returns.
+// Roles per CTA: warp 0 lane 0 issues TMA loads (a 3-stage ring of page
+// slots, plus L2 prefetch of pages further ahead), warp 1 lane 0 issues the
+// tcgen05 MMAs, warps 4..7 (one thread per query row = TMEM lane) swap
+// partials, run the online softmax, write P (bf16, 128-byte swizzled, the A
+// operand of P V) and the epilogue.  The softmax keeps a per-row reference
+// max and rescales the TMEM accumulator only when the running max grows past
+// it by more than 2^8 (exact for any reference; only rounding differs), with
+// scores in log2 units.  Cache rows past the sequence end (last page only)
+// are zeroed in shared memory before P V so stale or NaN contents never reach
+// the accumulator.
+//
+// Every wait is bounded; a wait that runs out records MLA_ERR_TIMEOUT in the
+// workspace and raises a CTA-wide abort flag.  Loads and MMAs already issued
+// are drained, TMEM is freed and both CTAs meet at a final cluster barrier
+// before exiting (no CTA exits while its peer may still write into it).
 #include <math.h>
 
 #include "mla_internal.cuh"
@@ -46,38 +56,40 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 256;
-constexpr int kQBoxBytes = 128 * 64 * 2;   // 16 KB: 128 query rows x 64 bf16
-constexpr int kTileRows = 32;              // cache rows per tile (half a page)
-constexpr int kBoxBytes = kTileRows * 64 * 2;  // 4 KB: 32 cache rows x 64 bf16
-constexpr int kBoxes = 9;                  // 8 latent boxes + 1 RoPE box per row
-constexpr int kQTmemBoxes = 6;             // query column boxes 0..5 are held in TMEM
-constexpr int kQSmemBoxes = kBoxes - kQTmemBoxes;  // boxes 6, 7 (latent) and 8 (RoPE) in shared memory
-constexpr int kSlots = 40;
-constexpr int kSmemQ = 0;
-constexpr int kSmemRing = kSmemQ + kQSmemBoxes * kQBoxBytes;  // 49152
-constexpr int kSmemP = kSmemRing + kSlots * kBoxBytes;        // 212992
-constexpr int kSmemBar = kSmemP + 128 * 64 * 2;               // 229376
+constexpr int kBoxBytes = 64 * 64 * 2;         // 8 KB: one 64-row page x 64 bf16 columns
+constexpr int kQBoxBytes = 128 * 64 * 2;       // 16 KB: 128 query rows x 64 bf16
+constexpr int kOwnBoxes = 4;                   // latent column boxes per CTA
+constexpr int kSlotBytes = 5 * kBoxBytes;      // 4 latent boxes (+ the RoPE box on CTA 0)
+constexpr int kStages = 3;
+constexpr int kRecvBytes = 128 * 64 * 4;       // one partial score tile, fp32
+constexpr int kSmemQRope = 0;
+constexpr int kSmemP = kSmemQRope + kQBoxBytes;            // 16384
+constexpr int kSmemRecv = kSmemP + 128 * 64 * 2;           // 32768
+constexpr int kSmemRing = kSmemRecv + 2 * kRecvBytes;      // 98304
+constexpr int kSmemBar = kSmemRing + kStages * kSlotBytes; // 221184
 constexpr int kSmemBytes = kSmemBar + 1024;
-constexpr int kSmemAlloc = kSmemBytes + 1024;                 // slack to align the base to 1024 B
+constexpr int kSmemAlloc = kSmemBytes + 1024;              // slack to align the base to 1024 B
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;     // O half: 256 fp32 columns
-constexpr uint32_t kTmemS = 256;   // S: 2 x 32 fp32 columns
-constexpr uint32_t kTmemQ = 320;   // Q boxes 0..5: 6 x 32 columns of packed bf16 pairs
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+constexpr uint32_t kTmemO = 0;
+constexpr uint32_t kTmemS = 256;
+constexpr uint32_t kTmemQ = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kPrefetchPages = 3;          // L2 prefetch distance ahead of the page being loaded
 
 enum {
-  BAR_KV_FULL = 0,
-  BAR_KV_EMPTY = BAR_KV_FULL + kSlots,
-  BAR_Q_FULL = BAR_KV_EMPTY + kSlots,
+  BAR_FULL = 0,                     // kStages
+  BAR_EMPTY = BAR_FULL + kStages,   // kStages
+  BAR_Q_FULL = BAR_EMPTY + kStages,
   BAR_Q_EMPTY,
-  BAR_S_FULL,  // two
-  BAR_S_EMPTY = BAR_S_FULL + 2,  // two
+  BAR_QT_FULL,
+  BAR_S_FULL,                       // 2
+  BAR_S_EMPTY = BAR_S_FULL + 2,     // 2
   BAR_P_FULL = BAR_S_EMPTY + 2,
   BAR_P_EMPTY,
   BAR_O_EMPTY,
-  BAR_FINAL,
-  BAR_QT_FULL,
+  BAR_XFULL,                        // 2: the peer's partial landed in my receive buffer
+  BAR_XFREE = BAR_XFULL + 2,        // 2: the peer has read the partial I wrote into it
+  BAR_FINAL = BAR_XFREE + 2,
   kNumBars
 };
 static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
@@ -91,30 +103,18 @@ struct FastArgs {
   const __nv_bfloat16* ckv;  // pool base, for the L2 prefetch of whole pages
   int64_t ckv_block;         // elements between blocks
   int page_contiguous;       // 1 when a block's 64 rows x 576 values are one contiguous range
-  float scale_log2;  // softmax scale times log2(e)
+  float scale_log2;          // softmax scale times log2(e)
   __nv_bfloat16* o_lat;
   float* lse;
   WsLayout L;
 };
 
-// Box order within one tile: the five boxes this half only needs for Q K^T
-// come first (their slots are released right after the MMAs), then the four
-// latent boxes whose columns this half accumulates in P V (held until P V).
-// With 9 boxes per tile and 16 ring slots, box k of tile i reuses the slot of
-// box k+7 of tile i-2 or k-7... of tile i-1 (k >= 7): always a box whose
-// release precedes Q K^T of tile i in the MMA issue order (Q K^T(i-1), then
-// P V(i-2), then Q K^T(i)), so the ring never waits on P V(i-1).
-__device__ __forceinline__ int box_order(int half, int k) {
-  if (k == 4) return 8;
-  if (half == 0) return k < 4 ? 4 + k : k - 5;
-  return k < 4 ? k : k - 1;
-}
-
 struct Shared {
-  uint32_t base;  // shared-window address of the 1024-aligned base
-  __device__ uint32_t q(int box) const { return base + kSmemQ + (box - kQTmemBoxes) * kQBoxBytes; }
-  __device__ uint32_t slot(int s) const { return base + kSmemRing + s * kBoxBytes; }
+  uint32_t base;
+  __device__ uint32_t qrope() const { return base + kSmemQRope; }
   __device__ uint32_t p() const { return base + kSmemP; }
+  __device__ uint32_t recv(int b) const { return base + kSmemRecv + b * kRecvBytes; }
+  __device__ uint32_t slot(int s) const { return base + kSmemRing + s * kSlotBytes; }
   __device__ uint32_t bar(int i) const { return base + kSmemBar + i * 8; }
 };
 
@@ -124,9 +124,8 @@ __device__ __forceinline__ void fail(int* hdr, volatile int* abort_flag, int whe
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_sm103_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_constant__ CUtensorMap tm_qpe,
-                        const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
-                        FastArgs a, char* ws) {
+    decode_sm103_kernel(const __grid_constant__ CUtensorMap tm_qpe, const __grid_constant__ CUtensorMap tm_ckv,
+                        const __grid_constant__ CUtensorMap tm_kpe, FastArgs a, char* ws) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Shared sh{smem_addr(smem)};
@@ -140,31 +139,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* part_o = reinterpret_cast<float*>(ws + a.L.off_part_o);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int half = blockIdx.x & 1;
+  const int half = (int)cluster_ctarank();
+  const int peer = half ^ 1;
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
   const int num_ranges = hdr[MLA_HDR_NUM_RANGES];
   const int R = a.T * a.H;
 
   if (tid == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(sh.bar(BAR_KV_FULL + i), 1);
-      mbar_init(sh.bar(BAR_KV_EMPTY + i), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(sh.bar(BAR_FULL + i), 1);
+      mbar_init(sh.bar(BAR_EMPTY + i), 1);
     }
     mbar_init(sh.bar(BAR_Q_FULL), 1);
     mbar_init(sh.bar(BAR_Q_EMPTY), 1);
+    mbar_init(sh.bar(BAR_QT_FULL), 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(sh.bar(BAR_S_FULL + i), 1);
       mbar_init(sh.bar(BAR_S_EMPTY + i), 128);
+      mbar_init(sh.bar(BAR_XFULL + i), 128);
+      mbar_init(sh.bar(BAR_XFREE + i), 128);
     }
     mbar_init(sh.bar(BAR_P_FULL), 128);
     mbar_init(sh.bar(BAR_P_EMPTY), 1);
     mbar_init(sh.bar(BAR_O_EMPTY), 128);
     mbar_init(sh.bar(BAR_FINAL), 1);
-    mbar_init(sh.bar(BAR_QT_FULL), 128);
     *abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(&tm_qlat);
     prefetch_tmap(&tm_qpe);
     prefetch_tmap(&tm_ckv);
     prefetch_tmap(&tm_kpe);
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // the peer's barriers are initialised before anyone arrives on them
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
 
@@ -199,21 +201,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int gbox = 0, sc = 0;
-      bool q_in_flight = false;
-      bool ok = true;
+      int gt = 0, sc = 0;
+      bool q_in_flight = false, ok = true;
       for (int r = pair; ok && r < num_ranges; r += num_pairs) {
         for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
           const int* rec = seg + (size_t)si * kSegWords;
           const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3];
-          if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
-          const int row0 = b * R + rb * kRowsPerBlock;
-          mbar_arrive_expect_tx(sh.bar(BAR_Q_FULL), kQSmemBoxes * kQBoxBytes);
-          for (int box = kQTmemBoxes; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_FULL), 64 * box, row0);
-          tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_FULL), 0, row0);
-          q_in_flight = true;
-          // The page loads below are issued only a ring's depth ahead of use, so pages
-          // further ahead are pulled into L2 first; the CTA of half 0 does it for the pair.
+          if (half == 0) {
+            if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
+            mbar_arrive_expect_tx(sh.bar(BAR_Q_FULL), kQBoxBytes);
+            tma_load_2d(sh.qrope(), &tm_qpe, sh.bar(BAR_Q_FULL), 0, b * R + rb * kRowsPerBlock);
+            q_in_flight = true;
+          }
+          // Pages further ahead than the ring are pulled into L2 (CTA 0 does it for the pair).
           auto prefetch_page = [&](int pp) {
             if (half != 0 || pp >= p1) return;
             const int pb = a.block_table[(size_t)b * a.bt_stride + pp];
@@ -221,41 +221,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (a.page_contiguous) {
               prefetch_l2_bulk(a.ckv + (int64_t)pb * a.ckv_block, kPage * kDK * 2);
             } else {
-              for (int rr = 0; rr < kPage; rr += kTileRows) {
-                for (int box = 0; box < 8; ++box) prefetch_l2_tile_3d(&tm_ckv, 64 * box, rr, pb);
-                prefetch_l2_tile_3d(&tm_kpe, 0, rr, pb);
-              }
+              for (int box = 0; box < 8; ++box) prefetch_l2_tile_3d(&tm_ckv, 64 * box, 0, pb);
+              prefetch_l2_tile_3d(&tm_kpe, 0, 0, pb);
             }
           };
           for (int pp = p0; pp < p0 + kPrefetchPages; ++pp) prefetch_page(pp);
-          for (int tt = 2 * p0; ok && tt < 2 * p1; ++tt) {
-            const int p = tt >> 1, r0 = (tt & 1) * kTileRows;
-            if ((tt & 1) == 0) prefetch_page(p + kPrefetchPages);
+          for (int p = p0; p < p1; ++p, ++gt) {
+            prefetch_page(p + kPrefetchPages);
             int blk = a.block_table[(size_t)b * a.bt_stride + p];
             if (blk < 0 || blk >= a.num_blocks) {
               // An out-of-pool id reads as zeros through the tensor map; report it when checking.
               if (a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | p);
               blk = -1;
             }
-            for (int k = 0; k < kBoxes; ++k, ++gbox) {
-              const int s = gbox % kSlots;
-              if (!mbar_wait(sh.bar(BAR_KV_EMPTY + s), ((gbox / kSlots) & 1) ^ 1, abort_flag)) {
-                fail(hdr, abort_flag, 11); ok = false; break;
-              }
-              mbar_arrive_expect_tx(sh.bar(BAR_KV_FULL + s), kBoxBytes);
-              const int box = box_order(half, k);
-              if (box < 8) tma_load_3d(sh.slot(s), &tm_ckv, sh.bar(BAR_KV_FULL + s), 64 * box, r0, blk);
-              else tma_load_3d(sh.slot(s), &tm_kpe, sh.bar(BAR_KV_FULL + s), 0, r0, blk);
+            const int st = gt % kStages;
+            if (!mbar_wait(sh.bar(BAR_EMPTY + st), ((gt / kStages) & 1) ^ 1, abort_flag)) {
+              fail(hdr, abort_flag, 11); ok = false; break;
             }
+            mbar_arrive_expect_tx(sh.bar(BAR_FULL + st), (half == 0 ? 5 : 4) * kBoxBytes);
+            for (int j = 0; j < kOwnBoxes; ++j)
+              tma_load_3d(sh.slot(st) + j * kBoxBytes, &tm_ckv, sh.bar(BAR_FULL + st), 64 * (kOwnBoxes * half + j), 0, blk);
+            if (half == 0) tma_load_3d(sh.slot(st) + kOwnBoxes * kBoxBytes, &tm_kpe, sh.bar(BAR_FULL + st), 0, 0, blk);
           }
           ++sc;
         }
       }
       // Drain: every load issued must have landed before the CTA may exit.
-      const int first = gbox > kSlots ? gbox - kSlots : 0;
-      for (int g = first; g < gbox; ++g) {
+      const int first = gt > kStages ? gt - kStages : 0;
+      for (int g = first; g < gt; ++g) {
         volatile int never = 0;
-        mbar_wait(sh.bar(BAR_KV_FULL + g % kSlots), (g / kSlots) & 1, &never);
+        mbar_wait(sh.bar(BAR_FULL + g % kStages), (g / kStages) & 1, &never);
       }
       if (q_in_flight) {
         volatile int never = 0;
@@ -266,79 +261,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t id_qk = idesc_bf16_f32(128, kTileRows, 0);
-      const uint32_t id_pv = idesc_bf16_f32(128, 64, 1);
-      // Descriptors are built once; k-steps and slots only move the start-address field
-      // (16-byte units): +2 per 32-byte K step of a K-major tile, +128 per 16-row K step
-      // of an MN-major tile, +kBoxBytes/16 per ring slot.
-      uint64_t qdesc[kQSmemBoxes];
-#pragma unroll
-      for (int bx = 0; bx < kQSmemBoxes; ++bx) qdesc[bx] = sw128_desc(sh.q(kQTmemBoxes + bx), 16, 1024);
+      const uint32_t id_qk = idesc_bf16_f32(128, 64, 0);
+      const uint32_t id_pv = idesc_bf16_f32(128, 256, 1);
+      // Descriptors are built once; steps only move the start-address field (16-byte
+      // units): +2 per 32-byte K step of a K-major tile, +128 per 16-row K step of
+      // the MN-major value tile, +kBoxBytes/16 per box, +kSlotBytes/16 per slot.
       const uint64_t kdesc0 = sw128_desc(sh.slot(0), 16, 1024);
       const uint64_t vdesc0 = sw128_desc(sh.slot(0), kBoxBytes, 1024);
       const uint64_t pdesc = sw128_desc(sh.p(), 16, 1024);
-      int gbox = 0, ti = 0, sc = 0;
+      const uint64_t rdesc = sw128_desc(sh.qrope(), 16, 1024);
+      int ti = 0, sc = 0;
       bool ok = true;
-      int own[4] = {0, 0, 0, 0}, own_prev[4] = {0, 0, 0, 0};
-      auto issue_pv = [&](int t, const int (&slots)[4], bool first_of_seg) -> bool {
+      auto issue_pv = [&](int t, bool first_of_seg) -> bool {
         if (first_of_seg && sc > 0) {
           if (!mbar_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 20); return false; }
         }
         if (!mbar_wait(sh.bar(BAR_P_FULL), t & 1, abort_flag)) { fail(hdr, abort_flag, 21); return false; }
         tc_fence_after();
-        for (int c = 0; c < 4; ++c) {
-          const uint64_t vd = vdesc0 + (uint64_t)(slots[c] * (kBoxBytes >> 4));
+        const int st = t % kStages;
+        const uint64_t vd = vdesc0 + (uint64_t)(st * (kSlotBytes >> 4));
 #pragma unroll
-          for (int kk = 0; kk < kTileRows / 16; ++kk)
-            mma_bf16(tmem + kTmemO + 64 * c, pdesc + 2 * kk, vd + 128 * kk, id_pv, (first_of_seg && kk == 0) ? 0u : 1u);
-          mma_commit(sh.bar(BAR_KV_EMPTY + slots[c]));
-        }
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(tmem + kTmemO, pdesc + 2 * kk, vd + 128 * kk, id_pv, (first_of_seg && kk == 0) ? 0u : 1u);
+        mma_commit(sh.bar(BAR_EMPTY + st));
         mma_commit(sh.bar(BAR_P_EMPTY));
         return true;
       };
       for (int r = pair; ok && r < num_ranges; r += num_pairs) {
         for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
           const int* rec = seg + (size_t)si * kSegWords;
-          const int n_tiles = 2 * (rec[3] - rec[2]);
-          if (!mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag) ||
+          const int n_tiles = rec[3] - rec[2];
+          if ((half == 0 && !mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag)) ||
               !mbar_wait(sh.bar(BAR_QT_FULL), sc & 1, abort_flag)) {
             fail(hdr, abort_flag, 22); ok = false; break;
           }
           tc_fence_after();
           for (int i = 0; ok && i < n_tiles; ++i, ++ti) {
             const int buf = ti & 1;
-            if (!mbar_wait(sh.bar(BAR_S_EMPTY + buf), ((ti >> 1) & 1) ^ 1, abort_flag)) {
+            const int st = ti % kStages;
+            if (!mbar_wait(sh.bar(BAR_S_EMPTY + buf), ((ti >> 1) & 1) ^ 1, abort_flag) ||
+                !mbar_wait(sh.bar(BAR_FULL + st), (ti / kStages) & 1, abort_flag)) {
               fail(hdr, abort_flag, 23); ok = false; break;
             }
             tc_fence_after();
-            const uint32_t d = tmem + kTmemS + kTileRows * buf;
-            for (int k = 0; k < kBoxes; ++k, ++gbox) {
-              const int s = gbox % kSlots;
-              if (!mbar_wait(sh.bar(BAR_KV_FULL + s), (gbox / kSlots) & 1, abort_flag)) {
-                fail(hdr, abort_flag, 24); ok = false; break;
-              }
-              tc_fence_after();
-              const int box = box_order(half, k);
-              const uint64_t bd = kdesc0 + (uint64_t)(s * (kBoxBytes >> 4));
-              if (box < kQTmemBoxes) {
-                const uint32_t at = tmem + kTmemQ + 32 * box;   // 16 bf16 of K = 8 TMEM columns per step
+            const uint32_t d = tmem + kTmemS + 64 * buf;
+            const uint64_t kd = kdesc0 + (uint64_t)(st * (kSlotBytes >> 4));
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(d, at + 8 * kk, bd + 2 * kk, id_qk, (k | kk) ? 1u : 0u);
-              } else {
-                const uint64_t ad = qdesc[box - kQTmemBoxes];
+            for (int j = 0; j < kOwnBoxes; ++j) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id_qk, (k | kk) ? 1u : 0u);
-              }
-              if (k < 5) mma_commit(sh.bar(BAR_KV_EMPTY + s));
-              else own[k - 5] = s;
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_tmem_a(d, tmem + kTmemQ + 32 * j + 8 * kk, kd + j * (kBoxBytes >> 4) + 2 * kk, id_qk,
+                                (j | kk) ? 1u : 0u);
             }
-            if (!ok) break;
+            if (half == 0) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(d, rdesc + 2 * kk, kd + kOwnBoxes * (kBoxBytes >> 4) + 2 * kk, id_qk, 1u);
+            }
             mma_commit(sh.bar(BAR_S_FULL + buf));
             if (i == n_tiles - 1) mma_commit(sh.bar(BAR_Q_EMPTY));
-            if (i > 0 && !issue_pv(ti - 1, own_prev, i == 1)) { ok = false; break; }
-            for (int c = 0; c < 4; ++c) own_prev[c] = own[c];
+            if (i > 0 && !issue_pv(ti - 1, i == 1)) { ok = false; break; }
           }
-          if (ok && n_tiles > 0 && !issue_pv(ti - 1, own_prev, n_tiles == 1)) ok = false;
+          if (ok && n_tiles > 0 && !issue_pv(ti - 1, n_tiles == 1)) ok = false;
           ++sc;
         }
       }
@@ -349,10 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int row = tid - 128;            // query row within the group == TMEM lane
+    // ------------------------------------------------------------ exchange + softmax + epilogue
+    const int row = tid - 128;  // query row within the group == TMEM lane
     const int q4 = warp - 4;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t peer_recv0 = map_to_cta(sh.recv(0), peer);
+    const uint32_t peer_xfull0 = map_to_cta(sh.bar(BAR_XFULL), peer);
+    const uint32_t peer_xfree0 = map_to_cta(sh.bar(BAR_XFREE), peer);
     int ti = 0, sc = 0;
     bool ok = true;
     for (int r = pair; ok && r < num_ranges; r += num_pairs) {
@@ -364,15 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int fr = rb * kRowsPerBlock + row;
         const bool row_valid = fr < R;
         const int limit = row_valid ? visible_limit(S, a.T, fr / a.H, a.causal) : 0;
-        // Query columns 0..383 of this row go to TMEM (the A operand of Q K^T for
-        // boxes 0..5), once the previous segment's Q K^T MMAs have finished with it.
+        // This CTA's 256 latent query columns go to TMEM (A operand of its Q K^T
+        // partial) once the previous segment's Q K^T MMAs are done with them.
         {
           bool w_ok = sc == 0 || mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 33); ok = false; break; }
           tc_fence_after();
-          const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)b * R + fr) * kDLat);
+          const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)b * R + fr) * kDLat + 256 * half);
 #pragma unroll 1
-          for (int bx = 0; bx < kQTmemBoxes; ++bx) {
+          for (int bx = 0; bx < kOwnBoxes; ++bx) {
             uint32_t qv[32];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -386,27 +373,59 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(sh.bar(BAR_QT_FULL));
         }
         float m_ref = -INFINITY, l = 0.f;
-        const int n_tiles = 2 * (p1 - p0);
+        const int n_tiles = p1 - p0;
         for (int i = 0; i < n_tiles; ++i, ++ti) {
           const int buf = ti & 1;
+          const int p = p0 + i;
           bool w_ok = mbar_wait(sh.bar(BAR_S_FULL + buf), (ti >> 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 30); ok = false; break; }
           tc_fence_after();
-          uint32_t sr[kTileRows];
-          tmem_ld32(t_lane + kTmemS + kTileRows * buf, sr);
-          tmem_wait_ld();
+          uint32_t own[64];
+          {
+            uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&own[0]);
+            uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&own[32]);
+            tmem_ld32(t_lane + kTmemS + 64 * buf, lo);
+            tmem_ld32(t_lane + kTmemS + 64 * buf + 32, hi);
+            tmem_wait_ld();
+          }
           tc_fence_before();
           mbar_arrive(sh.bar(BAR_S_EMPTY + buf));
-          const int jbase = (2 * p0 + i) * kTileRows;   // first cache row of this tile
-          float s[kTileRows];
-          float tmax = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < kTileRows; ++j) {
-            float v = __uint_as_float(sr[j]) * a.scale_log2;
-            v = (jbase + j < limit) ? v : -INFINITY;
-            s[j] = v;
-            tmax = fmaxf(tmax, v);
+          // Swap partial tiles with the peer: my row goes into its receive buffer.
+          if (ti >= 2) {
+            w_ok = mbar_wait_cluster(sh.bar(BAR_XFREE + buf), ((ti >> 1) - 1) & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 34); ok = false; break; }
           }
+          {
+            const uint32_t dst = peer_recv0 + buf * kRecvBytes + row * 256;
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              st_cluster_v4(dst + 16 * e, own[4 * e], own[4 * e + 1], own[4 * e + 2], own[4 * e + 3]);
+            mbar_arrive_remote(peer_xfull0 + 8 * buf);
+          }
+          w_ok = mbar_wait_cluster(sh.bar(BAR_XFULL + buf), (ti >> 1) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 35); ok = false; break; }
+          const int jbase = p * kPage;
+          float s[64];
+          float tmax = -INFINITY;
+          {
+            const float4* src = reinterpret_cast<const float4*>(smem + kSmemRecv + buf * kRecvBytes + row * 256);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float4 pv = src[e];
+              const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+              for (int z = 0; z < 4; ++z) {
+                const int j = 4 * e + z;
+                const float mine = __uint_as_float(own[j]);
+                // Both CTAs add partial(CTA 0) + partial(CTA 1): identical bits on both sides.
+                float v = (half == 0 ? mine + pr[z] : pr[z] + mine) * a.scale_log2;
+                v = (jbase + j < limit) ? v : -INFINITY;
+                s[j] = v;
+                tmax = fmaxf(tmax, v);
+              }
+            }
+          }
+          mbar_arrive_remote(peer_xfree0 + 8 * buf);  // my receive buffer may be reused
           if (i > 0) {
             w_ok = mbar_wait(sh.bar(BAR_P_EMPTY), (ti - 1) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 31); ok = false; break; }
@@ -435,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float psum = 0.f;
           const uint32_t prow = sh.p() + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-          for (int c = 0; c < kTileRows / 8; ++c) {
+          for (int c = 0; c < 8; ++c) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -452,14 +471,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : "memory");
           }
           l += psum;
-          // Cache rows past the sequence end (last page only) are zeroed in the
+          // Rows of the last page past the sequence end are zeroed in this CTA's
           // four value boxes before P V reads them.
           const int valid = S - jbase;
-          if (valid < kTileRows) {
-            for (int idx = row; idx < 4 * kTileRows; idx += 128) {
-              const int c = idx / kTileRows, rr = idx % kTileRows;
+          if (valid < kPage) {
+            const uint32_t slot = sh.slot(ti % kStages);
+            for (int idx = row; idx < kOwnBoxes * kPage; idx += 128) {
+              const int c = idx / kPage, rr = idx % kPage;
               if (rr >= valid) {
-                const uint32_t dst = sh.slot((9 * ti + 5 + c) % kSlots) + rr * 128;
+                const uint32_t dst = slot + c * kBoxBytes + rr * 128;
 #pragma unroll
                 for (int z = 0; z < 8; ++z)
                   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst + 16 * z), "r"(0) : "memory");
@@ -471,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(sh.bar(BAR_P_FULL));
         }
         if (!ok) break;
-        // Epilogue: wait for the last P V, then normalise and store this half's columns.
+        // Epilogue: wait for the last P V, then normalise and store this CTA's columns.
         {
           const bool w_ok = mbar_wait(sh.bar(BAR_P_EMPTY), (ti - 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 32); ok = false; break; }
@@ -522,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // the peer has finished writing into this CTA's shared memory
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
@@ -555,11 +576,53 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
+bool set_kernel_attributes() {
+  static bool done = false;
+  if (!done) {
+    if (cudaFuncSetAttribute(decode_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+        cudaSuccess)
+      return false;
+    done = true;
+  }
+  return true;
+}
+
+void cluster_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pairs, cudaStream_t st) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->gridDim = dim3(2 * pairs, 1, 1);
+  cfg->blockDim = dim3(kThreads, 1, 1);
+  cfg->dynamicSmemBytes = kSmemAlloc;
+  cfg->stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
 }  // namespace
 
+// Clusters (CTA pairs) of the decode kernel that can be resident at once on the current device.
 int decode_sm103_pairs_per_device() {
-  const int sms = mla_device_sm_count();
-  return sms >= 2 ? sms / 2 : 1;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (set_kernel_attributes()) {
+      cudaLaunchConfig_t cfg;
+      cudaLaunchAttribute attr[1];
+      cluster_launch_config(&cfg, attr, 256, 0);
+      if (cudaOccupancyMaxActiveClusters(&n, decode_sm103_kernel, &cfg) != cudaSuccess) n = 0;
+    }
+    if (n <= 0) {
+      const int sms = mla_device_sm_count();
+      n = sms >= 2 ? sms / 2 : 1;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsLayout& L,
@@ -567,13 +630,7 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
                                 const int32_t* block_table, int bt_stride, const int32_t* seq_lens, int checked,
                                 __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st) {
   const long long rows_total = (long long)b->B * b->T * g->H;
-  CUtensorMap m_qlat, m_qpe, m_ckv, m_kpe;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)kDLat, (cuuint64_t)rows_total};
-    const cuuint64_t str[1] = {(cuuint64_t)kDLat * 2};
-    const cuuint32_t box[2] = {64, 128};
-    if (!make_map(&m_qlat, q_lat, 2, dims, str, box)) return cudaErrorInvalidValue;
-  }
+  CUtensorMap m_qpe, m_ckv, m_kpe;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)kDRope, (cuuint64_t)rows_total};
     const cuuint64_t str[1] = {(cuuint64_t)kDRope * 2};
@@ -583,13 +640,13 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
   {
     const cuuint64_t dims[3] = {(cuuint64_t)kDLat, (cuuint64_t)kPage, (cuuint64_t)cv.num_blocks};
     const cuuint64_t str[2] = {(cuuint64_t)cv.ckv_row * 2, (cuuint64_t)cv.ckv_block * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kTileRows, 1};
+    const cuuint32_t box[3] = {64, 64, 1};
     if (!make_map(&m_ckv, cv.ckv, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)kDRope, (cuuint64_t)kPage, (cuuint64_t)cv.num_blocks};
     const cuuint64_t str[2] = {(cuuint64_t)cv.kpe_row * 2, (cuuint64_t)cv.kpe_block * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kTileRows, 1};
+    const cuuint32_t box[3] = {64, 64, 1};
     if (!make_map(&m_kpe, cv.kpe, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   FastArgs a;
@@ -602,19 +659,15 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
                        cv.kpe_row == kDK && cv.kpe_block == cv.ckv_block) ? 1 : 0;
   a.scale_log2 = g->softmax_scale * 1.4426950408889634f;
   a.o_lat = o_lat; a.lse = lse; a.L = L;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (!set_kernel_attributes()) return cudaErrorInvalidValue;
   int pairs = L.cap_ranges;
   const int max_pairs = decode_sm103_pairs_per_device();
   if (pairs > max_pairs) pairs = max_pairs;
   if (pairs <= 0) return cudaSuccess;
-  decode_sm103_kernel<<<2 * pairs, kThreads, kSmemAlloc, st>>>(m_qlat, m_qpe, m_ckv, m_kpe, a,
-                                                              reinterpret_cast<char*>(ws));
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  cluster_launch_config(&cfg, attr, pairs, st);
+  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel, m_qpe, m_ckv, m_kpe, a, reinterpret_cast<char*>(ws));
 }
 
 }  // namespace mla
