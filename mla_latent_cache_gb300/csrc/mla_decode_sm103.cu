@@ -11,40 +11,37 @@
 // Work decomposition.  A query-row group is 128 flattened (t, h) rows of one
 // sequence (one token's 128 heads at V3 geometry).  Its fp32 accumulator,
 // 128 x 512, would take all 512 TMEM columns of an SM, so each group is
-// handled by a CLUSTER of two CTAs, and each CTA owns half of the latent
-// columns: CTA 0 latent 0..255 plus the 64 RoPE columns, CTA 1 latent
-// 256..511.  For each 64-row cache page:
-//   - each CTA loads only its own column boxes (the pair reads every cache
-//     byte exactly once) and forms a PARTIAL score tile over its columns,
-//     S_h = Q[:, cols_h] K[:, cols_h]^T (128 x 64, fp32, in TMEM);
-//   - the two partial tiles are swapped through distributed shared memory and
-//     both CTAs form S = S_0 + S_1 in the same order, so both hold bit-identical
-//     scores, maxima and P;
-//   - each CTA accumulates O[:, cols_h] += P V[:, cols_h] with the latent boxes
-//     it already holds (V is the leading 512 columns of the cached row).
-// Tensor-core shapes: Q K^T partials are M=128 x N=64 per K=16 step; P V is
-// M=128 x N=256 x K=16 (four steps per page).
+// handled by a CLUSTER of two CTAs: CTA h accumulates the output columns
+// [256 h, 256 h + 256).  For each 64-row cache page both CTAs form the full
+// 128 x 64 score tile S = Q K^T over all 576 columns (the second read of a
+// page usually hits L2; the pair is co-scheduled as a cluster), run the same
+// softmax, and each accumulates O[:, cols_h] += P V[:, cols_h], V being the
+// leading 512 columns of the cached rows.  Swapping partial score tiles
+// between the two CTAs instead of computing S twice was measured to cost more
+// than it saves: the exchange moves as many bytes as the cache itself through
+// distributed shared memory.
+// Tensor-core shapes: Q K^T is M=128 x N=64 per K=16 step (36 steps per page);
+// P V is M=128 x N=256 x K=16 (four steps per page).
 //
-// TMEM per CTA: O half at columns 0..255, a double-buffered 64-column S
-// partial at 256..383, and the CTA's 256 latent query columns (packed bf16
-// pairs, the TMEM A operand of Q K^T) at 384..511.  CTA 0 keeps the RoPE
-// query box in shared memory.
+// TMEM per CTA: O half at columns 0..255, the 64-column S tile at 256..319
+// (released as soon as the softmax has read it), and query columns 0..383
+// (packed bf16 pairs, the TMEM A operand of Q K^T) at 320..511; the rest of
+// the query tile (latent 384..511 and RoPE) stays in shared memory.
 //
-// Roles per CTA: warp 0 lane 0 issues TMA loads (a 3-stage ring of page
-// slots, plus L2 prefetch of pages further ahead), warp 1 lane 0 issues the
-// tcgen05 MMAs, warps 4..7 (one thread per query row = TMEM lane) swap
-// partials, run the online softmax, write P (bf16, 128-byte swizzled, the A
-// operand of P V) and the epilogue.  The softmax keeps a per-row reference
-// max and rescales the TMEM accumulator only when the running max grows past
-// it by more than 2^8 (exact for any reference; only rounding differs), with
-// scores in log2 units.  Cache rows past the sequence end (last page only)
-// are zeroed in shared memory before P V so stale or NaN contents never reach
-// the accumulator.
+// Roles per CTA: warp 0 lane 0 issues TMA loads (64 x 64 cache boxes through
+// an 18-slot ring, plus L2 prefetch of pages further ahead), warp 1 lane 0
+// issues the tcgen05 MMAs (Q K^T of page i, then P V of page i-1), warps 4..7
+// (one thread per query row = TMEM lane) run the online softmax, write P
+// (bf16, 128-byte swizzled, double-buffered: the A operand of P V) and the
+// epilogue.  The softmax keeps a per-row reference max and rescales the TMEM
+// accumulator only when the running max grows past it by more than 2^8 (exact
+// for any reference; only rounding differs), with scores in log2 units.
+// Cache rows past the sequence end (last page only) are zeroed in shared
+// memory before P V so stale or NaN contents never reach the accumulator.
 //
 // Every wait is bounded; a wait that runs out records MLA_ERR_TIMEOUT in the
 // workspace and raises a CTA-wide abort flag.  Loads and MMAs already issued
-// are drained, TMEM is freed and both CTAs meet at a final cluster barrier
-// before exiting (no CTA exits while its peer may still write into it).
+// are drained, TMEM is freed and both CTAs meet at a final cluster barrier.
 #include <math.h>
 
 #include "mla_internal.cuh"
@@ -58,41 +55,51 @@ using namespace ptx;
 constexpr int kThreads = 256;
 constexpr int kBoxBytes = 64 * 64 * 2;         // 8 KB: one 64-row page x 64 bf16 columns
 constexpr int kQBoxBytes = 128 * 64 * 2;       // 16 KB: 128 query rows x 64 bf16
-constexpr int kOwnBoxes = 4;                   // latent column boxes per CTA
-constexpr int kSlotBytes = 5 * kBoxBytes;      // 4 latent boxes (+ the RoPE box on CTA 0)
-constexpr int kStages = 3;
-constexpr int kRecvBytes = 128 * 64 * 4;       // one partial score tile, fp32
-constexpr int kSmemQRope = 0;
-constexpr int kSmemP = kSmemQRope + kQBoxBytes;            // 16384
-constexpr int kSmemRecv = kSmemP + 128 * 64 * 2;           // 32768
-constexpr int kSmemRing = kSmemRecv + 2 * kRecvBytes;      // 98304
-constexpr int kSmemBar = kSmemRing + kStages * kSlotBytes; // 221184
+constexpr int kBoxes = 9;                      // 8 latent boxes + 1 RoPE box per row
+constexpr int kOwnBoxes = 4;                   // latent boxes whose columns this CTA accumulates
+constexpr int kQTmemBoxes = 6;                 // query boxes 0..5 live in TMEM
+constexpr int kQSmemBoxes = kBoxes - kQTmemBoxes;
+constexpr int kSlots = 18;
+constexpr int kPBytes = 128 * 64 * 2;          // one P tile, bf16
+constexpr int kSmemQ = 0;
+constexpr int kSmemP = kSmemQ + kQSmemBoxes * kQBoxBytes;  // 49152
+constexpr int kSmemRing = kSmemP + 2 * kPBytes;            // 81920
+constexpr int kSmemBar = kSmemRing + kSlots * kBoxBytes;   // 229376
 constexpr int kSmemBytes = kSmemBar + 1024;
 constexpr int kSmemAlloc = kSmemBytes + 1024;              // slack to align the base to 1024 B
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemS = 256;
-constexpr uint32_t kTmemQ = 384;
+constexpr uint32_t kTmemQ = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kPrefetchPages = 3;          // L2 prefetch distance ahead of the page being loaded
 
 enum {
-  BAR_FULL = 0,                     // kStages
-  BAR_EMPTY = BAR_FULL + kStages,   // kStages
-  BAR_Q_FULL = BAR_EMPTY + kStages,
+  BAR_FULL = 0,                     // kSlots
+  BAR_EMPTY = BAR_FULL + kSlots,    // kSlots
+  BAR_Q_FULL = BAR_EMPTY + kSlots,
   BAR_Q_EMPTY,
   BAR_QT_FULL,
-  BAR_S_FULL,                       // 2
-  BAR_S_EMPTY = BAR_S_FULL + 2,     // 2
-  BAR_P_FULL = BAR_S_EMPTY + 2,
-  BAR_P_EMPTY,
-  BAR_O_EMPTY,
-  BAR_XFULL,                        // 2: the peer's partial landed in my receive buffer
-  BAR_XFREE = BAR_XFULL + 2,        // 2: the peer has read the partial I wrote into it
-  BAR_FINAL = BAR_XFREE + 2,
+  BAR_S_FULL,
+  BAR_S_EMPTY,
+  BAR_P_FULL,                       // 2
+  BAR_P_EMPTY = BAR_P_FULL + 2,     // 2
+  BAR_O_EMPTY = BAR_P_EMPTY + 2,
+  BAR_FINAL,
   kNumBars
 };
 static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
+
+// Box order within a page: the five boxes this CTA only needs for Q K^T first
+// (their slots are released right after the MMAs), then the four latent
+// boxes whose columns it accumulates in P V (held until P V).  With 9 boxes
+// per page and 18 slots, box k of page i reuses the slot of box k of page
+// i-2, released by Q K^T(i-2) or P V(i-2), both issued before Q K^T(i).
+__device__ __forceinline__ int box_order(int half, int k) {
+  if (k == 4) return 8;
+  if (half == 0) return k < 4 ? 4 + k : k - 5;
+  return k < 4 ? k : k - 1;
+}
 
 struct FastArgs {
   const __nv_bfloat16* q_lat;
@@ -111,10 +118,9 @@ struct FastArgs {
 
 struct Shared {
   uint32_t base;
-  __device__ uint32_t qrope() const { return base + kSmemQRope; }
-  __device__ uint32_t p() const { return base + kSmemP; }
-  __device__ uint32_t recv(int b) const { return base + kSmemRecv + b * kRecvBytes; }
-  __device__ uint32_t slot(int s) const { return base + kSmemRing + s * kSlotBytes; }
+  __device__ uint32_t q(int box) const { return base + kSmemQ + (box - kQTmemBoxes) * kQBoxBytes; }
+  __device__ uint32_t p(int b) const { return base + kSmemP + b * kPBytes; }
+  __device__ uint32_t slot(int s) const { return base + kSmemRing + s * kBoxBytes; }
   __device__ uint32_t bar(int i) const { return base + kSmemBar + i * 8; }
 };
 
@@ -124,8 +130,9 @@ __device__ __forceinline__ void fail(int* hdr, volatile int* abort_flag, int whe
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_sm103_kernel(const __grid_constant__ CUtensorMap tm_qpe, const __grid_constant__ CUtensorMap tm_ckv,
-                        const __grid_constant__ CUtensorMap tm_kpe, FastArgs a, char* ws) {
+    decode_sm103_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_constant__ CUtensorMap tm_qpe,
+                        const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
+                        FastArgs a, char* ws) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Shared sh{smem_addr(smem)};
@@ -140,32 +147,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int half = (int)cluster_ctarank();
-  const int peer = half ^ 1;
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
   const int num_ranges = hdr[MLA_HDR_NUM_RANGES];
   const int R = a.T * a.H;
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kSlots; ++i) {
       mbar_init(sh.bar(BAR_FULL + i), 1);
       mbar_init(sh.bar(BAR_EMPTY + i), 1);
     }
     mbar_init(sh.bar(BAR_Q_FULL), 1);
     mbar_init(sh.bar(BAR_Q_EMPTY), 1);
     mbar_init(sh.bar(BAR_QT_FULL), 128);
+    mbar_init(sh.bar(BAR_S_FULL), 1);
+    mbar_init(sh.bar(BAR_S_EMPTY), 128);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(sh.bar(BAR_S_FULL + i), 1);
-      mbar_init(sh.bar(BAR_S_EMPTY + i), 128);
-      mbar_init(sh.bar(BAR_XFULL + i), 128);
-      mbar_init(sh.bar(BAR_XFREE + i), 128);
+      mbar_init(sh.bar(BAR_P_FULL + i), 128);
+      mbar_init(sh.bar(BAR_P_EMPTY + i), 1);
     }
-    mbar_init(sh.bar(BAR_P_FULL), 128);
-    mbar_init(sh.bar(BAR_P_EMPTY), 1);
     mbar_init(sh.bar(BAR_O_EMPTY), 128);
     mbar_init(sh.bar(BAR_FINAL), 1);
     *abort_flag = 0;
     fence_mbar_init();
+    prefetch_tmap(&tm_qlat);
     prefetch_tmap(&tm_qpe);
     prefetch_tmap(&tm_ckv);
     prefetch_tmap(&tm_kpe);
@@ -176,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // the peer's barriers are initialised before anyone arrives on them
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
 
@@ -201,18 +206,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int gt = 0, sc = 0;
+      int gbox = 0, sc = 0;
       bool q_in_flight = false, ok = true;
       for (int r = pair; ok && r < num_ranges; r += num_pairs) {
         for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
           const int* rec = seg + (size_t)si * kSegWords;
           const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3];
-          if (half == 0) {
-            if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
-            mbar_arrive_expect_tx(sh.bar(BAR_Q_FULL), kQBoxBytes);
-            tma_load_2d(sh.qrope(), &tm_qpe, sh.bar(BAR_Q_FULL), 0, b * R + rb * kRowsPerBlock);
-            q_in_flight = true;
-          }
+          if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
+          const int row0 = b * R + rb * kRowsPerBlock;
+          mbar_arrive_expect_tx(sh.bar(BAR_Q_FULL), kQSmemBoxes * kQBoxBytes);
+          for (int box = kQTmemBoxes; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_FULL), 64 * box, row0);
+          tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_FULL), 0, row0);
+          q_in_flight = true;
           // Pages further ahead than the ring are pulled into L2 (CTA 0 does it for the pair).
           auto prefetch_page = [&](int pp) {
             if (half != 0 || pp >= p1) return;
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           };
           for (int pp = p0; pp < p0 + kPrefetchPages; ++pp) prefetch_page(pp);
-          for (int p = p0; p < p1; ++p, ++gt) {
+          for (int p = p0; ok && p < p1; ++p) {
             prefetch_page(p + kPrefetchPages);
             int blk = a.block_table[(size_t)b * a.bt_stride + p];
             if (blk < 0 || blk >= a.num_blocks) {
@@ -234,23 +239,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | p);
               blk = -1;
             }
-            const int st = gt % kStages;
-            if (!mbar_wait(sh.bar(BAR_EMPTY + st), ((gt / kStages) & 1) ^ 1, abort_flag)) {
-              fail(hdr, abort_flag, 11); ok = false; break;
+            for (int k = 0; k < kBoxes; ++k, ++gbox) {
+              const int s = gbox % kSlots;
+              if (!mbar_wait(sh.bar(BAR_EMPTY + s), ((gbox / kSlots) & 1) ^ 1, abort_flag)) {
+                fail(hdr, abort_flag, 11); ok = false; break;
+              }
+              mbar_arrive_expect_tx(sh.bar(BAR_FULL + s), kBoxBytes);
+              const int box = box_order(half, k);
+              if (box < 8) tma_load_3d(sh.slot(s), &tm_ckv, sh.bar(BAR_FULL + s), 64 * box, 0, blk);
+              else tma_load_3d(sh.slot(s), &tm_kpe, sh.bar(BAR_FULL + s), 0, 0, blk);
             }
-            mbar_arrive_expect_tx(sh.bar(BAR_FULL + st), (half == 0 ? 5 : 4) * kBoxBytes);
-            for (int j = 0; j < kOwnBoxes; ++j)
-              tma_load_3d(sh.slot(st) + j * kBoxBytes, &tm_ckv, sh.bar(BAR_FULL + st), 64 * (kOwnBoxes * half + j), 0, blk);
-            if (half == 0) tma_load_3d(sh.slot(st) + kOwnBoxes * kBoxBytes, &tm_kpe, sh.bar(BAR_FULL + st), 0, 0, blk);
           }
           ++sc;
         }
       }
       // Drain: every load issued must have landed before the CTA may exit.
-      const int first = gt > kStages ? gt - kStages : 0;
-      for (int g = first; g < gt; ++g) {
+      const int first = gbox > kSlots ? gbox - kSlots : 0;
+      for (int g = first; g < gbox; ++g) {
         volatile int never = 0;
-        mbar_wait(sh.bar(BAR_FULL + g % kStages), (g / kStages) & 1, &never);
+        mbar_wait(sh.bar(BAR_FULL + g % kSlots), (g / kSlots) & 1, &never);
       }
       if (q_in_flight) {
         volatile int never = 0;
@@ -262,67 +269,78 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(128, 64, 0);
-      const uint32_t id_pv = idesc_bf16_f32(128, 256, 1);
+      const uint32_t id_pv = idesc_bf16_f32(128, 64, 1);
       // Descriptors are built once; steps only move the start-address field (16-byte
-      // units): +2 per 32-byte K step of a K-major tile, +128 per 16-row K step of
-      // the MN-major value tile, +kBoxBytes/16 per box, +kSlotBytes/16 per slot.
+      // units): +2 per 32-byte K step of a K-major tile, +128 per 16-row K step of an
+      // MN-major value box, +kBoxBytes/16 per ring slot, +kPBytes/16 per P buffer.
+      uint64_t qdesc[kQSmemBoxes];
+#pragma unroll
+      for (int bx = 0; bx < kQSmemBoxes; ++bx) qdesc[bx] = sw128_desc(sh.q(kQTmemBoxes + bx), 16, 1024);
       const uint64_t kdesc0 = sw128_desc(sh.slot(0), 16, 1024);
       const uint64_t vdesc0 = sw128_desc(sh.slot(0), kBoxBytes, 1024);
-      const uint64_t pdesc = sw128_desc(sh.p(), 16, 1024);
-      const uint64_t rdesc = sw128_desc(sh.qrope(), 16, 1024);
-      int ti = 0, sc = 0;
+      const uint64_t pdesc0 = sw128_desc(sh.p(0), 16, 1024);
+      int gbox = 0, ti = 0, sc = 0;
       bool ok = true;
-      auto issue_pv = [&](int t, bool first_of_seg) -> bool {
+      int own[4] = {0, 0, 0, 0}, own_prev[4] = {0, 0, 0, 0};
+      auto issue_pv = [&](int t, const int (&slots)[4], bool first_of_seg) -> bool {
         if (first_of_seg && sc > 0) {
           if (!mbar_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 20); return false; }
         }
-        if (!mbar_wait(sh.bar(BAR_P_FULL), t & 1, abort_flag)) { fail(hdr, abort_flag, 21); return false; }
+        const int pb = t & 1;
+        if (!mbar_wait(sh.bar(BAR_P_FULL + pb), (t >> 1) & 1, abort_flag)) { fail(hdr, abort_flag, 21); return false; }
         tc_fence_after();
-        const int st = t % kStages;
-        const uint64_t vd = vdesc0 + (uint64_t)(st * (kSlotBytes >> 4));
+        const uint64_t pd = pdesc0 + (uint64_t)(pb * (kPBytes >> 4));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16(tmem + kTmemO, pdesc + 2 * kk, vd + 128 * kk, id_pv, (first_of_seg && kk == 0) ? 0u : 1u);
-        mma_commit(sh.bar(BAR_EMPTY + st));
-        mma_commit(sh.bar(BAR_P_EMPTY));
+        for (int c = 0; c < kOwnBoxes; ++c) {
+          const uint64_t vd = vdesc0 + (uint64_t)(slots[c] * (kBoxBytes >> 4));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem + kTmemO + 64 * c, pd + 2 * kk, vd + 128 * kk, id_pv, (first_of_seg && kk == 0) ? 0u : 1u);
+          mma_commit(sh.bar(BAR_EMPTY + slots[c]));
+        }
+        mma_commit(sh.bar(BAR_P_EMPTY + pb));
         return true;
       };
       for (int r = pair; ok && r < num_ranges; r += num_pairs) {
         for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
           const int* rec = seg + (size_t)si * kSegWords;
           const int n_tiles = rec[3] - rec[2];
-          if ((half == 0 && !mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag)) ||
-              !mbar_wait(sh.bar(BAR_QT_FULL), sc & 1, abort_flag)) {
+          if (!mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag) || !mbar_wait(sh.bar(BAR_QT_FULL), sc & 1, abort_flag)) {
             fail(hdr, abort_flag, 22); ok = false; break;
           }
           tc_fence_after();
           for (int i = 0; ok && i < n_tiles; ++i, ++ti) {
-            const int buf = ti & 1;
-            const int st = ti % kStages;
-            if (!mbar_wait(sh.bar(BAR_S_EMPTY + buf), ((ti >> 1) & 1) ^ 1, abort_flag) ||
-                !mbar_wait(sh.bar(BAR_FULL + st), (ti / kStages) & 1, abort_flag)) {
-              fail(hdr, abort_flag, 23); ok = false; break;
-            }
+            // S is single-buffered: the softmax releases it right after reading it.
+            if (!mbar_wait(sh.bar(BAR_S_EMPTY), (ti & 1) ^ 1, abort_flag)) { fail(hdr, abort_flag, 23); ok = false; break; }
             tc_fence_after();
-            const uint32_t d = tmem + kTmemS + 64 * buf;
-            const uint64_t kd = kdesc0 + (uint64_t)(st * (kSlotBytes >> 4));
+            const uint32_t d = tmem + kTmemS;
+            for (int k = 0; k < kBoxes; ++k, ++gbox) {
+              const int s = gbox % kSlots;
+              if (!mbar_wait(sh.bar(BAR_FULL + s), (gbox / kSlots) & 1, abort_flag)) {
+                fail(hdr, abort_flag, 24); ok = false; break;
+              }
+              tc_fence_after();
+              const int box = box_order(half, k);
+              const uint64_t bd = kdesc0 + (uint64_t)(s * (kBoxBytes >> 4));
+              if (box < kQTmemBoxes) {
+                const uint32_t at = tmem + kTmemQ + 32 * box;  // 16 bf16 of K = 8 TMEM columns per step
 #pragma unroll
-            for (int j = 0; j < kOwnBoxes; ++j) {
+                for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(d, at + 8 * kk, bd + 2 * kk, id_qk, (k | kk) ? 1u : 0u);
+              } else {
+                const uint64_t ad = qdesc[box - kQTmemBoxes];
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_tmem_a(d, tmem + kTmemQ + 32 * j + 8 * kk, kd + j * (kBoxBytes >> 4) + 2 * kk, id_qk,
-                                (j | kk) ? 1u : 0u);
+                for (int kk = 0; kk < 4; ++kk) mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id_qk, (k | kk) ? 1u : 0u);
+              }
+              if (k < 5) mma_commit(sh.bar(BAR_EMPTY + s));
+              else own[k - 5] = s;
             }
-            if (half == 0) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(d, rdesc + 2 * kk, kd + kOwnBoxes * (kBoxBytes >> 4) + 2 * kk, id_qk, 1u);
-            }
-            mma_commit(sh.bar(BAR_S_FULL + buf));
+            if (!ok) break;
+            mma_commit(sh.bar(BAR_S_FULL));
             if (i == n_tiles - 1) mma_commit(sh.bar(BAR_Q_EMPTY));
-            if (i > 0 && !issue_pv(ti - 1, i == 1)) { ok = false; break; }
+            if (i > 0 && !issue_pv(ti - 1, own_prev, i == 1)) { ok = false; break; }
+            for (int c = 0; c < 4; ++c) own_prev[c] = own[c];
           }
-          if (ok && n_tiles > 0 && !issue_pv(ti - 1, n_tiles == 1)) ok = false;
+          if (ok && n_tiles > 0 && !issue_pv(ti - 1, own_prev, n_tiles == 1)) ok = false;
           ++sc;
         }
       }
@@ -333,13 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ exchange + softmax + epilogue
+    // ------------------------------------------------------------ softmax + epilogue
     const int row = tid - 128;  // query row within the group == TMEM lane
     const int q4 = warp - 4;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint32_t peer_recv0 = map_to_cta(sh.recv(0), peer);
-    const uint32_t peer_xfull0 = map_to_cta(sh.bar(BAR_XFULL), peer);
-    const uint32_t peer_xfree0 = map_to_cta(sh.bar(BAR_XFREE), peer);
     int ti = 0, sc = 0;
     bool ok = true;
     for (int r = pair; ok && r < num_ranges; r += num_pairs) {
@@ -351,15 +366,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int fr = rb * kRowsPerBlock + row;
         const bool row_valid = fr < R;
         const int limit = row_valid ? visible_limit(S, a.T, fr / a.H, a.causal) : 0;
-        // This CTA's 256 latent query columns go to TMEM (A operand of its Q K^T
-        // partial) once the previous segment's Q K^T MMAs are done with them.
+        // Query columns 0..383 of this row go to TMEM (A operand of Q K^T for boxes
+        // 0..5) once the previous segment's Q K^T MMAs are done with them.
         {
           bool w_ok = sc == 0 || mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 33); ok = false; break; }
           tc_fence_after();
-          const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)b * R + fr) * kDLat + 256 * half);
+          const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)b * R + fr) * kDLat);
 #pragma unroll 1
-          for (int bx = 0; bx < kOwnBoxes; ++bx) {
+          for (int bx = 0; bx < kQTmemBoxes; ++bx) {
             uint32_t qv[32];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -375,67 +390,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         const int n_tiles = p1 - p0;
         for (int i = 0; i < n_tiles; ++i, ++ti) {
-          const int buf = ti & 1;
           const int p = p0 + i;
-          bool w_ok = mbar_wait(sh.bar(BAR_S_FULL + buf), (ti >> 1) & 1, abort_flag);
+          bool w_ok = mbar_wait(sh.bar(BAR_S_FULL), ti & 1, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 30); ok = false; break; }
           tc_fence_after();
-          uint32_t own[64];
+          uint32_t sr[64];
           {
-            uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&own[0]);
-            uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&own[32]);
-            tmem_ld32(t_lane + kTmemS + 64 * buf, lo);
-            tmem_ld32(t_lane + kTmemS + 64 * buf + 32, hi);
+            uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+            uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+            tmem_ld32(t_lane + kTmemS, lo);
+            tmem_ld32(t_lane + kTmemS + 32, hi);
             tmem_wait_ld();
           }
           tc_fence_before();
-          mbar_arrive(sh.bar(BAR_S_EMPTY + buf));
-          // Swap partial tiles with the peer: my row goes into its receive buffer.
-          if (ti >= 2) {
-            w_ok = mbar_wait_cluster(sh.bar(BAR_XFREE + buf), ((ti >> 1) - 1) & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 34); ok = false; break; }
-          }
-          {
-            const uint32_t dst = peer_recv0 + buf * kRecvBytes + row * 256;
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              st_cluster_v4(dst + 16 * e, own[4 * e], own[4 * e + 1], own[4 * e + 2], own[4 * e + 3]);
-            mbar_arrive_remote(peer_xfull0 + 8 * buf);
-          }
-          w_ok = mbar_wait_cluster(sh.bar(BAR_XFULL + buf), (ti >> 1) & 1, abort_flag);
-          if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 35); ok = false; break; }
+          mbar_arrive(sh.bar(BAR_S_EMPTY));
           const int jbase = p * kPage;
           float s[64];
           float tmax = -INFINITY;
-          {
-            const float4* src = reinterpret_cast<const float4*>(smem + kSmemRecv + buf * kRecvBytes + row * 256);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float4 pv = src[e];
-              const float pr[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-              for (int z = 0; z < 4; ++z) {
-                const int j = 4 * e + z;
-                const float mine = __uint_as_float(own[j]);
-                // Both CTAs add partial(CTA 0) + partial(CTA 1): identical bits on both sides.
-                float v = (half == 0 ? mine + pr[z] : pr[z] + mine) * a.scale_log2;
-                v = (jbase + j < limit) ? v : -INFINITY;
-                s[j] = v;
-                tmax = fmaxf(tmax, v);
-              }
-            }
+          for (int j = 0; j < 64; ++j) {
+            float v = __uint_as_float(sr[j]) * a.scale_log2;
+            v = (jbase + j < limit) ? v : -INFINITY;
+            s[j] = v;
+            tmax = fmaxf(tmax, v);
           }
-          mbar_arrive_remote(peer_xfree0 + 8 * buf);  // my receive buffer may be reused
-          if (i > 0) {
-            w_ok = mbar_wait(sh.bar(BAR_P_EMPTY), (ti - 1) & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 31); ok = false; break; }
-            tc_fence_after();
-          }
-          // Lazy rescale of the running state (per row; TMEM access per warp).
+          // Lazy rescale of the running state: needs the accumulator up to date (P V of
+          // the previous page complete); rare once the reference max has settled.
           const bool grow = tmax > m_ref + kRescaleThreshold;
           const float new_ref = grow ? tmax : m_ref;
           const float factor = (grow && m_ref != -INFINITY) ? ex2(m_ref - new_ref) : 1.f;
           if (i > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+            const int t1 = ti - 1;
+            w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + (t1 & 1)), (t1 >> 1) & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 31); ok = false; break; }
+            tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < 8; ++c) {
               uint32_t o[32];
@@ -450,9 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= factor;
           m_ref = new_ref;
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          // P buffer ti&1 is free once P V of page ti-2 has completed.
+          const int pb = ti & 1;
+          if (i >= 2) {
+            w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + pb), ((ti >> 1) - 1) & 1, abort_flag);
+            if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 36); ok = false; break; }
+          }
           // P row (bf16) into the 128-byte-swizzled A tile of P V.
           float psum = 0.f;
-          const uint32_t prow = sh.p() + (row >> 3) * 1024 + (row & 7) * 128;
+          const uint32_t prow = sh.p(pb) + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint32_t w[4];
@@ -471,15 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : "memory");
           }
           l += psum;
-          // Rows of the last page past the sequence end are zeroed in this CTA's
-          // four value boxes before P V reads them.
+          // Rows of the last page past the sequence end are zeroed in the four value
+          // boxes of this page (ring slots of its boxes 5..8) before P V reads them.
           const int valid = S - jbase;
           if (valid < kPage) {
-            const uint32_t slot = sh.slot(ti % kStages);
             for (int idx = row; idx < kOwnBoxes * kPage; idx += 128) {
               const int c = idx / kPage, rr = idx % kPage;
               if (rr >= valid) {
-                const uint32_t dst = slot + c * kBoxBytes + rr * 128;
+                const uint32_t dst = sh.slot((kBoxes * ti + 5 + c) % kSlots) + rr * 128;
 #pragma unroll
                 for (int z = 0; z < 8; ++z)
                   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst + 16 * z), "r"(0) : "memory");
@@ -488,12 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_proxy_async_smem();
           tc_fence_before();
-          mbar_arrive(sh.bar(BAR_P_FULL));
+          mbar_arrive(sh.bar(BAR_P_FULL + pb));
         }
         if (!ok) break;
         // Epilogue: wait for the last P V, then normalise and store this CTA's columns.
         {
-          const bool w_ok = mbar_wait(sh.bar(BAR_P_EMPTY), (ti - 1) & 1, abort_flag);
+          const int tl = ti - 1;
+          const bool w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + (tl & 1)), (tl >> 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 32); ok = false; break; }
           tc_fence_after();
         }
@@ -542,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // the peer has finished writing into this CTA's shared memory
+  cluster_sync_all();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
@@ -630,7 +624,13 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
                                 const int32_t* block_table, int bt_stride, const int32_t* seq_lens, int checked,
                                 __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st) {
   const long long rows_total = (long long)b->B * b->T * g->H;
-  CUtensorMap m_qpe, m_ckv, m_kpe;
+  CUtensorMap m_qlat, m_qpe, m_ckv, m_kpe;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)kDLat, (cuuint64_t)rows_total};
+    const cuuint64_t str[1] = {(cuuint64_t)kDLat * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!make_map(&m_qlat, q_lat, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
   {
     const cuuint64_t dims[2] = {(cuuint64_t)kDRope, (cuuint64_t)rows_total};
     const cuuint64_t str[1] = {(cuuint64_t)kDRope * 2};
@@ -667,7 +667,7 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   cluster_launch_config(&cfg, attr, pairs, st);
-  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel, m_qpe, m_ckv, m_kpe, a, reinterpret_cast<char*>(ws));
+  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel, m_qlat, m_qpe, m_ckv, m_kpe, a, reinterpret_cast<char*>(ws));
 }
 
 }  // namespace mla
