@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(128, 64, 0);
-      const uint32_t id_pv = idesc_bf16_f32(128, 64, 1);
+      const uint32_t id_pv = idesc_bf16_f32(128, 256, 1);
       // Descriptors are built once; steps only move the start-address field (16-byte
       // units): +2 per 32-byte K step of a K-major tile, +128 per 16-row K step of an
       // MN-major value box, +kBoxBytes/16 per ring slot, +kPBytes/16 per P buffer.
@@ -281,24 +281,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pdesc0 = sw128_desc(sh.p(0), 16, 1024);
       int gbox = 0, ti = 0, sc = 0;
       bool ok = true;
-      int own[4] = {0, 0, 0, 0}, own_prev[4] = {0, 0, 0, 0};
-      auto issue_pv = [&](int t, const int (&slots)[4], bool first_of_seg) -> bool {
+      // P V of page t: the page's four value boxes sit in consecutive ring slots
+      // (slot = (9 t + 5 + c) mod 18 and 18 = 2 x 9), so one N=256 MMA per K step
+      // covers them with the 64-column blocks kBoxBytes apart.
+      auto pv_body = [&](int t, bool first_of_seg) {
+        const int pb = t & 1;
+        const int s0 = (kBoxes * t + 5) % kSlots;
+        const uint64_t pd = pdesc0 + (uint64_t)(pb * (kPBytes >> 4));
+        const uint64_t vd = vdesc0 + (uint64_t)(s0 * (kBoxBytes >> 4));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(tmem + kTmemO, pd + 2 * kk, vd + 128 * kk, id_pv, (first_of_seg && kk == 0) ? 0u : 1u);
+#pragma unroll
+        for (int c = 0; c < kOwnBoxes; ++c) mma_commit(sh.bar(BAR_EMPTY + s0 + c));
+        mma_commit(sh.bar(BAR_P_EMPTY + pb));
+      };
+      auto issue_pv = [&](int t, bool first_of_seg) -> bool {
         if (first_of_seg && sc > 0) {
           if (!mbar_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 20); return false; }
         }
-        const int pb = t & 1;
-        if (!mbar_wait(sh.bar(BAR_P_FULL + pb), (t >> 1) & 1, abort_flag)) { fail(hdr, abort_flag, 21); return false; }
+        if (!mbar_wait(sh.bar(BAR_P_FULL + (t & 1)), (t >> 1) & 1, abort_flag)) { fail(hdr, abort_flag, 21); return false; }
         tc_fence_after();
-        const uint64_t pd = pdesc0 + (uint64_t)(pb * (kPBytes >> 4));
-#pragma unroll
-        for (int c = 0; c < kOwnBoxes; ++c) {
-          const uint64_t vd = vdesc0 + (uint64_t)(slots[c] * (kBoxBytes >> 4));
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem + kTmemO + 64 * c, pd + 2 * kk, vd + 128 * kk, id_pv, (first_of_seg && kk == 0) ? 0u : 1u);
-          mma_commit(sh.bar(BAR_EMPTY + slots[c]));
-        }
-        mma_commit(sh.bar(BAR_P_EMPTY + pb));
+        pv_body(t, first_of_seg);
         return true;
       };
       for (int r = pair; ok && r < num_ranges; r += num_pairs) {
@@ -314,6 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(sh.bar(BAR_S_EMPTY), (ti & 1) ^ 1, abort_flag)) { fail(hdr, abort_flag, 23); ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem + kTmemS;
+            // P V of the previous page is slotted in between Q K^T boxes as soon as its
+            // P is ready, so its value slots are released (and refilled) early.
+            bool pv_pending = i > 0;
             for (int k = 0; k < kBoxes; ++k, ++gbox) {
               const int s = gbox % kSlots;
               if (!mbar_wait(sh.bar(BAR_FULL + s), (gbox / kSlots) & 1, abort_flag)) {
@@ -332,15 +339,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < 4; ++kk) mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id_qk, (k | kk) ? 1u : 0u);
               }
               if (k < 5) mma_commit(sh.bar(BAR_EMPTY + s));
-              else own[k - 5] = s;
+              if (pv_pending && !(i == 1 && sc > 0) && mbar_try_wait(sh.bar(BAR_P_FULL + ((ti - 1) & 1)), ((ti - 1) >> 1) & 1)) {
+                tc_fence_after();
+                pv_body(ti - 1, i == 1);
+                pv_pending = false;
+              }
             }
             if (!ok) break;
             mma_commit(sh.bar(BAR_S_FULL));
             if (i == n_tiles - 1) mma_commit(sh.bar(BAR_Q_EMPTY));
-            if (i > 0 && !issue_pv(ti - 1, own_prev, i == 1)) { ok = false; break; }
-            for (int c = 0; c < 4; ++c) own_prev[c] = own[c];
+            if (pv_pending && !issue_pv(ti - 1, i == 1)) { ok = false; break; }
           }
-          if (ok && n_tiles > 0 && !issue_pv(ti - 1, own_prev, n_tiles == 1)) ok = false;
+          if (ok && n_tiles > 0 && !issue_pv(ti - 1, n_tiles == 1)) ok = false;
           ++sc;
         }
       }
