@@ -59,12 +59,14 @@ constexpr int kBoxes = 9;                      // 8 latent boxes + 1 RoPE box pe
 constexpr int kOwnBoxes = 4;                   // latent boxes whose columns this CTA accumulates
 constexpr int kQTmemBoxes = 6;                 // query boxes 0..5 live in TMEM
 constexpr int kQSmemBoxes = kBoxes - kQTmemBoxes;
-constexpr int kSlots = 18;
+constexpr int kStages = 2;                     // page stages in the ring
+constexpr int kGroupABoxes = 5;                // boxes only Q K^T needs (released after it)
+constexpr int kStageBytes = kBoxes * kBoxBytes;  // group A (5 boxes) then group B (4 value boxes)
 constexpr int kPBytes = 128 * 64 * 2;          // one P tile, bf16
 constexpr int kSmemQ = 0;
 constexpr int kSmemP = kSmemQ + kQSmemBoxes * kQBoxBytes;  // 49152
 constexpr int kSmemRing = kSmemP + 2 * kPBytes;            // 81920
-constexpr int kSmemBar = kSmemRing + kSlots * kBoxBytes;   // 229376
+constexpr int kSmemBar = kSmemRing + kStages * kStageBytes; // 229376
 constexpr int kSmemBytes = kSmemBar + 1024;
 constexpr int kSmemAlloc = kSmemBytes + 1024;              // slack to align the base to 1024 B
 constexpr uint32_t kTmemCols = 512;
@@ -75,9 +77,11 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kPrefetchPages = 3;          // L2 prefetch distance ahead of the page being loaded
 
 enum {
-  BAR_FULL = 0,                     // kSlots
-  BAR_EMPTY = BAR_FULL + kSlots,    // kSlots
-  BAR_Q_FULL = BAR_EMPTY + kSlots,
+  BAR_FULL_A = 0,                   // kStages: group A of a page landed
+  BAR_EMPTY_A = BAR_FULL_A + kStages,  // kStages: Q K^T done with group A
+  BAR_FULL_B = BAR_EMPTY_A + kStages,  // kStages: group B (value boxes) landed
+  BAR_EMPTY_B = BAR_FULL_B + kStages,  // kStages: P V done with group B
+  BAR_Q_FULL = BAR_EMPTY_B + kStages,
   BAR_Q_EMPTY,
   BAR_QT_FULL,
   BAR_S_FULL,
@@ -90,16 +94,16 @@ enum {
 };
 static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
 
-// Box order within a page: the five boxes this CTA only needs for Q K^T first
-// (their slots are released right after the MMAs), then the four latent
-// boxes whose columns it accumulates in P V (held until P V).  With 9 boxes
-// per page and 18 slots, box k of page i reuses the slot of box k of page
-// i-2, released by Q K^T(i-2) or P V(i-2), both issued before Q K^T(i).
-__device__ __forceinline__ int box_order(int half, int k) {
-  if (k == 4) return 8;
-  if (half == 0) return k < 4 ? 4 + k : k - 5;
-  return k < 4 ? k : k - 1;
-}
+// A page is staged as two groups of 64 x 64 boxes: group A holds the five
+// boxes this CTA needs only for Q K^T (the other CTA's four latent boxes and
+// the RoPE box), released as soon as those MMAs complete; group B holds the
+// four latent boxes whose columns this CTA accumulates, contiguous so that one
+// N=256 MMA per K step covers them in P V, and released after P V.  Box order
+// (by 64-column box index of the cached row; 8 = RoPE):
+template <int HALF> struct Boxes {
+  static constexpr int a(int j) { return j == 4 ? 8 : (HALF == 0 ? 4 + j : j); }
+  static constexpr int b(int c) { return 4 * HALF + c; }
+};
 
 struct FastArgs {
   const __nv_bfloat16* q_lat;
@@ -120,13 +124,109 @@ struct Shared {
   uint32_t base;
   __device__ uint32_t q(int box) const { return base + kSmemQ + (box - kQTmemBoxes) * kQBoxBytes; }
   __device__ uint32_t p(int b) const { return base + kSmemP + b * kPBytes; }
-  __device__ uint32_t slot(int s) const { return base + kSmemRing + s * kBoxBytes; }
+  __device__ uint32_t stage_a(int st) const { return base + kSmemRing + st * kStageBytes; }
+  __device__ uint32_t stage_b(int st) const { return stage_a(st) + kGroupABoxes * kBoxBytes; }
   __device__ uint32_t bar(int i) const { return base + kSmemBar + i * 8; }
 };
+
+// Issue the Q K^T MMAs of one group of boxes: A from TMEM (query boxes 0..5) or
+// shared memory (6..8), B from consecutive 8 KB boxes starting at b0 (descriptor).
+template <int HALF, bool GROUP_B>
+__device__ __forceinline__ void issue_qk_group(uint32_t d, uint32_t tmem, const uint64_t (&qdesc)[kQSmemBoxes],
+                                               uint64_t b0, uint32_t idesc) {
+  constexpr int n = GROUP_B ? kOwnBoxes : kGroupABoxes;
+#pragma unroll
+  for (int j = 0; j < n; ++j) {
+    const int box = GROUP_B ? Boxes<HALF>::b(j) : Boxes<HALF>::a(j);
+    const uint64_t bd = b0 + (uint64_t)(j * (kBoxBytes >> 4));
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint32_t acc = (GROUP_B || j || kk) ? 1u : 0u;
+      if (box < kQTmemBoxes)
+        mma_bf16_tmem_a(d, tmem + kTmemQ + 32 * box + 8 * kk, bd + 2 * kk, idesc, acc);
+      else
+        mma_bf16(d, qdesc[box - kQTmemBoxes] + 2 * kk, bd + 2 * kk, idesc, acc);
+    }
+  }
+}
 
 __device__ __forceinline__ void fail(int* hdr, volatile int* abort_flag, int where) {
   *abort_flag = 1;
   record_error(hdr, MLA_ERR_TIMEOUT, where);
+}
+
+// The single-thread MMA issuer of one CTA (HALF = its rank in the pair).  Per
+// page t: Q K^T over group A, release A, Q K^T over group B -> S; then P V of
+// page t-1 (one N=256 MMA per K step over its group B), release that group B.
+template <int HALF>
+__device__ __forceinline__ void mma_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
+                                         const int* seg, const int* rptr, int pair, int num_pairs, int num_ranges) {
+  const uint32_t id_qk = idesc_bf16_f32(128, 64, 0);
+  const uint32_t id_pv = idesc_bf16_f32(128, 256, 1);
+  // Descriptors are built once; steps only move the start-address field (16-byte
+  // units): +2 per 32-byte K step of a K-major tile, +128 per 16-row K step of an
+  // MN-major value box, +kBoxBytes/16 per box.
+  uint64_t qdesc[kQSmemBoxes];
+#pragma unroll
+  for (int bx = 0; bx < kQSmemBoxes; ++bx) qdesc[bx] = sw128_desc(sh.q(kQTmemBoxes + bx), 16, 1024);
+  // Per-stage / per-buffer descriptors differ only in the start address.
+  const uint64_t adesc0 = sw128_desc(sh.stage_a(0), 16, 1024);
+  const uint64_t bdesc0 = sw128_desc(sh.stage_b(0), 16, 1024);
+  const uint64_t vdesc0 = sw128_desc(sh.stage_b(0), kBoxBytes, 1024);
+  const uint64_t pdesc0 = sw128_desc(sh.p(0), 16, 1024);
+  constexpr uint32_t kStageStep = kStageBytes >> 4, kPStep = kPBytes >> 4;
+  const uint32_t d = tmem + kTmemS;
+  int ti = 0, sc = 0;
+  bool ok = true;
+  auto issue_pv = [&](int t, bool first_of_seg) -> bool {
+    if (first_of_seg && sc > 0) {
+      if (!mbar_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 20); return false; }
+    }
+    const int pb = t & 1, st = t % kStages;
+    if (!mbar_wait(sh.bar(BAR_P_FULL + pb), (t >> 1) & 1, abort_flag)) { fail(hdr, abort_flag, 21); return false; }
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_bf16(tmem + kTmemO, pdesc0 + pb * kPStep + 2 * kk, vdesc0 + st * kStageStep + 128 * kk, id_pv,
+               (first_of_seg && kk == 0) ? 0u : 1u);
+    mma_commit(sh.bar(BAR_EMPTY_B + st));
+    mma_commit(sh.bar(BAR_P_EMPTY + pb));
+    return true;
+  };
+  for (int r = pair; ok && r < num_ranges; r += num_pairs) {
+    for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
+      const int* rec = seg + (size_t)si * kSegWords;
+      const int n_tiles = rec[3] - rec[2];
+      if (!mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag) || !mbar_wait(sh.bar(BAR_QT_FULL), sc & 1, abort_flag)) {
+        fail(hdr, abort_flag, 22); ok = false; break;
+      }
+      tc_fence_after();
+      for (int i = 0; ok && i < n_tiles; ++i, ++ti) {
+        const int st = ti % kStages;
+        const uint32_t par = (ti / kStages) & 1;
+        // S is single-buffered: the softmax releases it right after reading it.
+        if (!mbar_wait(sh.bar(BAR_S_EMPTY), (ti & 1) ^ 1, abort_flag) ||
+            !mbar_wait(sh.bar(BAR_FULL_A + st), par, abort_flag)) {
+          fail(hdr, abort_flag, 23); ok = false; break;
+        }
+        tc_fence_after();
+        issue_qk_group<HALF, false>(d, tmem, qdesc, adesc0 + st * kStageStep, id_qk);
+        mma_commit(sh.bar(BAR_EMPTY_A + st));
+        if (!mbar_wait(sh.bar(BAR_FULL_B + st), par, abort_flag)) { fail(hdr, abort_flag, 24); ok = false; break; }
+        tc_fence_after();
+        issue_qk_group<HALF, true>(d, tmem, qdesc, bdesc0 + st * kStageStep, id_qk);
+        mma_commit(sh.bar(BAR_S_FULL));
+        if (i == n_tiles - 1) mma_commit(sh.bar(BAR_Q_EMPTY));
+        if (i > 0 && !issue_pv(ti - 1, i == 1)) { ok = false; break; }
+      }
+      if (ok && n_tiles > 0 && !issue_pv(ti - 1, n_tiles == 1)) ok = false;
+      ++sc;
+    }
+  }
+  // Wait for every MMA issued so far before TMEM is released.
+  mma_commit(sh.bar(BAR_FINAL));
+  volatile int never = 0;
+  mbar_wait(sh.bar(BAR_FINAL), 0, &never);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -153,9 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int R = a.T * a.H;
 
   if (tid == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(sh.bar(BAR_FULL + i), 1);
-      mbar_init(sh.bar(BAR_EMPTY + i), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(sh.bar(BAR_FULL_A + i), 1);
+      mbar_init(sh.bar(BAR_EMPTY_A + i), 1);
+      mbar_init(sh.bar(BAR_FULL_B + i), 1);
+      mbar_init(sh.bar(BAR_EMPTY_B + i), 1);
     }
     mbar_init(sh.bar(BAR_Q_FULL), 1);
     mbar_init(sh.bar(BAR_Q_EMPTY), 1);
@@ -206,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int gbox = 0, sc = 0;
-      bool q_in_flight = false, ok = true;
+      int gt = 0, sc = 0;
+      bool q_in_flight = false, ok = true, a_only = false;
       for (int r = pair; ok && r < num_ranges; r += num_pairs) {
         for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
           const int* rec = seg + (size_t)si * kSegWords;
@@ -239,25 +341,34 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | p);
               blk = -1;
             }
-            for (int k = 0; k < kBoxes; ++k, ++gbox) {
-              const int s = gbox % kSlots;
-              if (!mbar_wait(sh.bar(BAR_EMPTY + s), ((gbox / kSlots) & 1) ^ 1, abort_flag)) {
-                fail(hdr, abort_flag, 11); ok = false; break;
-              }
-              mbar_arrive_expect_tx(sh.bar(BAR_FULL + s), kBoxBytes);
-              const int box = box_order(half, k);
-              if (box < 8) tma_load_3d(sh.slot(s), &tm_ckv, sh.bar(BAR_FULL + s), 64 * box, 0, blk);
-              else tma_load_3d(sh.slot(s), &tm_kpe, sh.bar(BAR_FULL + s), 0, 0, blk);
+            const int st = gt % kStages;
+            const uint32_t par = ((gt / kStages) & 1) ^ 1;
+            if (!mbar_wait(sh.bar(BAR_EMPTY_A + st), par, abort_flag)) { fail(hdr, abort_flag, 11); ok = false; break; }
+            mbar_arrive_expect_tx(sh.bar(BAR_FULL_A + st), kGroupABoxes * kBoxBytes);
+            for (int j = 0; j < kGroupABoxes; ++j) {
+              const int box = half == 0 ? Boxes<0>::a(j) : Boxes<1>::a(j);
+              const uint32_t dst = sh.stage_a(st) + j * kBoxBytes;
+              if (box < 8) tma_load_3d(dst, &tm_ckv, sh.bar(BAR_FULL_A + st), 64 * box, 0, blk);
+              else tma_load_3d(dst, &tm_kpe, sh.bar(BAR_FULL_A + st), 0, 0, blk);
             }
+            if (!mbar_wait(sh.bar(BAR_EMPTY_B + st), par, abort_flag)) {
+              fail(hdr, abort_flag, 12); ok = false; a_only = true; break;
+            }
+            mbar_arrive_expect_tx(sh.bar(BAR_FULL_B + st), kOwnBoxes * kBoxBytes);
+            for (int c = 0; c < kOwnBoxes; ++c)
+              tma_load_3d(sh.stage_b(st) + c * kBoxBytes, &tm_ckv, sh.bar(BAR_FULL_B + st), 64 * (4 * half + c), 0, blk);
+            ++gt;
           }
           ++sc;
         }
       }
-      // Drain: every load issued must have landed before the CTA may exit.
-      const int first = gbox > kSlots ? gbox - kSlots : 0;
-      for (int g = first; g < gbox; ++g) {
+      // Drain: every load issued must have landed before the CTA may exit (a page
+      // whose group B was not issued after a failure is covered by its group A wait).
+      const int first = gt > kStages ? gt - kStages : 0;
+      for (int g = first; g < gt + (a_only ? 1 : 0); ++g) {
         volatile int never = 0;
-        mbar_wait(sh.bar(BAR_FULL + g % kSlots), (g / kSlots) & 1, &never);
+        mbar_wait(sh.bar(BAR_FULL_A + g % kStages), (g / kStages) & 1, &never);
+        if (g < gt) mbar_wait(sh.bar(BAR_FULL_B + g % kStages), (g / kStages) & 1, &never);
       }
       if (q_in_flight) {
         volatile int never = 0;
@@ -268,96 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t id_qk = idesc_bf16_f32(128, 64, 0);
-      const uint32_t id_pv = idesc_bf16_f32(128, 256, 1);
-      // Descriptors are built once; steps only move the start-address field (16-byte
-      // units): +2 per 32-byte K step of a K-major tile, +128 per 16-row K step of an
-      // MN-major value box, +kBoxBytes/16 per ring slot, +kPBytes/16 per P buffer.
-      uint64_t qdesc[kQSmemBoxes];
-#pragma unroll
-      for (int bx = 0; bx < kQSmemBoxes; ++bx) qdesc[bx] = sw128_desc(sh.q(kQTmemBoxes + bx), 16, 1024);
-      const uint64_t kdesc0 = sw128_desc(sh.slot(0), 16, 1024);
-      const uint64_t vdesc0 = sw128_desc(sh.slot(0), kBoxBytes, 1024);
-      const uint64_t pdesc0 = sw128_desc(sh.p(0), 16, 1024);
-      int gbox = 0, ti = 0, sc = 0;
-      bool ok = true;
-      // P V of page t: the page's four value boxes sit in consecutive ring slots
-      // (slot = (9 t + 5 + c) mod 18 and 18 = 2 x 9), so one N=256 MMA per K step
-      // covers them with the 64-column blocks kBoxBytes apart.
-      auto pv_body = [&](int t, bool first_of_seg) {
-        const int pb = t & 1;
-        const int s0 = (kBoxes * t + 5) % kSlots;
-        const uint64_t pd = pdesc0 + (uint64_t)(pb * (kPBytes >> 4));
-        const uint64_t vd = vdesc0 + (uint64_t)(s0 * (kBoxBytes >> 4));
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16(tmem + kTmemO, pd + 2 * kk, vd + 128 * kk, id_pv, (first_of_seg && kk == 0) ? 0u : 1u);
-#pragma unroll
-        for (int c = 0; c < kOwnBoxes; ++c) mma_commit(sh.bar(BAR_EMPTY + s0 + c));
-        mma_commit(sh.bar(BAR_P_EMPTY + pb));
-      };
-      auto issue_pv = [&](int t, bool first_of_seg) -> bool {
-        if (first_of_seg && sc > 0) {
-          if (!mbar_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 20); return false; }
-        }
-        if (!mbar_wait(sh.bar(BAR_P_FULL + (t & 1)), (t >> 1) & 1, abort_flag)) { fail(hdr, abort_flag, 21); return false; }
-        tc_fence_after();
-        pv_body(t, first_of_seg);
-        return true;
-      };
-      for (int r = pair; ok && r < num_ranges; r += num_pairs) {
-        for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
-          const int* rec = seg + (size_t)si * kSegWords;
-          const int n_tiles = rec[3] - rec[2];
-          if (!mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag) || !mbar_wait(sh.bar(BAR_QT_FULL), sc & 1, abort_flag)) {
-            fail(hdr, abort_flag, 22); ok = false; break;
-          }
-          tc_fence_after();
-          for (int i = 0; ok && i < n_tiles; ++i, ++ti) {
-            // S is single-buffered: the softmax releases it right after reading it.
-            if (!mbar_wait(sh.bar(BAR_S_EMPTY), (ti & 1) ^ 1, abort_flag)) { fail(hdr, abort_flag, 23); ok = false; break; }
-            tc_fence_after();
-            const uint32_t d = tmem + kTmemS;
-            // P V of the previous page is slotted in between Q K^T boxes as soon as its
-            // P is ready, so its value slots are released (and refilled) early.
-            bool pv_pending = i > 0;
-            for (int k = 0; k < kBoxes; ++k, ++gbox) {
-              const int s = gbox % kSlots;
-              if (!mbar_wait(sh.bar(BAR_FULL + s), (gbox / kSlots) & 1, abort_flag)) {
-                fail(hdr, abort_flag, 24); ok = false; break;
-              }
-              tc_fence_after();
-              const int box = box_order(half, k);
-              const uint64_t bd = kdesc0 + (uint64_t)(s * (kBoxBytes >> 4));
-              if (box < kQTmemBoxes) {
-                const uint32_t at = tmem + kTmemQ + 32 * box;  // 16 bf16 of K = 8 TMEM columns per step
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(d, at + 8 * kk, bd + 2 * kk, id_qk, (k | kk) ? 1u : 0u);
-              } else {
-                const uint64_t ad = qdesc[box - kQTmemBoxes];
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) mma_bf16(d, ad + 2 * kk, bd + 2 * kk, id_qk, (k | kk) ? 1u : 0u);
-              }
-              if (k < 5) mma_commit(sh.bar(BAR_EMPTY + s));
-              if (pv_pending && !(i == 1 && sc > 0) && mbar_try_wait(sh.bar(BAR_P_FULL + ((ti - 1) & 1)), ((ti - 1) >> 1) & 1)) {
-                tc_fence_after();
-                pv_body(ti - 1, i == 1);
-                pv_pending = false;
-              }
-            }
-            if (!ok) break;
-            mma_commit(sh.bar(BAR_S_FULL));
-            if (i == n_tiles - 1) mma_commit(sh.bar(BAR_Q_EMPTY));
-            if (pv_pending && !issue_pv(ti - 1, i == 1)) { ok = false; break; }
-          }
-          if (ok && n_tiles > 0 && !issue_pv(ti - 1, n_tiles == 1)) ok = false;
-          ++sc;
-        }
-      }
-      // Wait for every MMA issued so far before TMEM is released.
-      mma_commit(sh.bar(BAR_FINAL));
-      volatile int never = 0;
-      mbar_wait(sh.bar(BAR_FINAL), 0, &never);
+      if (half == 0) mma_role<0>(sh, tmem, hdr, abort_flag, seg, rptr, pair, num_pairs, num_ranges);
+      else mma_role<1>(sh, tmem, hdr, abort_flag, seg, rptr, pair, num_pairs, num_ranges);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -476,13 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           l += psum;
           // Rows of the last page past the sequence end are zeroed in the four value
-          // boxes of this page (ring slots of its boxes 5..8) before P V reads them.
+          // boxes of this page (its group B) before P V reads them.
           const int valid = S - jbase;
           if (valid < kPage) {
             for (int idx = row; idx < kOwnBoxes * kPage; idx += 128) {
               const int c = idx / kPage, rr = idx % kPage;
               if (rr >= valid) {
-                const uint32_t dst = sh.slot((kBoxes * ti + 5 + c) % kSlots) + rr * 128;
+                const uint32_t dst = sh.stage_b(ti % kStages) + c * kBoxBytes + rr * 128;
 #pragma unroll
                 for (int z = 0; z < 8; ++z)
                   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst + 16 * z), "r"(0) : "memory");
