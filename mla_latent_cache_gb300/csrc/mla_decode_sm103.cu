@@ -52,7 +52,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;                  // 2 issue warps, 2 idle, 8 softmax warps
+constexpr int kSoftmaxThreads = 256;
 constexpr int kBoxBytes = 64 * 64 * 2;         // 8 KB: one 64-row page x 64 bf16 columns
 constexpr int kQBoxBytes = 128 * 64 * 2;       // 16 KB: 128 query rows x 64 bf16
 constexpr int kBoxes = 9;                      // 8 latent boxes + 1 RoPE box per row
@@ -67,8 +68,9 @@ constexpr int kSmemQ = 0;
 constexpr int kSmemP = kSmemQ + kQSmemBoxes * kQBoxBytes;  // 49152
 constexpr int kSmemRing = kSmemP + 2 * kPBytes;            // 81920
 constexpr int kSmemBar = kSmemRing + kStages * kStageBytes; // 229376
-constexpr int kSmemBytes = kSmemBar + 1024;
-constexpr int kSmemAlloc = kSmemBytes + 1024;              // slack to align the base to 1024 B
+constexpr int kSmemXchg = kSmemBar + 256;                  // float [2 buffers][2 halves][128 rows]
+constexpr int kSmemBytes = kSmemXchg + 2048;
+constexpr int kSmemAlloc = kSmemBytes + 768;               // slack to align the base to 1024 B (checked)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemS = 256;
@@ -90,9 +92,11 @@ enum {
   BAR_P_EMPTY = BAR_P_FULL + 2,     // 2
   BAR_O_EMPTY = BAR_P_EMPTY + 2,
   BAR_FINAL,
-  kNumBars
+  BAR_XCH,                          // 4: the two softmax warps of a TMEM lane quadrant
+  kNumBars = BAR_XCH + 4
 };
-static_assert(kNumBars * 8 + 16 <= 1024, "barrier area");
+static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
+static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
 
 // A page is staged as two groups of 64 x 64 boxes: group A holds the five
 // boxes this CTA needs only for Q K^T (the other CTA's four latent boxes and
@@ -235,11 +239,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         FastArgs a, char* ws) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  int* hdr = reinterpret_cast<int*>(ws);
+  // The 128-byte-swizzled tiles need a 1024-byte-aligned base; the allocation
+  // carries kSmemAlloc - kSmemBytes bytes of slack for that.  Refuse (uniformly,
+  // before anything is set up) if the slack does not cover the misalignment.
+  if ((uintptr_t)(smem - smem_raw) + kSmemBytes > (uintptr_t)kSmemAlloc) {
+    if (threadIdx.x == 0) record_error(hdr, MLA_ERR_DEVICE_CHECK, -2);
+    return;
+  }
   Shared sh{smem_addr(smem)};
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + kSmemBar + kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemBar + kNumBars * 8 + 4);
 
-  int* hdr = reinterpret_cast<int*>(ws);
   const int* seg = reinterpret_cast<const int*>(ws + a.L.off_segments);
   const int* rptr = reinterpret_cast<const int*>(ws + a.L.off_range_ptr);
   float* part_lse = reinterpret_cast<float*>(ws + a.L.off_part_lse);
@@ -261,15 +272,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(sh.bar(BAR_Q_FULL), 1);
     mbar_init(sh.bar(BAR_Q_EMPTY), 1);
-    mbar_init(sh.bar(BAR_QT_FULL), 128);
+    mbar_init(sh.bar(BAR_QT_FULL), kSoftmaxThreads);
     mbar_init(sh.bar(BAR_S_FULL), 1);
-    mbar_init(sh.bar(BAR_S_EMPTY), 128);
+    mbar_init(sh.bar(BAR_S_EMPTY), kSoftmaxThreads);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(sh.bar(BAR_P_FULL + i), 128);
+      mbar_init(sh.bar(BAR_P_FULL + i), kSoftmaxThreads);
       mbar_init(sh.bar(BAR_P_EMPTY + i), 1);
     }
-    mbar_init(sh.bar(BAR_O_EMPTY), 128);
+    mbar_init(sh.bar(BAR_O_EMPTY), kSoftmaxThreads);
     mbar_init(sh.bar(BAR_FINAL), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(sh.bar(BAR_XCH + i), 64);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_qlat);
@@ -343,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int st = gt % kStages;
             const uint32_t par = ((gt / kStages) & 1) ^ 1;
-            if (!mbar_wait(sh.bar(BAR_EMPTY_A + st), par, abort_flag)) { fail(hdr, abort_flag, 11); ok = false; break; }
+            if (!mbar_wait_backoff(sh.bar(BAR_EMPTY_A + st), par, abort_flag)) { fail(hdr, abort_flag, 11); ok = false; break; }
             mbar_arrive_expect_tx(sh.bar(BAR_FULL_A + st), kGroupABoxes * kBoxBytes);
             for (int j = 0; j < kGroupABoxes; ++j) {
               const int box = half == 0 ? Boxes<0>::a(j) : Boxes<1>::a(j);
@@ -351,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (box < 8) tma_load_3d(dst, &tm_ckv, sh.bar(BAR_FULL_A + st), 64 * box, 0, blk);
               else tma_load_3d(dst, &tm_kpe, sh.bar(BAR_FULL_A + st), 0, 0, blk);
             }
-            if (!mbar_wait(sh.bar(BAR_EMPTY_B + st), par, abort_flag)) {
+            if (!mbar_wait_backoff(sh.bar(BAR_EMPTY_B + st), par, abort_flag)) {
               fail(hdr, abort_flag, 12); ok = false; a_only = true; break;
             }
             mbar_arrive_expect_tx(sh.bar(BAR_FULL_B + st), kOwnBoxes * kBoxBytes);
@@ -385,9 +397,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int row = tid - 128;  // query row within the group == TMEM lane
-    const int q4 = warp - 4;
+    // Two threads per query row: warps 4..7 take score columns 0..31 of their
+    // TMEM lane quadrant, warps 8..11 columns 32..63 (a warp may only touch the
+    // 32 TMEM lanes of quadrant warp % 4).  The row maximum is combined through
+    // shared memory; each thread owns half of the row's P and O columns.
+    const int q4 = warp & 3;
+    const int ch = (warp - 4) >> 2;           // column half
+    const int row = 32 * q4 + lane;           // query row within the group == TMEM lane
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
+    float* xrow = reinterpret_cast<float*>(smem + kSmemXchg);  // [buffer][half][row] partner exchange
+    // Exchange a value with the partner thread of the same row (bounded wait on the
+    // quadrant's mbarrier; double-buffered by exchange parity).
+    int xc = 0;
+    auto swap_with_partner = [&](float v, float* out) -> bool {
+      float* slot = xrow + (xc & 1) * 256;
+      slot[ch * 128 + row] = v;
+      mbar_arrive(sh.bar(BAR_XCH + q4));
+      const bool w = mbar_wait(sh.bar(BAR_XCH + q4), xc & 1, abort_flag);
+      *out = slot[(ch ^ 1) * 128 + row];
+      ++xc;
+      return __all_sync(0xffffffffu, w);
+    };
     int ti = 0, sc = 0;
     bool ok = true;
     for (int r = pair; ok && r < num_ranges; r += num_pairs) {
@@ -400,14 +430,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_valid = fr < R;
         const int limit = row_valid ? visible_limit(S, a.T, fr / a.H, a.causal) : 0;
         // Query columns 0..383 of this row go to TMEM (A operand of Q K^T for boxes
-        // 0..5) once the previous segment's Q K^T MMAs are done with them.
+        // 0..5; this thread stages three of them) once the previous segment's Q K^T
+        // MMAs are done with them.
         {
           bool w_ok = sc == 0 || mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 33); ok = false; break; }
           tc_fence_after();
           const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)b * R + fr) * kDLat);
 #pragma unroll 1
-          for (int bx = 0; bx < kQTmemBoxes; ++bx) {
+          for (int bx = 3 * ch; bx < 3 * ch + 3; ++bx) {
             uint32_t qv[32];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -420,32 +451,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(sh.bar(BAR_QT_FULL));
         }
-        float m_ref = -INFINITY, l = 0.f;
+        float m_ref = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
         const int n_tiles = p1 - p0;
         for (int i = 0; i < n_tiles; ++i, ++ti) {
-          const int p = p0 + i;
+          const int jbase = (p0 + i) * kPage + 32 * ch;   // first cache row of this thread's columns
           bool w_ok = mbar_wait(sh.bar(BAR_S_FULL), ti & 1, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 30); ok = false; break; }
           tc_fence_after();
-          uint32_t sr[64];
-          {
-            uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-            uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-            tmem_ld32(t_lane + kTmemS, lo);
-            tmem_ld32(t_lane + kTmemS + 32, hi);
-            tmem_wait_ld();
-          }
+          uint32_t sr[32];
+          tmem_ld32(t_lane + kTmemS + 32 * ch, sr);
+          tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(sh.bar(BAR_S_EMPTY));
-          const int jbase = p * kPage;
-          float s[64];
+          // Raw-score maximum over the visible columns (the scale is positive).
+          const bool full = jbase + 32 <= limit;
           float tmax = -INFINITY;
+          if (full) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            float v = __uint_as_float(sr[j]) * a.scale_log2;
-            v = (jbase + j < limit) ? v : -INFINITY;
-            s[j] = v;
-            tmax = fmaxf(tmax, v);
+            for (int j = 0; j < 32; ++j) tmax = fmaxf(tmax, __uint_as_float(sr[j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (jbase + j < limit) tmax = fmaxf(tmax, __uint_as_float(sr[j]));
+          }
+          {
+            float other;
+            if (!swap_with_partner(tmax, &other)) { fail(hdr, abort_flag, 37); ok = false; break; }
+            tmax = fmaxf(tmax, other) * a.scale_log2;
           }
           // Lazy rescale of the running state: needs the accumulator up to date (P V of
           // the previous page complete); rare once the reference max has settled.
@@ -458,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 31); ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 4 * ch; c < 4 * ch + 4; ++c) {
               uint32_t o[32];
               tmem_ld32(t_lane + kTmemO + 32 * c, o);
               tmem_wait_ld();
@@ -477,22 +509,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + pb), ((ti >> 1) - 1) & 1, abort_flag);
             if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 36); ok = false; break; }
           }
-          // P row (bf16) into the 128-byte-swizzled A tile of P V.
+          // This thread's 32 P values (bf16) into the 128-byte-swizzled A tile of P V:
+          // p = 2^(s * scale * log2 e - m), 16-byte chunks 4 ch .. 4 ch + 3 of the row.
           float psum = 0.f;
           const uint32_t prow = sh.p(pb) + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int j = 8 * c + 2 * e;
-              const float x0 = s[j] == -INFINITY ? 0.f : ex2(s[j] - m_use);
-              const float x1 = s[j + 1] == -INFINITY ? 0.f : ex2(s[j + 1] - m_use);
+              float x0 = ex2(fmaf(__uint_as_float(sr[j]), a.scale_log2, -m_use));
+              float x1 = ex2(fmaf(__uint_as_float(sr[j + 1]), a.scale_log2, -m_use));
+              if (!full) {
+                x0 = (jbase + j < limit) ? x0 : 0.f;
+                x1 = (jbase + j + 1 < limit) ? x1 : 0.f;
+              }
               psum += x0 + x1;
               const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
               w[e] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            const uint32_t dst = prow + ((c ^ (row & 7)) << 4);
+            const uint32_t dst = prow + (((4 * ch + c) ^ (row & 7)) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
                          "r"(w[3])
                          : "memory");
@@ -500,9 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           l += psum;
           // Rows of the last page past the sequence end are zeroed in the four value
           // boxes of this page (its group B) before P V reads them.
-          const int valid = S - jbase;
+          const int valid = S - (p0 + i) * kPage;
           if (valid < kPage) {
-            for (int idx = row; idx < kOwnBoxes * kPage; idx += 128) {
+            const int t256 = tid - 128;   // 0..255 over the two warpgroups
+            for (int idx = t256; idx < kOwnBoxes * kPage; idx += 256) {
               const int c = idx / kPage, rr = idx % kPage;
               if (rr >= valid) {
                 const uint32_t dst = sh.stage_b(ti % kStages) + c * kBoxBytes + rr * 128;
@@ -517,18 +555,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(sh.bar(BAR_P_FULL + pb));
         }
         if (!ok) break;
-        // Epilogue: wait for the last P V, then normalise and store this CTA's columns.
+        // Epilogue: wait for the last P V, combine the two halves of the row sum,
+        // then normalise and store this thread's 128 output columns.
         {
           const int tl = ti - 1;
           const bool w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + (tl & 1)), (tl >> 1) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 32); ok = false; break; }
           tc_fence_after();
         }
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float l_other;
+        if (!swap_with_partner(l, &l_other)) { fail(hdr, abort_flag, 38); ok = false; break; }
+        const float l_row = ch == 0 ? l + l_other : l_other + l;
+        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const float lse_v = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        const float lse_v = l_row > 0.f ? (m_use + __log2f(l_row)) * 0.69314718055994531f : -INFINITY;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 4 * ch; c < 4 * ch + 4; ++c) {
           uint32_t o[32];
           tmem_ld32(t_lane + kTmemO + 32 * c, o);
           tmem_wait_ld();
@@ -556,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (row_valid && half == 0) {
+        if (row_valid && half == 0 && ch == 0) {
           if (slot_out < 0) a.lse[(size_t)b * R + fr] = lse_v;
           else part_lse[(size_t)slot_out * kRowsPerBlock + row] = lse_v;
         }
