@@ -28,16 +28,18 @@
 // (packed bf16 pairs, the TMEM A operand of Q K^T) at 320..511; the rest of
 // the query tile (latent 384..511 and RoPE) stays in shared memory.
 //
-// Roles per CTA: warp 0 lane 0 issues TMA loads (64 x 64 cache boxes through
-// an 18-slot ring, plus L2 prefetch of pages further ahead), warp 1 lane 0
-// issues the tcgen05 MMAs (Q K^T of page i, then P V of page i-1), warps 4..7
-// (one thread per query row = TMEM lane) run the online softmax, write P
-// (bf16, 128-byte swizzled, double-buffered: the A operand of P V) and the
-// epilogue.  The softmax keeps a per-row reference max and rescales the TMEM
-// accumulator only when the running max grows past it by more than 2^8 (exact
-// for any reference; only rounding differs), with scores in log2 units.
-// Cache rows past the sequence end (last page only) are zeroed in shared
-// memory before P V so stale or NaN contents never reach the accumulator.
+// Roles per CTA (384 threads): warp 0 lane 0 issues TMA loads (each page as
+// two groups of 64 x 64 boxes through a 2-stage ring, plus L2 prefetch of
+// pages further ahead); warp 1 lane 0 issues Q K^T; warp 2 lane 0 issues P V
+// as soon as a P tile is ready (two issuing threads keep the tensor pipe fed
+// despite the per-instruction issue cost); warps 4..11 run the online softmax
+// with two threads per query row (TMEM lane), write P (bf16, 128-byte
+// swizzled, double-buffered: the A operand of P V) and the epilogue.  The
+// softmax keeps a per-row reference max and rescales the TMEM accumulator only
+// when the running max grows past it by more than 2^8 (exact for any
+// reference; only rounding differs), with scores in log2 units.  Cache rows
+// past the sequence end (last page only) are zeroed in shared memory before
+// P V so stale or NaN contents never reach the accumulator.
 //
 // Every wait is bounded; a wait that runs out records MLA_ERR_TIMEOUT in the
 // workspace and raises a CTA-wide abort flag.  Loads and MMAs already issued
@@ -52,7 +54,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 384;                  // 2 issue warps, 2 idle, 8 softmax warps
+constexpr int kThreads = 384;                  // TMA, Q K^T and P V issue warps, 1 idle, 8 softmax warps
 constexpr int kSoftmaxThreads = 256;
 constexpr int kBoxBytes = 64 * 64 * 2;         // 8 KB: one 64-row page x 64 bf16 columns
 constexpr int kQBoxBytes = 128 * 64 * 2;       // 16 KB: 128 query rows x 64 bf16
@@ -92,6 +94,7 @@ enum {
   BAR_P_EMPTY = BAR_P_FULL + 2,     // 2
   BAR_O_EMPTY = BAR_P_EMPTY + 2,
   BAR_FINAL,
+  BAR_FINAL_PV,
   BAR_XCH,                          // 4: the two softmax warps of a TMEM lane quadrant
   kNumBars = BAR_XCH + 4
 };
@@ -159,44 +162,24 @@ __device__ __forceinline__ void fail(int* hdr, volatile int* abort_flag, int whe
   record_error(hdr, MLA_ERR_TIMEOUT, where);
 }
 
-// The single-thread MMA issuer of one CTA (HALF = its rank in the pair).  Per
-// page t: Q K^T over group A, release A, Q K^T over group B -> S; then P V of
-// page t-1 (one N=256 MMA per K step over its group B), release that group B.
+// Q K^T issuer of one CTA (HALF = its rank in the pair), one thread.  Per page t:
+// Q K^T over group A, release A, Q K^T over group B -> S.
 template <int HALF>
-__device__ __forceinline__ void mma_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
-                                         const int* seg, const int* rptr, int pair, int num_pairs, int num_ranges) {
+__device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
+                                        const int* seg, const int* rptr, int pair, int num_pairs, int num_ranges) {
   const uint32_t id_qk = idesc_bf16_f32(128, 64, 0);
-  const uint32_t id_pv = idesc_bf16_f32(128, 256, 1);
   // Descriptors are built once; steps only move the start-address field (16-byte
-  // units): +2 per 32-byte K step of a K-major tile, +128 per 16-row K step of an
-  // MN-major value box, +kBoxBytes/16 per box.
+  // units): +2 per 32-byte K step of a K-major tile, +kBoxBytes/16 per box,
+  // +kStageBytes/16 per stage.
   uint64_t qdesc[kQSmemBoxes];
 #pragma unroll
   for (int bx = 0; bx < kQSmemBoxes; ++bx) qdesc[bx] = sw128_desc(sh.q(kQTmemBoxes + bx), 16, 1024);
-  // Per-stage / per-buffer descriptors differ only in the start address.
   const uint64_t adesc0 = sw128_desc(sh.stage_a(0), 16, 1024);
   const uint64_t bdesc0 = sw128_desc(sh.stage_b(0), 16, 1024);
-  const uint64_t vdesc0 = sw128_desc(sh.stage_b(0), kBoxBytes, 1024);
-  const uint64_t pdesc0 = sw128_desc(sh.p(0), 16, 1024);
-  constexpr uint32_t kStageStep = kStageBytes >> 4, kPStep = kPBytes >> 4;
+  constexpr uint32_t kStageStep = kStageBytes >> 4;
   const uint32_t d = tmem + kTmemS;
   int ti = 0, sc = 0;
   bool ok = true;
-  auto issue_pv = [&](int t, bool first_of_seg) -> bool {
-    if (first_of_seg && sc > 0) {
-      if (!mbar_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 20); return false; }
-    }
-    const int pb = t & 1, st = t % kStages;
-    if (!mbar_wait(sh.bar(BAR_P_FULL + pb), (t >> 1) & 1, abort_flag)) { fail(hdr, abort_flag, 21); return false; }
-    tc_fence_after();
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      mma_bf16(tmem + kTmemO, pdesc0 + pb * kPStep + 2 * kk, vdesc0 + st * kStageStep + 128 * kk, id_pv,
-               (first_of_seg && kk == 0) ? 0u : 1u);
-    mma_commit(sh.bar(BAR_EMPTY_B + st));
-    mma_commit(sh.bar(BAR_P_EMPTY + pb));
-    return true;
-  };
   for (int r = pair; ok && r < num_ranges; r += num_pairs) {
     for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
       const int* rec = seg + (size_t)si * kSegWords;
@@ -221,16 +204,50 @@ __device__ __forceinline__ void mma_role(const Shared& sh, uint32_t tmem, int* h
         issue_qk_group<HALF, true>(d, tmem, qdesc, bdesc0 + st * kStageStep, id_qk);
         mma_commit(sh.bar(BAR_S_FULL));
         if (i == n_tiles - 1) mma_commit(sh.bar(BAR_Q_EMPTY));
-        if (i > 0 && !issue_pv(ti - 1, i == 1)) { ok = false; break; }
       }
-      if (ok && n_tiles > 0 && !issue_pv(ti - 1, n_tiles == 1)) ok = false;
       ++sc;
     }
   }
-  // Wait for every MMA issued so far before TMEM is released.
+  // Wait for every MMA issued by this thread before TMEM is released.
   mma_commit(sh.bar(BAR_FINAL));
   volatile int never = 0;
   mbar_wait(sh.bar(BAR_FINAL), 0, &never);
+}
+
+// P V issuer, one thread: as soon as P of page t is written, O[:, own] += P V over
+// the page's group B (one N=256 MMA per K step), then release group B and P.
+__device__ __forceinline__ void pv_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
+                                        const int* seg, const int* rptr, int pair, int num_pairs, int num_ranges) {
+  const uint32_t id_pv = idesc_bf16_f32(128, 256, 1);
+  const uint64_t vdesc0 = sw128_desc(sh.stage_b(0), kBoxBytes, 1024);
+  const uint64_t pdesc0 = sw128_desc(sh.p(0), 16, 1024);
+  constexpr uint32_t kStageStep = kStageBytes >> 4, kPStep = kPBytes >> 4;
+  int ti = 0, sc = 0;
+  bool ok = true;
+  for (int r = pair; ok && r < num_ranges; r += num_pairs) {
+    for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
+      const int* rec = seg + (size_t)si * kSegWords;
+      const int n_tiles = rec[3] - rec[2];
+      for (int i = 0; i < n_tiles; ++i, ++ti) {
+        if (i == 0 && sc > 0 && !mbar_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag)) {
+          fail(hdr, abort_flag, 20); ok = false; break;
+        }
+        const int pb = ti & 1, st = ti % kStages;
+        if (!mbar_wait(sh.bar(BAR_P_FULL + pb), (ti >> 1) & 1, abort_flag)) { fail(hdr, abort_flag, 21); ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(tmem + kTmemO, pdesc0 + pb * kPStep + 2 * kk, vdesc0 + st * kStageStep + 128 * kk, id_pv,
+                   (i == 0 && kk == 0) ? 0u : 1u);
+        mma_commit(sh.bar(BAR_EMPTY_B + st));
+        mma_commit(sh.bar(BAR_P_EMPTY + pb));
+      }
+      ++sc;
+    }
+  }
+  mma_commit(sh.bar(BAR_FINAL_PV));
+  volatile int never = 0;
+  mbar_wait(sh.bar(BAR_FINAL_PV), 0, &never);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -281,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(sh.bar(BAR_O_EMPTY), kSoftmaxThreads);
     mbar_init(sh.bar(BAR_FINAL), 1);
+    mbar_init(sh.bar(BAR_FINAL_PV), 1);
     for (int i = 0; i < 4; ++i) mbar_init(sh.bar(BAR_XCH + i), 64);
     *abort_flag = 0;
     fence_mbar_init();
@@ -389,11 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ Q K^T issuer
     if (lane == 0) {
-      if (half == 0) mma_role<0>(sh, tmem, hdr, abort_flag, seg, rptr, pair, num_pairs, num_ranges);
-      else mma_role<1>(sh, tmem, hdr, abort_flag, seg, rptr, pair, num_pairs, num_ranges);
+      if (half == 0) qk_role<0>(sh, tmem, hdr, abort_flag, seg, rptr, pair, num_pairs, num_ranges);
+      else qk_role<1>(sh, tmem, hdr, abort_flag, seg, rptr, pair, num_pairs, num_ranges);
     }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ P V issuer
+    if (lane == 0) pv_role(sh, tmem, hdr, abort_flag, seg, rptr, pair, num_pairs, num_ranges);
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
