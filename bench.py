@@ -8,6 +8,13 @@ does not pace the GPU; the decode graph is bracketed by CUDA events on the
 launching stream to time the dominant kernel.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload uniform|tiny|ragged|long|extend] [--T T] [--splits N]
+
+The default workload is the uniform V3 batch; the others (the tiny V2-Lite
+case, the ragged batch, the single 131072-row sequence with --splits N, the
+causal extend batch with --T new rows) print the same JSON line for that
+workload.  A workload whose cache fits in L2 is timed with an L2 flush (a
+256 MB write) between steps, outside the timed events.
 
 Multi-GPU runs are replicas: each rank runs the same independent batch (the
 path shards by request and needs no collective); ``value`` is the tokens of
@@ -30,6 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD_INDEX = 2
+WORKLOADS = {"tiny": 1, "uniform": 2, "ragged": 3, "long": 4, "extend": 5}
 METRIC = "MLA decode tokens/s and achieved HBM GB/s (% of roofline) at V3 geometry"
 L2_BYTES = 129 * 2**20
 
@@ -193,7 +201,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     from mla_latent_cache_gb300 import workloads as W
-    w = W.config_workload(WORKLOAD_INDEX)
+    w = W.config_workload(WORKLOADS[args.workload], T=args.T if args.workload == "extend" else None)
     per_step = []
     samples = []
     for _ in range(args.warmup):
@@ -235,9 +243,11 @@ def run_ours(args):
     from mla_latent_cache_gb300 import workloads as W
     from mla_latent_cache_gb300.runtime import DecodeStep
 
-    w = W.config_workload(WORKLOAD_INDEX)
-    st = DecodeStep(w, device=dev)
+    w = W.config_workload(WORKLOADS[args.workload], T=args.T if args.workload == "extend" else None)
+    st = DecodeStep(w, device=dev, num_splits_override=args.splits)
     stream = torch.cuda.Stream(device=dev)
+    pool_bytes = w.num_blocks * 64 * 576 * 2
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev) if pool_bytes < 2 * L2_BYTES else None
     hbm_peak, tc_peak, peak_kind = _peaks()
     ab = algorithmic_bytes(w)
     fl = algorithmic_flops(w)
@@ -265,26 +275,38 @@ def run_ours(args):
             g_pre.replay(); g_dec.replay(); g_post.replay()
     stream.synchronize()
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    evs = [(ev(), ev()) for _ in range(args.steps)]
+    step_evs = [(ev(), ev()) for _ in range(args.steps)] if flush is not None else None
+    t_start, t_end = ev(), ev()
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         with torch.cuda.stream(stream):
             t_start.record(stream)
             for i in range(args.steps):
+                if flush is not None:
+                    flush.fill_(i & 0xff)          # evict the cache lines of the previous step
+                    step_evs[i][0].record(stream)
                 g_pre.replay()
                 evs[i][0].record(stream)
                 g_dec.replay()
                 evs[i][1].record(stream)
                 g_post.replay()
+                if flush is not None:
+                    step_evs[i][1].record(stream)
             t_end.record(stream)
         stream.synchronize()
     barrier()
     torch.cuda.synchronize()
     total_ms = t_start.elapsed_time(t_end)
     dec_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
-    ms = total_ms / args.steps
+    if flush is not None:
+        ms = sum(a.elapsed_time(b) for a, b in step_evs) / args.steps
+    else:
+        ms = total_ms / args.steps
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -334,18 +356,28 @@ def run_ours(args):
     e2e_value = tokens_per_step / (e2e_ms / 1000.0)
 
     achieved = ab["decode"] / (dec_ms / 1000.0) / 1e9
+    tflops = fl["decode"] / (dec_ms / 1000.0) / 1e12
+    ridge = tc_peak * 1e12 / (hbm_peak * 1e9)
+    if fl["decode"] / ab["decode"] > ridge:
+        roof = {"bound": "tensor", "kernel": "mla_decode (split-KV decode + merge)", "achieved": tflops,
+                "peak": tc_peak, "peak_kind": peak_kind, "unit": "TFLOP/s", "frac": tflops / tc_peak,
+                "traffic": None, "algorithmic_flops": fl["decode"], "decode_ms": dec_ms, "decode_gbs": achieved}
+    else:
+        roof = {"bound": "hbm", "kernel": "mla_decode (split-KV decode + merge)", "achieved": achieved,
+                "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "traffic": profiled_traffic() if WORKLOADS[args.workload] == WORKLOAD_INDEX else None,
+                "algorithmic_bytes": ab["decode"], "decode_ms": dec_ms, "decode_tflops": tflops}
+    l2_note = ("L2 flushed between steps (256 MB write, outside the timed events)" if flush is not None else
+               f"inputs larger than L2: {pool_bytes / 1e6:.0f} MB latent pool vs 129 MB L2")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "H": w.H, "B": w.B, "T": w.T, "S": int(w.seq_lens[0]), "page": 64,
-                   "pool_blocks": w.num_blocks, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2: 302 MB latent pool streamed per step vs 129 MB L2",
-                   "step": "plan + absorb + decode(+merge) + unabsorb, CUDA graphs"},
-        "roofline": {"bound": "hbm", "kernel": "mla_decode (split-KV decode + merge)", "achieved": achieved,
-                     "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "traffic": profiled_traffic(), "algorithmic_bytes": ab["decode"], "decode_ms": dec_ms,
-                     "decode_tflops": fl["decode"] / (dec_ms / 1000.0) / 1e12},
+        "config": {"workload": w.name, "H": w.H, "B": w.B, "T": w.T, "S": int(w.seq_lens[0]),
+                   "S_total": int(np.asarray(w.seq_lens, dtype=np.int64).sum()), "page": 64,
+                   "pool_blocks": w.num_blocks, "parallelism": f"replicas{world}", "splits": args.splits or "auto",
+                   "l2": l2_note, "step": "plan + absorb + decode(+merge) + unabsorb, CUDA graphs"},
+        "roofline": roof,
         "step_hbm_gbs": ab["step"] / (ms / 1000.0) / 1e9,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
@@ -372,6 +404,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of CPU oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS, key=WORKLOADS.get), default="uniform")
+    ap.add_argument("--T", type=int, default=1, help="new rows per sequence (extend workload)")
+    ap.add_argument("--splits", type=int, default=0, help="split count override (0 = the automatic plan)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

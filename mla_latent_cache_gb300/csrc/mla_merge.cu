@@ -14,59 +14,49 @@ namespace mla {
 namespace {
 
 constexpr int kMergeThreads = 256;
-constexpr int kMaxCached = 64;  // partial weights kept in shared memory per row chunk
+constexpr int kBatch = 8;  // partial loads kept in flight per thread
 
-// Merge `count` partials for `nrows` rows of width D starting at partial `first`.
-// part_o rows are addressed as part_o[(first + r) * row_pitch + row * D + c].
-__device__ void merge_rows(const float* part_o, const float* part_lse, size_t o_pitch, size_t lse_pitch,
-                           int first, int count, int nrows, int D, __nv_bfloat16* o_out, float* lse_out) {
-  __shared__ float s_w[kMaxCached];
-  __shared__ float s_inv;
-  __shared__ float s_lse;
-  for (int row = 0; row < nrows; ++row) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float m = -INFINITY;
-      for (int r = 0; r < count; ++r) m = fmaxf(m, part_lse[(size_t)(first + r) * lse_pitch + row]);
-      float l = 0.f;
-      const float m_use = (m == -INFINITY) ? 0.f : m;
-      for (int r = 0; r < count; ++r) {
-        const float x = part_lse[(size_t)(first + r) * lse_pitch + row];
-        const float w = (x == -INFINITY) ? 0.f : __expf(x - m_use);
-        if (r < kMaxCached) s_w[r] = w;
-        l += w;
-      }
-      s_inv = l > 0.f ? 1.f / l : 0.f;
-      s_lse = l > 0.f ? m_use + logf(l) : -INFINITY;
+// Merge four adjacent columns of one row from `count` partials: partial r of
+// those columns starts at part_o[r * o_pitch], its LSE is part_lse[r * lse_pitch].
+// Every thread of a row recomputes the (few) weights from the LSEs (broadcast
+// loads); the loads of kBatch partials are issued before any is used so that
+// the merge is bound by bandwidth, not by one load latency per partial.  The
+// sums run over r in increasing order, and a partial of weight 0 is skipped
+// (select, so that whatever its slot holds cannot reach the result).
+__device__ __forceinline__ void merge4(const float* part_o, const float* part_lse, size_t o_pitch, size_t lse_pitch,
+                                       int count, __nv_bfloat16* o_out, float* lse_out) {
+  float m = -INFINITY;
+  for (int r = 0; r < count; ++r) m = fmaxf(m, part_lse[(size_t)r * lse_pitch]);
+  const float m_use = (m == -INFINITY) ? 0.f : m;
+  float l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  for (int r0 = 0; r0 < count; r0 += kBatch) {
+    float w[kBatch];
+    float4 v[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int r = r0 + k < count ? r0 + k : count - 1;
+      const float x = part_lse[(size_t)r * lse_pitch];
+      w[k] = (r0 + k < count && x != -INFINITY) ? __expf(x - m_use) : 0.f;
+      v[k] = *reinterpret_cast<const float4*>(part_o + (size_t)r * o_pitch);
     }
-    __syncthreads();
-    const float inv = s_inv;
-    float m_use = 0.f;
-    if (count > kMaxCached) {  // recompute the max for weights past the cache
-      m_use = -INFINITY;
-      for (int r = 0; r < count; ++r) m_use = fmaxf(m_use, part_lse[(size_t)(first + r) * lse_pitch + row]);
-      if (m_use == -INFINITY) m_use = 0.f;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const bool use = w[k] != 0.f;
+      l += w[k];
+      a0 = use ? fmaf(w[k], v[k].x, a0) : a0;
+      a1 = use ? fmaf(w[k], v[k].y, a1) : a1;
+      a2 = use ? fmaf(w[k], v[k].z, a2) : a2;
+      a3 = use ? fmaf(w[k], v[k].w, a3) : a3;
     }
-    for (int c2 = threadIdx.x * 2; c2 < D; c2 += blockDim.x * 2) {
-      float a0 = 0.f, a1 = 0.f;
-      for (int r = 0; r < count; ++r) {
-        float w;
-        if (r < kMaxCached) {
-          w = s_w[r];
-        } else {
-          const float x = part_lse[(size_t)(first + r) * lse_pitch + row];
-          w = (x == -INFINITY) ? 0.f : __expf(x - m_use);
-        }
-        if (w != 0.f) {
-          const float2 v = *reinterpret_cast<const float2*>(part_o + (size_t)(first + r) * o_pitch + (size_t)row * D + c2);
-          a0 = fmaf(w, v.x, a0);
-          a1 = fmaf(w, v.y, a1);
-        }
-      }
-      *reinterpret_cast<__nv_bfloat162*>(o_out + (size_t)row * D + c2) = __floats2bfloat162_rn(a0 * inv, a1 * inv);
-    }
-    if (threadIdx.x == 0) lse_out[row] = s_lse;
   }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(a0 * inv, a1 * inv);
+  const __nv_bfloat162 h1 = __floats2bfloat162_rn(a2 * inv, a3 * inv);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&h0);
+  u.y = *reinterpret_cast<const uint32_t*>(&h1);
+  *reinterpret_cast<uint2*>(o_out) = u;
+  if (lse_out) *lse_out = l > 0.f ? m_use + logf(l) : -INFINITY;
 }
 
 struct PlanMergeArgs {
@@ -76,7 +66,9 @@ struct PlanMergeArgs {
   WsLayout L;
 };
 
-// One CTA per merge record of the plan (groups that were split, or are empty).
+// Merge records of the plan (groups that were split, or are empty).  A thread
+// owns four columns of one row: CTA (x, y) covers rows 2y, 2y + 1 of records
+// x, x + gridDim.x, ...
 __global__ void __launch_bounds__(kMergeThreads) plan_merge_kernel(PlanMergeArgs a, const char* ws) {
   const int* hdr = reinterpret_cast<const int*>(ws);
   const int* mrg = reinterpret_cast<const int*>(ws + a.L.off_merge);
@@ -84,14 +76,18 @@ __global__ void __launch_bounds__(kMergeThreads) plan_merge_kernel(PlanMergeArgs
   const float* part_o = reinterpret_cast<const float*>(ws + a.L.off_part_o);
   const int num_merge = hdr[MLA_HDR_NUM_MERGE];
   const int R = a.T * a.H;
+  constexpr int kChunks = kDLat / 4;
+  const int row = blockIdx.y * (kMergeThreads / kChunks) + threadIdx.x / kChunks;
+  const int c = 4 * (threadIdx.x % kChunks);
   for (int i = blockIdx.x; i < num_merge; i += gridDim.x) {
     const int b = mrg[i * kMergeWords + 0], rb = mrg[i * kMergeWords + 1];
     const int first = mrg[i * kMergeWords + 2], count = mrg[i * kMergeWords + 3];
-    const int row0 = rb * kRowsPerBlock;
-    const int nrows = min(kRowsPerBlock, R - row0);
-    const size_t grow = (size_t)b * R + row0;
-    merge_rows(part_o, part_lse, (size_t)kRowsPerBlock * kDLat, kRowsPerBlock, first, count, nrows, kDLat,
-               a.o_lat + grow * kDLat, a.lse + grow);
+    const int fr = rb * kRowsPerBlock + row;
+    if (fr >= R) continue;
+    const size_t grow = (size_t)b * R + fr;
+    merge4(part_o + ((size_t)first * kRowsPerBlock + row) * kDLat + c, part_lse + (size_t)first * kRowsPerBlock + row,
+           (size_t)kRowsPerBlock * kDLat, kRowsPerBlock, count, a.o_lat + grow * kDLat + c,
+           c == 0 ? a.lse + grow : nullptr);
   }
 }
 
@@ -104,16 +100,21 @@ struct SplitMergeArgs {
   float* lse;
 };
 
-// Public contract: one CTA per (output m, chunk of 32 rows).
+// Public contract: CTAs (m, *) merge output m; work item k (stepping by the
+// y-grid) owns columns 4 (k % (D/4)) .. +3 of row k / (D/4).
 __global__ void __launch_bounds__(kMergeThreads) split_merge_kernel(SplitMergeArgs a) {
   const int m = blockIdx.x;
-  const int row0 = blockIdx.y * 32;
-  const int nrows = min(32, a.rows - row0);
-  if (m >= a.M || nrows <= 0) return;
+  if (m >= a.M) return;
+  const int chunks = a.D / 4;
+  const long long items = (long long)a.rows * chunks;
   const int first = a.indptr[m], count = a.indptr[m + 1] - a.indptr[m];
-  merge_rows(a.part_o + (size_t)row0 * a.D, a.part_lse + row0, (size_t)a.rows * a.D, a.rows, first,
-             count < 0 ? 0 : count, nrows, a.D, a.o + ((size_t)m * a.rows + row0) * a.D,
-             a.lse + (size_t)m * a.rows + row0);
+  for (long long k = (long long)blockIdx.y * blockDim.x + threadIdx.x; k < items;
+       k += (long long)gridDim.y * blockDim.x) {
+    const int row = (int)(k / chunks), c = 4 * (int)(k % chunks);
+    merge4(a.part_o + ((size_t)first * a.rows + row) * a.D + c, a.part_lse + (size_t)first * a.rows + row,
+           (size_t)a.rows * a.D, a.rows, count < 0 ? 0 : count, a.o + ((size_t)m * a.rows + row) * a.D + c,
+           c == 0 ? a.lse + (size_t)m * a.rows + row : nullptr);
+  }
 }
 
 }  // namespace
@@ -122,9 +123,10 @@ cudaError_t launch_plan_merge(const mla_geom* g, const mla_batch* b, const WsLay
                               float* lse, void* ws, cudaStream_t st) {
   PlanMergeArgs a;
   a.T = b->T; a.H = g->H; a.o_lat = o_lat; a.lse = lse; a.L = L;
-  int grid = L.cap_groups;
-  if (grid <= 0) return cudaSuccess;
-  if (grid > 4096) grid = 4096;
+  int gx = L.cap_groups;
+  if (gx <= 0) return cudaSuccess;
+  if (gx > 4096) gx = 4096;
+  const dim3 grid(gx, kRowsPerBlock * (kDLat / 4) / kMergeThreads);
   plan_merge_kernel<<<grid, kMergeThreads, 0, st>>>(a, reinterpret_cast<const char*>(ws));
   return cudaGetLastError();
 }
@@ -133,7 +135,8 @@ cudaError_t launch_split_merge(const float* part_o, const float* part_lse, const
                                int D, __nv_bfloat16* o, float* lse, cudaStream_t st) {
   if (M <= 0 || rows <= 0) return cudaSuccess;
   SplitMergeArgs a{part_o, part_lse, indptr, M, rows, D, o, lse};
-  dim3 grid(M, (rows + 31) / 32);
+  const long long blocks = ((long long)rows * (D / 4) + kMergeThreads - 1) / kMergeThreads;
+  const dim3 grid(M, (unsigned)(blocks < 65535 ? blocks : 65535));
   split_merge_kernel<<<grid, kMergeThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
