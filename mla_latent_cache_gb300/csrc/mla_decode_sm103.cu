@@ -1,5 +1,5 @@
 // Split-KV absorbed-MLA decode on the sm_103a tensor cores (TMA + tcgen05/TMEM,
-// 2-CTA clusters exchanging partial scores through distributed shared memory).
+// 2-CTA clusters).
 //
 // What it computes ("MLA in full detail", Step 3; "M5.8" 0x04 absorbed
 // reference): for every query row (b, t, h) of a plan segment,
@@ -21,25 +21,28 @@
 // than it saves: the exchange moves as many bytes as the cache itself through
 // distributed shared memory.
 // Tensor-core shapes: Q K^T is M=128 x N=64 per K=16 step (36 steps per page);
-// P V is M=128 x N=256 x K=16 (four steps per page).
+// P V is M=128 x N=256 x K=16 (four steps per page), P read from TMEM.
 //
-// TMEM per CTA: O half at columns 0..255, the 64-column S tile at 256..319
-// (released as soon as the softmax has read it), and query columns 0..383
-// (packed bf16 pairs, the TMEM A operand of Q K^T) at 320..511; the rest of
-// the query tile (latent 384..511 and RoPE) stays in shared memory.
+// TMEM per CTA (512 columns): O half at 0..255; two 64-column score tiles at
+// 256..383 (page t uses tile t % 2, so Q K^T of page t+1 runs while the
+// softmax of page t reads its tile); the softmax writes P (bf16 pairs) over
+// the first 32 columns of the tile it has read, which is where P V takes its
+// A operand; query columns 0..255 (bf16 pairs, the TMEM A operand of Q K^T)
+// at 384..511.  The rest of the query tile (latent 256..511 and RoPE) stays in
+// shared memory next to a 2-stage page ring.
 //
 // Roles per CTA (384 threads): warp 0 lane 0 issues TMA loads (each page as
-// two groups of 64 x 64 boxes through a 2-stage ring, plus L2 prefetch of
-// pages further ahead); warp 1 lane 0 issues Q K^T; warp 2 lane 0 issues P V
-// as soon as a P tile is ready (two issuing threads keep the tensor pipe fed
-// despite the per-instruction issue cost); warps 4..11 run the online softmax
-// with two threads per query row (TMEM lane), write P (bf16, 128-byte
-// swizzled, double-buffered: the A operand of P V) and the epilogue.  The
-// softmax keeps a per-row reference max and rescales the TMEM accumulator only
-// when the running max grows past it by more than 2^8 (exact for any
-// reference; only rounding differs), with scores in log2 units.  Cache rows
-// past the sequence end (last page only) are zeroed in shared memory before
-// P V so stale or NaN contents never reach the accumulator.
+// two groups of 64 x 64 boxes, block-table entries read a few pages ahead);
+// warp 1 lane 0 issues Q K^T; warp 2 lane 0 issues P V; warps 4..11 run the
+// online softmax with two threads per query row (TMEM lane), write P and the
+// epilogue.  At a segment boundary the softmax stages the next segment's
+// query columns before it writes the finished segment out, so Q K^T of the
+// next segment overlaps that epilogue.  The softmax keeps a per-row
+// reference max and rescales the TMEM accumulator only when the running max
+// grows past it by more than 2^8 (exact for any reference; only rounding
+// differs), with scores in log2 units.  Cache rows past the sequence end
+// (last page only) are zeroed in shared memory before P V so stale or NaN
+// contents never reach the accumulator.
 //
 // Every wait is bounded; a wait that runs out records MLA_ERR_TIMEOUT in the
 // workspace and raises a CTA-wide abort flag.  Loads and MMAs already issued
@@ -60,42 +63,38 @@ constexpr int kBoxBytes = 64 * 64 * 2;         // 8 KB: one 64-row page x 64 bf1
 constexpr int kQBoxBytes = 128 * 64 * 2;       // 16 KB: 128 query rows x 64 bf16
 constexpr int kBoxes = 9;                      // 8 latent boxes + 1 RoPE box per row
 constexpr int kOwnBoxes = 4;                   // latent boxes whose columns this CTA accumulates
-constexpr int kQTmemBoxes = 6;                 // query boxes 0..5 live in TMEM
+constexpr int kQTmemBoxes = 4;                 // query boxes 0..3 live in TMEM
 constexpr int kQSmemBoxes = kBoxes - kQTmemBoxes;
 constexpr int kStages = 2;                     // page stages in the ring
 constexpr int kGroupABoxes = 5;                // boxes only Q K^T needs (released after it)
 constexpr int kStageBytes = kBoxes * kBoxBytes;  // group A (5 boxes) then group B (4 value boxes)
-constexpr int kPBytes = 128 * 64 * 2;          // one P tile, bf16
 constexpr int kSmemQ = 0;
-constexpr int kSmemP = kSmemQ + kQSmemBoxes * kQBoxBytes;  // 49152
-constexpr int kSmemRing = kSmemP + 2 * kPBytes;            // 81920
-constexpr int kSmemBar = kSmemRing + kStages * kStageBytes; // 229376
-constexpr int kSmemXchg = kSmemBar + 256;                  // float [2 buffers][2 halves][128 rows]
+constexpr int kSmemRing = kSmemQ + kQSmemBoxes * kQBoxBytes;  // 81920
+constexpr int kSmemBar = kSmemRing + kStages * kStageBytes;   // 229376
+constexpr int kSmemXchg = kSmemBar + 256;                     // float [2 buffers][2 halves][128 rows]
 constexpr int kSmemBytes = kSmemXchg + 2048;
-constexpr int kSmemAlloc = kSmemBytes + 768;               // slack to align the base to 1024 B (checked)
+constexpr int kSmemAlloc = kSmemBytes + 768;                  // slack to align the base to 1024 B (checked)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
-constexpr uint32_t kTmemS = 256;
-constexpr uint32_t kTmemQ = 320;
+constexpr uint32_t kTmemS = 256;   // tile t % 2 at kTmemS + 64 (t % 2)
+constexpr uint32_t kTmemQ = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kPrefetchPages = 3;          // L2 prefetch distance ahead of the page being loaded
 
 enum {
-  BAR_FULL_A = 0,                   // kStages: group A of a page landed
+  BAR_FULL_A = 0,                      // kStages: group A of a page landed
   BAR_EMPTY_A = BAR_FULL_A + kStages,  // kStages: Q K^T done with group A
   BAR_FULL_B = BAR_EMPTY_A + kStages,  // kStages: group B (value boxes) landed
   BAR_EMPTY_B = BAR_FULL_B + kStages,  // kStages: P V done with group B
-  BAR_Q_FULL = BAR_EMPTY_B + kStages,
-  BAR_Q_EMPTY,
-  BAR_QT_FULL,
-  BAR_S_FULL,
-  BAR_S_EMPTY,
-  BAR_P_FULL,                       // 2
-  BAR_P_EMPTY = BAR_P_FULL + 2,     // 2
-  BAR_O_EMPTY = BAR_P_EMPTY + 2,
+  BAR_Q_FULL = BAR_EMPTY_B + kStages,  // query boxes in shared memory landed
+  BAR_Q_EMPTY,                         // Q K^T done with the segment's query
+  BAR_QT_FULL,                         // query columns staged in TMEM (256 arrivals)
+  BAR_S_FULL,                          // 2: score tile written
+  BAR_P_FULL = BAR_S_FULL + 2,         // 2: P written over the score tile (256 arrivals)
+  BAR_P_EMPTY = BAR_P_FULL + 2,        // 2: P V done with the tile (it may be overwritten)
+  BAR_O_EMPTY = BAR_P_EMPTY + 2,       // epilogue done with the accumulator (256 arrivals)
   BAR_FINAL,
   BAR_FINAL_PV,
-  BAR_XCH,                          // 4: the two softmax warps of a TMEM lane quadrant
+  BAR_XCH,                             // 4: the two softmax warps of a TMEM lane quadrant
   kNumBars = BAR_XCH + 4
 };
 static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
@@ -118,9 +117,6 @@ struct FastArgs {
   int bt_stride;
   const int32_t* seq_lens;
   int B, T, H, causal, checked, max_pages, num_blocks;
-  const __nv_bfloat16* ckv;  // pool base, for the L2 prefetch of whole pages
-  int64_t ckv_block;         // elements between blocks
-  int page_contiguous;       // 1 when a block's 64 rows x 576 values are one contiguous range
   float scale_log2;          // softmax scale times log2(e)
   __nv_bfloat16* o_lat;
   float* lse;
@@ -130,14 +126,34 @@ struct FastArgs {
 struct Shared {
   uint32_t base;
   __device__ uint32_t q(int box) const { return base + kSmemQ + (box - kQTmemBoxes) * kQBoxBytes; }
-  __device__ uint32_t p(int b) const { return base + kSmemP + b * kPBytes; }
   __device__ uint32_t stage_a(int st) const { return base + kSmemRing + st * kStageBytes; }
   __device__ uint32_t stage_b(int st) const { return stage_a(st) + kGroupABoxes * kBoxBytes; }
   __device__ uint32_t bar(int i) const { return base + kSmemBar + i * 8; }
 };
 
-// Issue the Q K^T MMAs of one group of boxes: A from TMEM (query boxes 0..5) or
-// shared memory (6..8), B from consecutive 8 KB boxes starting at b0 (descriptor).
+// The segments of this pair's work ranges, in order: ranges pair,
+// pair + num_pairs, ...; segment indices of range r are rptr[r] .. rptr[r+1).
+struct SegWalk {
+  const int* rptr;
+  int r, si, end, step, num_ranges;
+  __device__ SegWalk(const int* rp, int pair, int num_pairs, int nr)
+      : rptr(rp), r(pair), si(0), end(0), step(num_pairs), num_ranges(nr) {
+    if (r < nr) { si = rp[r]; end = rp[r + 1]; }
+  }
+  // Index of the current segment, or -1 once the walk is over.
+  __device__ int cur() {
+    while (r < num_ranges && si >= end) {
+      r += step;
+      if (r < num_ranges) { si = rptr[r]; end = rptr[r + 1]; }
+    }
+    return r < num_ranges ? si : -1;
+  }
+  __device__ void advance() { ++si; }
+};
+
+// Issue the Q K^T MMAs of one group of boxes into score tile d: A from TMEM
+// (query boxes 0..3) or shared memory (4..8), B from consecutive 8 KB boxes
+// starting at b0 (descriptor).
 template <int HALF, bool GROUP_B>
 __device__ __forceinline__ void issue_qk_group(uint32_t d, uint32_t tmem, const uint64_t (&qdesc)[kQSmemBoxes],
                                                uint64_t b0, uint32_t idesc) {
@@ -162,11 +178,12 @@ __device__ __forceinline__ void fail(int* hdr, volatile int* abort_flag, int whe
   record_error(hdr, MLA_ERR_TIMEOUT, where);
 }
 
-// Q K^T issuer of one CTA (HALF = its rank in the pair), one thread.  Per page t:
-// Q K^T over group A, release A, Q K^T over group B -> S.
+// Q K^T issuer of one CTA (HALF = its rank in the pair), one thread.  Page t
+// goes to score tile t % 2 once P V of page t-2 has released it: Q K^T over
+// group A, release A, Q K^T over group B -> S_FULL.
 template <int HALF>
 __device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
-                                        const int* seg, const int* rptr, int pair, int num_pairs, int num_ranges) {
+                                        const int* seg, SegWalk walk) {
   const uint32_t id_qk = idesc_bf16_f32(128, 64, 0);
   // Descriptors are built once; steps only move the start-address field (16-byte
   // units): +2 per 32-byte K step of a K-major tile, +kBoxBytes/16 per box,
@@ -177,36 +194,33 @@ __device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hd
   const uint64_t adesc0 = sw128_desc(sh.stage_a(0), 16, 1024);
   const uint64_t bdesc0 = sw128_desc(sh.stage_b(0), 16, 1024);
   constexpr uint32_t kStageStep = kStageBytes >> 4;
-  const uint32_t d = tmem + kTmemS;
   int ti = 0, sc = 0;
   bool ok = true;
-  for (int r = pair; ok && r < num_ranges; r += num_pairs) {
-    for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
-      const int* rec = seg + (size_t)si * kSegWords;
-      const int n_tiles = rec[3] - rec[2];
-      if (!mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag) || !mbar_wait(sh.bar(BAR_QT_FULL), sc & 1, abort_flag)) {
-        fail(hdr, abort_flag, 22); ok = false; break;
+  for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
+    const int* rec = seg + (size_t)si * kSegWords;
+    const int n_tiles = rec[3] - rec[2];
+    if (!mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag) || !mbar_wait(sh.bar(BAR_QT_FULL), sc & 1, abort_flag)) {
+      fail(hdr, abort_flag, 22); ok = false; break;
+    }
+    tc_fence_after();
+    for (int i = 0; ok && i < n_tiles; ++i, ++ti) {
+      const int st = ti % kStages, sb = ti & 1;
+      const uint32_t par = (ti / kStages) & 1;
+      if ((ti >= 2 && !mbar_wait(sh.bar(BAR_P_EMPTY + sb), ((ti >> 1) - 1) & 1, abort_flag)) ||
+          !mbar_wait(sh.bar(BAR_FULL_A + st), par, abort_flag)) {
+        fail(hdr, abort_flag, 23); ok = false; break;
       }
       tc_fence_after();
-      for (int i = 0; ok && i < n_tiles; ++i, ++ti) {
-        const int st = ti % kStages;
-        const uint32_t par = (ti / kStages) & 1;
-        // S is single-buffered: the softmax releases it right after reading it.
-        if (!mbar_wait(sh.bar(BAR_S_EMPTY), (ti & 1) ^ 1, abort_flag) ||
-            !mbar_wait(sh.bar(BAR_FULL_A + st), par, abort_flag)) {
-          fail(hdr, abort_flag, 23); ok = false; break;
-        }
-        tc_fence_after();
-        issue_qk_group<HALF, false>(d, tmem, qdesc, adesc0 + st * kStageStep, id_qk);
-        mma_commit(sh.bar(BAR_EMPTY_A + st));
-        if (!mbar_wait(sh.bar(BAR_FULL_B + st), par, abort_flag)) { fail(hdr, abort_flag, 24); ok = false; break; }
-        tc_fence_after();
-        issue_qk_group<HALF, true>(d, tmem, qdesc, bdesc0 + st * kStageStep, id_qk);
-        mma_commit(sh.bar(BAR_S_FULL));
-        if (i == n_tiles - 1) mma_commit(sh.bar(BAR_Q_EMPTY));
-      }
-      ++sc;
+      const uint32_t d = tmem + kTmemS + 64 * sb;
+      issue_qk_group<HALF, false>(d, tmem, qdesc, adesc0 + st * kStageStep, id_qk);
+      mma_commit(sh.bar(BAR_EMPTY_A + st));
+      if (!mbar_wait(sh.bar(BAR_FULL_B + st), par, abort_flag)) { fail(hdr, abort_flag, 24); ok = false; break; }
+      tc_fence_after();
+      issue_qk_group<HALF, true>(d, tmem, qdesc, bdesc0 + st * kStageStep, id_qk);
+      mma_commit(sh.bar(BAR_S_FULL + sb));
+      if (i == n_tiles - 1) mma_commit(sh.bar(BAR_Q_EMPTY));
     }
+    ++sc;
   }
   // Wait for every MMA issued by this thread before TMEM is released.
   mma_commit(sh.bar(BAR_FINAL));
@@ -215,39 +229,57 @@ __device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hd
 }
 
 // P V issuer, one thread: as soon as P of page t is written, O[:, own] += P V over
-// the page's group B (one N=256 MMA per K step), then release group B and P.
+// the page's group B (one N=256 MMA per K step, A = P from TMEM), then release
+// group B and the score tile.
 __device__ __forceinline__ void pv_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
-                                        const int* seg, const int* rptr, int pair, int num_pairs, int num_ranges) {
+                                        const int* seg, SegWalk walk) {
   const uint32_t id_pv = idesc_bf16_f32(128, 256, 1);
   const uint64_t vdesc0 = sw128_desc(sh.stage_b(0), kBoxBytes, 1024);
-  const uint64_t pdesc0 = sw128_desc(sh.p(0), 16, 1024);
-  constexpr uint32_t kStageStep = kStageBytes >> 4, kPStep = kPBytes >> 4;
+  constexpr uint32_t kStageStep = kStageBytes >> 4;
   int ti = 0, sc = 0;
   bool ok = true;
-  for (int r = pair; ok && r < num_ranges; r += num_pairs) {
-    for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
-      const int* rec = seg + (size_t)si * kSegWords;
-      const int n_tiles = rec[3] - rec[2];
-      for (int i = 0; i < n_tiles; ++i, ++ti) {
-        if (i == 0 && sc > 0 && !mbar_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag)) {
-          fail(hdr, abort_flag, 20); ok = false; break;
-        }
-        const int pb = ti & 1, st = ti % kStages;
-        if (!mbar_wait(sh.bar(BAR_P_FULL + pb), (ti >> 1) & 1, abort_flag)) { fail(hdr, abort_flag, 21); ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16(tmem + kTmemO, pdesc0 + pb * kPStep + 2 * kk, vdesc0 + st * kStageStep + 128 * kk, id_pv,
-                   (i == 0 && kk == 0) ? 0u : 1u);
-        mma_commit(sh.bar(BAR_EMPTY_B + st));
-        mma_commit(sh.bar(BAR_P_EMPTY + pb));
+  for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
+    const int* rec = seg + (size_t)si * kSegWords;
+    const int n_tiles = rec[3] - rec[2];
+    for (int i = 0; i < n_tiles; ++i, ++ti) {
+      if (i == 0 && sc > 0 && !mbar_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag)) {
+        fail(hdr, abort_flag, 20); ok = false; break;
       }
-      ++sc;
+      const int sb = ti & 1, st = ti % kStages;
+      if (!mbar_wait(sh.bar(BAR_P_FULL + sb), (ti >> 1) & 1, abort_flag)) { fail(hdr, abort_flag, 21); ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemS + 64 * sb + 8 * kk, vdesc0 + st * kStageStep + 128 * kk, id_pv,
+                        (i == 0 && kk == 0) ? 0u : 1u);
+      mma_commit(sh.bar(BAR_EMPTY_B + st));
+      mma_commit(sh.bar(BAR_P_EMPTY + sb));
     }
+    ++sc;
   }
   mma_commit(sh.bar(BAR_FINAL_PV));
   volatile int never = 0;
   mbar_wait(sh.bar(BAR_FINAL_PV), 0, &never);
+}
+
+// What a softmax thread needs to know about one segment.
+struct SegRows {
+  int b, p0, p1, slot_out, S, fr, limit;
+  bool row_valid;
+};
+
+__device__ __forceinline__ SegRows seg_rows(const int* rec, const FastArgs& a, int R, int row) {
+  SegRows s;
+  s.b = rec[0];
+  s.p0 = rec[2];
+  s.p1 = rec[3];
+  s.slot_out = rec[5];
+  int S = a.seq_lens[s.b];
+  s.S = S < 0 ? 0 : min(S, a.max_pages * kPage);
+  s.fr = rec[1] * kRowsPerBlock + row;
+  s.row_valid = s.fr < R;
+  s.limit = s.row_valid ? visible_limit(s.S, a.T, s.fr / a.H, a.causal) : 0;
+  return s;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -290,9 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sh.bar(BAR_Q_FULL), 1);
     mbar_init(sh.bar(BAR_Q_EMPTY), 1);
     mbar_init(sh.bar(BAR_QT_FULL), kSoftmaxThreads);
-    mbar_init(sh.bar(BAR_S_FULL), 1);
-    mbar_init(sh.bar(BAR_S_EMPTY), kSoftmaxThreads);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(sh.bar(BAR_S_FULL + i), 1);
       mbar_init(sh.bar(BAR_P_FULL + i), kSoftmaxThreads);
       mbar_init(sh.bar(BAR_P_EMPTY + i), 1);
     }
@@ -316,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
+  const SegWalk walk0(rptr, pair, num_pairs, num_ranges);
 
   if (a.checked && blockIdx.x == 0 && tid == 0) {
     if (hdr[MLA_HDR_MAGIC] != MLA_PLAN_MAGIC || hdr[MLA_HDR_B] != a.B || hdr[MLA_HDR_T] != a.T ||
@@ -338,59 +370,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      SegWalk walk = walk0;
       int gt = 0, sc = 0;
       bool q_in_flight = false, ok = true, a_only = false;
-      for (int r = pair; ok && r < num_ranges; r += num_pairs) {
-        for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
-          const int* rec = seg + (size_t)si * kSegWords;
-          const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3];
-          if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
-          const int row0 = b * R + rb * kRowsPerBlock;
-          mbar_arrive_expect_tx(sh.bar(BAR_Q_FULL), kQSmemBoxes * kQBoxBytes);
-          for (int box = kQTmemBoxes; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_FULL), 64 * box, row0);
-          tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_FULL), 0, row0);
-          q_in_flight = true;
-          // Pages further ahead than the ring are pulled into L2 (CTA 0 does it for the pair).
-          auto prefetch_page = [&](int pp) {
-            if (half != 0 || pp >= p1) return;
-            const int pb = a.block_table[(size_t)b * a.bt_stride + pp];
-            if (pb < 0 || pb >= a.num_blocks) return;
-            if (a.page_contiguous) {
-              prefetch_l2_bulk(a.ckv + (int64_t)pb * a.ckv_block, kPage * kDK * 2);
-            } else {
-              for (int box = 0; box < 8; ++box) prefetch_l2_tile_3d(&tm_ckv, 64 * box, 0, pb);
-              prefetch_l2_tile_3d(&tm_kpe, 0, 0, pb);
-            }
-          };
-          for (int pp = p0; pp < p0 + kPrefetchPages; ++pp) prefetch_page(pp);
-          for (int p = p0; ok && p < p1; ++p) {
-            prefetch_page(p + kPrefetchPages);
-            int blk = a.block_table[(size_t)b * a.bt_stride + p];
-            if (blk < 0 || blk >= a.num_blocks) {
-              // An out-of-pool id reads as zeros through the tensor map; report it when checking.
-              if (a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | p);
-              blk = -1;
-            }
-            const int st = gt % kStages;
-            const uint32_t par = ((gt / kStages) & 1) ^ 1;
-            if (!mbar_wait_backoff(sh.bar(BAR_EMPTY_A + st), par, abort_flag)) { fail(hdr, abort_flag, 11); ok = false; break; }
-            mbar_arrive_expect_tx(sh.bar(BAR_FULL_A + st), kGroupABoxes * kBoxBytes);
-            for (int j = 0; j < kGroupABoxes; ++j) {
-              const int box = half == 0 ? Boxes<0>::a(j) : Boxes<1>::a(j);
-              const uint32_t dst = sh.stage_a(st) + j * kBoxBytes;
-              if (box < 8) tma_load_3d(dst, &tm_ckv, sh.bar(BAR_FULL_A + st), 64 * box, 0, blk);
-              else tma_load_3d(dst, &tm_kpe, sh.bar(BAR_FULL_A + st), 0, 0, blk);
-            }
-            if (!mbar_wait_backoff(sh.bar(BAR_EMPTY_B + st), par, abort_flag)) {
-              fail(hdr, abort_flag, 12); ok = false; a_only = true; break;
-            }
-            mbar_arrive_expect_tx(sh.bar(BAR_FULL_B + st), kOwnBoxes * kBoxBytes);
-            for (int c = 0; c < kOwnBoxes; ++c)
-              tma_load_3d(sh.stage_b(st) + c * kBoxBytes, &tm_ckv, sh.bar(BAR_FULL_B + st), 64 * (4 * half + c), 0, blk);
-            ++gt;
+      for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
+        const int* rec = seg + (size_t)si * kSegWords;
+        const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3];
+        if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
+        const int row0 = b * R + rb * kRowsPerBlock;
+        mbar_arrive_expect_tx(sh.bar(BAR_Q_FULL), kQSmemBoxes * kQBoxBytes);
+        for (int box = kQTmemBoxes; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_FULL), 64 * box, row0);
+        tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_FULL), 0, row0);
+        q_in_flight = true;
+        // Block ids are read a few pages ahead of their use (independent loads in flight).
+        const int32_t* btrow = a.block_table + (size_t)b * a.bt_stride;
+        int bq0 = p0 < p1 ? btrow[p0] : 0;
+        int bq1 = p0 + 1 < p1 ? btrow[p0 + 1] : 0;
+        int bq2 = p0 + 2 < p1 ? btrow[p0 + 2] : 0;
+        int bq3 = p0 + 3 < p1 ? btrow[p0 + 3] : 0;
+        for (int p = p0; ok && p < p1; ++p) {
+          int blk = bq0;
+          bq0 = bq1; bq1 = bq2; bq2 = bq3;
+          bq3 = p + 4 < p1 ? btrow[p + 4] : 0;
+          if (blk < 0 || blk >= a.num_blocks) {
+            // An out-of-pool id reads as zeros through the tensor map; report it when checking.
+            if (a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | p);
+            blk = -1;
           }
-          ++sc;
+          const int st = gt % kStages;
+          const uint32_t par = ((gt / kStages) & 1) ^ 1;
+          if (!mbar_wait_backoff(sh.bar(BAR_EMPTY_A + st), par, abort_flag)) { fail(hdr, abort_flag, 11); ok = false; break; }
+          mbar_arrive_expect_tx(sh.bar(BAR_FULL_A + st), kGroupABoxes * kBoxBytes);
+          for (int j = 0; j < kGroupABoxes; ++j) {
+            const int box = half == 0 ? Boxes<0>::a(j) : Boxes<1>::a(j);
+            const uint32_t dst = sh.stage_a(st) + j * kBoxBytes;
+            if (box < 8) tma_load_3d(dst, &tm_ckv, sh.bar(BAR_FULL_A + st), 64 * box, 0, blk);
+            else tma_load_3d(dst, &tm_kpe, sh.bar(BAR_FULL_A + st), 0, 0, blk);
+          }
+          if (!mbar_wait_backoff(sh.bar(BAR_EMPTY_B + st), par, abort_flag)) {
+            fail(hdr, abort_flag, 12); ok = false; a_only = true; break;
+          }
+          mbar_arrive_expect_tx(sh.bar(BAR_FULL_B + st), kOwnBoxes * kBoxBytes);
+          for (int c = 0; c < kOwnBoxes; ++c)
+            tma_load_3d(sh.stage_b(st) + c * kBoxBytes, &tm_ckv, sh.bar(BAR_FULL_B + st), 64 * (4 * half + c), 0, blk);
+          ++gt;
         }
+        ++sc;
       }
       // Drain: every load issued must have landed before the CTA may exit (a page
       // whose group B was not issued after a failure is covered by its group A wait).
@@ -409,13 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ Q K^T issuer
     if (lane == 0) {
-      if (half == 0) qk_role<0>(sh, tmem, hdr, abort_flag, seg, rptr, pair, num_pairs, num_ranges);
-      else qk_role<1>(sh, tmem, hdr, abort_flag, seg, rptr, pair, num_pairs, num_ranges);
+      if (half == 0) qk_role<0>(sh, tmem, hdr, abort_flag, seg, walk0);
+      else qk_role<1>(sh, tmem, hdr, abort_flag, seg, walk0);
     }
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ P V issuer
-    if (lane == 0) pv_role(sh, tmem, hdr, abort_flag, seg, rptr, pair, num_pairs, num_ranges);
+    if (lane == 0) pv_role(sh, tmem, hdr, abort_flag, seg, walk0);
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
@@ -429,205 +454,210 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
     float* xrow = reinterpret_cast<float*>(smem + kSmemXchg);  // [buffer][half][row] partner exchange
     // Exchange a value with the partner thread of the same row (bounded wait on the
-    // quadrant's mbarrier; double-buffered by exchange parity).
+    // quadrant's mbarrier; double-buffered by exchange parity).  It also orders this
+    // thread's earlier TMEM reads before the partner's later TMEM writes.
     int xc = 0;
     auto swap_with_partner = [&](float v, float* out) -> bool {
       float* slot = xrow + (xc & 1) * 256;
       slot[ch * 128 + row] = v;
+      tc_fence_before();
       mbar_arrive(sh.bar(BAR_XCH + q4));
       const bool w = mbar_wait(sh.bar(BAR_XCH + q4), xc & 1, abort_flag);
+      tc_fence_after();
       *out = slot[(ch ^ 1) * 128 + row];
       ++xc;
       return __all_sync(0xffffffffu, w);
     };
+    // Query columns 0..255 of this row go to TMEM (A operand of Q K^T for boxes
+    // 0..3; this thread stages boxes 2 ch and 2 ch + 1) once the previous
+    // segment's Q K^T MMAs are done with them.
+    auto stage_q = [&](const SegRows& s, int sc_of) -> bool {
+      const bool w_ok = sc_of == 0 || mbar_wait(sh.bar(BAR_Q_EMPTY), (sc_of - 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, w_ok)) return false;
+      tc_fence_after();
+      const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)s.b * R + (s.row_valid ? s.fr : 0)) * kDLat) +
+                         16 * ch;
+      uint32_t q0[32], q1[32];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint4 v0 = s.row_valid ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
+        const uint4 v1 = s.row_valid ? __ldg(src + 8 + e) : make_uint4(0, 0, 0, 0);
+        q0[4 * e] = v0.x; q0[4 * e + 1] = v0.y; q0[4 * e + 2] = v0.z; q0[4 * e + 3] = v0.w;
+        q1[4 * e] = v1.x; q1[4 * e + 1] = v1.y; q1[4 * e + 2] = v1.z; q1[4 * e + 3] = v1.w;
+      }
+      tmem_st32(t_lane + kTmemQ + 32 * (2 * ch), q0);
+      tmem_st32(t_lane + kTmemQ + 32 * (2 * ch + 1), q1);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(sh.bar(BAR_QT_FULL));
+      return true;
+    };
+
+    SegWalk walk = walk0;
+    int si = walk.cur();
     int ti = 0, sc = 0;
     bool ok = true;
-    for (int r = pair; ok && r < num_ranges; r += num_pairs) {
-      for (int si = rptr[r]; ok && si < rptr[r + 1]; ++si) {
-        const int* rec = seg + (size_t)si * kSegWords;
-        const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3], slot_out = rec[5];
-        int S = a.seq_lens[b];
-        S = S < 0 ? 0 : min(S, a.max_pages * kPage);
-        const int fr = rb * kRowsPerBlock + row;
-        const bool row_valid = fr < R;
-        const int limit = row_valid ? visible_limit(S, a.T, fr / a.H, a.causal) : 0;
-        // Query columns 0..383 of this row go to TMEM (A operand of Q K^T for boxes
-        // 0..5; this thread stages three of them) once the previous segment's Q K^T
-        // MMAs are done with them.
-        {
-          bool w_ok = sc == 0 || mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag);
-          if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 33); ok = false; break; }
-          tc_fence_after();
-          const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)b * R + fr) * kDLat);
-#pragma unroll 1
-          for (int bx = 3 * ch; bx < 3 * ch + 3; ++bx) {
-            uint32_t qv[32];
+    SegRows cur;
+    if (si >= 0) {
+      cur = seg_rows(seg + (size_t)si * kSegWords, a, R, row);
+      if (!stage_q(cur, 0)) { fail(hdr, abort_flag, 33); ok = false; }
+    }
+    while (ok && si >= 0) {
+      float m_ref = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
+      const int n_tiles = cur.p1 - cur.p0;
+      for (int i = 0; i < n_tiles; ++i, ++ti) {
+        const int sb = ti & 1;
+        const uint32_t s_col = kTmemS + 64 * sb;
+        const int jbase = (cur.p0 + i) * kPage + 32 * ch;   // first cache row of this thread's columns
+        bool w_ok = mbar_wait(sh.bar(BAR_S_FULL + sb), (ti >> 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 30); ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[32];
+        tmem_ld32(t_lane + s_col + 32 * ch, sr);
+        tmem_wait_ld();
+        // Raw-score maximum over the visible columns (the scale is positive).
+        const bool full = jbase + 32 <= cur.limit;
+        float tmax = -INFINITY;
+        if (full) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const uint4 v = row_valid ? __ldg(src + 8 * bx + e) : make_uint4(0, 0, 0, 0);
-              qv[4 * e] = v.x; qv[4 * e + 1] = v.y; qv[4 * e + 2] = v.z; qv[4 * e + 3] = v.w;
-            }
-            tmem_st32(t_lane + kTmemQ + 32 * bx, qv);
+          for (int j = 0; j < 32; ++j) tmax = fmaxf(tmax, __uint_as_float(sr[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (jbase + j < cur.limit) tmax = fmaxf(tmax, __uint_as_float(sr[j]));
+        }
+        {
+          float other;
+          if (!swap_with_partner(tmax, &other)) { fail(hdr, abort_flag, 37); ok = false; break; }
+          tmax = fmaxf(tmax, other) * a.scale_log2;
+        }
+        // Lazy rescale of the running state: needs the accumulator up to date (P V of
+        // the previous page complete); rare once the reference max has settled.
+        const bool grow = tmax > m_ref + kRescaleThreshold;
+        const float new_ref = grow ? tmax : m_ref;
+        const float factor = (grow && m_ref != -INFINITY) ? ex2(m_ref - new_ref) : 1.f;
+        if (i > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+          const int t1 = ti - 1;
+          w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + (t1 & 1)), (t1 >> 1) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 31); ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 4 * ch; c < 4 * ch + 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_lane + kTmemO + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+            tmem_st32(t_lane + kTmemO + 32 * c, o);
           }
           tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(sh.bar(BAR_QT_FULL));
         }
-        float m_ref = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
-        const int n_tiles = p1 - p0;
-        for (int i = 0; i < n_tiles; ++i, ++ti) {
-          const int jbase = (p0 + i) * kPage + 32 * ch;   // first cache row of this thread's columns
-          bool w_ok = mbar_wait(sh.bar(BAR_S_FULL), ti & 1, abort_flag);
-          if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 30); ok = false; break; }
-          tc_fence_after();
-          uint32_t sr[32];
-          tmem_ld32(t_lane + kTmemS + 32 * ch, sr);
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(sh.bar(BAR_S_EMPTY));
-          // Raw-score maximum over the visible columns (the scale is positive).
-          const bool full = jbase + 32 <= limit;
-          float tmax = -INFINITY;
-          if (full) {
+        l *= factor;
+        m_ref = new_ref;
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // This thread's 32 P values, p = 2^(s * scale * log2 e - m), as bf16 pairs over
+        // columns 16 ch .. 16 ch + 15 of the score tile it has read (the partner has
+        // read its scores too: the exchange above came after both reads).
+        float psum = 0.f;
+        uint32_t pw[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) tmax = fmaxf(tmax, __uint_as_float(sr[j]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (jbase + j < limit) tmax = fmaxf(tmax, __uint_as_float(sr[j]));
+        for (int e = 0; e < 16; ++e) {
+          const int j = 2 * e;
+          float x0 = ex2(fmaf(__uint_as_float(sr[j]), a.scale_log2, -m_use));
+          float x1 = ex2(fmaf(__uint_as_float(sr[j + 1]), a.scale_log2, -m_use));
+          if (!full) {
+            x0 = (jbase + j < cur.limit) ? x0 : 0.f;
+            x1 = (jbase + j + 1 < cur.limit) ? x1 : 0.f;
           }
-          {
-            float other;
-            if (!swap_with_partner(tmax, &other)) { fail(hdr, abort_flag, 37); ok = false; break; }
-            tmax = fmaxf(tmax, other) * a.scale_log2;
-          }
-          // Lazy rescale of the running state: needs the accumulator up to date (P V of
-          // the previous page complete); rare once the reference max has settled.
-          const bool grow = tmax > m_ref + kRescaleThreshold;
-          const float new_ref = grow ? tmax : m_ref;
-          const float factor = (grow && m_ref != -INFINITY) ? ex2(m_ref - new_ref) : 1.f;
-          if (i > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
-            const int t1 = ti - 1;
-            w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + (t1 & 1)), (t1 >> 1) & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 31); ok = false; break; }
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 4 * ch; c < 4 * ch + 4; ++c) {
-              uint32_t o[32];
-              tmem_ld32(t_lane + kTmemO + 32 * c, o);
-              tmem_wait_ld();
+          psum += x0 + x1;
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+          pw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        tmem_st16(t_lane + s_col + 16 * ch, pw);
+        l += psum;
+        // Rows of the last page past the sequence end are zeroed in the four value
+        // boxes of this page (its group B) before P V reads them.
+        const int valid = cur.S - (cur.p0 + i) * kPage;
+        if (valid < kPage) {
+          const int t256 = tid - 128;   // 0..255 over the two warpgroups
+          for (int idx = t256; idx < kOwnBoxes * kPage; idx += 256) {
+            const int c = idx / kPage, rr = idx % kPage;
+            if (rr >= valid) {
+              const uint32_t dst = sh.stage_b(ti % kStages) + c * kBoxBytes + rr * 128;
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-              tmem_st32(t_lane + kTmemO + 32 * c, o);
-            }
-            tmem_wait_st();
-          }
-          l *= factor;
-          m_ref = new_ref;
-          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-          // P buffer ti&1 is free once P V of page ti-2 has completed.
-          const int pb = ti & 1;
-          if (i >= 2) {
-            w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + pb), ((ti >> 1) - 1) & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 36); ok = false; break; }
-          }
-          // This thread's 32 P values (bf16) into the 128-byte-swizzled A tile of P V:
-          // p = 2^(s * scale * log2 e - m), 16-byte chunks 4 ch .. 4 ch + 3 of the row.
-          float psum = 0.f;
-          const uint32_t prow = sh.p(pb) + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 8 * c + 2 * e;
-              float x0 = ex2(fmaf(__uint_as_float(sr[j]), a.scale_log2, -m_use));
-              float x1 = ex2(fmaf(__uint_as_float(sr[j + 1]), a.scale_log2, -m_use));
-              if (!full) {
-                x0 = (jbase + j < limit) ? x0 : 0.f;
-                x1 = (jbase + j + 1 < limit) ? x1 : 0.f;
-              }
-              psum += x0 + x1;
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
-              w[e] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
-            const uint32_t dst = prow + (((4 * ch + c) ^ (row & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                         "r"(w[3])
-                         : "memory");
-          }
-          l += psum;
-          // Rows of the last page past the sequence end are zeroed in the four value
-          // boxes of this page (its group B) before P V reads them.
-          const int valid = S - (p0 + i) * kPage;
-          if (valid < kPage) {
-            const int t256 = tid - 128;   // 0..255 over the two warpgroups
-            for (int idx = t256; idx < kOwnBoxes * kPage; idx += 256) {
-              const int c = idx / kPage, rr = idx % kPage;
-              if (rr >= valid) {
-                const uint32_t dst = sh.stage_b(ti % kStages) + c * kBoxBytes + rr * 128;
-#pragma unroll
-                for (int z = 0; z < 8; ++z)
-                  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst + 16 * z), "r"(0) : "memory");
-              }
+              for (int z = 0; z < 8; ++z)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst + 16 * z), "r"(0) : "memory");
             }
           }
           fence_proxy_async_smem();
-          tc_fence_before();
-          mbar_arrive(sh.bar(BAR_P_FULL + pb));
         }
-        if (!ok) break;
-        // Epilogue: wait for the last P V, combine the two halves of the row sum,
-        // then normalise and store this thread's 128 output columns.
-        {
-          const int tl = ti - 1;
-          const bool w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + (tl & 1)), (tl >> 1) & 1, abort_flag);
-          if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 32); ok = false; break; }
-          tc_fence_after();
-        }
-        float l_other;
-        if (!swap_with_partner(l, &l_other)) { fail(hdr, abort_flag, 38); ok = false; break; }
-        const float l_row = ch == 0 ? l + l_other : l_other + l;
-        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const float lse_v = l_row > 0.f ? (m_use + __log2f(l_row)) * 0.69314718055994531f : -INFINITY;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(sh.bar(BAR_P_FULL + sb));
+      }
+      if (!ok) break;
+      // The next segment's query goes to TMEM now, so that its Q K^T can run while
+      // this segment is written out.
+      walk.advance();
+      const int si_next = walk.cur();
+      SegRows nxt = cur;
+      if (si_next >= 0) {
+        nxt = seg_rows(seg + (size_t)si_next * kSegWords, a, R, row);
+        if (!stage_q(nxt, sc + 1)) { fail(hdr, abort_flag, 33); ok = false; break; }
+      }
+      // Epilogue: wait for the last P V, combine the two halves of the row sum,
+      // then normalise and store this thread's 128 output columns.
+      {
+        const int tl = ti - 1;
+        const bool w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + (tl & 1)), (tl >> 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 32); ok = false; break; }
+        tc_fence_after();
+      }
+      float l_other;
+      if (!swap_with_partner(l, &l_other)) { fail(hdr, abort_flag, 38); ok = false; break; }
+      const float l_row = ch == 0 ? l + l_other : l_other + l;
+      const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const float lse_v = l_row > 0.f ? (m_use + __log2f(l_row)) * 0.69314718055994531f : -INFINITY;
+      const int b = cur.b, fr = cur.fr, slot_out = cur.slot_out;
 #pragma unroll 1
-        for (int c = 4 * ch; c < 4 * ch + 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(t_lane + kTmemO + 32 * c, o);
-          tmem_wait_ld();
-          if (row_valid) {
-            if (slot_out < 0) {
-              __nv_bfloat16* dst = a.o_lat + ((size_t)b * R + fr) * kDLat + 256 * half + 32 * c;
+      for (int c = 4 * ch; c < 4 * ch + 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_lane + kTmemO + 32 * c, o);
+        tmem_wait_ld();
+        if (cur.row_valid) {
+          if (slot_out < 0) {
+            __nv_bfloat16* dst = a.o_lat + ((size_t)b * R + fr) * kDLat + 256 * half + 32 * c;
 #pragma unroll
-              for (int e = 0; e < 32; e += 8) {
-                uint4 v;
-                __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-                __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                __nv_bfloat162 h3 = __floats2bfloat162_rn(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                v.x = *reinterpret_cast<uint32_t*>(&h0); v.y = *reinterpret_cast<uint32_t*>(&h1);
-                v.z = *reinterpret_cast<uint32_t*>(&h2); v.w = *reinterpret_cast<uint32_t*>(&h3);
-                *reinterpret_cast<uint4*>(dst + e) = v;
-              }
-            } else {
-              float* dst = part_o + ((size_t)slot_out * kRowsPerBlock + row) * kDLat + 256 * half + 32 * c;
-#pragma unroll
-              for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<float4*>(dst + e) =
-                    make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                                __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            for (int e = 0; e < 32; e += 8) {
+              uint4 v;
+              __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+              __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+              __nv_bfloat162 h3 = __floats2bfloat162_rn(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+              v.x = *reinterpret_cast<uint32_t*>(&h0); v.y = *reinterpret_cast<uint32_t*>(&h1);
+              v.z = *reinterpret_cast<uint32_t*>(&h2); v.w = *reinterpret_cast<uint32_t*>(&h3);
+              *reinterpret_cast<uint4*>(dst + e) = v;
             }
+          } else {
+            float* dst = part_o + ((size_t)slot_out * kRowsPerBlock + row) * kDLat + 256 * half + 32 * c;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(dst + e) =
+                  make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                              __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
           }
         }
-        if (row_valid && half == 0 && ch == 0) {
-          if (slot_out < 0) a.lse[(size_t)b * R + fr] = lse_v;
-          else part_lse[(size_t)slot_out * kRowsPerBlock + row] = lse_v;
-        }
-        tc_fence_before();
-        mbar_arrive(sh.bar(BAR_O_EMPTY));
-        ++sc;
       }
+      if (cur.row_valid && half == 0 && ch == 0) {
+        if (slot_out < 0) a.lse[(size_t)b * R + fr] = lse_v;
+        else part_lse[(size_t)slot_out * kRowsPerBlock + row] = lse_v;
+      }
+      tc_fence_before();
+      mbar_arrive(sh.bar(BAR_O_EMPTY));
+      ++sc;
+      si = si_next;
+      cur = nxt;
     }
   }
 
@@ -751,9 +781,6 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
   a.block_table = block_table; a.bt_stride = bt_stride; a.seq_lens = seq_lens;
   a.B = b->B; a.T = b->T; a.H = g->H; a.causal = b->causal ? 1 : 0; a.checked = checked;
   a.max_pages = b->max_pages; a.num_blocks = cv.num_blocks;
-  a.ckv = cv.ckv; a.ckv_block = cv.ckv_block;
-  a.page_contiguous = (cv.ckv_row == kDK && cv.ckv_block == (int64_t)kPage * kDK && cv.kpe == cv.ckv + kDLat &&
-                       cv.kpe_row == kDK && cv.kpe_block == cv.ckv_block) ? 1 : 0;
   a.scale_log2 = g->softmax_scale * 1.4426950408889634f;
   a.o_lat = o_lat; a.lse = lse; a.L = L;
   if (!set_kernel_attributes()) return cudaErrorInvalidValue;
