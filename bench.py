@@ -9,11 +9,14 @@ launching stream to time the dominant kernel.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload uniform|tiny|ragged|long|extend] [--T T] [--splits N]
+                  [--arm absorb|normal]
 
 The default workload is the uniform V3 batch; the others (the tiny V2-Lite
 case, the ragged batch, the single 131072-row sequence with --splits N, the
 causal extend batch with --T new rows) print the same JSON line for that
-workload.  A workload whose cache fits in L2 is timed with an L2 flush (a
+workload.  ``--arm normal`` times the decompressed comparison arm (expansion
+of the latent cache into per-head keys and values, then causal MHA) on the
+same workload instead.  A workload whose cache fits in L2 is timed with an L2 flush (a
 256 MB write) between steps, outside the timed events.
 
 Multi-GPU runs are replicas: each rank runs the same independent batch (the
@@ -396,6 +399,92 @@ def run_ours(args):
     return 0
 
 
+def normal_flops_bytes(w) -> dict:
+    """Algorithmic FLOPs and bytes of the Normal arm's two kernels."""
+    H, rows = w.H, int(np.asarray(w.seq_lens, dtype=np.int64).sum())
+    pairs = 0
+    for S in w.seq_lens:
+        S = int(S)
+        for t in range(w.T):
+            pairs += S if not w.causal else max(0, min(S, S - w.T + t + 1))
+    BT = w.B * w.T
+    expand_f = 2 * rows * 512 * 256 * H
+    attn_f = 2 * H * pairs * (192 + 128)
+    expand_b = rows * 512 * 2 + 2 * H * 128 * 512 * 2 + rows * H * 256 * 2
+    attn_b = rows * H * 256 * 2 + rows * 64 * 2 + BT * H * (128 + 64 + 128) * 2 + BT * H * 4
+    return {"expand_flops": expand_f, "attn_flops": attn_f, "expand_bytes": expand_b, "attn_bytes": attn_b}
+
+
+def run_normal(args):
+    """The Normal (decompressed) arm on the same workload: expansion + causal MHA."""
+    import torch
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from mla_latent_cache_gb300 import binding as L
+    from mla_latent_cache_gb300 import workloads as W
+    from mla_latent_cache_gb300.runtime import NormalStep
+    w = W.config_workload(WORKLOADS[args.workload], T=args.T if args.workload == "extend" else None)
+    st = NormalStep(w, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    hbm_peak, tc_peak, peak_kind = _peaks()
+    nf = normal_flops_bytes(w)
+    with torch.cuda.stream(stream):
+        st.step(stream)
+    stream.synchronize()
+    g_exp, g_att = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_exp, stream=stream):
+        st.expand(stream)
+    with torch.cuda.graph(g_att, stream=stream):
+        st.attention(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            g_exp.replay(); g_att.replay()
+    stream.synchronize()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    marks = [(ev(), ev(), ev()) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                marks[i][0].record(stream)
+                g_exp.replay()
+                marks[i][1].record(stream)
+                g_att.replay()
+                marks[i][2].record(stream)
+        stream.synchronize()
+    exp_ms = sum(a.elapsed_time(b) for a, b, _ in marks) / args.steps
+    att_ms = sum(b.elapsed_time(c) for _, b, c in marks) / args.steps
+    ms = exp_ms + att_ms
+    status, info = L.mla_read_device_status(None, stream)
+    if status != L.MLA_OK:
+        raise RuntimeError(f"device status after timing: {L.mla_status_string(status)} ({info})")
+    tokens = w.B * w.T
+    exp_tf = nf["expand_flops"] / (exp_ms / 1e3) / 1e12
+    att_tf = nf["attn_flops"] / (att_ms / 1e3) / 1e12
+    dominant = ("mla_normal_expand", exp_tf, exp_ms) if exp_ms >= att_ms else ("mla_normal_attention", att_tf, att_ms)
+    line = {
+        "impl": "ours", "arm": "normal", "metric": METRIC, "value": tokens / (ms / 1e3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "H": w.H, "B": w.B, "T": w.T, "S": int(w.seq_lens[0]), "page": 64,
+                   "step": "expand (latent -> per-head k_nope, v) + causal MHA, CUDA graphs",
+                   "l2": "inputs larger than L2 (expanded keys/values: %.0f MB)" % (st.kv_exp.numel() * 2 / 1e6)},
+        "roofline": {"bound": "tensor", "kernel": dominant[0], "achieved": dominant[1], "peak": tc_peak,
+                     "peak_kind": peak_kind, "unit": "TFLOP/s", "frac": dominant[1] / tc_peak, "traffic": None},
+        "kernels": {"expand_ms": exp_ms, "expand_tflops": exp_tf,
+                    "expand_gbs": nf["expand_bytes"] / (exp_ms / 1e3) / 1e9,
+                    "attention_ms": att_ms, "attention_tflops": att_tf,
+                    "attention_gbs": nf["attn_bytes"] / (att_ms / 1e3) / 1e9},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    _emit(line)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -407,11 +496,15 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS, key=WORKLOADS.get), default="uniform")
     ap.add_argument("--T", type=int, default=1, help="new rows per sequence (extend workload)")
     ap.add_argument("--splits", type=int, default=0, help="split count override (0 = the automatic plan)")
+    ap.add_argument("--arm", choices=["absorb", "normal"], default="absorb",
+                    help="absorb: the latent-cache path (default); normal: the decompressed comparison arm")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.arm == "normal":
+        return run_normal(args)
     return run_ours(args)
 
 

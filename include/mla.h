@@ -213,8 +213,49 @@ mla_status mla_decode_noalloc(const mla_geom* geom, const mla_batch* batch, cons
                               const mla_cache* cache, const int32_t* block_table, int bt_stride,
                               const int32_t* seq_lens, void* o_lat, float* lse, mla_stream_t stream);
 
+/*
+ * The Normal (decompressed) arm, the baseline the absorbed path is compared
+ * with ("MLA in full detail", the naive path of Step 1; "M5.8" 0x02 and
+ * 0x06): every cached latent is up-projected into per-head keys and values,
+ * then ordinary multi-head attention runs with 192-wide keys [k_nope | k_pe]
+ * (k_pe shared by the heads) and 128-wide values, scale geom->softmax_scale.
+ *
+ * Expanded rows: kv_exp bf16 [H][B * rows_per_seq][256]; row b * rows_per_seq + j
+ * of head h holds [W_UK[h] c_j (128) | W_UV[h] c_j (128)] for cache row j of
+ * sequence b, rows_per_seq = mla_normal_rows_per_seq(max_pages) (max_pages
+ * rounded up to an even count, times 64).  The caller allocates kv_exp
+ * (mla_normal_expanded_bytes).
+ *
+ * mla_normal_expand: writes the rows j < S_b of every sequence, and zeros up
+ *   to the next multiple of 128; later rows are not touched.  w_uk, w_uv bf16
+ *   [H, 128, 512].  Uses block_table[b, 0 .. ceil(S_b/64)); an id outside
+ *   [0, num_blocks) reads as zeros.
+ * mla_normal_attention: o bf16 [B, T, H, 128] and lse fp32 [B, T, H] (natural
+ *   log) for q_nope bf16 [B, T, H, 128], q_pe bf16 [B, T, H, 64], keys and
+ *   values from kv_exp (as written by mla_normal_expand for the same
+ *   batch->max_pages and seq_lens) and k_pe from the cache; token t of
+ *   sequence b sees cache rows j < S_b - T + t + 1 when batch->causal, else all
+ *   S_b.  A row that sees no key gets o = 0, lse = -inf.  batch->num_slots and
+ *   num_splits_override are ignored.
+ * Both validate on the host (MLA_ERR_ARG / SHAPE / ALIGN as elsewhere) and run
+ * asynchronously; a bounded wait that ran out in either is reported by
+ * mla_read_device_status (with or without a workspace).
+ */
+int64_t mla_normal_rows_per_seq(int max_pages);
+size_t mla_normal_expanded_bytes(const mla_geom* geom, int B, int max_pages);
+mla_status mla_normal_expand(const mla_geom* geom, const mla_cache* cache, const int32_t* block_table, int bt_stride,
+                             const int32_t* seq_lens, int B, int max_pages, const void* w_uk, const void* w_uv,
+                             void* kv_exp, mla_stream_t stream);
+mla_status mla_normal_attention(const mla_geom* geom, const mla_batch* batch, const void* q_nope, const void* q_pe,
+                                const mla_cache* cache, const int32_t* block_table, int bt_stride,
+                                const int32_t* seq_lens, const void* kv_exp, void* o, float* lse,
+                                mla_stream_t stream);
+
 /* Synchronise `stream`, then return the status word a kernel recorded in the
- * workspace (MLA_OK if none) and, if info != NULL, its detail word. */
+ * workspace (MLA_OK if none) and, if info != NULL, its detail word.  The
+ * workspace-free kernels (absorption, un-absorption, the Normal arm) keep one
+ * status word per device, also returned (and cleared) here; workspace may be
+ * NULL to read only that one. */
 mla_status mla_read_device_status(const void* workspace, int* info, mla_stream_t stream);
 
 /* Static description of a status code. */

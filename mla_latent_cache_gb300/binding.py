@@ -74,6 +74,10 @@ def _load() -> ctypes.CDLL:
         "mla_decode_noalloc": (I, [G, Bt, P, P, C, P, I, P, P, P, P]),
         "mla_split_merge": (I, [P, P, P, I, I, I, P, P, P]),
         "mla_debug_gather": (I, [C, P, I, P, I, P, P]),
+        "mla_normal_rows_per_seq": (ctypes.c_int64, [I]),
+        "mla_normal_expanded_bytes": (ctypes.c_size_t, [G, I, I]),
+        "mla_normal_expand": (I, [G, C, P, I, P, I, I, P, P, P, P]),
+        "mla_normal_attention": (I, [G, Bt, P, P, C, P, I, P, P, P, P, P]),
         "mla_read_device_status": (I, [P, ctypes.POINTER(ctypes.c_int), P]),
         "mla_status_string": (ctypes.c_char_p, [I]),
         "mla_device_sm_count": (I, []),
@@ -87,7 +91,8 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 EXPORTED = ("mla_workspace_size", "mla_plan", "mla_absorb_q", "mla_unabsorb_o", "mla_decode", "mla_decode_noalloc",
-            "mla_split_merge",
+            "mla_split_merge", "mla_normal_rows_per_seq", "mla_normal_expanded_bytes", "mla_normal_expand",
+            "mla_normal_attention",
             "mla_debug_gather", "mla_read_device_status", "mla_status_string", "mla_device_sm_count")
 
 
@@ -195,6 +200,27 @@ def mla_split_merge(part_o, part_lse, indptr, M: int, rows: int, D: int, o, lse,
 def mla_debug_gather(cache: mla_cache, block_table, bt_stride: int, seq_lens, b: int, out, stream=None) -> int:
     return _lib.mla_debug_gather(ctypes.byref(cache), _ptr(block_table), bt_stride, _ptr(seq_lens), b, _ptr(out),
                                  _stream(stream))
+
+
+def mla_normal_rows_per_seq(max_pages: int) -> int:
+    return int(_lib.mla_normal_rows_per_seq(max_pages))
+
+
+def mla_normal_expanded_bytes(geom: mla_geom, B: int, max_pages: int) -> int:
+    return int(_lib.mla_normal_expanded_bytes(ctypes.byref(geom), B, max_pages))
+
+
+def mla_normal_expand(geom, cache: mla_cache, block_table, bt_stride: int, seq_lens, B: int, max_pages: int, w_uk,
+                      w_uv, kv_exp, stream=None) -> int:
+    return _lib.mla_normal_expand(ctypes.byref(geom), ctypes.byref(cache), _ptr(block_table), bt_stride,
+                                  _ptr(seq_lens), B, max_pages, _ptr(w_uk), _ptr(w_uv), _ptr(kv_exp), _stream(stream))
+
+
+def mla_normal_attention(geom, batch, q_nope, q_pe, cache: mla_cache, block_table, bt_stride: int, seq_lens, kv_exp,
+                         o, lse, stream=None) -> int:
+    return _lib.mla_normal_attention(ctypes.byref(geom), ctypes.byref(batch), _ptr(q_nope), _ptr(q_pe),
+                                     ctypes.byref(cache), _ptr(block_table), bt_stride, _ptr(seq_lens), _ptr(kv_exp),
+                                     _ptr(o), _ptr(lse), _stream(stream))
 
 
 def mla_read_device_status(workspace, stream=None) -> tuple[int, int]:

@@ -216,15 +216,67 @@ mla_status mla_debug_gather(const mla_cache* cache, const int32_t* block_table, 
                                          (cudaStream_t)stream));
 }
 
+int64_t mla_normal_rows_per_seq(int max_pages) { return max_pages < 1 ? 0 : normal_rows_per_seq(max_pages); }
+
+size_t mla_normal_expanded_bytes(const mla_geom* geom, int B, int max_pages) {
+  if (check_geom(geom) != MLA_OK || B < 0 || max_pages < 1) return 0;
+  return (size_t)geom->H * (size_t)B * (size_t)normal_rows_per_seq(max_pages) * 256 * 2;
+}
+
+mla_status mla_normal_expand(const mla_geom* geom, const mla_cache* cache, const int32_t* block_table, int bt_stride,
+                             const int32_t* seq_lens, int B, int max_pages, const void* w_uk, const void* w_uv,
+                             void* kv_exp, mla_stream_t stream) {
+  mla_status s = check_geom(geom);
+  if (s != MLA_OK) return s;
+  if (B < 0 || max_pages < 1) return MLA_ERR_ARG;
+  if (B == 0) return MLA_OK;
+  if (!block_table || !seq_lens || !w_uk || !w_uv || !kv_exp || bt_stride < max_pages) return MLA_ERR_ARG;
+  if ((long long)B * normal_rows_per_seq(max_pages) >= (1LL << 31)) return MLA_ERR_SHAPE;
+  if (!aligned16(block_table) || !aligned16(seq_lens) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(kv_exp))
+    return MLA_ERR_ALIGN;
+  CacheView cv;
+  if ((s = check_cache(cache, &cv)) != MLA_OK) return s;
+  return cuda_status(launch_normal_expand(geom, cv, block_table, bt_stride, seq_lens, B, max_pages,
+                                          static_cast<const __nv_bfloat16*>(w_uk),
+                                          static_cast<const __nv_bfloat16*>(w_uv),
+                                          static_cast<__nv_bfloat16*>(kv_exp), (cudaStream_t)stream));
+}
+
+mla_status mla_normal_attention(const mla_geom* geom, const mla_batch* batch, const void* q_nope, const void* q_pe,
+                                const mla_cache* cache, const int32_t* block_table, int bt_stride,
+                                const int32_t* seq_lens, const void* kv_exp, void* o, float* lse,
+                                mla_stream_t stream) {
+  mla_status s = check_geom(geom);
+  if (s != MLA_OK) return s;
+  if ((s = check_batch(batch)) != MLA_OK) return s;
+  if (batch->B == 0) return MLA_OK;
+  if (!q_nope || !q_pe || !block_table || !seq_lens || !kv_exp || !o || !lse) return MLA_ERR_ARG;
+  if (bt_stride < batch->max_pages) return MLA_ERR_ARG;
+  if ((long long)batch->B * normal_rows_per_seq(batch->max_pages) >= (1LL << 31) || batch->B > 65535 ||
+      (batch->T + 127) / 128 > 65535)
+    return MLA_ERR_SHAPE;
+  if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(block_table) || !aligned16(seq_lens) ||
+      !aligned16(kv_exp) || !aligned16(o) || !aligned16(lse))
+    return MLA_ERR_ALIGN;
+  CacheView cv;
+  if ((s = check_cache(cache, &cv)) != MLA_OK) return s;
+  return cuda_status(launch_normal_attention(geom, batch, static_cast<const __nv_bfloat16*>(q_nope),
+                                             static_cast<const __nv_bfloat16*>(q_pe), cv, block_table, bt_stride,
+                                             seq_lens, static_cast<const __nv_bfloat16*>(kv_exp),
+                                             static_cast<__nv_bfloat16*>(o), lse, (cudaStream_t)stream));
+}
+
 mla_status mla_read_device_status(const void* workspace, int* info, mla_stream_t stream) {
-  if (!workspace) return MLA_ERR_ARG;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MLA_ERR_CUDA;
-  int words[2] = {0, 0};
-  const char* base = static_cast<const char*>(workspace) + MLA_HDR_ERROR * sizeof(int);
-  if (cudaMemcpy(words, base, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
-  if (info) *info = words[1];
-  if (words[0] != 0) return (mla_status)words[0];
-  // The absorption kernels have no workspace; their (rare) timeout is kept per device.
+  if (info) *info = 0;
+  if (workspace) {
+    int words[2] = {0, 0};
+    const char* base = static_cast<const char*>(workspace) + MLA_HDR_ERROR * sizeof(int);
+    if (cudaMemcpy(words, base, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+    if (info) *info = words[1];
+    if (words[0] != 0) return (mla_status)words[0];
+  }
+  // Kernels without a workspace keep their (rare) timeout in one word per device.
   int* bmm = bmm_status_ptr();
   if (bmm) {
     int v = 0;

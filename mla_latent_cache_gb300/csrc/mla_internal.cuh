@@ -79,6 +79,14 @@ cudaError_t launch_absorb_sm103(const __nv_bfloat16* q_nope, const __nv_bfloat16
 cudaError_t launch_unabsorb_sm103(const __nv_bfloat16* o_lat, const __nv_bfloat16* w_uv, __nv_bfloat16* o,
                                   int BT, int H, cudaStream_t st);
 int* bmm_status_ptr();
+int64_t normal_rows_per_seq(int max_pages);
+cudaError_t launch_normal_expand(const mla_geom* g, const CacheView& cv, const int32_t* block_table, int bt_stride,
+                                 const int32_t* seq_lens, int B, int max_pages, const __nv_bfloat16* w_uk,
+                                 const __nv_bfloat16* w_uv, __nv_bfloat16* kv_exp, cudaStream_t st);
+cudaError_t launch_normal_attention(const mla_geom* g, const mla_batch* b, const __nv_bfloat16* q_nope,
+                                    const __nv_bfloat16* q_pe, const CacheView& cv, const int32_t* block_table,
+                                    int bt_stride, const int32_t* seq_lens, const __nv_bfloat16* kv_exp,
+                                    __nv_bfloat16* o, float* lse, cudaStream_t st);
 cudaError_t launch_debug_gather(const CacheView& cv, const int32_t* block_table, int bt_stride,
                                 const int32_t* seq_lens, int b, __nv_bfloat16* out, cudaStream_t st);
 

@@ -108,3 +108,52 @@ def read_plan_tables(torch, workspace):
     rp = words(int(hdr[L.HDR["OFF_RANGE_PTR"]]), nr + 1)
     mg = words(int(hdr[L.HDR["OFF_MERGE"]]), nm * 4).reshape(nm, 4)
     return seg, rp, mg
+
+
+class NormalStep:
+    """The Normal (decompressed) arm on one workload: expand the latent cache into
+    per-head keys and values (mla_normal_expand), then causal MHA over them
+    (mla_normal_attention).  Inputs are q_nope / q_pe directly; no absorption."""
+
+    def __init__(self, w: Workload, device="cuda"):
+        import torch
+        self.torch = torch
+        self.w = w
+        self.device = torch.device(device)
+        dev = self.device
+        self.geom = L.make_geom(w.H)
+        self.batch = L.make_batch(w.B, w.T, w.causal, w.max_pages)
+        self.pool = pool_to_device(torch, w, dev)
+        self.cache = L.cache_from_pool(self.pool)
+        self.block_table = torch.from_numpy(w.block_table).to(dev)
+        self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
+        self.q_nope = _u16_to_bf16(torch, w.q_nope, dev)
+        self.q_pe = _u16_to_bf16(torch, w.q_pe, dev)
+        self.w_uk = _u16_to_bf16(torch, w.w_uk, dev)
+        self.w_uv = _u16_to_bf16(torch, w.w_uv, dev)
+        self.rows_per_seq = L.mla_normal_rows_per_seq(w.max_pages)
+        nbytes = L.mla_normal_expanded_bytes(self.geom, w.B, w.max_pages)
+        if nbytes == 0 and w.B > 0:
+            raise L.MlaError(L.MLA_ERR_ARG, "mla_normal_expanded_bytes")
+        self.kv_exp = torch.empty(max(1, nbytes // 2), dtype=torch.bfloat16, device=dev)
+        self.o = torch.empty((w.B, w.T, w.H, 128), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.B, w.T, w.H), dtype=torch.float32, device=dev)
+
+    def expand(self, stream=None):
+        L.check(L.mla_normal_expand(self.geom, self.cache, self.block_table, self.block_table.shape[1], self.seq_lens,
+                                    self.w.B, self.w.max_pages, self.w_uk, self.w_uv, self.kv_exp, stream),
+                "mla_normal_expand")
+
+    def attention(self, stream=None):
+        L.check(L.mla_normal_attention(self.geom, self.batch, self.q_nope, self.q_pe, self.cache, self.block_table,
+                                       self.block_table.shape[1], self.seq_lens, self.kv_exp, self.o, self.lse,
+                                       stream), "mla_normal_attention")
+
+    def step(self, stream=None):
+        self.expand(stream)
+        self.attention(stream)
+
+    def expanded(self):
+        """kv_exp viewed as [H, B * rows_per_seq, 256] (k_nope | v)."""
+        return self.kv_exp[: self.w.H * self.w.B * self.rows_per_seq * 256].view(
+            self.w.H, self.w.B * self.rows_per_seq, 256)

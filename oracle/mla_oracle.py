@@ -175,6 +175,12 @@ def absorbed_layer_ref(q_nope, q_pe, pool, block_table, seq_lens, w_uk, w_uv, ca
 # ---------------------------------------------------------------------------
 # Normal (decompressed) path  ([zdszero] Normal mode; [MLA-in-depth] Step 1 "what the naive path does")
 # ---------------------------------------------------------------------------
+def decompress_ref(c, w_uk, w_uv):
+    """Per-head keys and values of cached latents c [S, d_c] ([MLA-in-depth] naive path):
+    k_nope[j,h,n] = sum_c W_UK[h,n,c] c_j[c],  v[j,h,v] = sum_c W_UV[h,v,c] c_j[c]."""
+    return np.einsum("hnc,jc->jhn", w_uk, c), np.einsum("hvc,jc->jhv", w_uv, c)
+
+
 def normal_ref(q_nope, q_pe, pool, block_table, seq_lens, w_uk, w_uv, causal, scale=SCALE, batches=None):
     """Up-project every cached latent into per-head keys/values, then ordinary MHA.
 
@@ -195,8 +201,7 @@ def normal_ref(q_nope, q_pe, pool, block_table, seq_lens, w_uk, w_uv, causal, sc
         rows = gather_rows(pool, block_table[b], S)
         c = rows[:, :d_c]
         kpe = rows[:, d_c:]
-        k_nope = np.einsum("hnc,jc->jhn", w_uk, c)
-        v = np.einsum("hvc,jc->jhv", w_uv, c)
+        k_nope, v = decompress_ref(c, w_uk, w_uv)
         k = np.concatenate([k_nope, np.broadcast_to(kpe[:, None, :], (S, H, d_r))], axis=-1)
         q = np.concatenate([q_nope[b], q_pe[b]], axis=-1)
         s = np.einsum("thd,jhd->thj", q, k) * scale

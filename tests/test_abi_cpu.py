@@ -64,3 +64,23 @@ def test_host_validation_rejects_before_launch(mla):
                           1 << 30, 0) == mla.MLA_ERR_ALIGN
     assert mla.mla_split_merge(None, None, None, 2, 4, 12, None, None, 0) == mla.MLA_ERR_ARG
     assert mla.mla_split_merge(0x1000, 0x2000, 0x3000, 0, 4, 16, 0x4000, 0x5000, 0) == mla.MLA_OK
+
+
+def test_normal_arm_host_side(mla):
+    g = mla.make_geom(128)
+    assert mla.mla_normal_rows_per_seq(1) == 128 and mla.mla_normal_rows_per_seq(2) == 128
+    assert mla.mla_normal_rows_per_seq(137) == 69 * 128 and mla.mla_normal_rows_per_seq(0) == 0
+    assert mla.mla_normal_expanded_bytes(g, 8, 136) == 128 * 8 * 68 * 128 * 256 * 2
+    assert mla.mla_normal_expanded_bytes(mla.make_geom(96), 8, 136) == 0
+    cache = mla.mla_cache(0x1000, 0x1400, 576, 64 * 576, 576, 64 * 576, 8)
+    # null pointers and misalignment are rejected on the host before any CUDA call
+    assert mla.mla_normal_expand(g, cache, None, 8, None, 2, 8, None, None, None, 0) == mla.MLA_ERR_ARG
+    assert mla.mla_normal_expand(g, cache, 0x1000, 4, 0x2000, 2, 8, 0x3000, 0x4000, 0x5000, 0) == mla.MLA_ERR_ARG
+    assert mla.mla_normal_expand(g, cache, 0x1000, 8, 0x2000, 2, 8, 0x3000, 0x4000, 0x5008, 0) == mla.MLA_ERR_ALIGN
+    assert mla.mla_normal_expand(g, cache, 0x1000, 8, 0x2000, 0, 8, 0x3000, 0x4000, 0x5000, 0) == mla.MLA_OK
+    b = mla.make_batch(2, 16, True, 8)
+    assert mla.mla_normal_attention(g, b, None, None, cache, None, 8, None, None, None, None, 0) == mla.MLA_ERR_ARG
+    assert mla.mla_normal_attention(g, b, 0x1000, 0x2000, cache, 0x3000, 8, 0x4000, 0x5000, 0x6000, 0x7004,
+                                    0) == mla.MLA_ERR_ALIGN
+    assert mla.mla_normal_attention(mla.make_geom(24), b, 0x1000, 0x2000, cache, 0x3000, 8, 0x4000, 0x5000, 0x6000,
+                                    0x7000, 0) == mla.MLA_ERR_SHAPE

@@ -137,6 +137,29 @@ def test_paged_gather_brute_force():
             assert np.array_equal(rows[j], flat[bt[j // page] * page + j % page])
 
 
+def test_decompress_brute_force_and_absorption_identity():
+    """decompress_ref against explicit loops on tiny ranks, and the absorption
+    identity q_nope . (W_UK c) == (q_nope W_UK) . c that ties W_UK's orientation."""
+    rng = np.random.default_rng(12)
+    H, dn, dv, dc, S = 2, 3, 2, 5, 4
+    c = rng.normal(size=(S, dc))
+    w_uk = rng.normal(size=(H, dn, dc))
+    w_uv = rng.normal(size=(H, dv, dc))
+    k, v = O.decompress_ref(c, w_uk, w_uv)
+    assert k.shape == (S, H, dn) and v.shape == (S, H, dv)
+    for j in range(S):
+        for h in range(H):
+            for n in range(dn):
+                assert abs(k[j, h, n] - sum(w_uk[h, n, x] * c[j, x] for x in range(dc))) < 1e-12
+            for m in range(dv):
+                assert abs(v[j, h, m] - sum(w_uv[h, m, x] * c[j, x] for x in range(dc))) < 1e-12
+    q = rng.normal(size=(1, 1, H, dn))
+    q_lat = O.absorb_ref(q, w_uk)[0, 0]                  # [H, dc]
+    lhs = np.einsum("hn,jhn->jh", q[0, 0], k)
+    rhs = np.einsum("hc,jc->jh", q_lat, c)
+    assert np.max(np.abs(lhs - rhs)) < 1e-12
+
+
 # ---------------------------------------------------------------------------
 # closed-form identity: absorbed == Normal (decompressed) path
 # ---------------------------------------------------------------------------
