@@ -195,6 +195,23 @@ def cpu_oracle_sample(w, budget_s: float = 15.0):
     return done * w.T / dt, done, dt, min(cores, threads) if threads else cores
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The slowest rank's value (replicas are timed by the slowest one): an all-reduce
+    MAX over the process group, the identity when there is none."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput of `world` replicas: every rank's units over the slowest time."""
+    return units_per_rank * world / (ms / 1000.0)
+
+
 def _emit(line: dict):
     print(json.dumps(line), flush=True)
 
@@ -310,12 +327,8 @@ def run_ours(args):
         ms = sum(a.elapsed_time(b) for a, b in step_evs) / args.steps
     else:
         ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens_per_step = w.B * w.T * world
-    value = tokens_per_step / (ms / 1000.0)
+    ms = max_over_ranks(ms, dev)
+    value = replica_throughput(w.B * w.T, world, ms)
     status, info = L.mla_read_device_status(st.workspace, stream)
     if status != L.MLA_OK:
         raise RuntimeError(f"device status after timing: {L.mla_status_string(status)} ({info})")
@@ -351,12 +364,8 @@ def run_ours(args):
             e2e_step()
         e1.record(stream)
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = tokens_per_step / (e2e_ms / 1000.0)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
+    e2e_value = replica_throughput(w.B * w.T, world, e2e_ms)
 
     achieved = ab["decode"] / (dec_ms / 1000.0) / 1e9
     tflops = fl["decode"] / (dec_ms / 1000.0) / 1e12
