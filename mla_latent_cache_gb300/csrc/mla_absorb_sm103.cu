@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -196,8 +198,8 @@ cudaError_t launch_bmm(const CUtensorMap& ma, const CUtensorMap& mb, __nv_bfloat
     attr = true;
   }
   dim3 grid(H, n_total / NT, (BT + 127) / 128);
-  bmm_sm103_kernel<KB, NT, BMN><<<grid, kThreads, C::kSmemAlloc, st>>>(ma, mb, out, BT, H, n_total, status);
-  return cudaGetLastError();
+  return launch_pdl(bmm_sm103_kernel<KB, NT, BMN>, grid, dim3(kThreads), C::kSmemAlloc, st, ma, mb, out, BT, H,
+                    n_total, status);
 }
 
 __device__ int g_bmm_status;  // timeouts of these kernels (they have no workspace)

@@ -293,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // carries kSmemAlloc - kSmemBytes bytes of slack for that.  Refuse (uniformly,
   // before anything is set up) if the slack does not cover the misalignment.
   if ((uintptr_t)(smem - smem_raw) + kSmemBytes > (uintptr_t)kSmemAlloc) {
+    pdl_wait();
     if (threadIdx.x == 0) record_error(hdr, MLA_ERR_DEVICE_CHECK, -2);
     return;
   }
@@ -309,7 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int half = (int)cluster_ctarank();
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
-  const int num_ranges = hdr[MLA_HDR_NUM_RANGES];
   const int R = a.T * a.H;
 
   if (tid == 0) {
@@ -347,6 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
+  // No early trigger: the merge that follows should be placed on the SMs as they
+  // free up together, not packed onto the first few that do.
+  pdl_wait();
+  const int num_ranges = hdr[MLA_HDR_NUM_RANGES];
   const SegWalk walk0(rptr, pair, num_pairs, num_ranges);
 
   if (a.checked && blockIdx.x == 0 && tid == 0) {
@@ -708,7 +712,10 @@ bool set_kernel_attributes() {
   return true;
 }
 
-void cluster_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pairs, cudaStream_t st) {
+// Launch configuration: clusters of two CTAs; with `pdl`, also programmatic
+// stream serialisation (the kernel waits for its predecessor in pdl_wait).
+void cluster_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pairs, cudaStream_t st,
+                           bool pdl) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(2 * pairs, 1, 1);
   cfg->blockDim = dim3(kThreads, 1, 1);
@@ -718,8 +725,10 @@ void cluster_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, i
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg->attrs = attr;
-  cfg->numAttrs = 1;
+  cfg->numAttrs = pdl ? 2 : 1;
 }
 
 }  // namespace
@@ -733,8 +742,8 @@ int decode_sm103_pairs_per_device() {
     int n = 0;
     if (set_kernel_attributes()) {
       cudaLaunchConfig_t cfg;
-      cudaLaunchAttribute attr[1];
-      cluster_launch_config(&cfg, attr, 256, 0);
+      cudaLaunchAttribute attr[2];
+      cluster_launch_config(&cfg, attr, 256, 0, false);
       if (cudaOccupancyMaxActiveClusters(&n, decode_sm103_kernel, &cfg) != cudaSuccess) n = 0;
     }
     if (n <= 0) {
@@ -789,8 +798,8 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
   if (pairs > max_pairs) pairs = max_pairs;
   if (pairs <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  cluster_launch_config(&cfg, attr, pairs, st);
+  cudaLaunchAttribute attr[2];
+  cluster_launch_config(&cfg, attr, pairs, st, true);
   return cudaLaunchKernelEx(&cfg, decode_sm103_kernel, m_qlat, m_qpe, m_ckv, m_kpe, a, reinterpret_cast<char*>(ws));
 }
 

@@ -31,6 +31,30 @@ struct WsLayout {
 bool compute_layout(const mla_geom* g, const mla_batch* b, WsLayout* L);
 int resolve_slots(const mla_batch* b);
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation and waits for the grid before it in the
+// stream (pdl_wait) before its first global-memory access, so its set-up
+// (barriers, TMEM, tensor-map prefetch) overlaps the tail of that grid; it
+// lets the next grid start its own set-up (pdl_trigger) once all of its CTAs
+// are running.  Without a programmatic predecessor the wait returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Status word helpers (device): first error wins.
 __device__ __forceinline__ void record_error(int* hdr, int code, int info) {
   if (atomicCAS(&hdr[MLA_HDR_ERROR], 0, code) == 0) {

@@ -67,9 +67,13 @@ struct PlanMergeArgs {
 };
 
 // Merge records of the plan (groups that were split, or are empty).  A thread
-// owns four columns of one row: CTA (x, y) covers rows 2y, 2y + 1 of records
-// x, x + gridDim.x, ...
+// owns four columns of one row (128 threads per row, two rows per CTA); the
+// work items are (record, row pair), taken in turn by the CTAs of a grid sized
+// to what the device holds at once, so a plan without merges costs one read
+// per CTA.
 __global__ void __launch_bounds__(kMergeThreads) plan_merge_kernel(PlanMergeArgs a, const char* ws) {
+  pdl_wait();
+  pdl_trigger();
   const int* hdr = reinterpret_cast<const int*>(ws);
   const int* mrg = reinterpret_cast<const int*>(ws + a.L.off_merge);
   const float* part_lse = reinterpret_cast<const float*>(ws + a.L.off_part_lse);
@@ -77,9 +81,13 @@ __global__ void __launch_bounds__(kMergeThreads) plan_merge_kernel(PlanMergeArgs
   const int num_merge = hdr[MLA_HDR_NUM_MERGE];
   const int R = a.T * a.H;
   constexpr int kChunks = kDLat / 4;
-  const int row = blockIdx.y * (kMergeThreads / kChunks) + threadIdx.x / kChunks;
+  constexpr int kRowsPerCta = kMergeThreads / kChunks;
+  constexpr int kItemsPerRecord = kRowsPerBlock / kRowsPerCta;
   const int c = 4 * (threadIdx.x % kChunks);
-  for (int i = blockIdx.x; i < num_merge; i += gridDim.x) {
+  const long long items = (long long)num_merge * kItemsPerRecord;
+  for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+    const int i = (int)(it / kItemsPerRecord);
+    const int row = (int)(it % kItemsPerRecord) * kRowsPerCta + threadIdx.x / kChunks;
     const int b = mrg[i * kMergeWords + 0], rb = mrg[i * kMergeWords + 1];
     const int first = mrg[i * kMergeWords + 2], count = mrg[i * kMergeWords + 3];
     const int fr = rb * kRowsPerBlock + row;
@@ -103,6 +111,8 @@ struct SplitMergeArgs {
 // Public contract: CTAs (m, *) merge output m; work item k (stepping by the
 // y-grid) owns columns 4 (k % (D/4)) .. +3 of row k / (D/4).
 __global__ void __launch_bounds__(kMergeThreads) split_merge_kernel(SplitMergeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x;
   if (m >= a.M) return;
   const int chunks = a.D / 4;
@@ -123,12 +133,14 @@ cudaError_t launch_plan_merge(const mla_geom* g, const mla_batch* b, const WsLay
                               float* lse, void* ws, cudaStream_t st) {
   PlanMergeArgs a;
   a.T = b->T; a.H = g->H; a.o_lat = o_lat; a.lse = lse; a.L = L;
-  int gx = L.cap_groups;
-  if (gx <= 0) return cudaSuccess;
-  if (gx > 4096) gx = 4096;
-  const dim3 grid(gx, kRowsPerBlock * (kDLat / 4) / kMergeThreads);
-  plan_merge_kernel<<<grid, kMergeThreads, 0, st>>>(a, reinterpret_cast<const char*>(ws));
-  return cudaGetLastError();
+  if (L.cap_groups <= 0) return cudaSuccess;
+  // Eight 256-thread CTAs fill an SM; the grid never exceeds the possible items.
+  const long long cap_items = (long long)L.cap_groups * (kRowsPerBlock / (kMergeThreads / (kDLat / 4)));
+  const int sms = mla_device_sm_count();
+  long long nctas = 8LL * (sms > 0 ? sms : 148);
+  if (nctas > cap_items) nctas = cap_items;
+  const dim3 grid((unsigned)nctas);
+  return launch_pdl(plan_merge_kernel, grid, dim3(kMergeThreads), 0, st, a, reinterpret_cast<const char*>(ws));
 }
 
 cudaError_t launch_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M, int rows,
@@ -137,8 +149,7 @@ cudaError_t launch_split_merge(const float* part_o, const float* part_lse, const
   SplitMergeArgs a{part_o, part_lse, indptr, M, rows, D, o, lse};
   const long long blocks = ((long long)rows * (D / 4) + kMergeThreads - 1) / kMergeThreads;
   const dim3 grid(M, (unsigned)(blocks < 65535 ? blocks : 65535));
-  split_merge_kernel<<<grid, kMergeThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(split_merge_kernel, grid, dim3(kMergeThreads), 0, st, a);
 }
 
 }  // namespace mla

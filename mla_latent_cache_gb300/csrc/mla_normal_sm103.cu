@@ -83,6 +83,8 @@ __device__ __forceinline__ void fail_status(int* status, volatile int* abort_fla
 __global__ void __launch_bounds__(kExpThreads, 1)
     normal_expand_kernel(const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_wuk,
                          const __grid_constant__ CUtensorMap tm_wuv, ExpArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x / a.tiles_per_seq, tile = blockIdx.x % a.tiles_per_seq;
   int S = a.seq_lens[b];
   S = S < 0 ? 0 : min(S, a.max_pages * kPage);
@@ -300,6 +302,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     normal_attention_kernel(const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qp,
                             const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kpe,
                             AttArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int t0 = blockIdx.x * 128, h = blockIdx.y, b = blockIdx.z;
   int S = a.seq_lens[b];
   S = S < 0 ? 0 : min(S, a.max_pages * kPage);
@@ -629,8 +633,7 @@ cudaError_t launch_normal_expand(const mla_geom* g, const CacheView& cv, const i
   a.kv_exp = kv_exp;
   a.status = status;
   const dim3 grid((unsigned)(B * a.tiles_per_seq), (unsigned)((g->H + kExpHeads - 1) / kExpHeads));
-  normal_expand_kernel<<<grid, kExpThreads, kExpSmemAlloc, st>>>(m_ckv, m_wuk, m_wuv, a);
-  return cudaGetLastError();
+  return launch_pdl(normal_expand_kernel, grid, dim3(kExpThreads), kExpSmemAlloc, st, m_ckv, m_wuk, m_wuv, a);
 }
 
 cudaError_t launch_normal_attention(const mla_geom* g, const mla_batch* bt, const __nv_bfloat16* q_nope,
@@ -681,8 +684,7 @@ cudaError_t launch_normal_attention(const mla_geom* g, const mla_batch* bt, cons
   a.scale_log2 = g->softmax_scale * 1.4426950408889634f;
   a.o = o; a.lse = lse; a.status = status;
   const dim3 grid((unsigned)((T + 127) / 128), (unsigned)H, (unsigned)B);
-  normal_attention_kernel<<<grid, kAttThreads, kAttSmemAlloc, st>>>(m_qn, m_qp, m_kv, m_kpe, a);
-  return cudaGetLastError();
+  return launch_pdl(normal_attention_kernel, grid, dim3(kAttThreads), kAttSmemAlloc, st, m_qn, m_qp, m_kv, m_kpe, a);
 }
 
 }  // namespace mla

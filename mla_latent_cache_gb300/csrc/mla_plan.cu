@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
   if (tid == 0) {
     s_W = 0; s_nonempty = 0; s_maxn = 0; s_err = 0; s_errinfo = 0; s_hash = 0;
   }
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
 
   // Sequence-length stamp and validation.
@@ -224,8 +226,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, const mla_geom* g, const mla_ba
   a.RB = (b->T * g->H + kRowsPerBlock - 1) / kRowsPerBlock;
   a.num_groups = b->B * a.RB;
   a.L = L;
-  plan_kernel<<<1, kPlanThreads, 0, st>>>(a, reinterpret_cast<char*>(ws));
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, a, reinterpret_cast<char*>(ws));
 }
 
 }  // namespace mla
