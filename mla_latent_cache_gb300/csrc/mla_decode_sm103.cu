@@ -33,7 +33,8 @@
 //
 // Roles per CTA (384 threads): warp 0 lane 0 issues TMA loads (each page as
 // two groups of 64 x 64 boxes, block-table entries read a few pages ahead);
-// warp 1 lane 0 issues Q K^T; warp 2 lane 0 issues P V; warps 4..11 run the
+// warp 1 issues Q K^T and warp 2 P V, each as a converged warp whose elected
+// lane issues the MMAs (warp-uniform descriptors); warps 4..11 run the
 // online softmax with two threads per query row (TMEM lane), write P and the
 // epilogue.  At a segment boundary the softmax stages the next segment's
 // query columns before it writes the finished segment out, so Q K^T of the
@@ -153,7 +154,7 @@ struct SegWalk {
 
 // Issue the Q K^T MMAs of one group of boxes into score tile d: A from TMEM
 // (query boxes 0..3) or shared memory (4..8), B from consecutive 8 KB boxes
-// starting at b0 (descriptor).
+// starting at b0 (descriptor).  Called by the whole warp; one lane issues.
 template <int HALF, bool GROUP_B>
 __device__ __forceinline__ void issue_qk_group(uint32_t d, uint32_t tmem, const uint64_t (&qdesc)[kQSmemBoxes],
                                                uint64_t b0, uint32_t idesc) {
@@ -166,9 +167,9 @@ __device__ __forceinline__ void issue_qk_group(uint32_t d, uint32_t tmem, const 
     for (int kk = 0; kk < 4; ++kk) {
       const uint32_t acc = (GROUP_B || j || kk) ? 1u : 0u;
       if (box < kQTmemBoxes)
-        mma_bf16_tmem_a(d, tmem + kTmemQ + 32 * box + 8 * kk, bd + 2 * kk, idesc, acc);
+        mma_bf16_tmem_a_e(d, tmem + kTmemQ + 32 * box + 8 * kk, bd + 2 * kk, idesc, acc);
       else
-        mma_bf16(d, qdesc[box - kQTmemBoxes] + 2 * kk, bd + 2 * kk, idesc, acc);
+        mma_bf16_e(d, qdesc[box - kQTmemBoxes] + 2 * kk, bd + 2 * kk, idesc, acc);
     }
   }
 }
@@ -178,9 +179,18 @@ __device__ __forceinline__ void fail(int* hdr, volatile int* abort_flag, int whe
   record_error(hdr, MLA_ERR_TIMEOUT, where);
 }
 
-// Q K^T issuer of one CTA (HALF = its rank in the pair), one thread.  Page t
-// goes to score tile t % 2 once P V of page t-2 has released it: Q K^T over
-// group A, release A, Q K^T over group B -> S_FULL.
+// A bounded wait taken by every lane of a warp; true only if all lanes saw the
+// phase complete (on a timeout lane 0 records it and raises the abort flag).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* hdr,
+                                          int where) {
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+  if (!ok && (threadIdx.x & 31) == 0) fail(hdr, abort_flag, where);
+  return ok;
+}
+
+// Q K^T issuer of one CTA (HALF = its rank in the pair), one converged warp.
+// Page t goes to score tile t % 2 once P V of page t-2 has released it: Q K^T
+// over group A, release A, Q K^T over group B -> S_FULL.
 template <int HALF>
 __device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
                                         const int* seg, SegWalk walk) {
@@ -199,38 +209,40 @@ __device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hd
   for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
     const int* rec = seg + (size_t)si * kSegWords;
     const int n_tiles = rec[3] - rec[2];
-    if (!mbar_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag) || !mbar_wait(sh.bar(BAR_QT_FULL), sc & 1, abort_flag)) {
-      fail(hdr, abort_flag, 22); ok = false; break;
+    if (!warp_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag, hdr, 22) ||
+        !warp_wait(sh.bar(BAR_QT_FULL), sc & 1, abort_flag, hdr, 22)) {
+      ok = false; break;
     }
     tc_fence_after();
     for (int i = 0; ok && i < n_tiles; ++i, ++ti) {
       const int st = ti % kStages, sb = ti & 1;
       const uint32_t par = (ti / kStages) & 1;
-      if ((ti >= 2 && !mbar_wait(sh.bar(BAR_P_EMPTY + sb), ((ti >> 1) - 1) & 1, abort_flag)) ||
-          !mbar_wait(sh.bar(BAR_FULL_A + st), par, abort_flag)) {
-        fail(hdr, abort_flag, 23); ok = false; break;
+      if ((ti >= 2 && !warp_wait(sh.bar(BAR_P_EMPTY + sb), ((ti >> 1) - 1) & 1, abort_flag, hdr, 23)) ||
+          !warp_wait(sh.bar(BAR_FULL_A + st), par, abort_flag, hdr, 23)) {
+        ok = false; break;
       }
       tc_fence_after();
       const uint32_t d = tmem + kTmemS + 64 * sb;
       issue_qk_group<HALF, false>(d, tmem, qdesc, adesc0 + st * kStageStep, id_qk);
-      mma_commit(sh.bar(BAR_EMPTY_A + st));
-      if (!mbar_wait(sh.bar(BAR_FULL_B + st), par, abort_flag)) { fail(hdr, abort_flag, 24); ok = false; break; }
+      mma_commit_e(sh.bar(BAR_EMPTY_A + st));
+      if (!warp_wait(sh.bar(BAR_FULL_B + st), par, abort_flag, hdr, 24)) { ok = false; break; }
       tc_fence_after();
       issue_qk_group<HALF, true>(d, tmem, qdesc, bdesc0 + st * kStageStep, id_qk);
-      mma_commit(sh.bar(BAR_S_FULL + sb));
-      if (i == n_tiles - 1) mma_commit(sh.bar(BAR_Q_EMPTY));
+      mma_commit_e(sh.bar(BAR_S_FULL + sb));
+      if (i == n_tiles - 1) mma_commit_e(sh.bar(BAR_Q_EMPTY));
     }
     ++sc;
   }
-  // Wait for every MMA issued by this thread before TMEM is released.
-  mma_commit(sh.bar(BAR_FINAL));
+  // Wait for every MMA issued by this warp before TMEM is released.
+  mma_commit_e(sh.bar(BAR_FINAL));
   volatile int never = 0;
   mbar_wait(sh.bar(BAR_FINAL), 0, &never);
+  __syncwarp();
 }
 
-// P V issuer, one thread: as soon as P of page t is written, O[:, own] += P V over
-// the page's group B (one N=256 MMA per K step, A = P from TMEM), then release
-// group B and the score tile.
+// P V issuer, one converged warp: as soon as P of page t is written, O[:, own] +=
+// P V over the page's group B (one N=256 MMA per K step, A = P from TMEM), then
+// release group B and the score tile.
 __device__ __forceinline__ void pv_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
                                         const int* seg, SegWalk walk) {
   const uint32_t id_pv = idesc_bf16_f32(128, 256, 1);
@@ -242,24 +254,25 @@ __device__ __forceinline__ void pv_role(const Shared& sh, uint32_t tmem, int* hd
     const int* rec = seg + (size_t)si * kSegWords;
     const int n_tiles = rec[3] - rec[2];
     for (int i = 0; i < n_tiles; ++i, ++ti) {
-      if (i == 0 && sc > 0 && !mbar_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag)) {
-        fail(hdr, abort_flag, 20); ok = false; break;
+      if (i == 0 && sc > 0 && !warp_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag, hdr, 20)) {
+        ok = false; break;
       }
       const int sb = ti & 1, st = ti % kStages;
-      if (!mbar_wait(sh.bar(BAR_P_FULL + sb), (ti >> 1) & 1, abort_flag)) { fail(hdr, abort_flag, 21); ok = false; break; }
+      if (!warp_wait(sh.bar(BAR_P_FULL + sb), (ti >> 1) & 1, abort_flag, hdr, 21)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemS + 64 * sb + 8 * kk, vdesc0 + st * kStageStep + 128 * kk, id_pv,
-                        (i == 0 && kk == 0) ? 0u : 1u);
-      mma_commit(sh.bar(BAR_EMPTY_B + st));
-      mma_commit(sh.bar(BAR_P_EMPTY + sb));
+        mma_bf16_tmem_a_e(tmem + kTmemO, tmem + kTmemS + 64 * sb + 8 * kk, vdesc0 + st * kStageStep + 128 * kk, id_pv,
+                          (i == 0 && kk == 0) ? 0u : 1u);
+      mma_commit_e(sh.bar(BAR_EMPTY_B + st));
+      mma_commit_e(sh.bar(BAR_P_EMPTY + sb));
     }
     ++sc;
   }
-  mma_commit(sh.bar(BAR_FINAL_PV));
+  mma_commit_e(sh.bar(BAR_FINAL_PV));
   volatile int never = 0;
   mbar_wait(sh.bar(BAR_FINAL_PV), 0, &never);
+  __syncwarp();
 }
 
 // What a softmax thread needs to know about one segment.
@@ -436,16 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ Q K^T issuer
-    if (lane == 0) {
-      if (half == 0) qk_role<0>(sh, tmem, hdr, abort_flag, seg, walk0);
-      else qk_role<1>(sh, tmem, hdr, abort_flag, seg, walk0);
-    }
-    __syncwarp();
+    // ------------------------------------------------------------ Q K^T issuer (whole warp)
+    if (half == 0) qk_role<0>(sh, tmem, hdr, abort_flag, seg, walk0);
+    else qk_role<1>(sh, tmem, hdr, abort_flag, seg, walk0);
   } else if (warp == 2) {
-    // ------------------------------------------------------------ P V issuer
-    if (lane == 0) pv_role(sh, tmem, hdr, abort_flag, seg, walk0);
-    __syncwarp();
+    // ------------------------------------------------------------ P V issuer (whole warp)
+    pv_role(sh, tmem, hdr, abort_flag, seg, walk0);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
     // Two threads per query row: warps 4..7 take score columns 0..31 of their
