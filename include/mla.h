@@ -39,7 +39,10 @@
  *     errors seen by kernels are recorded in the workspace's status word and
  *     read back with mla_read_device_status.
  *   Alignment: every device pointer must be 16-byte aligned, and strides must
- *     keep rows 16-byte aligned (MLA_ERR_ALIGN otherwise).
+ *     keep rows 16-byte aligned (MLA_ERR_ALIGN otherwise); the outputs written
+ *     with 32-byte stores (q_lat of mla_absorb_q, o of mla_unabsorb_o, o_lat
+ *     and the workspace of mla_plan / mla_decode, kv_exp of mla_normal_expand,
+ *     o of mla_normal_attention) must be 32-byte aligned.
  *   Causality: with causal != 0, query token t of sequence b sees cache rows
  *     0 .. S_b - T + t (bottom-right aligned); otherwise all S_b rows.
  *   Empty sequences: S_b = 0 gives o_lat = 0 and lse = -inf.
@@ -64,7 +67,7 @@ typedef enum {
   MLA_OK = 0,
   MLA_ERR_ARG = -1,          /* null pointer, negative size, unsupported flag */
   MLA_ERR_SHAPE = -2,        /* geometry not supported (d_* must be 512/64/128/128, P = 64, 1 <= H <= 128, 128 % H == 0) */
-  MLA_ERR_ALIGN = -3,        /* pointer or stride not 16-byte aligned */
+  MLA_ERR_ALIGN = -3,        /* pointer or stride not 16-byte (outputs: 32-byte) aligned */
   MLA_ERR_WORKSPACE = -4,    /* workspace smaller than mla_workspace_size() */
   MLA_ERR_PLAN_STALE = -5,   /* (device) plan built for other lengths/geometry */
   MLA_ERR_CUDA = -6,         /* a CUDA runtime call or launch failed */

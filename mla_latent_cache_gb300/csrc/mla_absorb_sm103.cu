@@ -142,15 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tok < BT) {
           __nv_bfloat16* dst = out + ((size_t)tok * H + h) * n_total + n0 + 32 * c;
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 w;
-            __nv_bfloat162 p0 = __floats2bfloat162_rn(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-            __nv_bfloat162 p1 = __floats2bfloat162_rn(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-            __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
-            __nv_bfloat162 p3 = __floats2bfloat162_rn(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
-            w.x = *reinterpret_cast<uint32_t*>(&p0); w.y = *reinterpret_cast<uint32_t*>(&p1);
-            w.z = *reinterpret_cast<uint32_t*>(&p2); w.w = *reinterpret_cast<uint32_t*>(&p3);
-            *reinterpret_cast<uint4*>(dst + e) = w;
+          for (int e = 0; e < 32; e += 16) {
+            uint32_t w[8];
+            pack_bf16x8(v + e, 1.f, w);
+            pack_bf16x8(v + e + 8, 1.f, w + 4);
+            st_global_v8(dst + e, w);
           }
         }
       }

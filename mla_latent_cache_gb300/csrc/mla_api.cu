@@ -14,6 +14,7 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 mla_status check_geom(const mla_geom* g) {
   if (!g) return MLA_ERR_ARG;
@@ -118,7 +119,7 @@ mla_status mla_plan(const mla_geom* geom, const mla_batch* batch, const int32_t*
   if (s != MLA_OK) return s;
   if ((s = check_batch(batch)) != MLA_OK) return s;
   if (!workspace || (batch->B > 0 && !seq_lens)) return MLA_ERR_ARG;
-  if (!aligned16(workspace) || !aligned16(seq_lens)) return MLA_ERR_ALIGN;
+  if (!aligned32(workspace) || !aligned16(seq_lens)) return MLA_ERR_ALIGN;
   WsLayout L;
   if (!compute_layout(geom, batch, &L)) return MLA_ERR_SHAPE;
   if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
@@ -132,7 +133,7 @@ mla_status mla_absorb_q(const mla_geom* geom, const void* q_nope, const void* w_
   if (BT < 0) return MLA_ERR_ARG;
   if (BT == 0) return MLA_OK;
   if (!q_nope || !w_uk || !q_lat) return MLA_ERR_ARG;
-  if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_lat)) return MLA_ERR_ALIGN;
+  if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned32(q_lat)) return MLA_ERR_ALIGN;
   return cuda_status(launch_absorb_sm103(static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(w_uk),
                                    static_cast<__nv_bfloat16*>(q_lat), BT, geom->H, (cudaStream_t)stream));
 }
@@ -144,7 +145,7 @@ mla_status mla_unabsorb_o(const mla_geom* geom, const void* o_lat, const void* w
   if (BT < 0) return MLA_ERR_ARG;
   if (BT == 0) return MLA_OK;
   if (!o_lat || !w_uv || !o) return MLA_ERR_ARG;
-  if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(o)) return MLA_ERR_ALIGN;
+  if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned32(o)) return MLA_ERR_ALIGN;
   return cuda_status(launch_unabsorb_sm103(static_cast<const __nv_bfloat16*>(o_lat), static_cast<const __nv_bfloat16*>(w_uv),
                                      static_cast<__nv_bfloat16*>(o), BT, geom->H, (cudaStream_t)stream));
 }
@@ -177,7 +178,7 @@ mla_status mla_decode(const mla_geom* geom, const mla_batch* batch, const void* 
   if (batch->B == 0) return MLA_OK;
   if (!q_lat || !q_pe || !block_table || !seq_lens || !o_lat || !lse || !workspace) return MLA_ERR_ARG;
   if (bt_stride < batch->max_pages) return MLA_ERR_ARG;
-  if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned16(o_lat) || !aligned16(lse) || !aligned16(workspace) ||
+  if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned32(o_lat) || !aligned16(lse) || !aligned32(workspace) ||
       !aligned16(block_table) || !aligned16(seq_lens))
     return MLA_ERR_ALIGN;
   CacheView cv;
@@ -232,7 +233,7 @@ mla_status mla_normal_expand(const mla_geom* geom, const mla_cache* cache, const
   if (B == 0) return MLA_OK;
   if (!block_table || !seq_lens || !w_uk || !w_uv || !kv_exp || bt_stride < max_pages) return MLA_ERR_ARG;
   if ((long long)B * normal_rows_per_seq(max_pages) >= (1LL << 31)) return MLA_ERR_SHAPE;
-  if (!aligned16(block_table) || !aligned16(seq_lens) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(kv_exp))
+  if (!aligned16(block_table) || !aligned16(seq_lens) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned32(kv_exp))
     return MLA_ERR_ALIGN;
   CacheView cv;
   if ((s = check_cache(cache, &cv)) != MLA_OK) return s;
@@ -256,7 +257,7 @@ mla_status mla_normal_attention(const mla_geom* geom, const mla_batch* batch, co
       (batch->T + 127) / 128 > 65535)
     return MLA_ERR_SHAPE;
   if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(block_table) || !aligned16(seq_lens) ||
-      !aligned16(kv_exp) || !aligned16(o) || !aligned16(lse))
+      !aligned16(kv_exp) || !aligned32(o) || !aligned16(lse))
     return MLA_ERR_ALIGN;
   CacheView cv;
   if ((s = check_cache(cache, &cv)) != MLA_OK) return s;

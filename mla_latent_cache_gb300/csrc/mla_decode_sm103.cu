@@ -639,26 +639,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(t_lane + kTmemO + 32 * c, o);
         tmem_wait_ld();
         if (cur.row_valid) {
+          // 32-byte stores: each thread writes whole sectors of its row.
           if (slot_out < 0) {
             __nv_bfloat16* dst = a.o_lat + ((size_t)b * R + fr) * kDLat + 256 * half + 32 * c;
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 v;
-              __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-              __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-              __nv_bfloat162 h3 = __floats2bfloat162_rn(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-              v.x = *reinterpret_cast<uint32_t*>(&h0); v.y = *reinterpret_cast<uint32_t*>(&h1);
-              v.z = *reinterpret_cast<uint32_t*>(&h2); v.w = *reinterpret_cast<uint32_t*>(&h3);
-              *reinterpret_cast<uint4*>(dst + e) = v;
+            for (int e = 0; e < 32; e += 16) {
+              uint32_t w[8];
+              pack_bf16x8(o + e, inv, w);
+              pack_bf16x8(o + e + 8, inv, w + 4);
+              st_global_v8(dst + e, w);
             }
           } else {
             float* dst = part_o + ((size_t)slot_out * kRowsPerBlock + row) * kDLat + 256 * half + 32 * c;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(dst + e) =
-                  make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                              __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            for (int e = 0; e < 32; e += 8) {
+              uint32_t w[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(__uint_as_float(o[e + k]) * inv);
+              st_global_v8(dst + e, w);
+            }
           }
         }
       }

@@ -237,15 +237,11 @@ __global__ void __launch_bounds__(kExpThreads, 1)
         tmem_ld32(t_lane + 256 * acc + 32 * c, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint4 w;
-          __nv_bfloat162 p0 = __floats2bfloat162_rn(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-          __nv_bfloat162 p1 = __floats2bfloat162_rn(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-          __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
-          __nv_bfloat162 p3 = __floats2bfloat162_rn(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
-          w.x = *reinterpret_cast<uint32_t*>(&p0); w.y = *reinterpret_cast<uint32_t*>(&p1);
-          w.z = *reinterpret_cast<uint32_t*>(&p2); w.w = *reinterpret_cast<uint32_t*>(&p3);
-          *reinterpret_cast<uint4*>(dst + 32 * c + e) = w;
+        for (int e = 0; e < 32; e += 16) {
+          uint32_t w[8];
+          pack_bf16x8(v + e, 1.f, w);
+          pack_bf16x8(v + e + 8, 1.f, w + 4);
+          st_global_v8(dst + 32 * c + e, w);
         }
       }
       tc_fence_before();
@@ -550,15 +546,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         }
         if (row_valid) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 v;
-            __nv_bfloat162 p0 = __floats2bfloat162_rn(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-            __nv_bfloat162 p1 = __floats2bfloat162_rn(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-            __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-            __nv_bfloat162 p3 = __floats2bfloat162_rn(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-            v.x = *reinterpret_cast<uint32_t*>(&p0); v.y = *reinterpret_cast<uint32_t*>(&p1);
-            v.z = *reinterpret_cast<uint32_t*>(&p2); v.w = *reinterpret_cast<uint32_t*>(&p3);
-            *reinterpret_cast<uint4*>(dst + 32 * c + e) = v;
+          for (int e = 0; e < 32; e += 16) {
+            uint32_t w[8];
+            pack_bf16x8(o + e, inv, w);
+            pack_bf16x8(o + e + 8, inv, w + 4);
+            st_global_v8(dst + 32 * c + e, w);
           }
         }
       }

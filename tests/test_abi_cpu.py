@@ -52,6 +52,9 @@ def test_host_validation_rejects_before_launch(mla):
     assert mla.mla_absorb_q(g, None, None, None, 4, 0) == mla.MLA_ERR_ARG
     assert mla.mla_unabsorb_o(g, None, None, None, 4, 0) == mla.MLA_ERR_ARG
     assert mla.mla_absorb_q(g, 0x1000, 0x2000, 0x3008, 4, 0) == mla.MLA_ERR_ALIGN
+    # outputs written with 32-byte stores must be 32-byte aligned (16 is not enough)
+    assert mla.mla_absorb_q(g, 0x1000, 0x2000, 0x3010, 4, 0) == mla.MLA_ERR_ALIGN
+    assert mla.mla_unabsorb_o(g, 0x1000, 0x2000, 0x3010, 4, 0) == mla.MLA_ERR_ALIGN
     assert mla.mla_absorb_q(mla.make_geom(24), 0x1000, 0x2000, 0x3000, 4, 0) == mla.MLA_ERR_SHAPE
     assert mla.mla_absorb_q(g, 0x1000, 0x2000, 0x3000, 0, 0) == mla.MLA_OK  # nothing to do
     b = mla.make_batch(2, 1, False, 8, num_slots=4)
