@@ -1,5 +1,5 @@
-// Split-KV absorbed-MLA decode on the sm_103a tensor cores (TMA + tcgen05/TMEM,
-// 2-CTA clusters).
+// Split-KV absorbed-MLA decode on the sm_103a tensor cores: TMA, tcgen05 pair
+// MMAs (cta_group::2) with tensor-memory accumulators, 2-CTA clusters.
 //
 // What it computes ("MLA in full detail", Step 3; "M5.8" 0x04 absorbed
 // reference): for every query row (b, t, h) of a plan segment,
@@ -9,45 +9,55 @@
 // j / 64 is found through the block table ("M5.8" 0x05).
 //
 // Work decomposition.  A query-row group is 128 flattened (t, h) rows of one
-// sequence (one token's 128 heads at V3 geometry).  Its fp32 accumulator,
-// 128 x 512, would take all 512 TMEM columns of an SM, so each group is
-// handled by a CLUSTER of two CTAs: CTA h accumulates the output columns
-// [256 h, 256 h + 256).  For each 64-row cache page both CTAs form the full
-// 128 x 64 score tile S = Q K^T over all 576 columns (the second read of a
-// page usually hits L2; the pair is co-scheduled as a cluster), run the same
-// softmax, and each accumulates O[:, cols_h] += P V[:, cols_h], V being the
-// leading 512 columns of the cached rows.  Swapping partial score tiles
-// between the two CTAs instead of computing S twice was measured to cost more
-// than it saves: the exchange moves as many bytes as the cache itself through
-// distributed shared memory.
-// Tensor-core shapes: Q K^T is M=128 x N=64 per K=16 step (36 steps per page);
-// P V is M=128 x N=256 x K=16 (four steps per page), P read from TMEM.
+// sequence (one token's 128 heads at V3 geometry), handled by a CLUSTER of two
+// CTAs: CTA r owns rows [64 r, 64 r + 64) and everything per row (softmax
+// state, accumulator, outputs).  Every product is a pair MMA issued by CTA 0:
+//   S = Q K^T   M=128 (64 rows per CTA), N=64 (one page), K=576: each CTA
+//               holds half of the page's cache rows (rows [32 r, 32 r + 32))
+//               as its half of B, so the page is read once per pair and no
+//               score is computed twice;
+//   O += P V    M=128, N=256 per MMA (two MMAs cover the 512 latent columns),
+//               K=64 page rows: A = P of the CTA's own rows (shared memory),
+//               B = V split along N: CTA r supplies latent columns
+//               [256 m + 128 r, +128) of MMA m for all 64 rows of the page.
+// For P V each CTA therefore also needs the other half's rows of its latent
+// columns; once Q K^T is done with a page, the four slots that held this
+// CTA's Q K^T-only latent boxes are reloaded with exactly those rows (an L2 hit:
+// the partner CTA fetched them from HBM), which puts every P V operand at the
+// same shared-memory offset in both CTAs.
 //
-// TMEM per CTA (512 columns): O half at 0..255; two 64-column score tiles at
-// 256..383 (page t uses tile t % 2, so Q K^T of page t+1 runs while the
-// softmax of page t reads its tile); the softmax writes P (bf16 pairs) over
-// the first 32 columns of the tile it has read, which is where P V takes its
-// A operand; query columns 0..255 (bf16 pairs, the TMEM A operand of Q K^T)
-// at 384..511.  The rest of the query tile (latent 256..511 and RoPE) stays in
-// shared memory next to a 2-stage page ring.
+// Tensor memory per CTA (512 columns, allocated for the pair):
+//   O:  columns 0..255: 64 rows x 512 latent columns, packed two rows per TMEM
+//       lane: lane i < 64 holds row i, latent [256 m, +128) of MMA m at columns
+//       128 m ..; lane 64 + i holds row i, latent [256 m + 128, +128);
+//   S:  two 32-column score tiles (page t uses tile t % 2): lane i < 64 holds
+//       row i's scores for page rows 0..31, lane 64 + i for rows 32..63;
+//   Q:  query columns 0..383 (bf16 pairs), the TMEM A operand of the first 24
+//       K steps; query columns 384..575 stay in shared memory.  Row i sits in
+//       lane i AND lane 64 + i: with the packed M=128 pair layout, the lanes
+//       that produce the second half of N read their A rows from lanes 64..127
+//       (measured on this part: the lower copy alone leaves that half without
+//       those K steps).
+// Shared memory per CTA: a ring of page stages (nine 32-row x 64-column boxes,
+// 36 KB), the P tiles (64 rows x 64 page rows, bf16, K-major) and the shared
+// part of the query.
 //
-// Roles per CTA (384 threads): warp 0 lane 0 issues TMA loads (each page as
-// two groups of 64 x 64 boxes, block-table entries read a few pages ahead);
-// warp 1 issues Q K^T and warp 2 P V, each as a converged warp whose elected
-// lane issues the MMAs (warp-uniform descriptors); warps 4..11 run the
-// online softmax with two threads per query row (TMEM lane), write P and the
-// epilogue.  At a segment boundary the softmax stages the next segment's
-// query columns before it writes the finished segment out, so Q K^T of the
-// next segment overlaps that epilogue.  The softmax keeps a per-row
-// reference max and rescales the TMEM accumulator only when the running max
-// grows past it by more than 2^8 (exact for any reference; only rounding
-// differs), with scores in log2 units.  Cache rows past the sequence end
-// (last page only) are zeroed in shared memory before P V so stale or NaN
-// contents never reach the accumulator.
+// Roles (256 threads per CTA): warp 0 issues the page loads and warp 3 the
+// reloads; in CTA 0 warp 1 issues the Q K^T MMAs and warp 2 the P V MMAs (two
+// issuers, so that Q K^T of the next pages keeps the tensor pipe busy while
+// P V waits for the softmax); in CTA 1 warps 2 and 1 forward the arrival of
+// its page halves and of its reloads to CTA 0; warps 4..7 run the online
+// softmax (one thread per TMEM lane: row i % 64, page half i / 64), write P,
+// stage the query and write the outputs.  The softmax keeps a per-row reference max and rescales its accumulator rows only
+// when the running max grows past it by more than 2^8 (exact for any
+// reference; only rounding differs), with scores in log2 units.  Cache rows
+// past the sequence end (last page only) are zeroed in shared memory before
+// P V so stale or NaN contents never reach the accumulator.
 //
 // Every wait is bounded; a wait that runs out records MLA_ERR_TIMEOUT in the
 // workspace and raises a CTA-wide abort flag.  Loads and MMAs already issued
-// are drained, TMEM is freed and both CTAs meet at a final cluster barrier.
+// are drained, and both CTAs meet at a final cluster barrier before the
+// tensor memory is freed.
 #include <math.h>
 
 #include "mla_internal.cuh"
@@ -58,59 +68,62 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 384;                  // TMA, Q K^T and P V issue warps, 1 idle, 8 softmax warps
-constexpr int kSoftmaxThreads = 256;
-constexpr int kBoxBytes = 64 * 64 * 2;         // 8 KB: one 64-row page x 64 bf16 columns
-constexpr int kQBoxBytes = 128 * 64 * 2;       // 16 KB: 128 query rows x 64 bf16
-constexpr int kBoxes = 9;                      // 8 latent boxes + 1 RoPE box per row
-constexpr int kOwnBoxes = 4;                   // latent boxes whose columns this CTA accumulates
-constexpr int kQTmemBoxes = 4;                 // query boxes 0..3 live in TMEM
+constexpr int kThreads = 256;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kCtaRows = 64;                   // query rows per CTA
+constexpr int kHalfRows = 32;                  // page rows loaded by each CTA
+constexpr int kBoxes = 9;                      // 8 latent boxes + 1 RoPE box per cached row
+constexpr int kSlotBytes = kHalfRows * 128;    // 4 KB: 32 rows x 64 bf16, 128-byte swizzled
+constexpr int kStageBytes = kBoxes * kSlotBytes;
+constexpr int kStages = 4;
+constexpr int kQTmemBoxes = 6;                 // query boxes 0..5 in TMEM
 constexpr int kQSmemBoxes = kBoxes - kQTmemBoxes;
-constexpr int kStages = 2;                     // page stages in the ring
-constexpr int kGroupABoxes = 5;                // boxes only Q K^T needs (released after it)
-constexpr int kStageBytes = kBoxes * kBoxBytes;  // group A (5 boxes) then group B (4 value boxes)
+constexpr int kQBoxBytes = kCtaRows * 128;     // 8 KB
+constexpr int kPBufs = 3;
+constexpr int kPBytes = kCtaRows * 128;        // 8 KB: 64 rows x 64 page rows bf16
 constexpr int kSmemQ = 0;
-constexpr int kSmemRing = kSmemQ + kQSmemBoxes * kQBoxBytes;  // 81920
-constexpr int kSmemBar = kSmemRing + kStages * kStageBytes;   // 229376
-constexpr int kSmemXchg = kSmemBar + 256;                     // float [2 buffers][2 halves][128 rows]
-constexpr int kSmemBytes = kSmemXchg + 2048;
-constexpr int kSmemAlloc = kSmemBytes + 768;                  // slack to align the base to 1024 B (checked)
+constexpr int kSmemP = kSmemQ + kQSmemBoxes * kQBoxBytes;
+constexpr int kSmemRing = kSmemP + kPBufs * kPBytes;
+constexpr int kSmemBar = kSmemRing + kStages * kStageBytes;
+constexpr int kSmemXchg = kSmemBar + 512;                     // float [2 buffers][2 halves][64 rows]
+constexpr int kSmemBytes = kSmemXchg + 1024;
+constexpr int kSmemAlloc = kSmemBytes + 1024;                 // slack to align the base to 1024 B (checked)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
-constexpr uint32_t kTmemS = 256;   // tile t % 2 at kTmemS + 64 (t % 2)
-constexpr uint32_t kTmemQ = 384;
+constexpr uint32_t kTmemS = 256;   // tile t % 2 at kTmemS + 32 (t % 2)
+constexpr uint32_t kTmemQ = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-enum {
-  BAR_FULL_A = 0,                      // kStages: group A of a page landed
-  BAR_EMPTY_A = BAR_FULL_A + kStages,  // kStages: Q K^T done with group A
-  BAR_FULL_B = BAR_EMPTY_A + kStages,  // kStages: group B (value boxes) landed
-  BAR_EMPTY_B = BAR_FULL_B + kStages,  // kStages: P V done with group B
-  BAR_Q_FULL = BAR_EMPTY_B + kStages,  // query boxes in shared memory landed
-  BAR_Q_EMPTY,                         // Q K^T done with the segment's query
-  BAR_QT_FULL,                         // query columns staged in TMEM (256 arrivals)
-  BAR_S_FULL,                          // 2: score tile written
-  BAR_P_FULL = BAR_S_FULL + 2,         // 2: P written over the score tile (256 arrivals)
-  BAR_P_EMPTY = BAR_P_FULL + 2,        // 2: P V done with the tile (it may be overwritten)
-  BAR_O_EMPTY = BAR_P_EMPTY + 2,       // epilogue done with the accumulator (256 arrivals)
-  BAR_FINAL,
-  BAR_FINAL_PV,
-  BAR_XCH,                             // 4: the two softmax warps of a TMEM lane quadrant
-  kNumBars = BAR_XCH + 4
-};
-static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
+static_assert(kTmemQ + 32 * kQTmemBoxes <= kTmemCols, "tensor memory");
 static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
+static_assert(kSmemRing % 1024 == 0 && kSmemP % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle atoms");
 
-// A page is staged as two groups of 64 x 64 boxes: group A holds the five
-// boxes this CTA needs only for Q K^T (the other CTA's four latent boxes and
-// the RoPE box), released as soon as those MMAs complete; group B holds the
-// four latent boxes whose columns this CTA accumulates, contiguous so that one
-// N=256 MMA per K step covers them in P V, and released after P V.  Box order
-// (by 64-column box index of the cached row; 8 = RoPE):
-template <int HALF> struct Boxes {
-  static constexpr int a(int j) { return j == 4 ? 8 : (HALF == 0 ? 4 + j : j); }
-  static constexpr int b(int c) { return 4 * HALF + c; }
+enum {
+  BAR_FULL = 0,                        // kStages: this CTA's half-page landed (TMA)
+  BAR_PEER = BAR_FULL + kStages,       // kStages: (CTA 0) CTA 1's half-page landed (relayed)
+  BAR_RELOAD = BAR_PEER + kStages,     // kStages: the reloaded partner rows landed (TMA)
+  BAR_PEER_RL = BAR_RELOAD + kStages,  // kStages: (CTA 0) CTA 1's reload landed (relayed)
+  BAR_QK_DONE = BAR_PEER_RL + kStages, // kStages: Q K^T of the page done (both CTAs)
+  BAR_PV_DONE = BAR_QK_DONE + kStages, // kStages: P V of the page done (both CTAs)
+  BAR_S_FULL = BAR_PV_DONE + kStages,  // 2: score tile written (both CTAs)
+  BAR_S_FREE = BAR_S_FULL + 2,         // 2: (CTA 0) both CTAs' softmax read the tile (8 warp arrivals)
+  BAR_P_FULL = BAR_S_FREE + 2,         // kPBufs: (CTA 0) both CTAs wrote P (8 warp arrivals)
+  BAR_Q_TMA = BAR_P_FULL + kPBufs,     // query boxes in shared memory landed (TMA)
+  BAR_Q_READY = BAR_Q_TMA + 1,         // (CTA 0) both CTAs staged the query (8 warp arrivals)
+  BAR_Q_FREE = BAR_Q_READY + 1,        // Q K^T of the segment done with the query (both CTAs)
+  BAR_O_FREE = BAR_Q_FREE + 1,         // (CTA 0) both CTAs' epilogues read the accumulator (8 warp arrivals)
+  BAR_XCH = BAR_O_FREE + 1,            // 2: the two softmax warps sharing a row range (64 arrivals)
+  BAR_FINAL_QK = BAR_XCH + 2,
+  BAR_FINAL_PV,
+  kNumBars = BAR_FINAL_PV + 1
 };
+static_assert(kNumBars * 8 + 8 <= 512, "barrier area");
+
+// Slots: box b of a page half is slot b.  CTA r accumulates latent boxes
+// {2r, 2r+1, 4+2r, 5+2r}; after Q K^T the slots of the other four latent boxes
+// receive those boxes' rows of the other page half.
+__device__ __forceinline__ int own_pv_box(int r, int i) { return (i < 2 ? 0 : 4) + 2 * r + (i & 1); }
+__device__ __forceinline__ int reload_slot(int r, int i) { return (i < 2 ? 0 : 4) + 2 * (1 - r) + (i & 1); }
 
 struct FastArgs {
   const __nv_bfloat16* q_lat;
@@ -127,8 +140,9 @@ struct FastArgs {
 struct Shared {
   uint32_t base;
   __device__ uint32_t q(int box) const { return base + kSmemQ + (box - kQTmemBoxes) * kQBoxBytes; }
-  __device__ uint32_t stage_a(int st) const { return base + kSmemRing + st * kStageBytes; }
-  __device__ uint32_t stage_b(int st) const { return stage_a(st) + kGroupABoxes * kBoxBytes; }
+  __device__ uint32_t p(int buf) const { return base + kSmemP + buf * kPBytes; }
+  __device__ uint32_t stage(int st) const { return base + kSmemRing + st * kStageBytes; }
+  __device__ uint32_t slot(int st, int s) const { return stage(st) + s * kSlotBytes; }
   __device__ uint32_t bar(int i) const { return base + kSmemBar + i * 8; }
 };
 
@@ -152,28 +166,6 @@ struct SegWalk {
   __device__ void advance() { ++si; }
 };
 
-// Issue the Q K^T MMAs of one group of boxes into score tile d: A from TMEM
-// (query boxes 0..3) or shared memory (4..8), B from consecutive 8 KB boxes
-// starting at b0 (descriptor).  Called by the whole warp; one lane issues.
-template <int HALF, bool GROUP_B>
-__device__ __forceinline__ void issue_qk_group(uint32_t d, uint32_t tmem, const uint64_t (&qdesc)[kQSmemBoxes],
-                                               uint64_t b0, uint32_t idesc) {
-  constexpr int n = GROUP_B ? kOwnBoxes : kGroupABoxes;
-#pragma unroll
-  for (int j = 0; j < n; ++j) {
-    const int box = GROUP_B ? Boxes<HALF>::b(j) : Boxes<HALF>::a(j);
-    const uint64_t bd = b0 + (uint64_t)(j * (kBoxBytes >> 4));
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint32_t acc = (GROUP_B || j || kk) ? 1u : 0u;
-      if (box < kQTmemBoxes)
-        mma_bf16_tmem_a_e(d, tmem + kTmemQ + 32 * box + 8 * kk, bd + 2 * kk, idesc, acc);
-      else
-        mma_bf16_e(d, qdesc[box - kQTmemBoxes] + 2 * kk, bd + 2 * kk, idesc, acc);
-    }
-  }
-}
-
 __device__ __forceinline__ void fail(int* hdr, volatile int* abort_flag, int where) {
   *abort_flag = 1;
   record_error(hdr, MLA_ERR_TIMEOUT, where);
@@ -188,92 +180,28 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return ok;
 }
 
-// Q K^T issuer of one CTA (HALF = its rank in the pair), one converged warp.
-// Page t goes to score tile t % 2 once P V of page t-2 has released it: Q K^T
-// over group A, release A, Q K^T over group B -> S_FULL.
-template <int HALF>
-__device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
-                                        const int* seg, SegWalk walk) {
-  const uint32_t id_qk = idesc_bf16_f32(128, 64, 0);
-  // Descriptors are built once; steps only move the start-address field (16-byte
-  // units): +2 per 32-byte K step of a K-major tile, +kBoxBytes/16 per box,
-  // +kStageBytes/16 per stage.
-  uint64_t qdesc[kQSmemBoxes];
-#pragma unroll
-  for (int bx = 0; bx < kQSmemBoxes; ++bx) qdesc[bx] = sw128_desc(sh.q(kQTmemBoxes + bx), 16, 1024);
-  const uint64_t adesc0 = sw128_desc(sh.stage_a(0), 16, 1024);
-  const uint64_t bdesc0 = sw128_desc(sh.stage_b(0), 16, 1024);
-  constexpr uint32_t kStageStep = kStageBytes >> 4;
-  int ti = 0, sc = 0;
-  bool ok = true;
-  for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
-    const int* rec = seg + (size_t)si * kSegWords;
-    const int n_tiles = rec[3] - rec[2];
-    if (!warp_wait(sh.bar(BAR_Q_FULL), sc & 1, abort_flag, hdr, 22) ||
-        !warp_wait(sh.bar(BAR_QT_FULL), sc & 1, abort_flag, hdr, 22)) {
-      ok = false; break;
-    }
-    tc_fence_after();
-    for (int i = 0; ok && i < n_tiles; ++i, ++ti) {
-      const int st = ti % kStages, sb = ti & 1;
-      const uint32_t par = (ti / kStages) & 1;
-      if ((ti >= 2 && !warp_wait(sh.bar(BAR_P_EMPTY + sb), ((ti >> 1) - 1) & 1, abort_flag, hdr, 23)) ||
-          !warp_wait(sh.bar(BAR_FULL_A + st), par, abort_flag, hdr, 23)) {
-        ok = false; break;
-      }
-      tc_fence_after();
-      const uint32_t d = tmem + kTmemS + 64 * sb;
-      issue_qk_group<HALF, false>(d, tmem, qdesc, adesc0 + st * kStageStep, id_qk);
-      mma_commit_e(sh.bar(BAR_EMPTY_A + st));
-      if (!warp_wait(sh.bar(BAR_FULL_B + st), par, abort_flag, hdr, 24)) { ok = false; break; }
-      tc_fence_after();
-      issue_qk_group<HALF, true>(d, tmem, qdesc, bdesc0 + st * kStageStep, id_qk);
-      mma_commit_e(sh.bar(BAR_S_FULL + sb));
-      if (i == n_tiles - 1) mma_commit_e(sh.bar(BAR_Q_EMPTY));
-    }
-    ++sc;
+// One arrival per warp on a barrier of CTA 0 (local for CTA 0, through the
+// cluster window for CTA 1).  What these arrivals order is either in the
+// arriving CTA's own shared or tensor memory, read by its own SM's half of the
+// pair MMA (P and the query after fence.proxy.async / tcgen05 fences), or a
+// read the arriving CTA has finished (score and accumulator loads), so the
+// default CTA-scope release suffices; a cluster-scope release was measured to
+// cost ~1000 cycles per arrival.
+__device__ __forceinline__ void warp_arrive_leader(uint32_t bar, int rank) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (rank == 0) mbar_arrive(bar);
+    else asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(map_to_cta(bar, 0)) : "memory");
   }
-  // Wait for every MMA issued by this warp before TMEM is released.
-  mma_commit_e(sh.bar(BAR_FINAL));
-  volatile int never = 0;
-  mbar_wait(sh.bar(BAR_FINAL), 0, &never);
   __syncwarp();
 }
 
-// P V issuer, one converged warp: as soon as P of page t is written, O[:, own] +=
-// P V over the page's group B (one N=256 MMA per K step, A = P from TMEM), then
-// release group B and the score tile.
-__device__ __forceinline__ void pv_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
-                                        const int* seg, SegWalk walk) {
-  const uint32_t id_pv = idesc_bf16_f32(128, 256, 1);
-  const uint64_t vdesc0 = sw128_desc(sh.stage_b(0), kBoxBytes, 1024);
-  constexpr uint32_t kStageStep = kStageBytes >> 4;
-  int ti = 0, sc = 0;
-  bool ok = true;
-  for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
-    const int* rec = seg + (size_t)si * kSegWords;
-    const int n_tiles = rec[3] - rec[2];
-    for (int i = 0; i < n_tiles; ++i, ++ti) {
-      if (i == 0 && sc > 0 && !warp_wait(sh.bar(BAR_O_EMPTY), (sc - 1) & 1, abort_flag, hdr, 20)) {
-        ok = false; break;
-      }
-      const int sb = ti & 1, st = ti % kStages;
-      if (!warp_wait(sh.bar(BAR_P_FULL + sb), (ti >> 1) & 1, abort_flag, hdr, 21)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_bf16_tmem_a_e(tmem + kTmemO, tmem + kTmemS + 64 * sb + 8 * kk, vdesc0 + st * kStageStep + 128 * kk, id_pv,
-                          (i == 0 && kk == 0) ? 0u : 1u);
-      mma_commit_e(sh.bar(BAR_EMPTY_B + st));
-      mma_commit_e(sh.bar(BAR_P_EMPTY + sb));
-    }
-    ++sc;
-  }
-  mma_commit_e(sh.bar(BAR_FINAL_PV));
-  volatile int never = 0;
-  mbar_wait(sh.bar(BAR_FINAL_PV), 0, &never);
-  __syncwarp();
-}
+// Descriptors.  K-major 128-byte-swizzled tiles: rows of 128 bytes, 8-row atoms
+// 1024 bytes apart; a 16-element K step moves the start address by 32 bytes.
+// V (B of P V) is N-major: 64-column blocks one slot (LBO) apart, 8-row atoms
+// 1024 bytes apart; a 16-row K step moves the start by 2048 bytes.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t saddr) { return sw128_desc(saddr, 16, 1024); }
+__device__ __forceinline__ uint64_t vdesc(uint32_t saddr) { return sw128_desc(saddr, kSlotBytes, 1024); }
 
 // What a softmax thread needs to know about one segment.
 struct SegRows {
@@ -295,6 +223,124 @@ __device__ __forceinline__ SegRows seg_rows(const int* rec, const FastArgs& a, i
   return s;
 }
 
+// Block id of page p of sequence b (-1 = outside the pool, reads as zeros).
+__device__ __forceinline__ int page_block(const FastArgs& a, int b, int p, int* hdr, bool report) {
+  int blk = a.block_table[(size_t)b * a.bt_stride + p];
+  if (blk < 0 || blk >= a.num_blocks) {
+    if (report && a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | p);
+    blk = -1;
+  }
+  return blk;
+}
+
+// Q K^T issuer (CTA 0, one converged warp): page t goes to score tile t % 2
+// once both CTAs' halves of the page have landed and both softmaxes have read
+// the tile's previous scores (page t - 2).
+__device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
+                                        const int* seg, SegWalk walk) {
+  const uint32_t id_qk = idesc_bf16_f32(128, 64, 0);
+  uint64_t qdesc[kQSmemBoxes];
+#pragma unroll
+  for (int bx = 0; bx < kQSmemBoxes; ++bx) qdesc[bx] = kmajor_desc(sh.q(kQTmemBoxes + bx));
+  int gt = 0, sc = 0;
+  bool ok = true;
+  for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
+    const int* rec = seg + (size_t)si * kSegWords;
+    const int n_tiles = rec[3] - rec[2];
+    if (!warp_wait(sh.bar(BAR_Q_READY), sc & 1, abort_flag, hdr, 22)) { ok = false; break; }
+    tc_fence_after();
+    for (int i = 0; ok && i < n_tiles; ++i, ++gt) {
+      const int st = gt % kStages, sb = gt & 1;
+      const uint32_t par = (gt / kStages) & 1;
+      if (!warp_wait(sh.bar(BAR_FULL + st), par, abort_flag, hdr, 23) ||
+          !warp_wait(sh.bar(BAR_PEER + st), par, abort_flag, hdr, 24) ||
+          (gt >= 2 && !warp_wait(sh.bar(BAR_S_FREE + sb), ((gt >> 1) - 1) & 1, abort_flag, hdr, 25))) {
+        ok = false; break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + kTmemS + 32 * sb;
+#pragma unroll
+      for (int bx = 0; bx < kBoxes; ++bx) {
+        const uint64_t bd = kmajor_desc(sh.slot(st, bx));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acc = (bx || kk) ? 1u : 0u;
+          if (bx < kQTmemBoxes) mma2_ts_e(d, tmem + kTmemQ + 32 * bx + 8 * kk, bd + 2 * kk, id_qk, acc);
+          else mma2_ss_e(d, qdesc[bx - kQTmemBoxes] + 2 * kk, bd + 2 * kk, id_qk, acc);
+        }
+      }
+      commit2_both_e(sh.bar(BAR_S_FULL + sb));
+      commit2_both_e(sh.bar(BAR_QK_DONE + st));
+      if (i == n_tiles - 1) commit2_both_e(sh.bar(BAR_Q_FREE));
+    }
+    ++sc;
+  }
+  // Every MMA issued by this warp must be complete before the CTAs may leave.
+  commit2_both_e(sh.bar(BAR_FINAL_QK));
+  volatile int never = 0;
+  mbar_wait(sh.bar(BAR_FINAL_QK), 0, &never);
+  __syncwarp();
+}
+
+// P V issuer (CTA 0, one converged warp): O += P V for page t once both CTAs
+// wrote P and both CTAs' reloads of the other half's rows landed; the first
+// page of a segment overwrites O, after the previous segment's epilogue.
+__device__ __forceinline__ void pv_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
+                                        const int* seg, SegWalk walk) {
+  const uint32_t id_pv = idesc_bf16_f32(128, 256, 1);
+  int gv = 0, sc = 0;
+  bool ok = true;
+  for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
+    const int* rec = seg + (size_t)si * kSegWords;
+    const int n_tiles = rec[3] - rec[2];
+    for (int i = 0; ok && i < n_tiles; ++i, ++gv) {
+      const int st = gv % kStages, pb = gv % kPBufs;
+      const uint32_t par = (gv / kStages) & 1;
+      if ((i == 0 && sc > 0 && !warp_wait(sh.bar(BAR_O_FREE), (sc - 1) & 1, abort_flag, hdr, 20)) ||
+          !warp_wait(sh.bar(BAR_RELOAD + st), par, abort_flag, hdr, 26) ||
+          !warp_wait(sh.bar(BAR_PEER_RL + st), par, abort_flag, hdr, 27) ||
+          !warp_wait(sh.bar(BAR_P_FULL + pb), (gv / kPBufs) & 1, abort_flag, hdr, 21)) {
+        ok = false; break;
+      }
+      tc_fence_after();
+      const uint64_t pdesc = kmajor_desc(sh.p(pb));
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t vaddr = sh.slot(st, 4 * m + 2 * (kk >> 1)) + (kk & 1) * 2048;
+          mma2_ss_e(tmem + kTmemO + 128 * m, pdesc + 2 * kk, vdesc(vaddr), id_pv, (i == 0 && kk == 0) ? 0u : 1u);
+        }
+      }
+      commit2_both_e(sh.bar(BAR_PV_DONE + st));
+    }
+    ++sc;
+  }
+  commit2_both_e(sh.bar(BAR_FINAL_PV));
+  volatile int never = 0;
+  mbar_wait(sh.bar(BAR_FINAL_PV), 0, &never);
+  __syncwarp();
+}
+
+// CTA 1: forward the completion of a per-page local barrier (its page half or
+// its reload) to the matching barrier of CTA 0, page by page.
+__device__ __forceinline__ void relay_role(const Shared& sh, int* hdr, volatile int* abort_flag, const int* seg,
+                                           SegWalk walk, int from, int to, int where) {
+  const uint32_t dst0 = map_to_cta(sh.bar(to), 0);
+  int gt = 0;
+  bool ok = true;
+  for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
+    const int* rec = seg + (size_t)si * kSegWords;
+    for (int p = rec[2]; p < rec[3]; ++p, ++gt) {
+      const int st = gt % kStages;
+      if (!mbar_wait(sh.bar(from + st), (gt / kStages) & 1, abort_flag)) {
+        fail(hdr, abort_flag, where); ok = false; break;
+      }
+      asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(dst0 + 8 * st) : "memory");
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     decode_sm103_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_constant__ CUtensorMap tm_qpe,
                         const __grid_constant__ CUtensorMap tm_ckv, const __grid_constant__ CUtensorMap tm_kpe,
@@ -302,8 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   int* hdr = reinterpret_cast<int*>(ws);
-  // The 128-byte-swizzled tiles need a 1024-byte-aligned base; the allocation
-  // carries kSmemAlloc - kSmemBytes bytes of slack for that.  Refuse (uniformly,
+  // The 128-byte-swizzled tiles need a 1024-byte-aligned base, at the same offset
+  // in both CTAs (pair MMAs address both with one descriptor).  Refuse (uniformly,
   // before anything is set up) if the slack does not cover the misalignment.
   if ((uintptr_t)(smem - smem_raw) + kSmemBytes > (uintptr_t)kSmemAlloc) {
     pdl_wait();
@@ -320,30 +366,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* part_o = reinterpret_cast<float*>(ws + a.L.off_part_o);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int half = (int)cluster_ctarank();
+  const int rank = (int)cluster_ctarank();
   const int pair = blockIdx.x >> 1;
   const int num_pairs = gridDim.x >> 1;
   const int R = a.T * a.H;
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(sh.bar(BAR_FULL_A + i), 1);
-      mbar_init(sh.bar(BAR_EMPTY_A + i), 1);
-      mbar_init(sh.bar(BAR_FULL_B + i), 1);
-      mbar_init(sh.bar(BAR_EMPTY_B + i), 1);
+      mbar_init(sh.bar(BAR_FULL + i), 1);
+      mbar_init(sh.bar(BAR_PEER + i), 1);
+      mbar_init(sh.bar(BAR_RELOAD + i), 1);
+      mbar_init(sh.bar(BAR_PEER_RL + i), 1);
+      mbar_init(sh.bar(BAR_QK_DONE + i), 1);
+      mbar_init(sh.bar(BAR_PV_DONE + i), 1);
     }
-    mbar_init(sh.bar(BAR_Q_FULL), 1);
-    mbar_init(sh.bar(BAR_Q_EMPTY), 1);
-    mbar_init(sh.bar(BAR_QT_FULL), kSoftmaxThreads);
     for (int i = 0; i < 2; ++i) {
       mbar_init(sh.bar(BAR_S_FULL + i), 1);
-      mbar_init(sh.bar(BAR_P_FULL + i), kSoftmaxThreads);
-      mbar_init(sh.bar(BAR_P_EMPTY + i), 1);
+      mbar_init(sh.bar(BAR_S_FREE + i), 8);
+      mbar_init(sh.bar(BAR_XCH + i), 64);
     }
-    mbar_init(sh.bar(BAR_O_EMPTY), kSoftmaxThreads);
-    mbar_init(sh.bar(BAR_FINAL), 1);
+    for (int i = 0; i < kPBufs; ++i) mbar_init(sh.bar(BAR_P_FULL + i), 8);
+    mbar_init(sh.bar(BAR_Q_TMA), 1);
+    mbar_init(sh.bar(BAR_Q_READY), 8);
+    mbar_init(sh.bar(BAR_Q_FREE), 1);
+    mbar_init(sh.bar(BAR_O_FREE), 8);
+    mbar_init(sh.bar(BAR_FINAL_QK), 1);
     mbar_init(sh.bar(BAR_FINAL_PV), 1);
-    for (int i = 0; i < 4; ++i) mbar_init(sh.bar(BAR_XCH + i), 64);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_qlat);
@@ -352,8 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_kpe);
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_base_slot), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_addr(tmem_base_slot), kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
@@ -385,130 +433,141 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ page-half and query loads
     if (lane == 0) {
       SegWalk walk = walk0;
       int gt = 0, sc = 0;
-      bool q_in_flight = false, ok = true, a_only = false;
+      bool ok = true, q_in_flight = false;
       for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
         const int* rec = seg + (size_t)si * kSegWords;
         const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3];
-        if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_EMPTY), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
-        const int row0 = b * R + rb * kRowsPerBlock;
-        mbar_arrive_expect_tx(sh.bar(BAR_Q_FULL), kQSmemBoxes * kQBoxBytes);
-        for (int box = kQTmemBoxes; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_FULL), 64 * box, row0);
-        tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_FULL), 0, row0);
+        if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_FREE), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
+        const int row0 = b * R + rb * kRowsPerBlock + kCtaRows * rank;
+        mbar_arrive_expect_tx(sh.bar(BAR_Q_TMA), kQSmemBoxes * kQBoxBytes);
+        for (int box = kQTmemBoxes; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_TMA), 64 * box, row0);
+        tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_TMA), 0, row0);
         q_in_flight = true;
-        // Block ids are read a few pages ahead of their use (independent loads in flight).
-        const int32_t* btrow = a.block_table + (size_t)b * a.bt_stride;
-        int bq0 = p0 < p1 ? btrow[p0] : 0;
-        int bq1 = p0 + 1 < p1 ? btrow[p0 + 1] : 0;
-        int bq2 = p0 + 2 < p1 ? btrow[p0 + 2] : 0;
-        int bq3 = p0 + 3 < p1 ? btrow[p0 + 3] : 0;
-        for (int p = p0; ok && p < p1; ++p) {
-          int blk = bq0;
-          bq0 = bq1; bq1 = bq2; bq2 = bq3;
-          bq3 = p + 4 < p1 ? btrow[p + 4] : 0;
-          if (blk < 0 || blk >= a.num_blocks) {
-            // An out-of-pool id reads as zeros through the tensor map; report it when checking.
-            if (a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | p);
-            blk = -1;
-          }
+        for (int p = p0; ok && p < p1; ++p, ++gt) {
+          const int blk = page_block(a, b, p, hdr, true);
           const int st = gt % kStages;
-          const uint32_t par = ((gt / kStages) & 1) ^ 1;
-          if (!mbar_wait_backoff(sh.bar(BAR_EMPTY_A + st), par, abort_flag)) { fail(hdr, abort_flag, 11); ok = false; break; }
-          mbar_arrive_expect_tx(sh.bar(BAR_FULL_A + st), kGroupABoxes * kBoxBytes);
-          for (int j = 0; j < kGroupABoxes; ++j) {
-            const int box = half == 0 ? Boxes<0>::a(j) : Boxes<1>::a(j);
-            const uint32_t dst = sh.stage_a(st) + j * kBoxBytes;
-            if (box < 8) tma_load_3d(dst, &tm_ckv, sh.bar(BAR_FULL_A + st), 64 * box, 0, blk);
-            else tma_load_3d(dst, &tm_kpe, sh.bar(BAR_FULL_A + st), 0, 0, blk);
+          if (gt >= kStages && !mbar_wait_backoff(sh.bar(BAR_PV_DONE + st), ((gt / kStages) - 1) & 1, abort_flag)) {
+            fail(hdr, abort_flag, 11); ok = false; break;
           }
-          if (!mbar_wait_backoff(sh.bar(BAR_EMPTY_B + st), par, abort_flag)) {
-            fail(hdr, abort_flag, 12); ok = false; a_only = true; break;
-          }
-          mbar_arrive_expect_tx(sh.bar(BAR_FULL_B + st), kOwnBoxes * kBoxBytes);
-          for (int c = 0; c < kOwnBoxes; ++c)
-            tma_load_3d(sh.stage_b(st) + c * kBoxBytes, &tm_ckv, sh.bar(BAR_FULL_B + st), 64 * (4 * half + c), 0, blk);
-          ++gt;
+          mbar_arrive_expect_tx(sh.bar(BAR_FULL + st), kStageBytes);
+          for (int bx = 0; bx < 8; ++bx)
+            tma_load_3d(sh.slot(st, bx), &tm_ckv, sh.bar(BAR_FULL + st), 64 * bx, kHalfRows * rank, blk);
+          tma_load_3d(sh.slot(st, 8), &tm_kpe, sh.bar(BAR_FULL + st), 0, kHalfRows * rank, blk);
         }
         ++sc;
       }
-      // Drain: every load issued must have landed before the CTA may exit (a page
-      // whose group B was not issued after a failure is covered by its group A wait).
+      // Drain: every load issued must have landed before the CTA may exit.
       const int first = gt > kStages ? gt - kStages : 0;
-      for (int g = first; g < gt + (a_only ? 1 : 0); ++g) {
+      for (int g = first; g < gt; ++g) {
         volatile int never = 0;
-        mbar_wait(sh.bar(BAR_FULL_A + g % kStages), (g / kStages) & 1, &never);
-        if (g < gt) mbar_wait(sh.bar(BAR_FULL_B + g % kStages), (g / kStages) & 1, &never);
+        mbar_wait(sh.bar(BAR_FULL + g % kStages), (g / kStages) & 1, &never);
       }
       if (q_in_flight) {
         volatile int never = 0;
-        mbar_wait(sh.bar(BAR_Q_FULL), (sc - 1) & 1, &never);
+        mbar_wait(sh.bar(BAR_Q_TMA), (sc - 1) & 1, &never);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ Q K^T issuer (whole warp)
-    if (half == 0) qk_role<0>(sh, tmem, hdr, abort_flag, seg, walk0);
-    else qk_role<1>(sh, tmem, hdr, abort_flag, seg, walk0);
+    // ------------------------------------------------------------ CTA 0: Q K^T issuer; CTA 1: reload relay
+    if (rank == 0) qk_role(sh, tmem, hdr, abort_flag, seg, walk0);
+    else if (lane == 0) relay_role(sh, hdr, abort_flag, seg, walk0, BAR_RELOAD, BAR_PEER_RL, 14);
+    __syncwarp();
   } else if (warp == 2) {
-    // ------------------------------------------------------------ P V issuer (whole warp)
-    pv_role(sh, tmem, hdr, abort_flag, seg, walk0);
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax + epilogue
-    // Two threads per query row: warps 4..7 take score columns 0..31 of their
-    // TMEM lane quadrant, warps 8..11 columns 32..63 (a warp may only touch the
-    // 32 TMEM lanes of quadrant warp % 4).  The row maximum is combined through
-    // shared memory; each thread owns half of the row's P and O columns.
+    // ------------------------------------------------------------ CTA 0: P V issuer; CTA 1: page-half relay
+    if (rank == 0) pv_role(sh, tmem, hdr, abort_flag, seg, walk0);
+    else if (lane == 0) relay_role(sh, hdr, abort_flag, seg, walk0, BAR_FULL, BAR_PEER, 12);
+    __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ reloads of the other half's rows
+    if (lane == 0) {
+      SegWalk walk = walk0;
+      int gt = 0;
+      bool ok = true;
+      for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
+        const int* rec = seg + (size_t)si * kSegWords;
+        const int b = rec[0];
+        for (int p = rec[2]; ok && p < rec[3]; ++p, ++gt) {
+          const int blk = page_block(a, b, p, hdr, false);
+          const int st = gt % kStages;
+          if (!mbar_wait_backoff(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
+            fail(hdr, abort_flag, 13); ok = false; break;
+          }
+          mbar_arrive_expect_tx(sh.bar(BAR_RELOAD + st), 4 * kSlotBytes);
+          for (int i = 0; i < 4; ++i)
+            tma_load_3d(sh.slot(st, reload_slot(rank, i)), &tm_ckv, sh.bar(BAR_RELOAD + st), 64 * own_pv_box(rank, i),
+                        kHalfRows * (1 - rank), blk);
+        }
+      }
+      const int first = gt > kStages ? gt - kStages : 0;
+      for (int g = first; g < gt; ++g) {
+        volatile int never = 0;
+        mbar_wait(sh.bar(BAR_RELOAD + g % kStages), (g / kStages) & 1, &never);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue (warps 4..7)
+    // Thread = TMEM lane ln: query row hr = ln % 64 of this CTA, page half kh = ln / 64.
     const int q4 = warp & 3;
-    const int ch = (warp - 4) >> 2;           // column half
-    const int row = 32 * q4 + lane;           // query row within the group == TMEM lane
+    const int ln = 32 * q4 + lane;
+    const int hr = ln & 63, kh = ln >> 6;
+    const int row = kCtaRows * rank + hr;          // row within the 128-row group
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
     float* xrow = reinterpret_cast<float*>(smem + kSmemXchg);  // [buffer][half][row] partner exchange
-    // Exchange a value with the partner thread of the same row (bounded wait on the
-    // quadrant's mbarrier; double-buffered by exchange parity).  It also orders this
-    // thread's earlier TMEM reads before the partner's later TMEM writes.
+    const uint32_t xbar = sh.bar(BAR_XCH + (q4 & 1));
+    // Exchange a value with the thread holding the other page half of the same row
+    // (bounded wait on the pair's mbarrier; double-buffered by exchange parity).
     int xc = 0;
     auto swap_with_partner = [&](float v, float* out) -> bool {
-      float* slot = xrow + (xc & 1) * 256;
-      slot[ch * 128 + row] = v;
-      tc_fence_before();
-      mbar_arrive(sh.bar(BAR_XCH + q4));
-      const bool w = mbar_wait(sh.bar(BAR_XCH + q4), xc & 1, abort_flag);
-      tc_fence_after();
-      *out = slot[(ch ^ 1) * 128 + row];
+      float* slot = xrow + (xc & 1) * 128;
+      slot[kh * 64 + hr] = v;
+      mbar_arrive(xbar);
+      const bool w = mbar_wait(xbar, xc & 1, abort_flag);
+      *out = slot[(kh ^ 1) * 64 + hr];
       ++xc;
       return __all_sync(0xffffffffu, w);
     };
-    // Query columns 0..255 of this row go to TMEM (A operand of Q K^T for boxes
-    // 0..3; this thread stages boxes 2 ch and 2 ch + 1) once the previous
-    // segment's Q K^T MMAs are done with them.
+    // Query columns 0..383 of this row go to this thread's TMEM lane (A operand of
+    // the first 24 K steps; both lanes of the row hold a copy) once the previous
+    // segment's Q K^T is done with them; then each warp reports (with the query
+    // TMA) to CTA 0.
     auto stage_q = [&](const SegRows& s, int sc_of) -> bool {
-      const bool w_ok = sc_of == 0 || mbar_wait(sh.bar(BAR_Q_EMPTY), (sc_of - 1) & 1, abort_flag);
+      const bool w_ok = sc_of == 0 || mbar_wait(sh.bar(BAR_Q_FREE), (sc_of - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, w_ok)) return false;
       tc_fence_after();
-      const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)s.b * R + (s.row_valid ? s.fr : 0)) * kDLat) +
-                         16 * ch;
-      uint32_t q0[32], q1[32];
+      const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)s.b * R + (s.row_valid ? s.fr : 0)) * kDLat);
+#pragma unroll 1
+      for (int b0 = 0; b0 < kQTmemBoxes; b0 += 3) {
+        uint4 v[24];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint4 v0 = s.row_valid ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
-        const uint4 v1 = s.row_valid ? __ldg(src + 8 + e) : make_uint4(0, 0, 0, 0);
-        q0[4 * e] = v0.x; q0[4 * e + 1] = v0.y; q0[4 * e + 2] = v0.z; q0[4 * e + 3] = v0.w;
-        q1[4 * e] = v1.x; q1[4 * e + 1] = v1.y; q1[4 * e + 2] = v1.z; q1[4 * e + 3] = v1.w;
+        for (int e = 0; e < 24; ++e) v[e] = s.row_valid ? __ldg(src + 8 * b0 + e) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int bb = 0; bb < 3; ++bb) {
+          uint32_t q[32];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            q[4 * e] = v[8 * bb + e].x; q[4 * e + 1] = v[8 * bb + e].y;
+            q[4 * e + 2] = v[8 * bb + e].z; q[4 * e + 3] = v[8 * bb + e].w;
+          }
+          tmem_st32(t_lane + kTmemQ + 32 * (b0 + bb), q);
+        }
       }
-      tmem_st32(t_lane + kTmemQ + 32 * (2 * ch), q0);
-      tmem_st32(t_lane + kTmemQ + 32 * (2 * ch + 1), q1);
       tmem_wait_st();
+      const bool t_ok = mbar_wait(sh.bar(BAR_Q_TMA), sc_of & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, t_ok)) return false;
       tc_fence_before();
-      mbar_arrive(sh.bar(BAR_QT_FULL));
+      warp_arrive_leader(sh.bar(BAR_Q_READY), rank);
       return true;
     };
 
     SegWalk walk = walk0;
     int si = walk.cur();
-    int ti = 0, sc = 0;
+    int g = 0, sc = 0;
     bool ok = true;
     SegRows cur;
     if (si >= 0) {
@@ -518,18 +577,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && si >= 0) {
       float m_ref = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
       const int n_tiles = cur.p1 - cur.p0;
-      for (int i = 0; i < n_tiles; ++i, ++ti) {
-        const int sb = ti & 1;
-        const uint32_t s_col = kTmemS + 64 * sb;
-        const int jbase = (cur.p0 + i) * kPage + 32 * ch;   // first cache row of this thread's columns
-        bool w_ok = mbar_wait(sh.bar(BAR_S_FULL + sb), (ti >> 1) & 1, abort_flag);
+      for (int i = 0; i < n_tiles; ++i, ++g) {
+        const int sb = g & 1, st = g % kStages, pb = g % kPBufs;
+        const int page = cur.p0 + i;
+        const int jbase = page * kPage + kHalfRows * kh;   // first cache row of this thread's columns
+        bool w_ok = mbar_wait(sh.bar(BAR_S_FULL + sb), (g >> 1) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 30); ok = false; break; }
         tc_fence_after();
         uint32_t sr[32];
-        tmem_ld32(t_lane + s_col + 32 * ch, sr);
+        tmem_ld32(t_lane + kTmemS + 32 * sb, sr);
         tmem_wait_ld();
+        tc_fence_before();
+        warp_arrive_leader(sh.bar(BAR_S_FREE + sb), rank);
         // Raw-score maximum over the visible columns (the scale is positive).
-        const bool full = jbase + 32 <= cur.limit;
+        const bool full = jbase + kHalfRows <= cur.limit;
         float tmax = -INFINITY;
         if (full) {
 #pragma unroll
@@ -550,12 +611,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float new_ref = grow ? tmax : m_ref;
         const float factor = (grow && m_ref != -INFINITY) ? ex2(m_ref - new_ref) : 1.f;
         if (i > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
-          const int t1 = ti - 1;
-          w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + (t1 & 1)), (t1 >> 1) & 1, abort_flag);
+          const int g1 = g - 1;
+          w_ok = mbar_wait(sh.bar(BAR_PV_DONE + g1 % kStages), (g1 / kStages) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 31); ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 4 * ch; c < 4 * ch + 4; ++c) {
+          for (int c = 0; c < 8; ++c) {
             uint32_t o[32];
             tmem_ld32(t_lane + kTmemO + 32 * c, o);
             tmem_wait_ld();
@@ -568,9 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= factor;
         m_ref = new_ref;
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        // This thread's 32 P values, p = 2^(s * scale * log2 e - m), as bf16 pairs over
-        // columns 16 ch .. 16 ch + 15 of the score tile it has read (the partner has
-        // read its scores too: the exchange above came after both reads).
+        // This thread's 32 P values, p = 2^(s * scale * log2 e - m), as bf16 pairs.
         float psum = 0.f;
         uint32_t pw[16];
 #pragma unroll
@@ -586,27 +645,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
           pw[e] = *reinterpret_cast<const uint32_t*>(&h2);
         }
-        tmem_st16(t_lane + s_col + 16 * ch, pw);
         l += psum;
-        // Rows of the last page past the sequence end are zeroed in the four value
-        // boxes of this page (its group B) before P V reads them.
-        const int valid = cur.S - (cur.p0 + i) * kPage;
+        // P tile pb is free once P V of page g - kPBufs is done.
+        if (g >= kPBufs) {
+          const int g2 = g - kPBufs;
+          w_ok = mbar_wait(sh.bar(BAR_PV_DONE + g2 % kStages), (g2 / kStages) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 34); ok = false; break; }
+        }
+        {
+          // Row hr of P (128 bytes, K-major, 128-byte swizzle): this thread's four 16-byte chunks.
+          const uint32_t prow = sh.p(pb) + hr * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t chunk = (uint32_t)((4 * kh + c) ^ (hr & 7));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + 16 * chunk), "r"(pw[4 * c]),
+                         "r"(pw[4 * c + 1]), "r"(pw[4 * c + 2]), "r"(pw[4 * c + 3])
+                         : "memory");
+          }
+        }
+        // Rows of the last page past the sequence end are zeroed in the eight latent
+        // slots P V reads, once the other half's rows (reloaded after Q K^T) landed.
+        const int valid = cur.S - page * kPage;
         if (valid < kPage) {
-          const int t256 = tid - 128;   // 0..255 over the two warpgroups
-          for (int idx = t256; idx < kOwnBoxes * kPage; idx += 256) {
-            const int c = idx / kPage, rr = idx % kPage;
-            if (rr >= valid) {
-              const uint32_t dst = sh.stage_b(ti % kStages) + c * kBoxBytes + rr * 128;
+          w_ok = mbar_wait(sh.bar(BAR_RELOAD + st), (g / kStages) & 1, abort_flag);
+          if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 35); ok = false; break; }
+          for (int idx = ln; idx < 8 * kHalfRows; idx += kSoftmaxThreads) {
+            // After the reload, latent slot s holds rows of page half (s >> 1) & 1 in both CTAs.
+            const int s = idx / kHalfRows, rr = idx % kHalfRows;
+            if (((s >> 1) & 1) * kHalfRows + rr >= valid) {
+              const uint32_t dst = sh.slot(st, s) + rr * 128;
 #pragma unroll
               for (int z = 0; z < 8; ++z)
                 asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst + 16 * z), "r"(0) : "memory");
             }
           }
-          fence_proxy_async_smem();
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(sh.bar(BAR_P_FULL + sb));
+        fence_proxy_async_smem();
+        warp_arrive_leader(sh.bar(BAR_P_FULL + pb), rank);
       }
       if (!ok) break;
       // The next segment's query goes to TMEM now, so that its Q K^T can run while
@@ -619,29 +694,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!stage_q(nxt, sc + 1)) { fail(hdr, abort_flag, 33); ok = false; break; }
       }
       // Epilogue: wait for the last P V, combine the two halves of the row sum,
-      // then normalise and store this thread's 128 output columns.
+      // then normalise and store this thread's 256 output columns.
       {
-        const int tl = ti - 1;
-        const bool w_ok = mbar_wait(sh.bar(BAR_P_EMPTY + (tl & 1)), (tl >> 1) & 1, abort_flag);
+        const int gl = g - 1;
+        const bool w_ok = mbar_wait(sh.bar(BAR_PV_DONE + gl % kStages), (gl / kStages) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 32); ok = false; break; }
         tc_fence_after();
       }
       float l_other;
       if (!swap_with_partner(l, &l_other)) { fail(hdr, abort_flag, 38); ok = false; break; }
-      const float l_row = ch == 0 ? l + l_other : l_other + l;
+      const float l_row = kh == 0 ? l + l_other : l_other + l;
       const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       const float lse_v = l_row > 0.f ? (m_use + __log2f(l_row)) * 0.69314718055994531f : -INFINITY;
       const int b = cur.b, fr = cur.fr, slot_out = cur.slot_out;
 #pragma unroll 1
-      for (int c = 4 * ch; c < 4 * ch + 4; ++c) {
+      for (int c = 0; c < 8; ++c) {
         uint32_t o[32];
         tmem_ld32(t_lane + kTmemO + 32 * c, o);
         tmem_wait_ld();
+        // TMEM column 128 m + cc of this lane = latent column 256 m + 128 kh + cc.
+        const int col0 = 256 * (c >> 2) + 128 * kh + 32 * (c & 3);
         if (cur.row_valid) {
           // 32-byte stores: each thread writes whole sectors of its row.
           if (slot_out < 0) {
-            __nv_bfloat16* dst = a.o_lat + ((size_t)b * R + fr) * kDLat + 256 * half + 32 * c;
+            __nv_bfloat16* dst = a.o_lat + ((size_t)b * R + fr) * kDLat + col0;
 #pragma unroll
             for (int e = 0; e < 32; e += 16) {
               uint32_t w[8];
@@ -650,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               st_global_v8(dst + e, w);
             }
           } else {
-            float* dst = part_o + ((size_t)slot_out * kRowsPerBlock + row) * kDLat + 256 * half + 32 * c;
+            float* dst = part_o + ((size_t)slot_out * kRowsPerBlock + row) * kDLat + col0;
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
               uint32_t w[8];
@@ -661,12 +738,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (cur.row_valid && half == 0 && ch == 0) {
+      if (cur.row_valid && kh == 0) {
         if (slot_out < 0) a.lse[(size_t)b * R + fr] = lse_v;
         else part_lse[(size_t)slot_out * kRowsPerBlock + row] = lse_v;
       }
       tc_fence_before();
-      mbar_arrive(sh.bar(BAR_O_EMPTY));
+      warp_arrive_leader(sh.bar(BAR_O_FREE), rank);
       ++sc;
       si = si_next;
       cur = nxt;
@@ -677,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   cluster_sync_all();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 // --------------------------------------------------------------------------- host side
@@ -772,25 +849,25 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
   {
     const cuuint64_t dims[2] = {(cuuint64_t)kDLat, (cuuint64_t)rows_total};
     const cuuint64_t str[1] = {(cuuint64_t)kDLat * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, kCtaRows};
     if (!make_map(&m_qlat, q_lat, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[2] = {(cuuint64_t)kDRope, (cuuint64_t)rows_total};
     const cuuint64_t str[1] = {(cuuint64_t)kDRope * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, kCtaRows};
     if (!make_map(&m_qpe, q_pe, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)kDLat, (cuuint64_t)kPage, (cuuint64_t)cv.num_blocks};
     const cuuint64_t str[2] = {(cuuint64_t)cv.ckv_row * 2, (cuuint64_t)cv.ckv_block * 2};
-    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t box[3] = {64, kHalfRows, 1};
     if (!make_map(&m_ckv, cv.ckv, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)kDRope, (cuuint64_t)kPage, (cuuint64_t)cv.num_blocks};
     const cuuint64_t str[2] = {(cuuint64_t)cv.kpe_row * 2, (cuuint64_t)cv.kpe_block * 2};
-    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t box[3] = {64, kHalfRows, 1};
     if (!make_map(&m_kpe, cv.kpe, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   FastArgs a;
