@@ -42,13 +42,13 @@
 // 36 KB), the P tiles (64 rows x 64 page rows, bf16, K-major) and the shared
 // part of the query.
 //
-// Roles (256 threads per CTA): warp 0 issues the page loads and warp 3 the
+// Roles (384 threads per CTA): warp 0 issues the page loads and warp 3 the
 // reloads; in CTA 0 warp 1 issues the Q K^T MMAs and warp 2 the P V MMAs (two
 // issuers, so that Q K^T of the next pages keeps the tensor pipe busy while
 // P V waits for the softmax); in CTA 1 warps 2 and 1 forward the arrival of
-// its page halves and of its reloads to CTA 0; warps 4..7 run the online
-// softmax (one thread per TMEM lane: row i % 64, page half i / 64), write P,
-// stage the query and write the outputs.  The softmax keeps a per-row reference max and rescales its accumulator rows only
+// its page halves and of its reloads to CTA 0; warps 4..11 run the online
+// softmax (two threads per TMEM lane: row i % 64, page half i / 64, half of
+// the lane's columns each), write P, stage the query and write the outputs.  The softmax keeps a per-row reference max and rescales its accumulator rows only
 // when the running max grows past it by more than 2^8 (exact for any
 // reference; only rounding differs), with scores in log2 units.  Cache rows
 // past the sequence end (last page only) are zeroed in shared memory before
@@ -68,8 +68,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 256;
 constexpr int kCtaRows = 64;                   // query rows per CTA
 constexpr int kHalfRows = 32;                  // page rows loaded by each CTA
 constexpr int kBoxes = 9;                      // 8 latent boxes + 1 RoPE box per cached row
@@ -85,8 +85,8 @@ constexpr int kSmemQ = 0;
 constexpr int kSmemP = kSmemQ + kQSmemBoxes * kQBoxBytes;
 constexpr int kSmemRing = kSmemP + kPBufs * kPBytes;
 constexpr int kSmemBar = kSmemRing + kStages * kStageBytes;
-constexpr int kSmemXchg = kSmemBar + 512;                     // float [2 buffers][2 halves][64 rows]
-constexpr int kSmemBytes = kSmemXchg + 1024;
+constexpr int kSmemXchg = kSmemBar + 512;                     // float [2 buffers][4 quarters][64 rows]
+constexpr int kSmemBytes = kSmemXchg + 2048;
 constexpr int kSmemAlloc = kSmemBytes + 1024;                 // slack to align the base to 1024 B (checked)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
@@ -99,20 +99,18 @@ static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
 static_assert(kSmemRing % 1024 == 0 && kSmemP % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle atoms");
 
 enum {
-  BAR_FULL = 0,                        // kStages: this CTA's half-page landed (TMA)
-  BAR_PEER = BAR_FULL + kStages,       // kStages: (CTA 0) CTA 1's half-page landed (relayed)
-  BAR_RELOAD = BAR_PEER + kStages,     // kStages: the reloaded partner rows landed (TMA)
-  BAR_PEER_RL = BAR_RELOAD + kStages,  // kStages: (CTA 0) CTA 1's reload landed (relayed)
-  BAR_QK_DONE = BAR_PEER_RL + kStages, // kStages: Q K^T of the page done (both CTAs)
+  BAR_FULL = 0,                        // kStages: this CTA's half-page landed (TMA); at CTA 0 also CTA 1's (relayed)
+  BAR_RELOAD = BAR_FULL + kStages,     // kStages: the reloaded rows landed (TMA); at CTA 0 also CTA 1's (relayed)
+  BAR_QK_DONE = BAR_RELOAD + kStages,  // kStages: Q K^T of the page done (both CTAs)
   BAR_PV_DONE = BAR_QK_DONE + kStages, // kStages: P V of the page done (both CTAs)
   BAR_S_FULL = BAR_PV_DONE + kStages,  // 2: score tile written (both CTAs)
-  BAR_S_FREE = BAR_S_FULL + 2,         // 2: (CTA 0) both CTAs' softmax read the tile (8 warp arrivals)
-  BAR_P_FULL = BAR_S_FREE + 2,         // kPBufs: (CTA 0) both CTAs wrote P (8 warp arrivals)
+  BAR_S_FREE = BAR_S_FULL + 2,         // 2: (CTA 0) both CTAs' softmax read the tile (16 warp arrivals)
+  BAR_P_FULL = BAR_S_FREE + 2,         // kPBufs: (CTA 0) both CTAs wrote P (16 warp arrivals)
   BAR_Q_TMA = BAR_P_FULL + kPBufs,     // query boxes in shared memory landed (TMA)
-  BAR_Q_READY = BAR_Q_TMA + 1,         // (CTA 0) both CTAs staged the query (8 warp arrivals)
+  BAR_Q_READY = BAR_Q_TMA + 1,         // (CTA 0) both CTAs staged the query (16 warp arrivals)
   BAR_Q_FREE = BAR_Q_READY + 1,        // Q K^T of the segment done with the query (both CTAs)
-  BAR_O_FREE = BAR_Q_FREE + 1,         // (CTA 0) both CTAs' epilogues read the accumulator (8 warp arrivals)
-  BAR_XCH = BAR_O_FREE + 1,            // 2: the two softmax warps sharing a row range (64 arrivals)
+  BAR_O_FREE = BAR_Q_FREE + 1,         // (CTA 0) both CTAs' epilogues read the accumulator (16 warp arrivals)
+  BAR_XCH = BAR_O_FREE + 1,            // 2: the four softmax warps sharing a row range (4 warp arrivals)
   BAR_FINAL_QK = BAR_XCH + 2,
   BAR_FINAL_PV,
   kNumBars = BAR_FINAL_PV + 1
@@ -175,7 +173,7 @@ __device__ __forceinline__ void fail(int* hdr, volatile int* abort_flag, int whe
 // phase complete (on a timeout lane 0 records it and raises the abort flag).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* hdr,
                                           int where) {
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar, parity, abort_flag));
   if (!ok && (threadIdx.x & 31) == 0) fail(hdr, abort_flag, where);
   return ok;
 }
@@ -234,8 +232,9 @@ __device__ __forceinline__ int page_block(const FastArgs& a, int b, int p, int* 
 }
 
 // Q K^T issuer (CTA 0, one converged warp): page t goes to score tile t % 2
-// once both CTAs' halves of the page have landed and both softmaxes have read
-// the tile's previous scores (page t - 2).
+// once both CTAs' halves of the page have landed (CTA 0's load barrier also
+// counts CTA 1's, relayed) and both softmaxes have read the tile's previous
+// scores (page t - 2).
 __device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
                                         const int* seg, SegWalk walk) {
   const uint32_t id_qk = idesc_bf16_f32(128, 64, 0);
@@ -253,7 +252,6 @@ __device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hd
       const int st = gt % kStages, sb = gt & 1;
       const uint32_t par = (gt / kStages) & 1;
       if (!warp_wait(sh.bar(BAR_FULL + st), par, abort_flag, hdr, 23) ||
-          !warp_wait(sh.bar(BAR_PEER + st), par, abort_flag, hdr, 24) ||
           (gt >= 2 && !warp_wait(sh.bar(BAR_S_FREE + sb), ((gt >> 1) - 1) & 1, abort_flag, hdr, 25))) {
         ok = false; break;
       }
@@ -283,7 +281,8 @@ __device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hd
 }
 
 // P V issuer (CTA 0, one converged warp): O += P V for page t once both CTAs
-// wrote P and both CTAs' reloads of the other half's rows landed; the first
+// wrote P and both CTAs' reloads of the other half's rows landed (CTA 0's
+// reload barrier also counts CTA 1's, relayed); the first
 // page of a segment overwrites O, after the previous segment's epilogue.
 __device__ __forceinline__ void pv_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
                                         const int* seg, SegWalk walk) {
@@ -298,7 +297,6 @@ __device__ __forceinline__ void pv_role(const Shared& sh, uint32_t tmem, int* hd
       const uint32_t par = (gv / kStages) & 1;
       if ((i == 0 && sc > 0 && !warp_wait(sh.bar(BAR_O_FREE), (sc - 1) & 1, abort_flag, hdr, 20)) ||
           !warp_wait(sh.bar(BAR_RELOAD + st), par, abort_flag, hdr, 26) ||
-          !warp_wait(sh.bar(BAR_PEER_RL + st), par, abort_flag, hdr, 27) ||
           !warp_wait(sh.bar(BAR_P_FULL + pb), (gv / kPBufs) & 1, abort_flag, hdr, 21)) {
         ok = false; break;
       }
@@ -333,7 +331,7 @@ __device__ __forceinline__ void relay_role(const Shared& sh, int* hdr, volatile 
     const int* rec = seg + (size_t)si * kSegWords;
     for (int p = rec[2]; p < rec[3]; ++p, ++gt) {
       const int st = gt % kStages;
-      if (!mbar_wait(sh.bar(from + st), (gt / kStages) & 1, abort_flag)) {
+      if (!mbar_wait_sleep(sh.bar(from + st), (gt / kStages) & 1, abort_flag)) {
         fail(hdr, abort_flag, where); ok = false; break;
       }
       asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(dst0 + 8 * st) : "memory");
@@ -373,23 +371,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(sh.bar(BAR_FULL + i), 1);
-      mbar_init(sh.bar(BAR_PEER + i), 1);
-      mbar_init(sh.bar(BAR_RELOAD + i), 1);
-      mbar_init(sh.bar(BAR_PEER_RL + i), 1);
+      // CTA 0's load barriers also count the arrival relayed from CTA 1.
+      mbar_init(sh.bar(BAR_FULL + i), rank == 0 ? 2 : 1);
+      mbar_init(sh.bar(BAR_RELOAD + i), rank == 0 ? 2 : 1);
       mbar_init(sh.bar(BAR_QK_DONE + i), 1);
       mbar_init(sh.bar(BAR_PV_DONE + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(sh.bar(BAR_S_FULL + i), 1);
-      mbar_init(sh.bar(BAR_S_FREE + i), 8);
-      mbar_init(sh.bar(BAR_XCH + i), 64);
+      mbar_init(sh.bar(BAR_S_FREE + i), 16);
+      mbar_init(sh.bar(BAR_XCH + i), 4);
     }
-    for (int i = 0; i < kPBufs; ++i) mbar_init(sh.bar(BAR_P_FULL + i), 8);
+    for (int i = 0; i < kPBufs; ++i) mbar_init(sh.bar(BAR_P_FULL + i), 16);
     mbar_init(sh.bar(BAR_Q_TMA), 1);
-    mbar_init(sh.bar(BAR_Q_READY), 8);
+    mbar_init(sh.bar(BAR_Q_READY), 16);
     mbar_init(sh.bar(BAR_Q_FREE), 1);
-    mbar_init(sh.bar(BAR_O_FREE), 8);
+    mbar_init(sh.bar(BAR_O_FREE), 16);
     mbar_init(sh.bar(BAR_FINAL_QK), 1);
     mbar_init(sh.bar(BAR_FINAL_PV), 1);
     *abort_flag = 0;
@@ -450,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int p = p0; ok && p < p1; ++p, ++gt) {
           const int blk = page_block(a, b, p, hdr, true);
           const int st = gt % kStages;
-          if (gt >= kStages && !mbar_wait_backoff(sh.bar(BAR_PV_DONE + st), ((gt / kStages) - 1) & 1, abort_flag)) {
+          if (gt >= kStages && !mbar_wait_sleep(sh.bar(BAR_PV_DONE + st), ((gt / kStages) - 1) & 1, abort_flag)) {
             fail(hdr, abort_flag, 11); ok = false; break;
           }
           mbar_arrive_expect_tx(sh.bar(BAR_FULL + st), kStageBytes);
@@ -475,12 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ CTA 0: Q K^T issuer; CTA 1: reload relay
     if (rank == 0) qk_role(sh, tmem, hdr, abort_flag, seg, walk0);
-    else if (lane == 0) relay_role(sh, hdr, abort_flag, seg, walk0, BAR_RELOAD, BAR_PEER_RL, 14);
+    else if (lane == 0) relay_role(sh, hdr, abort_flag, seg, walk0, BAR_RELOAD, BAR_RELOAD, 14);
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ CTA 0: P V issuer; CTA 1: page-half relay
     if (rank == 0) pv_role(sh, tmem, hdr, abort_flag, seg, walk0);
-    else if (lane == 0) relay_role(sh, hdr, abort_flag, seg, walk0, BAR_FULL, BAR_PEER, 12);
+    else if (lane == 0) relay_role(sh, hdr, abort_flag, seg, walk0, BAR_FULL, BAR_FULL, 12);
     __syncwarp();
   } else if (warp == 3) {
     // ------------------------------------------------------------ reloads of the other half's rows
@@ -494,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int p = rec[2]; ok && p < rec[3]; ++p, ++gt) {
           const int blk = page_block(a, b, p, hdr, false);
           const int st = gt % kStages;
-          if (!mbar_wait_backoff(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
+          if (!mbar_wait_sleep(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
             fail(hdr, abort_flag, 13); ok = false; break;
           }
           mbar_arrive_expect_tx(sh.bar(BAR_RELOAD + st), 4 * kSlotBytes);
@@ -511,51 +508,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax + epilogue (warps 4..7)
-    // Thread = TMEM lane ln: query row hr = ln % 64 of this CTA, page half kh = ln / 64.
+    // ------------------------------------------------------------ softmax + epilogue (warps 4..11)
+    // TMEM lane ln holds query row hr = ln % 64 of this CTA and page half kh = ln / 64;
+    // two threads share a lane (warps w and w + 4): thread half cw takes score
+    // columns [16 cw, 16 cw + 16) of the lane, and accumulator columns
+    // [128 cw, 128 cw + 128), i.e. latent block m = cw.
     const int q4 = warp & 3;
+    const int cw = (warp - 4) >> 2;
     const int ln = 32 * q4 + lane;
     const int hr = ln & 63, kh = ln >> 6;
+    const int part = 2 * kh + cw;                  // this thread's quarter of its row
     const int row = kCtaRows * rank + hr;          // row within the 128-row group
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
-    float* xrow = reinterpret_cast<float*>(smem + kSmemXchg);  // [buffer][half][row] partner exchange
+    float* xrow = reinterpret_cast<float*>(smem + kSmemXchg);  // [buffer][quarter][row]
     const uint32_t xbar = sh.bar(BAR_XCH + (q4 & 1));
-    // Exchange a value with the thread holding the other page half of the same row
-    // (bounded wait on the pair's mbarrier; double-buffered by exchange parity).
+    // Combine a value over the four threads of a row (bounded wait on the mbarrier
+    // of the four warps holding rows 32 (q4 & 1) .. + 31; double-buffered by parity).
     int xc = 0;
-    auto swap_with_partner = [&](float v, float* out) -> bool {
-      float* slot = xrow + (xc & 1) * 128;
-      slot[kh * 64 + hr] = v;
-      mbar_arrive(xbar);
+    auto row_exchange = [&](float v, float* out) -> bool {
+      float* slot = xrow + (xc & 1) * 256;
+      slot[part * 64 + hr] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar);   // one arrival per warp, after the warp's stores
       const bool w = mbar_wait(xbar, xc & 1, abort_flag);
-      *out = slot[(kh ^ 1) * 64 + hr];
+      out[0] = slot[hr];
+      out[1] = slot[64 + hr];
+      out[2] = slot[128 + hr];
+      out[3] = slot[192 + hr];
       ++xc;
       return __all_sync(0xffffffffu, w);
     };
     // Query columns 0..383 of this row go to this thread's TMEM lane (A operand of
-    // the first 24 K steps; both lanes of the row hold a copy) once the previous
-    // segment's Q K^T is done with them; then each warp reports (with the query
-    // TMA) to CTA 0.
+    // the first 24 K steps; both lanes of the row hold a copy, each thread three of
+    // the six boxes) once the previous segment's Q K^T is done with them; then each
+    // warp reports (with the query TMA) to CTA 0.
     auto stage_q = [&](const SegRows& s, int sc_of) -> bool {
       const bool w_ok = sc_of == 0 || mbar_wait(sh.bar(BAR_Q_FREE), (sc_of - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, w_ok)) return false;
       tc_fence_after();
-      const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)s.b * R + (s.row_valid ? s.fr : 0)) * kDLat);
-#pragma unroll 1
-      for (int b0 = 0; b0 < kQTmemBoxes; b0 += 3) {
-        uint4 v[24];
+      const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)s.b * R + (s.row_valid ? s.fr : 0)) * kDLat) +
+                         8 * 3 * cw;
+      uint4 v[24];
 #pragma unroll
-        for (int e = 0; e < 24; ++e) v[e] = s.row_valid ? __ldg(src + 8 * b0 + e) : make_uint4(0, 0, 0, 0);
+      for (int e = 0; e < 24; ++e) v[e] = s.row_valid ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int bb = 0; bb < 3; ++bb) {
-          uint32_t q[32];
+      for (int bb = 0; bb < 3; ++bb) {
+        uint32_t q[32];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            q[4 * e] = v[8 * bb + e].x; q[4 * e + 1] = v[8 * bb + e].y;
-            q[4 * e + 2] = v[8 * bb + e].z; q[4 * e + 3] = v[8 * bb + e].w;
-          }
-          tmem_st32(t_lane + kTmemQ + 32 * (b0 + bb), q);
+        for (int e = 0; e < 8; ++e) {
+          q[4 * e] = v[8 * bb + e].x; q[4 * e + 1] = v[8 * bb + e].y;
+          q[4 * e + 2] = v[8 * bb + e].z; q[4 * e + 3] = v[8 * bb + e].w;
         }
+        tmem_st32(t_lane + kTmemQ + 32 * (3 * cw + bb), q);
       }
       tmem_wait_st();
       const bool t_ok = mbar_wait(sh.bar(BAR_Q_TMA), sc_of & 1, abort_flag);
@@ -575,35 +579,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!stage_q(cur, 0)) { fail(hdr, abort_flag, 33); ok = false; }
     }
     while (ok && si >= 0) {
-      float m_ref = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
+      float m_ref = -INFINITY, l = 0.f;   // l: this thread's quarter of the row sum
       const int n_tiles = cur.p1 - cur.p0;
       for (int i = 0; i < n_tiles; ++i, ++g) {
         const int sb = g & 1, st = g % kStages, pb = g % kPBufs;
         const int page = cur.p0 + i;
-        const int jbase = page * kPage + kHalfRows * kh;   // first cache row of this thread's columns
+        const int jbase = page * kPage + kHalfRows * kh + 16 * cw;   // first cache row of this thread's columns
         bool w_ok = mbar_wait(sh.bar(BAR_S_FULL + sb), (g >> 1) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 30); ok = false; break; }
         tc_fence_after();
-        uint32_t sr[32];
-        tmem_ld32(t_lane + kTmemS + 32 * sb, sr);
+        uint32_t sr[16];
+        tmem_ld16(t_lane + kTmemS + 32 * sb + 16 * cw, sr);
         tmem_wait_ld();
         tc_fence_before();
         warp_arrive_leader(sh.bar(BAR_S_FREE + sb), rank);
         // Raw-score maximum over the visible columns (the scale is positive).
-        const bool full = jbase + kHalfRows <= cur.limit;
-        float tmax = -INFINITY;
+        const bool full = jbase + 16 <= cur.limit;
+        float mx[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx[k] = -INFINITY;
         if (full) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) tmax = fmaxf(tmax, __uint_as_float(sr[j]));
+          for (int j = 0; j < 16; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(sr[j]));
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (jbase + j < cur.limit) tmax = fmaxf(tmax, __uint_as_float(sr[j]));
+          for (int j = 0; j < 16; ++j)
+            if (jbase + j < cur.limit) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(sr[j]));
         }
+        float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         {
-          float other;
-          if (!swap_with_partner(tmax, &other)) { fail(hdr, abort_flag, 37); ok = false; break; }
-          tmax = fmaxf(tmax, other) * a.scale_log2;
+          float o4[4];
+          if (!row_exchange(tmax, o4)) { fail(hdr, abort_flag, 37); ok = false; break; }
+          tmax = fmaxf(fmaxf(o4[0], o4[1]), fmaxf(o4[2], o4[3])) * a.scale_log2;
         }
         // Lazy rescale of the running state: needs the accumulator up to date (P V of
         // the previous page complete); rare once the reference max has settled.
@@ -616,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 31); ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 4 * cw; c < 4 * cw + 4; ++c) {
             uint32_t o[32];
             tmem_ld32(t_lane + kTmemO + 32 * c, o);
             tmem_wait_ld();
@@ -629,23 +636,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= factor;
         m_ref = new_ref;
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        // This thread's 32 P values, p = 2^(s * scale * log2 e - m), as bf16 pairs.
-        float psum = 0.f;
-        uint32_t pw[16];
+        // This thread's 16 P values, p = 2^(s * scale * log2 e - m), as bf16 pairs.
+        float x[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j = 2 * e;
-          float x0 = ex2(fmaf(__uint_as_float(sr[j]), a.scale_log2, -m_use));
-          float x1 = ex2(fmaf(__uint_as_float(sr[j + 1]), a.scale_log2, -m_use));
-          if (!full) {
-            x0 = (jbase + j < cur.limit) ? x0 : 0.f;
-            x1 = (jbase + j + 1 < cur.limit) ? x1 : 0.f;
-          }
-          psum += x0 + x1;
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+        for (int j = 0; j < 16; ++j) x[j] = ex2(fmaf(__uint_as_float(sr[j]), a.scale_log2, -m_use));
+        if (!full) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) x[j] = (jbase + j < cur.limit) ? x[j] : 0.f;
+        }
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pw[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          ps[e & 3] += x[2 * e] + x[2 * e + 1];
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
           pw[e] = *reinterpret_cast<const uint32_t*>(&h2);
         }
-        l += psum;
+        l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         // P tile pb is free once P V of page g - kPBufs is done.
         if (g >= kPBufs) {
           const int g2 = g - kPBufs;
@@ -653,11 +660,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 34); ok = false; break; }
         }
         {
-          // Row hr of P (128 bytes, K-major, 128-byte swizzle): this thread's four 16-byte chunks.
+          // Row hr of P (128 bytes, K-major, 128-byte swizzle): this thread's two 16-byte chunks.
           const uint32_t prow = sh.p(pb) + hr * 128;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t chunk = (uint32_t)((4 * kh + c) ^ (hr & 7));
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t chunk = (uint32_t)((4 * kh + 2 * cw + c) ^ (hr & 7));
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + 16 * chunk), "r"(pw[4 * c]),
                          "r"(pw[4 * c + 1]), "r"(pw[4 * c + 2]), "r"(pw[4 * c + 3])
                          : "memory");
@@ -669,15 +676,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid < kPage) {
           w_ok = mbar_wait(sh.bar(BAR_RELOAD + st), (g / kStages) & 1, abort_flag);
           if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 35); ok = false; break; }
-          for (int idx = ln; idx < 8 * kHalfRows; idx += kSoftmaxThreads) {
-            // After the reload, latent slot s holds rows of page half (s >> 1) & 1 in both CTAs.
-            const int s = idx / kHalfRows, rr = idx % kHalfRows;
-            if (((s >> 1) & 1) * kHalfRows + rr >= valid) {
-              const uint32_t dst = sh.slot(st, s) + rr * 128;
+          // After the reload, latent slot s holds rows of page half (s >> 1) & 1 in both CTAs.
+          const int idx = tid - 128;   // 0..255: slot idx / 32, row idx % 32
+          const int s_ = idx / kHalfRows, rr = idx % kHalfRows;
+          if (((s_ >> 1) & 1) * kHalfRows + rr >= valid) {
+            const uint32_t dst = sh.slot(st, s_) + rr * 128;
 #pragma unroll
-              for (int z = 0; z < 8; ++z)
-                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst + 16 * z), "r"(0) : "memory");
-            }
+            for (int z = 0; z < 8; ++z)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst + 16 * z), "r"(0) : "memory");
           }
         }
         fence_proxy_async_smem();
@@ -693,23 +699,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         nxt = seg_rows(seg + (size_t)si_next * kSegWords, a, R, row);
         if (!stage_q(nxt, sc + 1)) { fail(hdr, abort_flag, 33); ok = false; break; }
       }
-      // Epilogue: wait for the last P V, combine the two halves of the row sum,
-      // then normalise and store this thread's 256 output columns.
+      // Epilogue: wait for the last P V, combine the four quarters of the row sum,
+      // then normalise and store this thread's 128 output columns.
       {
         const int gl = g - 1;
         const bool w_ok = mbar_wait(sh.bar(BAR_PV_DONE + gl % kStages), (gl / kStages) & 1, abort_flag);
         if (!__all_sync(0xffffffffu, w_ok)) { fail(hdr, abort_flag, 32); ok = false; break; }
         tc_fence_after();
       }
-      float l_other;
-      if (!swap_with_partner(l, &l_other)) { fail(hdr, abort_flag, 38); ok = false; break; }
-      const float l_row = kh == 0 ? l + l_other : l_other + l;
+      float l4[4];
+      if (!row_exchange(l, l4)) { fail(hdr, abort_flag, 38); ok = false; break; }
+      const float l_row = (l4[0] + l4[1]) + (l4[2] + l4[3]);
       const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       const float lse_v = l_row > 0.f ? (m_use + __log2f(l_row)) * 0.69314718055994531f : -INFINITY;
       const int b = cur.b, fr = cur.fr, slot_out = cur.slot_out;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 4 * cw; c < 4 * cw + 4; ++c) {
         uint32_t o[32];
         tmem_ld32(t_lane + kTmemO + 32 * c, o);
         tmem_wait_ld();
@@ -738,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (cur.row_valid && kh == 0) {
+      if (cur.row_valid && part == 0) {
         if (slot_out < 0) a.lse[(size_t)b * R + fr] = lse_v;
         else part_lse[(size_t)slot_out * kRowsPerBlock + row] = lse_v;
       }
