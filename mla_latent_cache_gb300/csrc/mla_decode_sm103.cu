@@ -75,11 +75,11 @@ constexpr int kHalfRows = 32;                  // page rows loaded by each CTA
 constexpr int kBoxes = 9;                      // 8 latent boxes + 1 RoPE box per cached row
 constexpr int kSlotBytes = kHalfRows * 128;    // 4 KB: 32 rows x 64 bf16, 128-byte swizzled
 constexpr int kStageBytes = kBoxes * kSlotBytes;
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kQTmemBoxes = 6;                 // query boxes 0..5 in TMEM
 constexpr int kQSmemBoxes = kBoxes - kQTmemBoxes;
 constexpr int kQBoxBytes = kCtaRows * 128;     // 8 KB
-constexpr int kPBufs = 3;
+constexpr int kPBufs = 2;
 constexpr int kPBytes = kCtaRows * 128;        // 8 KB: 64 rows x 64 page rows bf16
 constexpr int kSmemQ = 0;
 constexpr int kSmemP = kSmemQ + kQSmemBoxes * kQBoxBytes;
