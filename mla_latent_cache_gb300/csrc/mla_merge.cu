@@ -66,36 +66,132 @@ struct PlanMergeArgs {
   WsLayout L;
 };
 
-// Merge records of the plan (groups that were split, or are empty).  A thread
-// owns four columns of one row (128 threads per row, two rows per CTA); the
-// work items are (record, row pair), taken in turn by the CTAs of a grid sized
-// to what the device holds at once, so a plan without merges costs one read
-// per CTA.
-__global__ void __launch_bounds__(kMergeThreads) plan_merge_kernel(PlanMergeArgs a, const char* ws) {
+constexpr int kPlanMergeThreads = 512;             // four groups of 128 threads, one float4 column chunk each
+constexpr int kGroups = kPlanMergeThreads / (kDLat / 4);
+constexpr int kPartBatch = 8;                      // partial loads a thread keeps in flight
+
+// Running merge state of one thread: m = max LSE seen, l = sum of e^{lse - m},
+// acc = sum of e^{lse - m} o (four columns).  Folding in a batch whose maximum
+// raises m rescales what is already there by e^{m_old - m_new}.
+struct MergeState {
+  float m, l, a0, a1, a2, a3;
+};
+
+// Fold partials r = r0, r0 + step, ... (< count) of one row into st, in batches
+// whose loads are all issued before any is used.  A partial of LSE -inf has
+// weight 0 and is skipped (select), whatever its slot holds.
+__device__ __forceinline__ void fold_partials(MergeState& st, const float* po, const float* pl, size_t o_pitch,
+                                              size_t l_pitch, int r0, int step, int count) {
+  for (int rb = r0; rb < count; rb += kPartBatch * step) {
+    float x[kPartBatch];
+    float4 v[kPartBatch];
+#pragma unroll
+    for (int k = 0; k < kPartBatch; ++k) {
+      const int r = rb + k * step;
+      const int rr = r < count ? r : r0;
+      x[k] = r < count ? __ldcg(pl + (size_t)rr * l_pitch) : -INFINITY;
+      v[k] = __ldcg(reinterpret_cast<const float4*>(po + (size_t)rr * o_pitch));
+    }
+    float mb = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kPartBatch; ++k) mb = fmaxf(mb, x[k]);
+    const float mn = fmaxf(st.m, mb);
+    if (mn == -INFINITY) continue;                 // nothing with weight yet
+    const float sc = st.m == -INFINITY ? 0.f : __expf(st.m - mn);
+    st.l *= sc; st.a0 *= sc; st.a1 *= sc; st.a2 *= sc; st.a3 *= sc;
+#pragma unroll
+    for (int k = 0; k < kPartBatch; ++k) {
+      const float w = x[k] == -INFINITY ? 0.f : __expf(x[k] - mn);
+      const bool use = w != 0.f;
+      st.l += w;
+      st.a0 = use ? fmaf(w, v[k].x, st.a0) : st.a0;
+      st.a1 = use ? fmaf(w, v[k].y, st.a1) : st.a1;
+      st.a2 = use ? fmaf(w, v[k].z, st.a2) : st.a2;
+      st.a3 = use ? fmaf(w, v[k].w, st.a3) : st.a3;
+    }
+    st.m = mn;
+  }
+}
+
+// Merge records of the plan (groups that were split, or are empty).  The work
+// is the rows of all records (record-major); CTA k takes a contiguous share, so
+// it reads each record it touches once.  A record of `count` partials is
+// merged S = 1, 2 or 4 ways (count <= 8, <= 16, more): the CTA's four groups of
+// 128 threads take 4/S rows at a time, each row split over S groups that fold
+// every S-th partial and then combine their states through shared memory in
+// group order.  Each thread owns four columns of its row.
+__global__ void __launch_bounds__(kPlanMergeThreads) plan_merge_kernel(PlanMergeArgs a, const char* ws) {
+  __shared__ float s_st[kGroups][6][kDLat / 4];
   pdl_wait();
   pdl_trigger();
   const int* hdr = reinterpret_cast<const int*>(ws);
   const int* mrg = reinterpret_cast<const int*>(ws + a.L.off_merge);
   const float* part_lse = reinterpret_cast<const float*>(ws + a.L.off_part_lse);
   const float* part_o = reinterpret_cast<const float*>(ws + a.L.off_part_o);
-  const int num_merge = hdr[MLA_HDR_NUM_MERGE];
   const int R = a.T * a.H;
-  constexpr int kChunks = kDLat / 4;
-  constexpr int kRowsPerCta = kMergeThreads / kChunks;
-  constexpr int kItemsPerRecord = kRowsPerBlock / kRowsPerCta;
-  const int c = 4 * (threadIdx.x % kChunks);
-  const long long items = (long long)num_merge * kItemsPerRecord;
-  for (long long it = blockIdx.x; it < items; it += gridDim.x) {
-    const int i = (int)(it / kItemsPerRecord);
-    const int row = (int)(it % kItemsPerRecord) * kRowsPerCta + threadIdx.x / kChunks;
-    const int b = mrg[i * kMergeWords + 0], rb = mrg[i * kMergeWords + 1];
-    const int first = mrg[i * kMergeWords + 2], count = mrg[i * kMergeWords + 3];
+  const long long V = (long long)hdr[MLA_HDR_NUM_MERGE] * kRowsPerBlock;
+  const long long per = (V + gridDim.x - 1) / gridDim.x;
+  const long long v_end = min(V, (blockIdx.x + 1) * per);
+  const int grp = threadIdx.x / (kDLat / 4);
+  const int c = 4 * (threadIdx.x % (kDLat / 4));
+  int cur = -1, b = 0, rb = 0, first = 0, count = 0, S = 1;
+  for (long long v = blockIdx.x * per; v < v_end;) {
+    const int i = (int)(v / kRowsPerBlock);
+    const int row0 = (int)(v % kRowsPerBlock);
+    if (i != cur) {
+      cur = i;
+      b = mrg[i * kMergeWords + 0];
+      rb = mrg[i * kMergeWords + 1];
+      first = mrg[i * kMergeWords + 2];
+      count = mrg[i * kMergeWords + 3];
+      S = count <= kPartBatch ? 1 : (count <= 2 * kPartBatch ? 2 : 4);
+    }
+    const int nrows = (int)min((long long)min(kGroups / S, kRowsPerBlock - row0), v_end - v);
+    const int rl = grp / S, s = grp % S;
+    const int row = row0 + rl;
     const int fr = rb * kRowsPerBlock + row;
-    if (fr >= R) continue;
-    const size_t grow = (size_t)b * R + fr;
-    merge4(part_o + ((size_t)first * kRowsPerBlock + row) * kDLat + c, part_lse + (size_t)first * kRowsPerBlock + row,
-           (size_t)kRowsPerBlock * kDLat, kRowsPerBlock, count, a.o_lat + grow * kDLat + c,
-           c == 0 ? a.lse + grow : nullptr);
+    const bool valid = rl < nrows && fr < R;
+    MergeState st{-INFINITY, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (valid)
+      fold_partials(st, part_o + ((size_t)first * kRowsPerBlock + row) * kDLat + c,
+                    part_lse + (size_t)first * kRowsPerBlock + row, (size_t)kRowsPerBlock * kDLat, kRowsPerBlock, s,
+                    S, count);
+    if (S > 1) {
+      const int t = threadIdx.x % (kDLat / 4);
+      s_st[grp][0][t] = st.m; s_st[grp][1][t] = st.l;
+      s_st[grp][2][t] = st.a0; s_st[grp][3][t] = st.a1; s_st[grp][4][t] = st.a2; s_st[grp][5][t] = st.a3;
+      __syncthreads();
+      if (s == 0) {
+        float mx = -INFINITY;
+        for (int j = 0; j < S; ++j) mx = fmaxf(mx, s_st[grp + j][0][t]);
+        MergeState m{mx, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (mx != -INFINITY) {
+          for (int j = 0; j < S; ++j) {
+            const float mj = s_st[grp + j][0][t];
+            const float f = mj == -INFINITY ? 0.f : __expf(mj - mx);
+            m.l = fmaf(f, s_st[grp + j][1][t], m.l);
+            m.a0 = fmaf(f, s_st[grp + j][2][t], m.a0);
+            m.a1 = fmaf(f, s_st[grp + j][3][t], m.a1);
+            m.a2 = fmaf(f, s_st[grp + j][4][t], m.a2);
+            m.a3 = fmaf(f, s_st[grp + j][5][t], m.a3);
+          }
+        }
+        st = m;
+      }
+      __syncthreads();
+    }
+    if (valid && s == 0) {
+      const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(st.a0 * inv, st.a1 * inv);
+      const __nv_bfloat162 h1 = __floats2bfloat162_rn(st.a2 * inv, st.a3 * inv);
+      uint2 u;
+      u.x = *reinterpret_cast<const uint32_t*>(&h0);
+      u.y = *reinterpret_cast<const uint32_t*>(&h1);
+      const size_t grow = (size_t)b * R + fr;
+      *reinterpret_cast<uint2*>(a.o_lat + grow * kDLat + c) = u;
+      if (c == 0) a.lse[grow] = st.l > 0.f ? st.m + logf(st.l) : -INFINITY;
+    }
+    v += nrows;
   }
 }
 
@@ -134,13 +230,13 @@ cudaError_t launch_plan_merge(const mla_geom* g, const mla_batch* b, const WsLay
   PlanMergeArgs a;
   a.T = b->T; a.H = g->H; a.o_lat = o_lat; a.lse = lse; a.L = L;
   if (L.cap_groups <= 0) return cudaSuccess;
-  // Eight 256-thread CTAs fill an SM; the grid never exceeds the possible items.
-  const long long cap_items = (long long)L.cap_groups * (kRowsPerBlock / (kMergeThreads / (kDLat / 4)));
+  // Two 512-thread CTAs per SM; never more CTAs than the possible rows.
+  const long long cap_rows = (long long)L.cap_groups * kRowsPerBlock;
   const int sms = mla_device_sm_count();
-  long long nctas = 8LL * (sms > 0 ? sms : 148);
-  if (nctas > cap_items) nctas = cap_items;
+  long long nctas = 2LL * (sms > 0 ? sms : 148);
+  if (nctas > cap_rows) nctas = cap_rows;
   const dim3 grid((unsigned)nctas);
-  return launch_pdl(plan_merge_kernel, grid, dim3(kMergeThreads), 0, st, a, reinterpret_cast<const char*>(ws));
+  return launch_pdl(plan_merge_kernel, grid, dim3(kPlanMergeThreads), 0, st, a, reinterpret_cast<const char*>(ws));
 }
 
 cudaError_t launch_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M, int rows,
