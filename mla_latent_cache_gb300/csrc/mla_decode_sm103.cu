@@ -408,9 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_slot;
-  // No early trigger: the merge that follows should be placed on the SMs as they
-  // free up together, not packed onto the first few that do.
   pdl_wait();
+  // Let the merge pass launch now: its CTAs cannot share an SM with this kernel's
+  // (shared memory), so they take idle SMs and those this grid frees, and wait
+  // there for this grid to finish instead of paying their launch after it.
+  pdl_trigger();
   const int num_ranges = hdr[MLA_HDR_NUM_RANGES];
   const SegWalk walk0(rptr, pair, num_pairs, num_ranges);
 
