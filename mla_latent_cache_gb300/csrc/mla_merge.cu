@@ -66,7 +66,7 @@ struct PlanMergeArgs {
   WsLayout L;
 };
 
-constexpr int kPlanMergeThreads = 512;             // four groups of 128 threads, one float4 column chunk each
+constexpr int kPlanMergeThreads = 1024;            // eight groups of 128 threads, one float4 column chunk each
 constexpr int kGroups = kPlanMergeThreads / (kDLat / 4);
 constexpr int kPartBatch = 8;                      // partial loads a thread keeps in flight
 
@@ -113,13 +113,72 @@ __device__ __forceinline__ void fold_partials(MergeState& st, const float* po, c
   }
 }
 
+// Store four merged columns of one row (and, from the thread of column 0, its LSE).
+__device__ __forceinline__ void store_row(const PlanMergeArgs& a, size_t grow, int c, const MergeState& st) {
+  const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(st.a0 * inv, st.a1 * inv);
+  const __nv_bfloat162 h1 = __floats2bfloat162_rn(st.a2 * inv, st.a3 * inv);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&h0);
+  u.y = *reinterpret_cast<const uint32_t*>(&h1);
+  *reinterpret_cast<uint2*>(a.o_lat + grow * kDLat + c) = u;
+  if (c == 0) a.lse[grow] = st.l > 0.f ? st.m + logf(st.l) : -INFINITY;
+}
+
+// A record of at most kPartBatch partials, padded to CP (2, 4 or 8): each
+// thread merges kPartBatch / CP rows at once (rows rl = grp + kGroups j of the
+// nrows starting at row0), so that every thread has kPartBatch loads in flight
+// whatever the count.
+template <int CP>
+__device__ __forceinline__ void merge_rows(const PlanMergeArgs& a, const float* part_o, const float* part_lse,
+                                           int first, int count, int b, int rb, int R, int row0, int nrows, int grp,
+                                           int c) {
+  constexpr int RG = kPartBatch / CP;
+  float x[kPartBatch];
+  float4 v[kPartBatch];
+#pragma unroll
+  for (int k = 0; k < kPartBatch; ++k) {
+    const int j = k / CP, r = k % CP;
+    const int rl = grp + kGroups * j;
+    const bool ok = rl < nrows && rb * kRowsPerBlock + row0 + rl < R && r < count;
+    const size_t pr = (size_t)(first + r) * kRowsPerBlock + row0 + rl;
+    x[k] = ok ? __ldcg(part_lse + pr) : -INFINITY;
+    v[k] = ok ? __ldcg(reinterpret_cast<const float4*>(part_o + pr * kDLat + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int j = 0; j < RG; ++j) {
+    const int rl = grp + kGroups * j;
+    const int fr = rb * kRowsPerBlock + row0 + rl;
+    if (rl >= nrows || fr >= R) continue;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < CP; ++r) mx = fmaxf(mx, x[j * CP + r]);
+    MergeState st{mx, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (mx != -INFINITY) {
+#pragma unroll
+      for (int r = 0; r < CP; ++r) {
+        const float xr = x[j * CP + r];
+        const float w = xr == -INFINITY ? 0.f : __expf(xr - mx);
+        const bool use = w != 0.f;
+        st.l += w;
+        st.a0 = use ? fmaf(w, v[j * CP + r].x, st.a0) : st.a0;
+        st.a1 = use ? fmaf(w, v[j * CP + r].y, st.a1) : st.a1;
+        st.a2 = use ? fmaf(w, v[j * CP + r].z, st.a2) : st.a2;
+        st.a3 = use ? fmaf(w, v[j * CP + r].w, st.a3) : st.a3;
+      }
+    }
+    store_row(a, (size_t)b * R + fr, c, st);
+  }
+}
+
 // Merge records of the plan (groups that were split, or are empty).  The work
 // is the rows of all records (record-major); CTA k takes a contiguous share, so
 // it reads each record it touches once.  A record of `count` partials is
-// merged S = 1, 2 or 4 ways (count <= 8, <= 16, more): the CTA's four groups of
-// 128 threads take 4/S rows at a time, each row split over S groups that fold
-// every S-th partial and then combine their states through shared memory in
-// group order.  Each thread owns four columns of its row.
+// merged by one thread per column chunk when count <= 8 (merge_rows: several
+// rows per thread for small counts), else S = 2, 4 or 8 ways (count <= 16, <= 32,
+// more): the CTA's eight groups of 128 threads take 8/S rows at a time, each row
+// split over S groups that fold every S-th partial and then combine their
+// states through shared memory in group order.  Each thread owns four columns.
 __global__ void __launch_bounds__(kPlanMergeThreads) plan_merge_kernel(PlanMergeArgs a, const char* ws) {
   __shared__ float s_st[kGroups][6][kDLat / 4];
   pdl_wait();
@@ -144,7 +203,16 @@ __global__ void __launch_bounds__(kPlanMergeThreads) plan_merge_kernel(PlanMerge
       rb = mrg[i * kMergeWords + 1];
       first = mrg[i * kMergeWords + 2];
       count = mrg[i * kMergeWords + 3];
-      S = count <= kPartBatch ? 1 : (count <= 2 * kPartBatch ? 2 : 4);
+      S = count <= kPartBatch ? 1 : count <= 2 * kPartBatch ? 2 : count <= 4 * kPartBatch ? 4 : 8;
+    }
+    if (S == 1) {
+      const int cp = count <= 2 ? 2 : count <= 4 ? 4 : 8;   // an empty group (count 0) takes 2
+      const int nrows = (int)min((long long)min(kGroups * (kPartBatch / cp), kRowsPerBlock - row0), v_end - v);
+      if (cp == 2) merge_rows<2>(a, part_o, part_lse, first, count, b, rb, R, row0, nrows, grp, c);
+      else if (cp == 4) merge_rows<4>(a, part_o, part_lse, first, count, b, rb, R, row0, nrows, grp, c);
+      else merge_rows<8>(a, part_o, part_lse, first, count, b, rb, R, row0, nrows, grp, c);
+      v += nrows;
+      continue;
     }
     const int nrows = (int)min((long long)min(kGroups / S, kRowsPerBlock - row0), v_end - v);
     const int rl = grp / S, s = grp % S;
@@ -156,7 +224,7 @@ __global__ void __launch_bounds__(kPlanMergeThreads) plan_merge_kernel(PlanMerge
       fold_partials(st, part_o + ((size_t)first * kRowsPerBlock + row) * kDLat + c,
                     part_lse + (size_t)first * kRowsPerBlock + row, (size_t)kRowsPerBlock * kDLat, kRowsPerBlock, s,
                     S, count);
-    if (S > 1) {
+    {
       const int t = threadIdx.x % (kDLat / 4);
       s_st[grp][0][t] = st.m; s_st[grp][1][t] = st.l;
       s_st[grp][2][t] = st.a0; s_st[grp][3][t] = st.a1; s_st[grp][4][t] = st.a2; s_st[grp][5][t] = st.a3;
@@ -180,17 +248,7 @@ __global__ void __launch_bounds__(kPlanMergeThreads) plan_merge_kernel(PlanMerge
       }
       __syncthreads();
     }
-    if (valid && s == 0) {
-      const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
-      const __nv_bfloat162 h0 = __floats2bfloat162_rn(st.a0 * inv, st.a1 * inv);
-      const __nv_bfloat162 h1 = __floats2bfloat162_rn(st.a2 * inv, st.a3 * inv);
-      uint2 u;
-      u.x = *reinterpret_cast<const uint32_t*>(&h0);
-      u.y = *reinterpret_cast<const uint32_t*>(&h1);
-      const size_t grow = (size_t)b * R + fr;
-      *reinterpret_cast<uint2*>(a.o_lat + grow * kDLat + c) = u;
-      if (c == 0) a.lse[grow] = st.l > 0.f ? st.m + logf(st.l) : -INFINITY;
-    }
+    if (valid && s == 0) store_row(a, (size_t)b * R + fr, c, st);
     v += nrows;
   }
 }
@@ -230,10 +288,10 @@ cudaError_t launch_plan_merge(const mla_geom* g, const mla_batch* b, const WsLay
   PlanMergeArgs a;
   a.T = b->T; a.H = g->H; a.o_lat = o_lat; a.lse = lse; a.L = L;
   if (L.cap_groups <= 0) return cudaSuccess;
-  // Two 512-thread CTAs per SM; never more CTAs than the possible rows.
+  // One 1024-thread CTA per SM; never more CTAs than the possible rows.
   const long long cap_rows = (long long)L.cap_groups * kRowsPerBlock;
   const int sms = mla_device_sm_count();
-  long long nctas = 2LL * (sms > 0 ? sms : 148);
+  long long nctas = sms > 0 ? sms : 148;
   if (nctas > cap_rows) nctas = cap_rows;
   const dim3 grid((unsigned)nctas);
   return launch_pdl(plan_merge_kernel, grid, dim3(kPlanMergeThreads), 0, st, a, reinterpret_cast<const char*>(ws));
