@@ -276,19 +276,13 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         st.step(stream)
     stream.synchronize()
-    # One graph per step: the plan (forked stream) and the absorption are
-    # independent; decode (+ merge) and un-absorption follow, every kernel chained
-    # to its predecessor with programmatic dependent launch.  A second graph holds
-    # the decode alone, replayed between CUDA events to time the dominant kernel.
+    # One graph per step: plan, absorb, decode (+ merge), un-absorb on one stream,
+    # every kernel chained to its predecessor with programmatic dependent launch
+    # (the absorption streams its weights in while the plan runs).  A second graph
+    # holds the decode alone, replayed between CUDA events to time the dominant kernel.
     g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream(device=dev)
     with torch.cuda.graph(g_step, stream=stream):
-        side.wait_stream(stream)
-        st.plan(side)
-        st.absorb(stream)
-        stream.wait_stream(side)
-        st.decode(stream)
-        st.unabsorb(stream)
+        st.step(stream)
     with torch.cuda.graph(g_dec, stream=stream):
         st.decode(stream)
     launches_per_step = 5  # plan, absorb, decode, merge, un-absorb
@@ -405,8 +399,8 @@ def run_ours(args):
                    "S_total": int(np.asarray(w.seq_lens, dtype=np.int64).sum()), "page": 64,
                    "pool_blocks": w.num_blocks, "parallelism": f"replicas{world}", "splits": args.splits or "auto",
                    "l2": l2_note,
-                   "step": "plan (forked stream) || absorb, decode(+merge), unabsorb; one CUDA graph per step, kernels "
-                           "chained with programmatic dependent launch; decode timed alone in its own graph"},
+                   "step": "plan, absorb, decode(+merge), unabsorb; one CUDA graph per step, kernels chained with "
+                           "programmatic dependent launch; decode timed alone in its own graph"},
         "roofline": roof,
         "step_hbm_gbs": ab["step"] / (ms / 1000.0) / 1e9,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -71,6 +71,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
+  // The weights are no kernel's output, so the first ring's worth of weight
+  // k-steps is requested before waiting on the previous kernel in the stream
+  // (in a decode step, the planner): their streaming overlaps that kernel.
+  if (warp == 0 && lane == 0) {
+    for (int kb = 0; kb < C::kSlots; ++kb) {
+      mbar_arrive_expect_tx(bar(kb), C::kSlot);
+      if (BMN) {
+        for (int j = 0; j < NT / 64; ++j) tma_load_3d(slot_b(kb) + j * 8192, &tm_b, bar(kb), n0 + 64 * j, 64 * kb, h);
+      } else {
+        tma_load_3d(slot_b(kb), &tm_b, bar(kb), 64 * kb, n0, h);
+      }
+    }
+  }
   pdl_wait();
   pdl_trigger();
 
@@ -79,6 +92,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int kb = 0; kb < KB; ++kb) {
         const int s = kb % C::kSlots;
+        if (kb < C::kSlots) {  // weight slice already requested
+          tma_load_3d(slot_a(s), &tm_a, bar(s), 64 * kb, h, m0);
+          ++issued;
+          continue;
+        }
         if (!mbar_wait(bar(C::kSlots + s), ((kb / C::kSlots) & 1) ^ 1, abort_flag)) {
           *abort_flag = 1;
           atomicCAS(status, 0, MLA_ERR_TIMEOUT);
