@@ -1,6 +1,8 @@
 // Device split planner: builds the work plan (segments, ranges, merge list) in
 // the workspace from the device-resident sequence lengths, with no host sync.
 // The rule is stated in include/mla.h next to the plan layout.
+#include <climits>
+
 #include "mla_internal.cuh"
 
 namespace mla {
@@ -8,32 +10,67 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-// Block-wide exclusive scan of one int per thread; *total gets the block sum.
-__device__ int block_excl_scan(int v, int* total, int* sh) {
+constexpr int kSmemGroups = 4096;   // groups whose segment bases the planner keeps in shared memory
+
+// Block-wide exclusive scans of three ints per thread at once; tot[] gets the
+// block sums.  sh holds 3 x 32 ints.
+__device__ void block_excl_scan3(int (&v)[3], int (&tot)[3], int* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
-  int x = v;
+  int x[3] = {v[0], v[1], v[2]};
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int y = __shfl_up_sync(0xffffffffu, x[j], o);
+      if (lane >= o) x[j] += y;
+    }
   }
-  if (lane == 31) sh[warp] = x;
+  if (lane == 31) {
+#pragma unroll
+    for (int j = 0; j < 3; ++j) sh[32 * j + warp] = x[j];
+  }
   __syncthreads();
-  if (warp == 0) {
-    int w = lane < nwarps ? sh[lane] : 0;
+  if (warp < 3) {
+    int w = lane < nwarps ? sh[32 * warp + lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, w, o);
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    sh[lane] = w;
+    sh[32 * warp + lane] = w;
   }
   __syncthreads();
-  int pre = warp ? sh[warp - 1] : 0;
-  *total = sh[nwarps - 1];
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int pre = warp ? sh[32 * j + warp - 1] : 0;
+    tot[j] = sh[32 * j + nwarps - 1];
+    v[j] = pre + x[j] - v[j];
+  }
   __syncthreads();
-  return pre + x - v;
+}
+
+// Block-wide (sum, max) of two ints and (wrapping sum, min) of an unsigned and
+// an int: warp shuffles, then one value per warp through shared memory.
+__device__ void block_reduce(unsigned& usum, int& imin, int& isum, int& imax, int* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    usum += __shfl_xor_sync(0xffffffffu, usum, o);
+    imin = min(imin, __shfl_xor_sync(0xffffffffu, imin, o));
+    isum += __shfl_xor_sync(0xffffffffu, isum, o);
+    imax = max(imax, __shfl_xor_sync(0xffffffffu, imax, o));
+  }
+  if (lane == 0) {
+    sh[warp] = (int)usum; sh[32 + warp] = imin; sh[64 + warp] = isum; sh[96 + warp] = imax;
+  }
+  __syncthreads();
+  usum = 0; imin = INT_MAX; isum = 0; imax = INT_MIN;
+  for (int w = 0; w < nwarps; ++w) {
+    usum += (unsigned)sh[w]; imin = min(imin, sh[32 + w]); isum += sh[64 + w]; imax = max(imax, sh[96 + w]);
+  }
+  __syncthreads();
 }
 
 __device__ __forceinline__ uint32_t mix32(uint32_t x) {
@@ -48,35 +85,55 @@ struct PlanArgs {
   WsLayout L;
 };
 
+// Segment s of a group with n pages starting at global page off, its first
+// segment sb, in the given mode; writes the record and, for a segment that
+// opens a work range, the range pointer.
+__device__ __forceinline__ void write_segment(int* seg, int* rptr, int mode, int q, int b, int rb, int n, int off,
+                                              int k, int sb, int pb, int s) {
+  int p0, p1, r;
+  if (mode == 2) {
+    p0 = (int)(((long long)s * n) / k);
+    p1 = (int)(((long long)(s + 1) * n) / k);
+    r = sb + s;
+  } else if (mode == 0) {
+    p0 = 0; p1 = n; r = sb;
+  } else {
+    r = off / q + s;
+    const int gs = max(off, r * q), ge = min(off + n, (r + 1) * q);
+    p0 = gs - off; p1 = ge - off;
+  }
+  int* rec = seg + (size_t)(sb + s) * kSegWords;
+  rec[0] = b; rec[1] = rb; rec[2] = p0; rec[3] = p1; rec[4] = r;
+  rec[5] = (k > 1) ? pb + s : -1; rec[6] = 0; rec[7] = 0;
+  // Every range starts with the segment holding its first page.
+  if (mode != 1 || (off + p0) % q == 0) rptr[r] = sb + s;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws) {
   int* hdr = reinterpret_cast<int*>(ws);
   int* grp = reinterpret_cast<int*>(ws + a.L.off_groups);
   int* seg = reinterpret_cast<int*>(ws + a.L.off_segments);
   int* rptr = reinterpret_cast<int*>(ws + a.L.off_range_ptr);
   int* mrg = reinterpret_cast<int*>(ws + a.L.off_merge);
-  __shared__ int sh[32];
-  __shared__ int s_W, s_nonempty, s_maxn, s_err, s_errinfo;
-  __shared__ unsigned s_hash;
-  __shared__ int s_q, s_mode, s_total_seg, s_total_part, s_total_merge;
+  __shared__ int sh[128];
+  __shared__ int s_sb[kSmemGroups];
+  __shared__ int s_q, s_mode;
   const int tid = threadIdx.x;
-  if (tid == 0) {
-    s_W = 0; s_nonempty = 0; s_maxn = 0; s_err = 0; s_errinfo = 0; s_hash = 0;
-  }
   pdl_wait();
   pdl_trigger();
-  __syncthreads();
 
-  // Sequence-length stamp and validation.
+  // Sequence-length stamp (a wrapping sum, so order-free) and validation (the
+  // smallest offending sequence is reported).
+  unsigned hsum = 0;
+  int errb = INT_MAX;
   for (int b = tid; b < a.B; b += blockDim.x) {
-    int S = a.seq_lens[b];
-    atomicAdd(&s_hash, mix32((uint32_t)S * 0x9E3779B1u + mix32((uint32_t)b + 0x632BE5ABu)));
-    if (S < 0 || S > a.max_pages * kPage || (S > 0 && S < a.T)) {
-      if (atomicCAS(&s_err, 0, MLA_ERR_DEVICE_CHECK) == 0) s_errinfo = b;
-    }
+    const int S = a.seq_lens[b];
+    hsum += mix32((uint32_t)S * 0x9E3779B1u + mix32((uint32_t)b + 0x632BE5ABu));
+    if (S < 0 || S > a.max_pages * kPage || (S > 0 && S < a.T)) errb = min(errb, b);
   }
 
   // Pass A: pages per group and their exclusive prefix.
-  int carry = 0;
+  int carry = 0, nonempty = 0, maxn = 0;
   const int R = a.T * a.H;
   for (int base = 0; base < a.num_groups; base += blockDim.x) {
     const int g = base + tid;
@@ -89,38 +146,37 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
       const int vis = visible_limit(S, a.T, r_last / a.H, a.causal);
       n = (vis + kPage - 1) / kPage;
     }
-    int tot;
-    int off = block_excl_scan(n, &tot, sh);
+    int v[3] = {n, 0, 0}, tot[3];
+    block_excl_scan3(v, tot, sh);
     if (g < a.num_groups) {
       grp[g * kGroupWords + 0] = n;
-      grp[g * kGroupWords + 1] = carry + off;
-      if (n > 0) {
-        atomicAdd(&s_nonempty, 1);
-        atomicMax(&s_maxn, n);
-      }
+      grp[g * kGroupWords + 1] = carry + v[0];
+      nonempty += n > 0;
+      maxn = max(maxn, n);
     }
-    carry += tot;
+    carry += tot[0];
   }
+  block_reduce(hsum, errb, nonempty, maxn, sh);
+  const int W = carry;
   if (tid == 0) {
-    s_W = carry;
-    int q = (carry + a.G - 1) / a.G;
+    int q = (W + a.G - 1) / a.G;
     q = q < kMinSplitPages ? kMinSplitPages : q;
     s_q = q;
     if (a.N > 0) s_mode = 2;
-    else if (s_nonempty <= a.G && s_maxn <= (5 * q + 3) / 4) s_mode = 0;
+    else if (nonempty <= a.G && maxn <= (5 * q + 3) / 4) s_mode = 0;
     else s_mode = 1;
   }
   __syncthreads();
   const int q = s_q, mode = s_mode;
 
-  // Pass B: segments per group, segment/slot/merge bases.
+  // Pass B: segments per group, segment/slot/merge bases; merge records.
   int cseg = 0, cpart = 0, cmrg = 0;
   for (int base = 0; base < a.num_groups; base += blockDim.x) {
     const int g = base + tid;
-    int k = 0, n = 0;
+    int k = 0, n = 0, off = 0;
     if (g < a.num_groups) {
       n = grp[g * kGroupWords + 0];
-      const int off = grp[g * kGroupWords + 1];
+      off = grp[g * kGroupWords + 1];
       if (n > 0) {
         if (mode == 2) k = min(n, a.N);
         else if (mode == 0) k = 1;
@@ -129,74 +185,60 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
     }
     const int part = k > 1 ? k : 0;
     const int mflag = (g < a.num_groups && k != 1) ? 1 : 0;
-    int t1, t2, t3;
-    int sb = block_excl_scan(k, &t1, sh);
-    int pb = block_excl_scan(part, &t2, sh);
-    int mb = block_excl_scan(mflag, &t3, sh);
+    int v[3] = {k, part, mflag}, tot[3];
+    block_excl_scan3(v, tot, sh);
     if (g < a.num_groups) {
+      const int sb = cseg + v[0];
+      const int pb = part ? cpart + v[1] : -1;
       grp[g * kGroupWords + 2] = k;
-      grp[g * kGroupWords + 3] = cseg + sb;
-      grp[g * kGroupWords + 4] = part ? cpart + pb : -1;
-      grp[g * kGroupWords + 5] = mflag ? cmrg + mb : -1;
-    }
-    cseg += t1; cpart += t2; cmrg += t3;
-  }
-  if (tid == 0) {
-    s_total_seg = cseg; s_total_part = cpart; s_total_merge = cmrg;
-  }
-  __syncthreads();
-  const int num_ranges = (mode == 1) ? (s_W + q - 1) / q : s_total_seg;
-
-  // Pass C: segment records, merge records and range pointers.
-  for (int g = tid; g < a.num_groups; g += blockDim.x) {
-    const int n = grp[g * kGroupWords + 0];
-    const int off = grp[g * kGroupWords + 1];
-    const int k = grp[g * kGroupWords + 2];
-    const int sb = grp[g * kGroupWords + 3];
-    const int pb = grp[g * kGroupWords + 4];
-    const int mi = grp[g * kGroupWords + 5];
-    const int b = g / a.RB, rb = g % a.RB;
-    for (int s = 0; s < k; ++s) {
-      int p0, p1, r;
-      if (mode == 2) {
-        p0 = (int)(((long long)s * n) / k);
-        p1 = (int)(((long long)(s + 1) * n) / k);
-        r = sb + s;
-      } else if (mode == 0) {
-        p0 = 0; p1 = n; r = sb;
-      } else {
-        const int r0 = off / q;
-        r = r0 + s;
-        const int gs = max(off, r * q), ge = min(off + n, (r + 1) * q);
-        p0 = gs - off; p1 = ge - off;
+      grp[g * kGroupWords + 3] = sb;
+      grp[g * kGroupWords + 4] = pb;
+      grp[g * kGroupWords + 5] = mflag ? cmrg + v[2] : -1;
+      if (g < kSmemGroups) s_sb[g] = sb;
+      if (mflag) {
+        int* m = mrg + (size_t)(cmrg + v[2]) * kMergeWords;
+        m[0] = g / a.RB; m[1] = g % a.RB; m[2] = (k > 1) ? pb : 0; m[3] = (k > 1) ? k : 0;
       }
-      int* rec = seg + (size_t)(sb + s) * kSegWords;
-      rec[0] = b; rec[1] = rb; rec[2] = p0; rec[3] = p1; rec[4] = r;
-      rec[5] = (k > 1) ? pb + s : -1; rec[6] = 0; rec[7] = 0;
     }
-    if (mi >= 0) {
-      int* m = mrg + (size_t)mi * kMergeWords;
-      m[0] = b; m[1] = rb; m[2] = (k > 1) ? pb : 0; m[3] = (k > 1) ? k : 0;
-    }
+    cseg += tot[0]; cpart += tot[1]; cmrg += tot[2];
   }
   __syncthreads();
-  // First segment of each range (segments are in nondecreasing range order).
-  for (int i = tid; i < s_total_seg; i += blockDim.x) {
-    const int r = seg[(size_t)i * kSegWords + 4];
-    const int rprev = i ? seg[(size_t)(i - 1) * kSegWords + 4] : -1;
-    for (int rr = rprev + 1; rr <= r; ++rr) rptr[rr] = i;
+  const int total_seg = cseg;
+  const int num_ranges = (mode == 1) ? (W + q - 1) / q : total_seg;
+
+  // Pass C: segment records and range pointers, one segment per thread (its
+  // group found by binary search over the segment bases), or one group per
+  // thread when there are more groups than shared memory holds.
+  if (a.num_groups <= kSmemGroups) {
+    for (int i = tid; i < total_seg; i += blockDim.x) {
+      int lo = 0, hi = a.num_groups;        // last group whose first segment is <= i
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_sb[mid] <= i) lo = mid; else hi = mid;
+      }
+      const int g = lo;
+      const int* gr = grp + g * kGroupWords;
+      write_segment(seg, rptr, mode, q, g / a.RB, g % a.RB, gr[0], gr[1], gr[2], gr[3], gr[4], i - gr[3]);
+    }
+  } else {
+    for (int g = tid; g < a.num_groups; g += blockDim.x) {
+      const int* gr = grp + g * kGroupWords;
+      const int k = gr[2];
+      for (int s = 0; s < k; ++s)
+        write_segment(seg, rptr, mode, q, g / a.RB, g % a.RB, gr[0], gr[1], k, gr[3], gr[4], s);
+    }
   }
   if (tid == 0) {
-    rptr[num_ranges] = s_total_seg;
+    rptr[num_ranges] = total_seg;
     hdr[MLA_HDR_B] = a.B; hdr[MLA_HDR_T] = a.T; hdr[MLA_HDR_H] = a.H; hdr[MLA_HDR_CAUSAL] = a.causal;
     hdr[MLA_HDR_NUM_GROUPS] = a.num_groups;
-    hdr[MLA_HDR_NUM_SEGMENTS] = s_total_seg;
+    hdr[MLA_HDR_NUM_SEGMENTS] = total_seg;
     hdr[MLA_HDR_NUM_RANGES] = num_ranges;
-    hdr[MLA_HDR_NUM_PARTIALS] = s_total_part;
-    hdr[MLA_HDR_NUM_MERGE] = s_total_merge;
-    hdr[MLA_HDR_SEQ_HASH] = (int)s_hash;
-    hdr[MLA_HDR_ERROR] = s_err;
-    hdr[MLA_HDR_ERROR_INFO] = s_errinfo;
+    hdr[MLA_HDR_NUM_PARTIALS] = cpart;
+    hdr[MLA_HDR_NUM_MERGE] = cmrg;
+    hdr[MLA_HDR_SEQ_HASH] = (int)hsum;
+    hdr[MLA_HDR_ERROR] = errb == INT_MAX ? 0 : MLA_ERR_DEVICE_CHECK;
+    hdr[MLA_HDR_ERROR_INFO] = errb == INT_MAX ? 0 : errb;
     hdr[MLA_HDR_PAGES_PER_RANGE] = q;
     hdr[MLA_HDR_NUM_SLOTS] = a.G;
     hdr[MLA_HDR_OVERRIDE] = a.N;
