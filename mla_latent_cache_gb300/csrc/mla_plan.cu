@@ -66,10 +66,25 @@ __device__ void block_reduce(unsigned& usum, int& imin, int& isum, int& imax, in
     sh[warp] = (int)usum; sh[32 + warp] = imin; sh[64 + warp] = isum; sh[96 + warp] = imax;
   }
   __syncthreads();
-  usum = 0; imin = INT_MAX; isum = 0; imax = INT_MIN;
-  for (int w = 0; w < nwarps; ++w) {
-    usum += (unsigned)sh[w]; imin = min(imin, sh[32 + w]); isum += sh[64 + w]; imax = max(imax, sh[96 + w]);
+  if (warp == 0) {
+    usum = lane < nwarps ? (unsigned)sh[lane] : 0u;
+    imin = lane < nwarps ? sh[32 + lane] : INT_MAX;
+    isum = lane < nwarps ? sh[64 + lane] : 0;
+    imax = lane < nwarps ? sh[96 + lane] : INT_MIN;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      usum += __shfl_xor_sync(0xffffffffu, usum, o);
+      imin = min(imin, __shfl_xor_sync(0xffffffffu, imin, o));
+      isum += __shfl_xor_sync(0xffffffffu, isum, o);
+      imax = max(imax, __shfl_xor_sync(0xffffffffu, imax, o));
+    }
+    // (the shuffles follow every lane's reads, so lane 0 may overwrite the slots)
+    if (lane == 0) {
+      sh[0] = (int)usum; sh[1] = imin; sh[2] = isum; sh[3] = imax;
+    }
   }
+  __syncthreads();
+  usum = (unsigned)sh[0]; imin = sh[1]; isum = sh[2]; imax = sh[3];
   __syncthreads();
 }
 
