@@ -111,6 +111,34 @@ def test_plan_bit_exact(mla, cuda, case):
     assert hdr[mla.HDR["ERROR"]] == 0 or case == "rand"
 
 
+@pytest.mark.parametrize("slots,ov", [(0, 0), (19, 0), (0, 5)])
+def test_plan_bit_exact_many_groups(mla, cuda, slots, ov):
+    """More row groups (70 sequences x 64 row blocks) than the planner keeps in
+    shared memory: the per-group segment path, compared bit for bit."""
+    import torch
+    from mla_latent_cache_gb300.runtime import read_plan_header, read_plan_tables
+    rng = np.random.default_rng(11)
+    B, T, H = 70, 64, 128
+    seq_lens = rng.integers(T, 3000, size=B).astype(np.int32)
+    max_pages = (3000 + 63) // 64
+    geom = mla.make_geom(H)
+    batch = mla.make_batch(B, T, True, max_pages, slots, ov)
+    ws_bytes = mla.mla_workspace_size(geom, batch)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=cuda)
+    seq = torch.from_numpy(seq_lens).to(cuda)
+    mla.check(mla.mla_plan(geom, batch, seq, ws, ws_bytes))
+    torch.cuda.synchronize()
+    G = slots if slots > 0 else mla.mla_device_sm_count() // 2
+    ref = O.plan_ref(seq_lens, T, H, True, G, ov)
+    assert len(O.group_pages(seq_lens, T, H, True)) == B * 64 > 4096
+    seg, rp, mg = read_plan_tables(torch, ws)
+    assert [tuple(int(x) for x in r[:6]) for r in seg] == [tuple(r) for r in ref["segments"]]
+    assert rp.tolist() == ref["range_ptr"]
+    assert [tuple(int(x) for x in r) for r in mg] == [tuple(r) for r in ref["merge"]]
+    hdr = read_plan_header(torch, ws)
+    assert hdr[mla.HDR["NUM_PARTIALS"]] == ref["num_partials"] and hdr[mla.HDR["ERROR"]] == 0
+
+
 @pytest.mark.parametrize("cfg", [1, 2, 3])
 def test_gather_bit_exact(mla, cuda, cfg):
     import torch
