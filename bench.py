@@ -351,34 +351,30 @@ def run_ours(args):
         raise RuntimeError(f"device status after timing: {L.mla_status_string(status)} ({info})")
 
     # end to end through the C ABI with host buffers: per step, copy the step's inputs
-    # (q_nope, q_pe, seq_lens, block table) from pinned host memory, run, read o back.
-    h_qn = torch.empty_like(st.q_nope, device="cpu").pin_memory(); h_qn.copy_(st.q_nope)
-    h_qp = torch.empty_like(st.q_pe, device="cpu").pin_memory(); h_qp.copy_(st.q_pe)
-    h_sl = torch.empty_like(st.seq_lens, device="cpu").pin_memory(); h_sl.copy_(st.seq_lens)
-    h_bt = torch.empty_like(st.block_table, device="cpu").pin_memory(); h_bt.copy_(st.block_table)
+    # (q_nope, q_pe, seq_lens, block table: one pinned host buffer mirroring the
+    # device buffer they live in) to the device, run, read o back; the copies and
+    # the step are one graph.
+    h_in = torch.empty_like(st.inputs, device="cpu").pin_memory(); h_in.copy_(st.inputs)
     h_o = torch.empty_like(st.o, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_qn, h_qp, h_sl, h_bt))
+    h2d = h_in.numel() * h_in.element_size()
     d2h = h_o.numel() * h_o.element_size()
     e_steps = max(3, min(args.steps, 200))
-
-    def e2e_step():
-        st.q_nope.copy_(h_qn, non_blocking=True)
-        st.q_pe.copy_(h_qp, non_blocking=True)
-        st.seq_lens.copy_(h_sl, non_blocking=True)
-        st.block_table.copy_(h_bt, non_blocking=True)
-        g_step.replay()
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        st.inputs.copy_(h_in, non_blocking=True)
+        st.step(stream)
         h_o.copy_(st.o, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
-            e2e_step()
+            g_e2e.replay()
     stream.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(e_steps):
-            e2e_step()
+            g_e2e.replay()
         e1.record(stream)
     stream.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)

@@ -50,6 +50,20 @@ class DecodeStep:
             self.o = torch.empty((w.B, w.T, w.H, 128), dtype=torch.bfloat16, device=dev)
         else:
             self.q_lat = _u16_to_bf16(torch, w.q_lat, dev)
+        # The per-step inputs (query halves, lengths, block table) become views of one
+        # device buffer, so that a step's host-to-device traffic can be one copy.
+        parts = [n for n in ("q_nope", "q_pe", "seq_lens", "block_table") if hasattr(self, n)]
+        offs, off = [], 0
+        for n in parts:
+            off = (off + 255) // 256 * 256
+            offs.append(off)
+            off += getattr(self, n).numel() * getattr(self, n).element_size()
+        self.inputs = torch.empty(off, dtype=torch.uint8, device=dev)
+        for n, o in zip(parts, offs):
+            src = getattr(self, n)
+            view = self.inputs[o: o + src.numel() * src.element_size()].view(src.dtype).view(src.shape)
+            view.copy_(src)
+            setattr(self, n, view)
         self.o_lat = torch.empty((w.B, w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((w.B, w.T, w.H), dtype=torch.float32, device=dev)
         self.ws_bytes = L.mla_workspace_size(self.geom, self.batch)
