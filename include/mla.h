@@ -38,6 +38,13 @@
  *     returned status covers host-side validation and launch errors only;
  *     errors seen by kernels are recorded in the workspace's status word and
  *     read back with mla_read_device_status.
+ *   Programmatic dependent launch: every kernel is launched so that it may
+ *     start while the previous kernel in the stream finishes, and waits for that
+ *     kernel before reading anything a previous kernel may produce or writing
+ *     anything it may read.  The weights (w_uk, w_uv), which no call of this
+ *     library writes, may be read before that wait: a caller's kernel that
+ *     writes them must not trigger programmatic launch before it has written
+ *     them (a kernel that never triggers is safe).
  *   Alignment: every device pointer must be 16-byte aligned, and strides must
  *     keep rows 16-byte aligned (MLA_ERR_ALIGN otherwise); the outputs written
  *     with 32-byte stores (q_lat of mla_absorb_q, o of mla_unabsorb_o, o_lat
