@@ -22,7 +22,8 @@ Sources (web pages, cited by title and section):
                   Absorption, and FlashMLA": 0x04 "Batched absorption trace"
                   (canonical einsum shapes), 0x05 "Paged and ragged address
                   translation", 0x06 "Numeric Cache Ledger", 0x09 (decode
-                  intensity), 0x0C (exact merge of sequence-split state).
+                  intensity), 0x0B "FP8 Cache Format And Sparse Selection" (the
+                  656-byte FP8 row), 0x0C (exact merge of sequence-split state).
 
 Parity status: every function below is pinned by a CPU test (closed forms,
 printed values, brute force, a library routine or an invariant) except
@@ -412,3 +413,86 @@ def crossover_T(S, H=128) -> float:
 def decode_intensity(H, d_c=D_C, d_r=D_R, elem=2) -> float:
     """Core FLOPs per cache byte at T=1 (query/output traffic excluded)."""
     return decode_core_flops(H, 1, d_c, d_r) / ((d_c + d_r) * elem)
+
+
+# ---------------------------------------------------------------------------
+# FP8 latent row  ([M5.8] 0x0B "FP8 Cache Format And Sparse Selection", "Exact
+# 656-byte FP8 row"): 512 E4M3 latent values + 4 fp32 scales + 64 bf16 RoPE
+# values; storage format only, attention runs on the dequantized bf16 values.
+# The pages give the three segments and their sizes; the readings taken where
+# they are silent: one scale per 128 consecutive latent values, scale = the
+# tile's largest magnitude / 448 rounded to fp32 (1 for an all-zero tile), the
+# segments stored in the order the pages sum them (codes, scales, RoPE), all
+# multi-byte words little-endian.  E4M3 is the OFP8 format: sign, 4 exponent
+# bits (bias 7), 3 mantissa bits, subnormals at exponent 0, S.1111.111 = NaN,
+# no infinities, largest finite value 448.
+# ---------------------------------------------------------------------------
+E4M3_MAX = 448.0
+FP8_TILE = 128
+FP8_ROW_BYTES = D_C * 1 + (D_C // FP8_TILE) * 4 + D_R * 2   # 656
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of each E4M3 byte (float64; NaN for the two NaN codes)."""
+    c = np.asarray(codes, dtype=np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest E4M3 byte to each value, ties to the even mantissa; magnitudes
+    beyond 448 saturate to +-448 (the quantizer's scale keeps them within it)."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.where(np.signbit(x), 0x80, 0).astype(np.int64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    out = np.empty(a.shape, dtype=np.int64)
+    flat_a, flat_o = a.reshape(-1), out.reshape(-1)
+    for i, v in enumerate(flat_a):
+        if v < 2.0 ** -6:                       # subnormal range: steps of 2^-9
+            m = int(np.rint(v / 2.0 ** -9))      # rint rounds half to even
+            flat_o[i] = m                        # m == 8 is the smallest normal, code 0x08
+            continue
+        e = int(math.floor(math.log2(v)))
+        frac = v / 2.0 ** e                      # in [1, 2)
+        if frac >= 2.0:                          # log2 rounding at a power of two
+            e, frac = e + 1, frac / 2.0
+        elif frac < 1.0:
+            e, frac = e - 1, frac * 2.0
+        m = int(np.rint((frac - 1.0) * 8.0))
+        if m == 8:
+            e, m = e + 1, 0
+        code = ((e + 7) << 3) | m
+        flat_o[i] = min(code, 0x7E)              # 1.875 * 2^8 would be the NaN code: saturate
+    return (out | sign).astype(np.uint8)
+
+
+def fp8_row_quantize(c: np.ndarray, k_pe_bits: np.ndarray) -> np.ndarray:
+    """Pack latent rows c [..., 512] (float64 values) and RoPE bf16 bit patterns
+    k_pe_bits [..., 64] (uint16) into 656-byte rows [..., 656] (uint8)."""
+    c = np.asarray(c, dtype=np.float64)
+    lead = c.shape[:-1]
+    tiles = c.reshape(lead + (D_C // FP8_TILE, FP8_TILE))
+    amax = np.abs(tiles).max(axis=-1)
+    scale = np.where(amax > 0, amax / E4M3_MAX, 1.0).astype(np.float32)
+    codes = e4m3_encode(tiles / scale.astype(np.float64)[..., None]).reshape(lead + (D_C,))
+    out = np.empty(lead + (FP8_ROW_BYTES,), dtype=np.uint8)
+    out[..., :D_C] = codes
+    out[..., D_C:D_C + 16] = scale.astype("<f4").view(np.uint8).reshape(lead + (16,))
+    out[..., D_C + 16:] = np.asarray(k_pe_bits, dtype="<u2").view(np.uint8).reshape(lead + (2 * D_R,))
+    return out
+
+
+def fp8_row_dequantize(rows: np.ndarray) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """(latent values [..., 512] float64, fp32 scales [..., 4], RoPE bf16 bits
+    [..., 64]) of 656-byte rows: value = E4M3 code value * its tile's scale."""
+    rows = np.asarray(rows, dtype=np.uint8)
+    lead = rows.shape[:-1]
+    scale = np.ascontiguousarray(rows[..., D_C:D_C + 16]).view("<f4").reshape(lead + (D_C // FP8_TILE,))
+    vals = e4m3_decode(rows[..., :D_C]).reshape(lead + (D_C // FP8_TILE, FP8_TILE))
+    c_hat = (vals * scale.astype(np.float64)[..., None]).reshape(lead + (D_C,))
+    k_pe_bits = np.ascontiguousarray(rows[..., D_C + 16:]).view("<u2").reshape(lead + (D_R,))
+    return c_hat, scale, k_pe_bits
