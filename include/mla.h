@@ -193,6 +193,20 @@ mla_status mla_split_merge(const float* part_o, const float* part_lse, const int
                            int rows, int D, void* o, float* lse, mla_stream_t stream);
 
 /*
+ * FP8 cache rows ("M5.8" 0x0B "Exact 656-byte FP8 row": 512 E4M3 latent values,
+ * 4 fp32 scales, 64 bf16 RoPE values).  Packs every row of the bf16 pool in
+ * `cache` into out uint8 [num_blocks, 64, 656] (device, 16-byte aligned), row
+ * layout: bytes [0,512) E4M3 codes of latent values 0..511; [512,528) fp32
+ * scales, scale t for latent values [128t, 128t+128); [528,656) the RoPE values,
+ * bf16 (all little-endian).  Scale t = (largest |value| of its tile) / 448 in
+ * fp32, 1 for an all-zero tile; code = E4M3 (round to nearest even, saturating
+ * at +-448) of value / scale in fp32; the row decodes as value = E4M3 * scale.
+ * The pages give the three segments and their sizes; the tile size, scale rule
+ * and order are readings.  NaN inputs are not supported.
+ */
+mla_status mla_fp8_pack_cache(const mla_cache* cache, void* out, mla_stream_t stream);
+
+/*
  * Test export: copy the S_b logical rows of sequence b, in order, through the
  * decode kernel's own address path, into out bf16 [S_b, 576] (latent | RoPE).
  */

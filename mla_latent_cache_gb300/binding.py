@@ -74,6 +74,7 @@ def _load() -> ctypes.CDLL:
         "mla_decode_noalloc": (I, [G, Bt, P, P, C, P, I, P, P, P, P]),
         "mla_split_merge": (I, [P, P, P, I, I, I, P, P, P]),
         "mla_debug_gather": (I, [C, P, I, P, I, P, P]),
+        "mla_fp8_pack_cache": (I, [C, P, P]),
         "mla_normal_rows_per_seq": (ctypes.c_int64, [I]),
         "mla_normal_expanded_bytes": (ctypes.c_size_t, [G, I, I]),
         "mla_normal_expand": (I, [G, C, P, I, P, I, I, P, P, P, P]),
@@ -93,7 +94,8 @@ _lib = _load()
 EXPORTED = ("mla_workspace_size", "mla_plan", "mla_absorb_q", "mla_unabsorb_o", "mla_decode", "mla_decode_noalloc",
             "mla_split_merge", "mla_normal_rows_per_seq", "mla_normal_expanded_bytes", "mla_normal_expand",
             "mla_normal_attention",
-            "mla_debug_gather", "mla_read_device_status", "mla_status_string", "mla_device_sm_count")
+            "mla_fp8_pack_cache", "mla_debug_gather", "mla_read_device_status", "mla_status_string",
+            "mla_device_sm_count")
 
 
 def lib() -> ctypes.CDLL:
@@ -195,6 +197,10 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 def mla_split_merge(part_o, part_lse, indptr, M: int, rows: int, D: int, o, lse, stream=None) -> int:
     return _lib.mla_split_merge(_ptr(part_o), _ptr(part_lse), _ptr(indptr), M, rows, D, _ptr(o), _ptr(lse),
                                 _stream(stream))
+
+
+def mla_fp8_pack_cache(cache: mla_cache, out, stream=None) -> int:
+    return _lib.mla_fp8_pack_cache(ctypes.byref(cache), _ptr(out), _stream(stream))
 
 
 def mla_debug_gather(cache: mla_cache, block_table, bt_stride: int, seq_lens, b: int, out, stream=None) -> int:

@@ -7,6 +7,8 @@
 
 namespace mla {
 
+cudaError_t launch_fp8_pack(const CacheView& cv, unsigned char* out, cudaStream_t st);  // mla_fp8.cu
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -204,6 +206,15 @@ mla_status mla_split_merge(const float* part_o, const float* part_lse, const int
   if (((size_t)rows * D * sizeof(float)) % 16 != 0) return MLA_ERR_ALIGN;
   return cuda_status(launch_split_merge(part_o, part_lse, indptr, M, rows, D, static_cast<__nv_bfloat16*>(o), lse,
                                         (cudaStream_t)stream));
+}
+
+mla_status mla_fp8_pack_cache(const mla_cache* cache, void* out, mla_stream_t stream) {
+  if (!out) return MLA_ERR_ARG;
+  if (!aligned16(out)) return MLA_ERR_ALIGN;
+  CacheView cv;
+  mla_status s = check_cache(cache, &cv);
+  if (s != MLA_OK) return s;
+  return cuda_status(launch_fp8_pack(cv, static_cast<unsigned char*>(out), (cudaStream_t)stream));
 }
 
 mla_status mla_debug_gather(const mla_cache* cache, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,

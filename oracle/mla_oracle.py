@@ -423,7 +423,9 @@ def decode_intensity(H, d_c=D_C, d_r=D_R, elem=2) -> float:
 # they are silent: one scale per 128 consecutive latent values, scale = the
 # tile's largest magnitude / 448 rounded to fp32 (1 for an all-zero tile), the
 # segments stored in the order the pages sum them (codes, scales, RoPE), all
-# multi-byte words little-endian.  E4M3 is the OFP8 format: sign, 4 exponent
+# multi-byte words little-endian.  The pages fix no precision for choosing a
+# code, so scale and quotient are taken in fp32 (IEEE, round to nearest), the
+# precision of the CUDA cache writer.  E4M3 is the OFP8 format: sign, 4 exponent
 # bits (bias 7), 3 mantissa bits, subnormals at exponent 0, S.1111.111 = NaN,
 # no infinities, largest finite value 448.
 # ---------------------------------------------------------------------------
@@ -471,14 +473,15 @@ def e4m3_encode(x) -> np.ndarray:
 
 
 def fp8_row_quantize(c: np.ndarray, k_pe_bits: np.ndarray) -> np.ndarray:
-    """Pack latent rows c [..., 512] (float64 values) and RoPE bf16 bit patterns
+    """Pack latent rows c [..., 512] (values, taken as fp32) and RoPE bf16 bit patterns
     k_pe_bits [..., 64] (uint16) into 656-byte rows [..., 656] (uint8)."""
-    c = np.asarray(c, dtype=np.float64)
+    c = np.asarray(c, dtype=np.float32)
     lead = c.shape[:-1]
     tiles = c.reshape(lead + (D_C // FP8_TILE, FP8_TILE))
     amax = np.abs(tiles).max(axis=-1)
-    scale = np.where(amax > 0, amax / E4M3_MAX, 1.0).astype(np.float32)
-    codes = e4m3_encode(tiles / scale.astype(np.float64)[..., None]).reshape(lead + (D_C,))
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    quot = (tiles / scale[..., None]).astype(np.float32)            # fp32 quotient, round to nearest
+    codes = e4m3_encode(quot.astype(np.float64)).reshape(lead + (D_C,))
     out = np.empty(lead + (FP8_ROW_BYTES,), dtype=np.uint8)
     out[..., :D_C] = codes
     out[..., D_C:D_C + 16] = scale.astype("<f4").view(np.uint8).reshape(lead + (16,))

@@ -229,6 +229,34 @@ def test_decode_split_cache_layout(mla, cuda):
     _compare(st, w, name="split cache")
 
 
+@pytest.mark.parametrize("split", [False, True])
+def test_fp8_pack_cache_bit_exact(mla, cuda, split):
+    """The 656-byte FP8 rows the CUDA writer packs ("M5.8" 0x0B) equal the
+    oracle's byte for byte (codes, fp32 scales, RoPE), combined and split pools."""
+    import torch
+    rng = np.random.default_rng(21)
+    nb = 24
+    vals = (rng.standard_normal((nb, 64, 576)) * 0.1).astype(np.float32)
+    vals[3, 5, 128:256] = 0.0                       # an all-zero tile: scale 1
+    vals[7, :, :512] *= 1e-3                        # small tiles
+    vals[9, 1, :512] = np.where(rng.random(512) < 0.5, -0.0, 0.0)   # signed zeros only
+    vals[11, 2, 0] = 3.0                            # one dominant value: the rest of its tile goes subnormal
+    bits = W.f32_to_bf16_bits(vals)
+    pool = torch.from_numpy(bits.view(np.int16)).to(cuda).view(torch.bfloat16)
+    if split:
+        ckv, kpe = pool[..., :512].contiguous(), pool[..., 512:].contiguous()   # kept alive: the cache holds raw pointers
+        cache = mla.cache_from_split(ckv, kpe)
+    else:
+        cache = mla.cache_from_pool(pool)
+    out = torch.zeros((nb, 64, 656), dtype=torch.uint8, device=cuda)
+    mla.check(mla.mla_fp8_pack_cache(cache, out))
+    torch.cuda.synchronize()
+    ref = O.fp8_row_quantize(W.bf16_bits_to_f32(bits[..., :512]), bits[..., 512:])
+    got = out.cpu().numpy()
+    assert np.array_equal(got[..., 512:], ref[..., 512:])     # scales and RoPE
+    assert np.array_equal(got, ref)
+
+
 # ---------------------------------------------------------------------------
 # absorption GEMMs and the whole chain
 # ---------------------------------------------------------------------------

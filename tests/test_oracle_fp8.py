@@ -80,12 +80,17 @@ def test_row_quantize_bounds_and_layout():
     assert np.array_equal(kpe_back, kpe)
     tiles = c.reshape(7, 4, 128)
     amax = np.abs(tiles).max(-1)
-    assert np.array_equal(scale, np.where(amax > 0, amax / 448.0, 1.0).astype(np.float32))
+    amax32 = np.abs(tiles.astype(np.float32)).max(-1)
+    assert np.array_equal(scale, np.where(amax32 > 0, amax32 / np.float32(448.0), np.float32(1.0)))
+    # fp32 division is correctly rounded: the scale is amax / 448 rounded once
+    nz32 = amax32 > 0
+    assert np.all(np.abs(scale[nz32].astype(np.float64) - amax32[nz32] / 448.0) <= amax32[nz32] / 448.0 * 2.0 ** -24)
     assert np.all(rows[3, 128:256] == 0) and scale[3, 1] == 1.0
     # per element: half a subnormal step (2^-10 * scale) or half a normal ulp (2^-4 relative)
     s = np.repeat(scale.astype(np.float64), 128, axis=1)
     err = np.abs(c_hat - c)
-    assert np.all(err <= np.maximum(s * 2.0 ** -10, np.abs(c) * 2.0 ** -4) * (1 + 1e-12))
+    # (plus the rounding of the inputs and the quotient to fp32)
+    assert np.all(err <= np.maximum(s * 2.0 ** -10, np.abs(c) * 2.0 ** -4) * (1 + 2.0 ** -20))
     # each tile's largest magnitude maps to code 448 and comes back within the scale's fp32 rounding
     idx = np.abs(tiles).argmax(-1)
     hat_max = np.take_along_axis(c_hat.reshape(7, 4, 128), idx[..., None], -1)[..., 0]
