@@ -67,6 +67,12 @@ def test_host_validation_rejects_before_launch(mla):
                           1 << 30, 0) == mla.MLA_ERR_ALIGN
     assert mla.mla_split_merge(None, None, None, 2, 4, 12, None, None, 0) == mla.MLA_ERR_ARG
     assert mla.mla_split_merge(0x1000, 0x2000, 0x3000, 0, 4, 16, 0x4000, 0x5000, 0) == mla.MLA_OK
+    # FP8 cache rows: output present and 16-byte aligned, cache valid
+    assert mla.mla_fp8_pack_cache(cache, None, 0) == mla.MLA_ERR_ARG
+    assert mla.mla_fp8_pack_cache(cache, 0x3008, 0) == mla.MLA_ERR_ALIGN
+    assert mla.mla_fp8_pack_cache(bad_cache, 0x3000, 0) == mla.MLA_ERR_ALIGN
+    empty = mla.mla_cache(0x1000, 0x1400, 576, 64 * 576, 576, 64 * 576, 0)
+    assert mla.mla_fp8_pack_cache(empty, 0x3000, 0) == mla.MLA_ERR_ARG
 
 
 def test_normal_arm_host_side(mla):
