@@ -14,7 +14,8 @@ Sources (web pages, cited by title and section):
                   and the closing float64 single-head parity reference.
   [zdszero]       "MLA" (zdszero.github.io): "Normal 与 Absorb" (the Normal and
                   Absorb forms), "计算量分析" (the MAC table), "谁更省" (the T~170
-                  crossover), the decoupled-RoPE note that the scale stays sqrt(192).
+                  crossover), the decoupled-RoPE note that the scale stays sqrt(192),
+                  "路径选择" (per-batch path choice: the MHA_CHUNKED_KV variant).
   [mlxcel]        "mlxcel: MLA absorbed decode": the bytes/token table and the
                   Stage-2 split-KV merge contract (partials normalised by their own
                   denominator, grouped by an indptr).
@@ -23,7 +24,8 @@ Sources (web pages, cited by title and section):
                   (canonical einsum shapes), 0x05 "Paged and ragged address
                   translation", 0x06 "Numeric Cache Ledger", 0x09 (decode
                   intensity), 0x0B "FP8 Cache Format And Sparse Selection" (the
-                  656-byte FP8 row), 0x0C (exact merge of sequence-split state).
+                  656-byte FP8 row, sparse physical indices), 0x0C (exact merge
+                  of sequence-split state).
 
 Parity status: every function below is pinned by a CPU test (closed forms,
 printed values, brute force, a library routine or an invariant) except
@@ -252,6 +254,75 @@ def merge_ref(part_o: np.ndarray, part_lse: np.ndarray) -> tuple[np.ndarray, np.
     with np.errstate(divide="ignore", invalid="ignore"):
         o = np.where(l[..., None] > 0, np.sum(w[..., None] * part_o, axis=0) / np.where(l > 0, l, 1.0)[..., None], 0.0)
         lse = np.where(l > 0, m_safe + np.log(np.where(l > 0, l, 1.0)), -np.inf)
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# Sparse index-driven decode  ([M5.8] 0x0B "Sparse indices are physical execution
+# metadata"; 0x08 dense vs sparse ABI).  indices [B, S_q, topk] name physical
+# cache rows; topk_length [B] bounds the valid left prefix of every index row of
+# sequence b; causal = False in this ABI.  Reading where the pages are silent: an
+# entry encodes row (block * 64 + offset); a row listed twice counts twice (the
+# softmax runs over the list); an empty list gives o = 0, lse = -inf.
+# ---------------------------------------------------------------------------
+def sparse_decode_ref(q_lat, q_pe, pool, indices, topk_length=None, scale=SCALE):
+    """q_lat [B,S_q,H,512], q_pe [B,S_q,H,64], pool [num_blocks,64,576] (float64
+    row values; FP8 rows pass their dequantized values), indices [B,S_q,topk].
+    Returns o_lat [B,S_q,H,512] and lse [B,S_q,H]."""
+    B, Sq, H, d_c = q_lat.shape
+    page = pool.shape[1]
+    topk = indices.shape[-1]
+    o = np.zeros((B, Sq, H, d_c))
+    lse = np.full((B, Sq, H), -np.inf)
+    for b in range(B):
+        n = topk if topk_length is None else int(topk_length[b])
+        if n <= 0:
+            continue
+        for t in range(Sq):
+            idx = np.asarray(indices[b, t, :n], dtype=np.int64)
+            rows = pool[idx // page, idx % page]
+            ob, lb = attend_latent(q_lat[b, t:t + 1], q_pe[b, t:t + 1], rows, np.ones((1, n), dtype=bool), scale)
+            o[b, t], lse[b, t] = ob[0], lb[0]
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# Chunked-prefix Normal path  ([zdszero] "路径选择" (path choice), the
+# MHA_CHUNKED_KV variant): the prefix is read in chunks, each chunk is expanded
+# with kv_b and attended, and the chunks' states are merged by LSE, so the
+# expanded prefix held at once is bounded by one chunk.
+# ---------------------------------------------------------------------------
+def normal_chunked_ref(q_nope, q_pe, pool, block_table, seq_lens, w_uk, w_uv, causal, chunk_rows: int,
+                       scale=SCALE, batches=None):
+    """The Normal path over the visible rows in chunks of chunk_rows rows: per
+    chunk, k_nope/v = kv_b expansion of its latents, attention restricted to its
+    keys (partial o normalised by its own sum, partial lse), then merge_ref over
+    the chunks.  Returns o [B,T,H,128] and lse [B,T,H]."""
+    B, T, H, _ = q_nope.shape
+    d_c = w_uk.shape[-1]
+    d_r = q_pe.shape[-1]
+    o = np.zeros((B, T, H, w_uv.shape[1]))
+    lse = np.full((B, T, H), -np.inf)
+    for b in (range(B) if batches is None else batches):
+        S = int(seq_lens[b])
+        if S == 0:
+            continue
+        rows = gather_rows(pool, block_table[b], S)
+        mask = causal_mask(S, T, causal)
+        q = np.concatenate([q_nope[b], q_pe[b]], axis=-1)
+        parts_o, parts_l = [], []
+        for j0 in range(0, S, chunk_rows):
+            j1 = min(S, j0 + chunk_rows)
+            c = rows[j0:j1, :d_c]
+            kpe = rows[j0:j1, d_c:]
+            k_nope, v = decompress_ref(c, w_uk, w_uv)
+            k = np.concatenate([k_nope, np.broadcast_to(kpe[:, None, :], (j1 - j0, H, d_r))], axis=-1)
+            s = np.einsum("thd,jhd->thj", q, k) * scale
+            s = np.where(mask[:, None, j0:j1], s, -np.inf)
+            p, l_part = softmax_rows(s)
+            parts_o.append(np.einsum("thj,jhv->thv", p, v))
+            parts_l.append(l_part)
+        o[b], lse[b] = merge_ref(np.stack(parts_o), np.stack(parts_l))
     return o, lse
 
 
