@@ -47,3 +47,33 @@ def test_step_inputs_share_one_buffer(mla):
     # writing through the buffer is seen by the views (they alias it)
     st.inputs.zero_()
     assert int(st.seq_lens.abs().sum()) == 0
+
+
+def test_profiled_traffic_only_for_the_profiled_sources(tmp_path, monkeypatch):
+    """bench.py reports ncu DRAM traffic only while the decode sources hash to
+    the value recorded beside it (a capture of an older kernel reads as null)."""
+    import hashlib
+    sys.path.insert(0, ROOT)
+    import bench
+    h = hashlib.sha256()
+    for f in bench.DECODE_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    sha = h.hexdigest()[:16]
+    prof = tmp_path / "p.md"
+    monkeypatch.setattr(bench, "PROFILE", str(prof))
+    assert bench.profiled_traffic() is None                      # no summary
+    prof.write_text(f"kernel_source_sha256: {sha}\n| dram_bytes_per_launch | 123456 |\n")
+    assert bench.profiled_traffic() == 123456
+    prof.write_text("kernel_source_sha256: 0000000000000000\n| dram_bytes_per_launch | 123456 |\n")
+    assert bench.profiled_traffic() is None                      # stale capture
+
+
+def test_peaks_measured_else_fallback(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    hbm, tc, kind = bench._peaks()
+    if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")):
+        assert kind == "measured" and hbm > 1000 and tc > 100
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._peaks() == (6800.0, 1900.0, "fallback")
