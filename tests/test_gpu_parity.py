@@ -4,8 +4,6 @@ Floating-point outputs (q_lat, o_lat, lse, o) must satisfy
 max|err| <= 2e-2 max|ref| and sum|err|/sum|ref| <= 5e-3 (tests/_tol.py);
 the split plan and the paged gather must be bit-exact.
 """
-import math
-
 import numpy as np
 import pytest
 

@@ -12,7 +12,6 @@ needing more than the fixed scratch is refused before anything runs.
 The file name sorts last so that a run stopping at the first failure has
 already run every other test.
 """
-import numpy as np
 import pytest
 
 from mla_latent_cache_gb300 import workloads as W
