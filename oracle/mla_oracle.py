@@ -494,9 +494,12 @@ def decode_intensity(H, d_c=D_C, d_r=D_R, elem=2) -> float:
 # they are silent: one scale per 128 consecutive latent values, scale = the
 # tile's largest magnitude / 448 rounded to fp32 (1 for an all-zero tile), the
 # segments stored in the order the pages sum them (codes, scales, RoPE), all
-# multi-byte words little-endian.  The pages fix no precision for choosing a
-# code, so scale and quotient are taken in fp32 (IEEE, round to nearest), the
-# precision of the CUDA cache writer.  E4M3 is the OFP8 format: sign, 4 exponent
+# multi-byte words little-endian.  The stored scale is fp32 (the segment the
+# pages give), so it is the exact quotient amax / 448 rounded once to fp32; each
+# code is then the E4M3 value nearest to the exact quotient value / scale (ties
+# to the even mantissa), decided exactly: |value| is compared with the
+# midpoints between neighbouring E4M3 values times the scale, products that
+# float64 holds exactly (at most 5 + 24 significant bits).  E4M3 is the OFP8 format: sign, 4 exponent
 # bits (bias 7), 3 mantissa bits, subnormals at exponent 0, S.1111.111 = NaN,
 # no infinities, largest finite value 448.
 # ---------------------------------------------------------------------------
@@ -543,16 +546,57 @@ def e4m3_encode(x) -> np.ndarray:
     return (out | sign).astype(np.uint8)
 
 
+def f32_nearest_quotient(num: float, den: float) -> np.float32:
+    """The fp32 value nearest to the exact quotient num / den (ties to the even
+    significand), for finite float64 num and den > 0."""
+    from fractions import Fraction
+    exact = Fraction(num) / Fraction(den)
+    x = np.float32(float(exact))
+    # the nearest fp32 value is x or one of its neighbours: compare all three exactly
+    cands = [np.nextafter(x, np.float32(-np.inf)), x, np.nextafter(x, np.float32(np.inf))]
+    dist = [abs(exact - Fraction(float(v))) for v in cands]
+    best = min(dist)
+    near = [v for v, d in zip(cands, dist) if d == best]
+    if len(near) == 1:
+        return near[0]
+    return [v for v in near if (int(np.asarray(v).view(np.uint32)) & 1) == 0][0]
+
+
+def e4m3_encode_scaled(values: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """E4M3 byte nearest to the exact quotient values / scale (ties to the even
+    mantissa; magnitudes beyond 448 saturate to +-448): values [..., n] float64,
+    scale [...] positive.  The decision compares |value| with each midpoint
+    between neighbouring E4M3 values times the scale; a midpoint has at most 5
+    significant bits and the fp32 scale 24, so every product is exact in
+    float64 and so is every comparison."""
+    values = np.asarray(values, dtype=np.float64)
+    pos = e4m3_decode(np.arange(0x7F))                       # 0 .. 448, ascending
+    mids = (pos[:-1] + pos[1:]) / 2.0                        # 126 midpoints, exact
+    thr = mids * np.asarray(scale, dtype=np.float64)[..., None]     # [..., 126], exact products
+    a = np.abs(values)
+    lead, n = values.shape[:-1], values.shape[-1]
+    thr_f = thr.reshape(-1, mids.size)
+    a_f = a.reshape(-1, n)
+    codes = np.empty(a_f.shape, dtype=np.int64)
+    for i in range(a_f.shape[0]):
+        k = np.searchsorted(thr_f[i], a_f[i], side="left")   # thresholds strictly below |value|
+        tie = (k < mids.size) & (thr_f[i][np.minimum(k, mids.size - 1)] == a_f[i])
+        codes[i] = np.where(tie & (k % 2 == 1), k + 1, k)    # a tie between codes k and k+1: the even one
+    sign = np.where(np.signbit(values), 0x80, 0).reshape(codes.shape)
+    return (codes | sign).astype(np.uint8).reshape(lead + (n,))
+
+
 def fp8_row_quantize(c: np.ndarray, k_pe_bits: np.ndarray) -> np.ndarray:
-    """Pack latent rows c [..., 512] (values, taken as fp32) and RoPE bf16 bit patterns
+    """Pack latent rows c [..., 512] (float64 values) and RoPE bf16 bit patterns
     k_pe_bits [..., 64] (uint16) into 656-byte rows [..., 656] (uint8)."""
-    c = np.asarray(c, dtype=np.float32)
+    c = np.asarray(c, dtype=np.float64)
     lead = c.shape[:-1]
     tiles = c.reshape(lead + (D_C // FP8_TILE, FP8_TILE))
     amax = np.abs(tiles).max(axis=-1)
-    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    quot = (tiles / scale[..., None]).astype(np.float32)            # fp32 quotient, round to nearest
-    codes = e4m3_encode(quot.astype(np.float64)).reshape(lead + (D_C,))
+    scale = np.ones(amax.shape, dtype=np.float32)
+    for idx in zip(*np.nonzero(amax > 0)):
+        scale[idx] = f32_nearest_quotient(float(amax[idx]), E4M3_MAX)
+    codes = e4m3_encode_scaled(tiles, scale).reshape(lead + (D_C,))
     out = np.empty(lead + (FP8_ROW_BYTES,), dtype=np.uint8)
     out[..., :D_C] = codes
     out[..., D_C:D_C + 16] = scale.astype("<f4").view(np.uint8).reshape(lead + (16,))
