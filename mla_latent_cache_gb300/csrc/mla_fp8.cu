@@ -5,9 +5,14 @@
 // Row layout (bytes): [0, 512) codes, latent value i in byte i; [512, 528) the
 // four scales, scale t covering latent values [128 t, 128 t + 128); [528, 656)
 // the RoPE values, bf16 little-endian.  Scale t = (largest |value| of its
-// tile) / 448 in fp32 (1 for an all-zero tile); code = E4M3 of value / scale,
-// rounded to nearest even and saturated at +-448; both divisions in fp32 with
-// round to nearest.  A row decodes as latent value i = E4M3(code i) * scale.
+// tile) / 448 rounded once to fp32 (1 for an all-zero tile); code = the E4M3
+// value nearest to the exact quotient value / scale, ties to the even mantissa,
+// saturated at +-448.  A row decodes as latent value i = E4M3(code i) * scale.
+// The code is decided exactly: the fp32 quotient (one rounding) gives a
+// candidate that is the exact answer or a neighbour of it, and the sign of
+// fma(midpoint, scale, -|value|) (one rounding of an exact product minus
+// |value|, so its sign is exact) says on which side of each neighbouring
+// midpoint |value| lies.
 //
 // This kernel packs a bf16 pool (combined or split) into such rows, HBM-bound:
 // 1152 bytes read and 656 written per row.  One warp per row: lane l owns
@@ -22,6 +27,35 @@ namespace {
 
 constexpr int kFp8RowBytes = 656;
 constexpr int kFp8Threads = 256;
+
+// Magnitude of the non-negative E4M3 code c (0 .. 0x7E): exact in fp32.
+__device__ __forceinline__ float e4m3_magnitude(uint32_t c) {
+  const uint32_t e = c >> 3, m = c & 7u;
+  // subnormal: m * 2^-9; normal: (8 + m) * 2^(e - 10)
+  const float p2 = __uint_as_float((uint32_t)(127 + (e ? (int)e - 10 : -9)) << 23);
+  return (float)(e ? 8u + m : m) * p2;
+}
+
+// E4M3 byte nearest to the exact quotient x / scale (scale > 0, finite), ties to
+// the even mantissa, saturating at +-448.
+__device__ __forceinline__ uint32_t e4m3_nearest(float x, float scale) {
+  const __nv_fp8_storage_t c0 = __nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t sign = (uint32_t)c0 & 0x80u;
+  uint32_t c = (uint32_t)c0 & 0x7Fu;
+  const float a = fabsf(x);
+  const float y = e4m3_magnitude(c);
+  if (c < 0x7Eu) {
+    const float mid = 0.5f * (y + e4m3_magnitude(c + 1));
+    const float r = fmaf(mid, scale, -a);           // > 0: below the midpoint; 0: on it
+    if (r < 0.f || (r == 0.f && (c & 1u))) c += 1;
+  }
+  if (c > 0u && c == ((uint32_t)c0 & 0x7Fu)) {
+    const float mid = 0.5f * (e4m3_magnitude(c - 1) + y);
+    const float r = fmaf(mid, scale, -a);
+    if (r > 0.f || (r == 0.f && (c & 1u))) c -= 1;
+  }
+  return sign | c;
+}
 
 __global__ void __launch_bounds__(kFp8Threads) fp8_pack_kernel(CacheView cv, unsigned char* out) {
   pdl_wait();
@@ -53,8 +87,7 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_pack_kernel(CacheView cv, uns
       uint32_t v = 0;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(__fdiv_rn(x[4 * k + e], scale), __NV_SATFINITE, __NV_E4M3);
-        v |= (uint32_t)c << (8 * e);
+        v |= e4m3_nearest(x[4 * k + e], scale) << (8 * e);
       }
       packed[k] = v;
     }
