@@ -5,7 +5,9 @@ executes this module: only the tests, ``__graft_entry__.smoke()`` and the
 bench's CPU-baseline / reference arm use it.  It shares no code with the CUDA
 path.  Every function is the plain definition (or, for the split planner, the
 rule written out step by step) in float64 NumPy, with no blocking, fusion or
-reordering beyond what the definition states.
+reordering beyond what the definition states.  Each contraction is written as
+one ``np.einsum`` over the definition's indices; ``optimize=True`` lets NumPy
+evaluate it through BLAS (the same sums, in another float64 summation order).
 
 Sources (web pages, cited by title and section):
   [MLA-in-depth]  "MLA in full detail" (mlinterviewnotes, ch. 7.2): Step 2 "fold
@@ -80,12 +82,12 @@ def gather_rows(pool: np.ndarray, block_table_row: np.ndarray, n_rows: int) -> n
 # ---------------------------------------------------------------------------
 def absorb_ref(q_nope: np.ndarray, w_uk: np.ndarray) -> np.ndarray:
     """q_lat[b,t,h,c] = sum_n q_nope[b,t,h,n] * W_UK[h,n,c]   (W_UK is [H, d_N, d_c])."""
-    return np.einsum("bthn,hnc->bthc", q_nope, w_uk)
+    return np.einsum("bthn,hnc->bthc", q_nope, w_uk, optimize=True)
 
 
 def unabsorb_ref(o_lat: np.ndarray, w_uv: np.ndarray) -> np.ndarray:
     """o[b,t,h,v] = sum_c o_lat[b,t,h,c] * W_UV[h,v,c]   (W_UV is [H, d_V, d_c])."""
-    return np.einsum("bthc,hvc->bthv", o_lat, w_uv)
+    return np.einsum("bthc,hvc->bthv", o_lat, w_uv, optimize=True)
 
 
 # ---------------------------------------------------------------------------
@@ -141,10 +143,10 @@ def attend_latent(q_lat: np.ndarray, q_pe: np.ndarray, rows: np.ndarray, mask: n
     d_c = q_lat.shape[-1]
     c = rows[:, :d_c]
     kpe = rows[:, d_c:]
-    s = (np.einsum("thc,jc->thj", q_lat, c) + np.einsum("thr,jr->thj", q_pe, kpe)) * scale
+    s = (np.einsum("thc,jc->thj", q_lat, c, optimize=True) + np.einsum("thr,jr->thj", q_pe, kpe, optimize=True)) * scale
     s = np.where(mask[:, None, :], s, -np.inf)
     p, lse = softmax_rows(s)
-    o = np.einsum("thj,jc->thc", p, c)
+    o = np.einsum("thj,jc->thc", p, c, optimize=True)
     return o, lse
 
 
@@ -181,7 +183,7 @@ def absorbed_layer_ref(q_nope, q_pe, pool, block_table, seq_lens, w_uk, w_uv, ca
 def decompress_ref(c, w_uk, w_uv):
     """Per-head keys and values of cached latents c [S, d_c] ([MLA-in-depth] naive path):
     k_nope[j,h,n] = sum_c W_UK[h,n,c] c_j[c],  v[j,h,v] = sum_c W_UV[h,v,c] c_j[c]."""
-    return np.einsum("hnc,jc->jhn", w_uk, c), np.einsum("hvc,jc->jhv", w_uv, c)
+    return np.einsum("hnc,jc->jhn", w_uk, c, optimize=True), np.einsum("hvc,jc->jhv", w_uv, c, optimize=True)
 
 
 def normal_ref(q_nope, q_pe, pool, block_table, seq_lens, w_uk, w_uv, causal, scale=SCALE, batches=None):
@@ -207,10 +209,10 @@ def normal_ref(q_nope, q_pe, pool, block_table, seq_lens, w_uk, w_uv, causal, sc
         k_nope, v = decompress_ref(c, w_uk, w_uv)
         k = np.concatenate([k_nope, np.broadcast_to(kpe[:, None, :], (S, H, d_r))], axis=-1)
         q = np.concatenate([q_nope[b], q_pe[b]], axis=-1)
-        s = np.einsum("thd,jhd->thj", q, k) * scale
+        s = np.einsum("thd,jhd->thj", q, k, optimize=True) * scale
         s = np.where(causal_mask(S, T, causal)[:, None, :], s, -np.inf)
         p, lse[b] = softmax_rows(s)
-        o[b] = np.einsum("thj,jhv->thv", p, v)
+        o[b] = np.einsum("thj,jhv->thv", p, v, optimize=True)
     return o, lse
 
 
@@ -317,10 +319,10 @@ def normal_chunked_ref(q_nope, q_pe, pool, block_table, seq_lens, w_uk, w_uv, ca
             kpe = rows[j0:j1, d_c:]
             k_nope, v = decompress_ref(c, w_uk, w_uv)
             k = np.concatenate([k_nope, np.broadcast_to(kpe[:, None, :], (j1 - j0, H, d_r))], axis=-1)
-            s = np.einsum("thd,jhd->thj", q, k) * scale
+            s = np.einsum("thd,jhd->thj", q, k, optimize=True) * scale
             s = np.where(mask[:, None, j0:j1], s, -np.inf)
             p, l_part = softmax_rows(s)
-            parts_o.append(np.einsum("thj,jhv->thv", p, v))
+            parts_o.append(np.einsum("thj,jhv->thv", p, v, optimize=True))
             parts_l.append(l_part)
         o[b], lse[b] = merge_ref(np.stack(parts_o), np.stack(parts_l))
     return o, lse
