@@ -143,6 +143,8 @@ enum {
 size_t mla_workspace_size(const mla_geom* geom, const mla_batch* batch);
 
 /*
+ * Split plan ("M5.8" 0x08 "FlashMLA Runtime ABI": scheduler metadata rebuilt
+ * whenever the batch geometry or the lengths change).
  * Build the split plan on the device from seq_lens (device int32 [B]) into the
  * workspace.  Must be re-run whenever B, T, causal, the lengths or num_slots
  * change (the plan is stamped with them; mla_decode with checked != 0 flags a
@@ -152,6 +154,8 @@ mla_status mla_plan(const mla_geom* geom, const mla_batch* batch, const int32_t*
                     void* workspace, size_t ws_bytes, mla_stream_t stream);
 
 /*
+ * Key absorption ("MLA in full detail", Step 2 "fold W_UK into the query";
+ * "M5.8" 0x04 "Batched absorption trace", the q_nope x W_UK einsum):
  * q_lat[b,t,h,:] = q_nope[b,t,h,:] @ W_UK[h]   over BT = B*T query tokens.
  * q_nope [BT,H,128], w_uk [H,128,512], q_lat [BT,H,512] (all bf16, device).
  * fp32 accumulation, bf16 output (round to nearest even).
@@ -160,6 +164,8 @@ mla_status mla_absorb_q(const mla_geom* geom, const void* q_nope, const void* w_
                         int BT, mla_stream_t stream);
 
 /*
+ * Value un-absorption ("MLA in full detail", Step 4 "fold W_UV into the
+ * output"; "M5.8" 0x04, the o_lat x W_UV einsum):
  * o[b,t,h,v] = sum_c o_lat[b,t,h,c] * W_UV[h,v,c]   over BT query tokens.
  * o_lat [BT,H,512], w_uv [H,128,512], o [BT,H,128] (bf16, device); fp32 accumulation.
  */
@@ -167,8 +173,10 @@ mla_status mla_unabsorb_o(const mla_geom* geom, const void* o_lat, const void* w
                           int BT, mla_stream_t stream);
 
 /*
- * Absorbed attention over the paged latent cache, using the plan in the
- * workspace: scores s = (q_lat . c_j + q_pe . k_pe_j) * scale, softmax over the
+ * Absorbed attention over the paged latent cache ("MLA in full detail", Step 3
+ * "attend against the latent directly"; "M5.8" 0x05 "Paged and ragged address
+ * translation" for the pages; 0x0C and "mlxcel" Stage 2 for the merge of split
+ * states), using the plan in the workspace: scores s = (q_lat . c_j + q_pe . k_pe_j) * scale, softmax over the
  * visible rows j, o_lat = sum_j p_j c_j, lse = log sum_j e^{s_j}.  Launches the
  * split-KV decode kernel and, when the plan has partial segments, the merge.
  * q_lat [B,T,H,512], q_pe [B,T,H,64] bf16; o_lat [B,T,H,512] bf16; lse [B,T,H] float32.
@@ -181,7 +189,8 @@ mla_status mla_decode(const mla_geom* geom, const mla_batch* batch, const void* 
                       void* workspace, size_t ws_bytes, mla_stream_t stream);
 
 /*
- * Exact merge of split partial states (mlxcel Stage-2 contract, natural-log LSE):
+ * Exact merge of split partial states ("M5.8" 0x0C; "mlxcel" Stage-2
+ * contract, here with natural-log LSE):
  * part_o float32 [N, rows, D] (each normalised by its own denominator),
  * part_lse float32 [N, rows] (natural log, -inf = empty), indptr int32 [M+1]
  * (partials indptr[m] .. indptr[m+1]-1 form output m).  Writes o bf16 [M, rows, D]
@@ -207,11 +216,19 @@ mla_status mla_split_merge(const float* part_o, const float* part_lse, const int
 mla_status mla_fp8_pack_cache(const mla_cache* cache, void* out, mla_stream_t stream);
 
 /*
- * Test export: copy the S_b logical rows of sequence b, in order, through the
- * decode kernel's own address path, into out bf16 [S_b, 576] (latent | RoPE).
+ * Test export of the paged gather ("M5.8" 0x05 "Paged and ragged address
+ * translation": logical row j of sequence b is row j % 64 of block
+ * block_table[b, j / 64]): copies the S_b logical rows of sequence b, in order,
+ * into out bf16 [S_b, 576] (latent | RoPE), fetching every page with the decode
+ * kernel's own tensor maps and load functions.  path 0: the page-half boxes the
+ * producer issues (rows [0, 32) and [32, 64), all 576 columns); path 1: the
+ * latent columns through the two-column-block boxes of the P V reloads, issued
+ * for every column pair of both halves, the RoPE columns as in path 0.  A block
+ * id outside [0, num_blocks) reads as zeros, as in the decode.  block_table,
+ * seq_lens and out must be 16-byte aligned; S_b is clamped to bt_stride * 64.
  */
 mla_status mla_debug_gather(const mla_cache* cache, const int32_t* block_table, int bt_stride,
-                            const int32_t* seq_lens, int b, void* out, mla_stream_t stream);
+                            const int32_t* seq_lens, int b, int path, void* out, mla_stream_t stream);
 
 /*
  * Decode for callers that cannot allocate device memory (no counterpart on the
@@ -222,9 +239,17 @@ mla_status mla_debug_gather(const mla_cache* cache, const int32_t* block_table, 
  * MLA_NOALLOC_SCRATCH_BYTES held in the library's device image, so the caller
  * passes only inputs and outputs (same meaning as mla_plan + mla_decode with
  * checked = 0).  It calls no allocator.
+ *   Checks: every host-side check of mla_decode runs before anything is
+ *     launched (the same MLA_ERR_* codes).
  *   Limit: returns MLA_ERR_WORKSPACE, before launching anything, when
  *     mla_workspace_size(geom, batch) exceeds MLA_NOALLOC_SCRATCH_BYTES; a
- *     smaller num_slots (or num_splits_override) shrinks the need.
+ *     smaller num_slots (or num_splits_override) shrinks the need.  With
+ *     num_slots = 0 and no override the call takes the largest range count, up
+ *     to the default, whose workspace fits (the default of one range per CTA
+ *     pair needs about 40 MB on a 152-SM GPU).
+ *   Errors seen on the device (a length beyond the block table, T > S_b, a
+ *     wait that ran out) are recorded in the scratch; mla_read_device_status
+ *     called with workspace = NULL returns that status (and clears it).
  *   Set-up: the first call on a device looks up the scratch address with that
  *     device current; make that first call before any stream capture.
  *   Sharing: all calls on a device share the one array (every GPU that loads
@@ -277,9 +302,11 @@ mla_status mla_normal_attention(const mla_geom* geom, const mla_batch* batch, co
 
 /* Synchronise `stream`, then return the status word a kernel recorded in the
  * workspace (MLA_OK if none) and, if info != NULL, its detail word.  The
- * workspace-free kernels (absorption, un-absorption, the Normal arm) keep one
- * status word per device, also returned (and cleared) here; workspace may be
- * NULL to read only that one. */
+ * workspace-free kernels (absorption, un-absorption, the Normal arm, the gather
+ * export) keep one status word per device, also returned (and cleared) here.
+ * With workspace = NULL the call reads that word and then the status and
+ * detail words of mla_decode_noalloc's scratch on the current device, returns
+ * the first that is set and clears it. */
 mla_status mla_read_device_status(const void* workspace, int* info, mla_stream_t stream);
 
 /* Static description of a status code. */

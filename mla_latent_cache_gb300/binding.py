@@ -73,7 +73,7 @@ def _load() -> ctypes.CDLL:
         "mla_decode": (I, [G, Bt, P, P, C, P, I, P, I, P, P, P, ctypes.c_size_t, P]),
         "mla_decode_noalloc": (I, [G, Bt, P, P, C, P, I, P, P, P, P]),
         "mla_split_merge": (I, [P, P, P, I, I, I, P, P, P]),
-        "mla_debug_gather": (I, [C, P, I, P, I, P, P]),
+        "mla_debug_gather": (I, [C, P, I, P, I, I, P, P]),
         "mla_fp8_pack_cache": (I, [C, P, P]),
         "mla_normal_rows_per_seq": (ctypes.c_int64, [I]),
         "mla_normal_expanded_bytes": (ctypes.c_size_t, [G, I, I]),
@@ -203,9 +203,12 @@ def mla_fp8_pack_cache(cache: mla_cache, out, stream=None) -> int:
     return _lib.mla_fp8_pack_cache(ctypes.byref(cache), _ptr(out), _stream(stream))
 
 
-def mla_debug_gather(cache: mla_cache, block_table, bt_stride: int, seq_lens, b: int, out, stream=None) -> int:
-    return _lib.mla_debug_gather(ctypes.byref(cache), _ptr(block_table), bt_stride, _ptr(seq_lens), b, _ptr(out),
-                                 _stream(stream))
+def mla_debug_gather(cache: mla_cache, block_table, bt_stride: int, seq_lens, b: int, path: int, out,
+                     stream=None) -> int:
+    """Copy sequence b's logical rows through the decode kernel's own page loads
+    (path 0: page-half boxes; path 1: latent columns through the reload boxes)."""
+    return _lib.mla_debug_gather(ctypes.byref(cache), _ptr(block_table), bt_stride, _ptr(seq_lens), b, int(path),
+                                 _ptr(out), _stream(stream))
 
 
 def mla_normal_rows_per_seq(max_pages: int) -> int:

@@ -3,6 +3,8 @@
 // (except mla_read_device_status).
 #include <string.h>
 
+#include <atomic>
+
 #include "mla_internal.cuh"
 
 namespace mla {
@@ -82,15 +84,16 @@ using namespace mla;
 extern "C" {
 
 int mla_device_sm_count(void) {
-  static int cached[64] = {0};
+  // Filled on first use per device; concurrent first calls store the same value.
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_acquire);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_release);
   }
-  return cached[dev];
+  return n;
 }
 
 const char* mla_status_string(mla_status s) {
@@ -152,6 +155,28 @@ mla_status mla_unabsorb_o(const mla_geom* geom, const void* o_lat, const void* w
                                      static_cast<__nv_bfloat16*>(o), BT, geom->H, (cudaStream_t)stream));
 }
 
+static mla_status check_cache(const mla_cache* cache, CacheView* cv);
+
+}  // extern "C"
+
+// Host validation of mla_decode's arguments other than the workspace.
+mla_status mla::check_decode_args(const mla_geom* geom, const mla_batch* batch, const void* q_lat, const void* q_pe,
+                                  const mla_cache* cache, const int32_t* block_table, int bt_stride,
+                                  const int32_t* seq_lens, const void* o_lat, const float* lse, CacheView* cv) {
+  mla_status s = check_geom(geom);
+  if (s != MLA_OK) return s;
+  if ((s = check_batch(batch)) != MLA_OK) return s;
+  if (batch->B == 0) return MLA_OK;
+  if (!q_lat || !q_pe || !block_table || !seq_lens || !o_lat || !lse) return MLA_ERR_ARG;
+  if (bt_stride < batch->max_pages) return MLA_ERR_ARG;
+  if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned32(o_lat) || !aligned16(lse) || !aligned16(block_table) ||
+      !aligned16(seq_lens))
+    return MLA_ERR_ALIGN;
+  return check_cache(cache, cv);
+}
+
+extern "C" {
+
 static mla_status check_cache(const mla_cache* cache, CacheView* cv) {
   if (!cache || !cache->ckv || !cache->kpe || cache->num_blocks < 1) return MLA_ERR_ARG;
   if (cache->ckv_row_stride < 1 || cache->kpe_row_stride < 1 || cache->ckv_block_stride < 1 ||
@@ -174,17 +199,12 @@ static mla_status check_cache(const mla_cache* cache, CacheView* cv) {
 mla_status mla_decode(const mla_geom* geom, const mla_batch* batch, const void* q_lat, const void* q_pe,
                       const mla_cache* cache, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                       int checked, void* o_lat, float* lse, void* workspace, size_t ws_bytes, mla_stream_t stream) {
-  mla_status s = check_geom(geom);
-  if (s != MLA_OK) return s;
-  if ((s = check_batch(batch)) != MLA_OK) return s;
-  if (batch->B == 0) return MLA_OK;
-  if (!q_lat || !q_pe || !block_table || !seq_lens || !o_lat || !lse || !workspace) return MLA_ERR_ARG;
-  if (bt_stride < batch->max_pages) return MLA_ERR_ARG;
-  if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned32(o_lat) || !aligned16(lse) || !aligned32(workspace) ||
-      !aligned16(block_table) || !aligned16(seq_lens))
-    return MLA_ERR_ALIGN;
   CacheView cv;
-  if ((s = check_cache(cache, &cv)) != MLA_OK) return s;
+  mla_status s = check_decode_args(geom, batch, q_lat, q_pe, cache, block_table, bt_stride, seq_lens, o_lat, lse, &cv);
+  if (s != MLA_OK) return s;
+  if (batch->B == 0) return MLA_OK;
+  if (!workspace) return MLA_ERR_ARG;
+  if (!aligned32(workspace)) return MLA_ERR_ALIGN;
   WsLayout L;
   if (!compute_layout(geom, batch, &L)) return MLA_ERR_SHAPE;
   if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
@@ -202,7 +222,8 @@ mla_status mla_split_merge(const float* part_o, const float* part_lse, const int
   if (M < 0 || rows < 0 || D <= 0 || (D % 8) != 0) return MLA_ERR_ARG;
   if (M == 0 || rows == 0) return MLA_OK;
   if (!part_o || !part_lse || !indptr || !o || !lse) return MLA_ERR_ARG;
-  if (!aligned16(part_o) || !aligned16(o) || !aligned16(indptr)) return MLA_ERR_ALIGN;
+  if (!aligned16(part_o) || !aligned16(part_lse) || !aligned16(o) || !aligned16(lse) || !aligned16(indptr))
+    return MLA_ERR_ALIGN;
   if (((size_t)rows * D * sizeof(float)) % 16 != 0) return MLA_ERR_ALIGN;
   return cuda_status(launch_split_merge(part_o, part_lse, indptr, M, rows, D, static_cast<__nv_bfloat16*>(o), lse,
                                         (cudaStream_t)stream));
@@ -218,14 +239,14 @@ mla_status mla_fp8_pack_cache(const mla_cache* cache, void* out, mla_stream_t st
 }
 
 mla_status mla_debug_gather(const mla_cache* cache, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
-                            int b, void* out, mla_stream_t stream) {
-  if (!block_table || !seq_lens || !out || b < 0 || bt_stride < 1) return MLA_ERR_ARG;
-  if (!aligned16(out)) return MLA_ERR_ALIGN;
+                            int b, int path, void* out, mla_stream_t stream) {
+  if (!block_table || !seq_lens || !out || b < 0 || bt_stride < 1 || (path != 0 && path != 1)) return MLA_ERR_ARG;
+  if (!aligned16(out) || !aligned16(block_table) || !aligned16(seq_lens)) return MLA_ERR_ALIGN;
   CacheView cv;
   mla_status s = check_cache(cache, &cv);
   if (s != MLA_OK) return s;
-  return cuda_status(launch_debug_gather(cv, block_table, bt_stride, seq_lens, b, static_cast<__nv_bfloat16*>(out),
-                                         (cudaStream_t)stream));
+  return cuda_status(launch_debug_gather(cv, block_table, bt_stride, seq_lens, b, path,
+                                         static_cast<__nv_bfloat16*>(out), (cudaStream_t)stream));
 }
 
 int64_t mla_normal_rows_per_seq(int max_pages) { return max_pages < 1 ? 0 : normal_rows_per_seq(max_pages); }
@@ -298,6 +319,21 @@ mla_status mla_read_device_status(const void* workspace, int* info, mla_stream_t
       cudaMemcpy(bmm, &zero, sizeof(int), cudaMemcpyHostToDevice);
       if (info) *info = -1;
       return (mla_status)v;
+    }
+  }
+  // mla_decode_noalloc plans and decodes in the library's own scratch: its status
+  // word (and detail) is read here, without a workspace, and cleared.
+  if (!workspace) {
+    int* na = noalloc_status_words();
+    if (na) {
+      int words[2] = {0, 0};
+      if (cudaMemcpy(words, na, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+      if (words[0] != 0) {
+        const int zero[2] = {0, 0};
+        cudaMemcpy(na, zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (info) *info = words[1];
+        return (mla_status)words[0];
+      }
     }
   }
   return MLA_OK;

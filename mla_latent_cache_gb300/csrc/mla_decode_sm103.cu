@@ -60,6 +60,8 @@
 // tensor memory is freed.
 #include <math.h>
 
+#include <atomic>
+
 #include "mla_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -122,6 +124,27 @@ static_assert(kNumBars * 8 + 8 <= 512, "barrier area");
 // receive those boxes' rows of the other page half.
 __device__ __forceinline__ int own_pv_box(int r, int i) { return (i < 2 ? 0 : 4) + 2 * r + (i & 1); }
 __device__ __forceinline__ int reload_slot(int r, int i) { return (i < 2 ? 0 : 4) + 2 * (1 - r) + (i & 1); }
+
+// The paged address translation of a load ("M5.8" 0x05): page rows are tensor-map
+// coordinates (64 columns, 64 rows of a block, column block, block id), so a
+// block id selects the page and a row offset selects the half; a block id of -1
+// (outside the pool) reads zeros.  These two functions are the only places that
+// form those coordinates; the debug gather export issues them too.
+//
+// Half `half` of a page (rows [32 half, 32 half + 32), all 576 columns) into the
+// nine 32-row slots of a stage, arriving on `bar` with the stage's byte count.
+__device__ __forceinline__ void load_page_half(uint32_t stage, const CUtensorMap* tm_page, const CUtensorMap* tm_kpe,
+                                               uint32_t bar, int half, int blk, int kpe_separate) {
+  mbar_arrive_expect_tx(bar, kStageBytes);
+  tma_load_4d(stage, tm_page, bar, 0, kHalfRows * half, 0, blk);
+  if (kpe_separate) tma_load_3d(stage + 8 * kSlotBytes, tm_kpe, bar, 0, kHalfRows * half, blk);
+}
+// Latent column blocks {box, box + 1} of rows [32 half, 32 half + 32) into two
+// adjacent slots at dst (8 KB; the caller accounts for the bytes on `bar`).
+__device__ __forceinline__ void load_pair_box(uint32_t dst, const CUtensorMap* tm_pair, uint32_t bar, int half,
+                                              int box, int blk) {
+  tma_load_4d(dst, tm_pair, bar, 0, kHalfRows * half, box, blk);
+}
 
 struct FastArgs {
   const __nv_bfloat16* q_lat;
@@ -457,9 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // One 4-D box per page half: 32 rows x all column blocks, landing as the nine
           // 32-row x 64-column slots (streams ~8 % faster than nine 3-D boxes).
-          mbar_arrive_expect_tx(sh.bar(BAR_FULL + st), kStageBytes);
-          tma_load_4d(sh.slot(st, 0), &tm_page, sh.bar(BAR_FULL + st), 0, kHalfRows * rank, 0, blk);
-          if (a.kpe_separate) tma_load_3d(sh.slot(st, 8), &tm_kpe, sh.bar(BAR_FULL + st), 0, kHalfRows * rank, blk);
+          load_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rank, blk, a.kpe_separate);
         }
         ++sc;
       }
@@ -503,8 +524,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Two 2-block boxes: latent boxes {2r, 2r+1} and {4+2r, 5+2r} of the other half.
           mbar_arrive_expect_tx(sh.bar(BAR_RELOAD + st), 4 * kSlotBytes);
           for (int i = 0; i < 4; i += 2)
-            tma_load_4d(sh.slot(st, reload_slot(rank, i)), &tm_pair, sh.bar(BAR_RELOAD + st), 0, kHalfRows * (1 - rank),
-                        own_pv_box(rank, i), blk);
+            load_pair_box(sh.slot(st, reload_slot(rank, i)), &tm_pair, sh.bar(BAR_RELOAD + st), 1 - rank,
+                          own_pv_box(rank, i), blk);
         }
       }
       const int first = gt > kStages ? gt - kStages : 0;
@@ -770,6 +791,72 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
+// Test export of the decode kernel's gather: page p of sequence b is fetched by
+// load_page_half (path 0: all 576 columns of both halves) or, after that, by
+// load_pair_box over every latent column pair of both halves (path 1: the
+// latent columns come through the reload map, the RoPE columns through the page
+// map), with the block id taken from the block table as the producer takes it,
+// then copied out of the 128-byte-swizzled slots as rows j = 64 p + r < S_b of
+// out [S_b, 576].  One CTA per page of the table row; a page past S_b returns.
+constexpr int kGatherThreads = 128;
+
+__global__ void __launch_bounds__(kGatherThreads)
+    debug_gather_sm103_kernel(const __grid_constant__ CUtensorMap tm_page, const __grid_constant__ CUtensorMap tm_pair,
+                              const __grid_constant__ CUtensorMap tm_kpe, const int32_t* block_table, int bt_stride,
+                              const int32_t* seq_lens, int b, int num_blocks, int kpe_separate, int path,
+                              __nv_bfloat16* out, int* status) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t stage = smem_addr(smem);
+  const uint32_t bar = stage + kStageBytes;
+  __shared__ int s_ok;
+  int S = seq_lens[b];
+  S = S < 0 ? 0 : min(S, bt_stride * kPage);
+  const int p = blockIdx.x;
+  if (p * kPage >= S) return;
+  int blk = block_table[(size_t)b * bt_stride + p];
+  if (blk < 0 || blk >= num_blocks) blk = -1;
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    s_ok = 1;
+  }
+  __syncthreads();
+  volatile int never = 0;
+  uint32_t phase = 0;
+  for (int half = 0; half < 2; ++half) {
+    for (int pass = 0; pass < (path == 0 ? 1 : 2); ++pass) {
+      if (threadIdx.x == 0) {
+        if (pass == 0) {
+          load_page_half(stage, &tm_page, &tm_kpe, bar, half, blk, kpe_separate);
+        } else {
+          mbar_arrive_expect_tx(bar, 8 * kSlotBytes);
+          for (int box = 0; box < 8; box += 2) load_pair_box(stage + box * kSlotBytes, &tm_pair, bar, half, box, blk);
+        }
+        if (!mbar_wait(bar, phase, &never)) {
+          s_ok = 0;
+          atomicCAS(status, 0, MLA_ERR_TIMEOUT);
+        }
+      }
+      phase ^= 1;
+      __syncthreads();
+    }
+    if (s_ok) {
+      // slot s, row r, 16-byte chunk c sits at s * 4 KB + r * 128 + 16 (c ^ (r % 8))
+      for (int idx = threadIdx.x; idx < kHalfRows * kBoxes * 8; idx += kGatherThreads) {
+        const int r = idx / (kBoxes * 8), sb = (idx / 8) % kBoxes, c = idx % 8;
+        const int j = p * kPage + half * kHalfRows + r;
+        if (j < S) {
+          const uint4 v = *reinterpret_cast<const uint4*>(smem + sb * kSlotBytes + r * 128 + 16 * (c ^ (r & 7)));
+          *reinterpret_cast<uint4*>(out + (size_t)j * kDK + 64 * sb + 8 * c) = v;
+        }
+      }
+    }
+    fence_proxy_async_smem();   // the reads above precede the next half's TMA writes
+    __syncthreads();
+  }
+}
+
 // --------------------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -799,13 +886,42 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
+// Tensor maps of the paged cache.  Page halves are 4-D boxes (64 columns, 32
+// rows, column blocks, 1 block): with the RoPE values at latent + 512 of the same
+// rows (the combined 576-wide row) the nine column blocks are one box; otherwise
+// the eight latent blocks, plus a 3-D RoPE box.  m_pair loads two adjacent latent
+// blocks (the reloads).
+bool make_cache_maps(const CacheView& cv, CUtensorMap* m_page, CUtensorMap* m_pair, CUtensorMap* m_kpe,
+                     bool* combined) {
+  *combined = cv.kpe == cv.ckv + kDLat && cv.kpe_row == cv.ckv_row && cv.kpe_block == cv.ckv_block;
+  const cuuint32_t ncb = *combined ? 9 : 8;
+  {
+    const cuuint64_t dims[4] = {64, (cuuint64_t)kPage, ncb, (cuuint64_t)cv.num_blocks};
+    const cuuint64_t str[3] = {(cuuint64_t)cv.ckv_row * 2, 128, (cuuint64_t)cv.ckv_block * 2};
+    const cuuint32_t box[4] = {64, kHalfRows, ncb, 1};
+    if (!make_map(m_page, cv.ckv, 4, dims, str, box)) return false;
+    const cuuint32_t box2[4] = {64, kHalfRows, 2, 1};
+    if (!make_map(m_pair, cv.ckv, 4, dims, str, box2)) return false;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)kDRope, (cuuint64_t)kPage, (cuuint64_t)cv.num_blocks};
+    const cuuint64_t str[2] = {(cuuint64_t)cv.kpe_row * 2, (cuuint64_t)cv.kpe_block * 2};
+    const cuuint32_t box[3] = {64, kHalfRows, 1};
+    if (!make_map(m_kpe, cv.kpe, 3, dims, str, box)) return false;
+  }
+  return true;
+}
+
+// The shared-memory opt-in, once per device (setting it twice is harmless).
 bool set_kernel_attributes() {
-  static bool done = false;
-  if (!done) {
+  static std::atomic<bool> done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (!done[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(decode_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
         cudaSuccess)
       return false;
-    done = true;
+    done[dev].store(true, std::memory_order_release);
   }
   return true;
 }
@@ -833,10 +949,12 @@ void cluster_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, i
 
 // Clusters (CTA pairs) of the decode kernel that can be resident at once on the current device.
 int decode_sm103_pairs_per_device() {
-  static int cached[64] = {0};
+  // Filled on first use per device; concurrent first calls compute and store the same value.
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (cached[dev] == 0) {
+  int got = cached[dev].load(std::memory_order_acquire);
+  if (got == 0) {
     int n = 0;
     if (set_kernel_attributes()) {
       cudaLaunchConfig_t cfg;
@@ -848,9 +966,10 @@ int decode_sm103_pairs_per_device() {
       const int sms = mla_device_sm_count();
       n = sms >= 2 ? sms / 2 : 1;
     }
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_release);
+    got = n;
   }
-  return cached[dev];
+  return got;
 }
 
 cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsLayout& L,
@@ -871,26 +990,8 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
     const cuuint32_t box[2] = {64, kCtaRows};
     if (!make_map(&m_qpe, q_pe, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
-  // Page halves as 4-D boxes (64 columns, 32 rows, column blocks, 1 block): with the
-  // RoPE values at latent + 512 of the same rows (the combined 576-wide row) the
-  // nine column blocks are one box; otherwise the eight latent blocks, plus a 3-D
-  // RoPE box.  tm_pair loads two adjacent latent blocks (the reloads).
-  const bool combined = cv.kpe == cv.ckv + kDLat && cv.kpe_row == cv.ckv_row && cv.kpe_block == cv.ckv_block;
-  const cuuint32_t ncb = combined ? 9 : 8;
-  {
-    const cuuint64_t dims[4] = {64, (cuuint64_t)kPage, ncb, (cuuint64_t)cv.num_blocks};
-    const cuuint64_t str[3] = {(cuuint64_t)cv.ckv_row * 2, 128, (cuuint64_t)cv.ckv_block * 2};
-    const cuuint32_t box[4] = {64, kHalfRows, ncb, 1};
-    if (!make_map(&m_page, cv.ckv, 4, dims, str, box)) return cudaErrorInvalidValue;
-    const cuuint32_t box2[4] = {64, kHalfRows, 2, 1};
-    if (!make_map(&m_pair, cv.ckv, 4, dims, str, box2)) return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[3] = {(cuuint64_t)kDRope, (cuuint64_t)kPage, (cuuint64_t)cv.num_blocks};
-    const cuuint64_t str[2] = {(cuuint64_t)cv.kpe_row * 2, (cuuint64_t)cv.kpe_block * 2};
-    const cuuint32_t box[3] = {64, kHalfRows, 1};
-    if (!make_map(&m_kpe, cv.kpe, 3, dims, str, box)) return cudaErrorInvalidValue;
-  }
+  bool combined = false;
+  if (!make_cache_maps(cv, &m_page, &m_pair, &m_kpe, &combined)) return cudaErrorInvalidValue;
   FastArgs a;
   a.q_lat = q_lat;
   a.block_table = block_table; a.bt_stride = bt_stride; a.seq_lens = seq_lens;
@@ -909,6 +1010,20 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
   cluster_launch_config(&cfg, attr, pairs, st, true);
   return cudaLaunchKernelEx(&cfg, decode_sm103_kernel, m_qlat, m_qpe, m_page, m_pair, m_kpe, a,
                             reinterpret_cast<char*>(ws));
+}
+
+cudaError_t launch_debug_gather(const CacheView& cv, const int32_t* block_table, int bt_stride,
+                                const int32_t* seq_lens, int b, int path, __nv_bfloat16* out, cudaStream_t st) {
+  int* status = bmm_status_ptr();
+  if (!status) return cudaErrorInvalidValue;
+  CUtensorMap m_page, m_pair, m_kpe;
+  bool combined = false;
+  if (!make_cache_maps(cv, &m_page, &m_pair, &m_kpe, &combined)) return cudaErrorInvalidValue;
+  const size_t smem = kStageBytes + 1024 + 64;
+  debug_gather_sm103_kernel<<<bt_stride, kGatherThreads, smem, st>>>(m_page, m_pair, m_kpe, block_table, bt_stride,
+                                                                    seq_lens, b, cv.num_blocks, combined ? 0 : 1,
+                                                                    path, out, status);
+  return cudaGetLastError();
 }
 
 }  // namespace mla

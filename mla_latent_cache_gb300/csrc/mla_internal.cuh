@@ -30,6 +30,14 @@ struct WsLayout {
 
 bool compute_layout(const mla_geom* g, const mla_batch* b, WsLayout* L);
 int resolve_slots(const mla_batch* b);
+struct CacheView;
+// Host validation of mla_decode's arguments other than the workspace (fills cv).
+mla_status check_decode_args(const mla_geom* geom, const mla_batch* batch, const void* q_lat, const void* q_pe,
+                             const mla_cache* cache, const int32_t* block_table, int bt_stride,
+                             const int32_t* seq_lens, const void* o_lat, const float* lse, CacheView* cv);
+// Status and detail words of mla_decode_noalloc's scratch on the current device,
+// or nullptr before that entry point's first call there.
+int* noalloc_status_words();
 
 // Programmatic dependent launch.  Every kernel of the library is launched with
 // programmatic stream serialisation and waits for the grid before it in the
@@ -112,6 +120,6 @@ cudaError_t launch_normal_attention(const mla_geom* g, const mla_batch* b, const
                                     int bt_stride, const int32_t* seq_lens, const __nv_bfloat16* kv_exp,
                                     __nv_bfloat16* o, float* lse, cudaStream_t st);
 cudaError_t launch_debug_gather(const CacheView& cv, const int32_t* block_table, int bt_stride,
-                                const int32_t* seq_lens, int b, __nv_bfloat16* out, cudaStream_t st);
+                                const int32_t* seq_lens, int b, int path, __nv_bfloat16* out, cudaStream_t st);
 
 }  // namespace mla

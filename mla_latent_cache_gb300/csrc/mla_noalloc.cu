@@ -21,6 +21,10 @@
 // the decode kernel writes each partial slot before the merge reads it.  Calls
 // whose work overlaps on the GPU (different streams, or different host threads
 // without ordering) race on the array; callers must order them.
+//
+// Errors the kernels see (a length beyond the block table, T > S_b, a wait that
+// ran out) land in the scratch's status word, which mla_read_device_status
+// returns, and clears, when it is called without a workspace.
 #include <mutex>
 
 #include "mla_internal.cuh"
@@ -51,19 +55,49 @@ mla_status scratch_for_current_device(void** out) {
 
 }  // namespace
 
+namespace mla {
+
+int* noalloc_status_words() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (g_scratch_ptr[dev] == nullptr) return nullptr;
+  return static_cast<int*>(g_scratch_ptr[dev]) + MLA_HDR_ERROR;   // {status, detail}
+}
+
+}  // namespace mla
+
 extern "C" mla_status mla_decode_noalloc(const mla_geom* geom, const mla_batch* batch, const void* q_lat,
                                          const void* q_pe, const mla_cache* cache, const int32_t* block_table,
                                          int bt_stride, const int32_t* seq_lens, void* o_lat, float* lse,
                                          mla_stream_t stream) {
-  const size_t need = mla_workspace_size(geom, batch);
+  // Every host-side check of the decode runs before anything is launched.
+  mla::CacheView cv;
+  mla_status s = mla::check_decode_args(geom, batch, q_lat, q_pe, cache, block_table, bt_stride, seq_lens, o_lat,
+                                        lse, &cv);
+  if (s != MLA_OK) return s;
+  mla_batch local = *batch;
+  if (local.num_slots == 0 && local.num_splits_override == 0) {
+    // The default (one work range per CTA pair) needs 2 x 128 x 512 fp32 partial
+    // rows per range, more than the scratch holds on a large GPU: take the largest
+    // range count whose workspace fits.
+    int G = mla::resolve_slots(&local);
+    for (; G > 1; --G) {
+      local.num_slots = G;
+      const size_t n = mla_workspace_size(geom, &local);
+      if (n != 0 && n <= kNoAllocScratchBytes) break;
+    }
+    local.num_slots = G;
+  }
+  const size_t need = mla_workspace_size(geom, &local);
   if (need == 0) return MLA_ERR_ARG;
   if (need > kNoAllocScratchBytes) return MLA_ERR_WORKSPACE;  // batch needs more than the fixed scratch
-  if (batch->B == 0) return MLA_OK;
+  if (local.B == 0) return MLA_OK;
   void* scratch = nullptr;
-  mla_status s = scratch_for_current_device(&scratch);
+  s = scratch_for_current_device(&scratch);
   if (s != MLA_OK) return s;
-  s = mla_plan(geom, batch, seq_lens, scratch, kNoAllocScratchBytes, stream);
+  s = mla_plan(geom, &local, seq_lens, scratch, kNoAllocScratchBytes, stream);
   if (s != MLA_OK) return s;
-  return mla_decode(geom, batch, q_lat, q_pe, cache, block_table, bt_stride, seq_lens, /*checked=*/0, o_lat, lse,
+  return mla_decode(geom, &local, q_lat, q_pe, cache, block_table, bt_stride, seq_lens, /*checked=*/0, o_lat, lse,
                     scratch, kNoAllocScratchBytes, stream);
 }

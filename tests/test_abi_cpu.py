@@ -65,6 +65,20 @@ def test_host_validation_rejects_before_launch(mla):
                           1 << 30, 0) == mla.MLA_ERR_ALIGN
     assert mla.mla_split_merge(None, None, None, 2, 4, 12, None, None, 0) == mla.MLA_ERR_ARG
     assert mla.mla_split_merge(0x1000, 0x2000, 0x3000, 0, 4, 16, 0x4000, 0x5000, 0) == mla.MLA_OK
+    # every pointer of the merge is checked, the LSE arrays included
+    assert mla.mla_split_merge(0x1000, 0x2004, 0x3000, 2, 4, 16, 0x4000, 0x5000, 0) == mla.MLA_ERR_ALIGN
+    assert mla.mla_split_merge(0x1000, 0x2000, 0x3000, 2, 4, 16, 0x4000, 0x5004, 0) == mla.MLA_ERR_ALIGN
+    # the gather export: a path other than 0 or 1, or a misaligned output, is refused
+    assert mla.mla_debug_gather(cache, 0x1000, 8, 0x2000, 0, 2, 0x3000, 0) == mla.MLA_ERR_ARG
+    assert mla.mla_debug_gather(cache, 0x1000, 8, 0x2000, 0, 0, 0x3008, 0) == mla.MLA_ERR_ALIGN
+    # the no-alloc decode runs every decode argument check before launching anything
+    assert mla.mla_decode_noalloc(g, b, None, None, cache, None, 8, None, None, None, 0) == mla.MLA_ERR_ARG
+    assert mla.mla_decode_noalloc(g, b, 0x1000, 0x2000, bad_cache, 0x3000, 8, 0x4000, 0x5000, 0x6000,
+                                  0) == mla.MLA_ERR_ALIGN
+    assert mla.mla_decode_noalloc(g, b, 0x1000, 0x2000, cache, 0x3000, 4, 0x4000, 0x5000, 0x6000,
+                                  0) == mla.MLA_ERR_ARG     # block-table row narrower than max_pages
+    assert mla.mla_decode_noalloc(g, b, 0x1000, 0x2000, cache, 0x3000, 8, 0x4000, 0x5010, 0x6000,
+                                  0) == mla.MLA_ERR_ALIGN   # o_lat is written with 32-byte stores
     # FP8 cache rows: output present and 16-byte aligned, cache valid
     assert mla.mla_fp8_pack_cache(cache, None, 0) == mla.MLA_ERR_ARG
     assert mla.mla_fp8_pack_cache(cache, 0x3008, 0) == mla.MLA_ERR_ALIGN

@@ -26,9 +26,10 @@ def _to_np(t):
 
 
 def _oracle_decode(w, batches=None, tokens=None):
-    """Oracle o_lat/lse for the listed sequences (and tokens) of a workload, from its own bf16 inputs."""
+    """Oracle o_lat/lse for the listed sequences (and tokens) of a workload, from its own bf16 inputs.
+    Each sequence's rows are gathered as bf16 bit patterns and widened after the gather
+    (the same values as widening the whole pool first)."""
     pool, bt = w.compact_view()
-    pool = _f64(pool)
     q_lat = _f64(w.q_lat)
     q_pe = _f64(w.q_pe)
     out = {}
@@ -38,10 +39,26 @@ def _oracle_decode(w, batches=None, tokens=None):
         if S == 0:
             out[b] = (np.zeros((len(ts), w.H, 512)), np.full((len(ts), w.H), -np.inf))
             continue
-        rows = O.gather_rows(pool, bt[b], S)
+        rows = _f64(O.gather_rows(pool, bt[b], S))
         mask = O.causal_mask(S, w.T, w.causal)[ts]
         out[b] = O.attend_latent(q_lat[b, ts], q_pe[b, ts], rows, mask)
     return out
+
+
+def _oracle_partials(w, b, segments):
+    """The oracle's partial states (o_r normalised, lse_r) of sequence b over the given page ranges."""
+    pool, bt = w.compact_view()
+    S = int(w.seq_lens[b])
+    rows = _f64(O.gather_rows(pool, bt[b], S))
+    q_lat, q_pe = _f64(w.q_lat)[b], _f64(w.q_pe)[b]
+    mask = O.causal_mask(S, w.T, w.causal)
+    parts_o, parts_l = [], []
+    for p0, p1 in segments:
+        j0, j1 = 64 * p0, min(S, 64 * p1)
+        o, l = O.attend_latent(q_lat, q_pe, rows[j0:j1], mask[:, j0:j1])
+        parts_o.append(o)
+        parts_l.append(l)
+    return np.stack(parts_o), np.stack(parts_l)
 
 
 def _run_decode(mla, w, cuda, num_slots=0, override=0, checked=False):
@@ -137,23 +154,67 @@ def test_plan_bit_exact_many_groups(mla, cuda, slots, ov):
     assert hdr[mla.HDR["NUM_PARTIALS"]] == ref["num_partials"] and hdr[mla.HDR["ERROR"]] == 0
 
 
+def _gather_expected(w, cpool, cbt, b, S, bad_pages=()):
+    """The oracle's gather of sequence b; pages whose block id is outside the pool read as zeros."""
+    ref = O.gather_rows(cpool, np.where(cbt[b] >= 0, cbt[b], 0), S).copy()
+    for p in bad_pages:
+        ref[64 * p: 64 * (p + 1)] = 0
+    return ref
+
+
+@pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("cfg", [1, 2, 3])
-def test_gather_bit_exact(mla, cuda, cfg):
+def test_gather_bit_exact(mla, cuda, cfg, split):
+    """The decode kernel's own page loads (tensor maps, box coordinates from the block
+    table, both the page-half boxes and the reload boxes) copy exactly the rows the
+    oracle's paged gather names ("M5.8" 0x05), on combined and split pools."""
     import torch
     from mla_latent_cache_gb300.runtime import pool_to_device
     w = W.config_workload(cfg)
     pool = pool_to_device(torch, w, cuda)
-    cache = mla.cache_from_pool(pool)
+    if split:
+        ckv, kpe = pool[..., :512].contiguous(), pool[..., 512:].contiguous()   # kept alive for the raw pointers
+        cache = mla.cache_from_split(ckv, kpe)
+    else:
+        cache = mla.cache_from_pool(pool)
     bt = torch.from_numpy(w.block_table).to(cuda)
     seq = torch.from_numpy(w.seq_lens).to(cuda)
     cpool, cbt = w.compact_view()
-    for b in sorted({0, w.B // 2, w.B - 1}):
+    picks = range(w.B) if w.B <= 64 else sorted({0, 1, w.B // 2, w.B - 1} | set(range(0, w.B, 9)))
+    for b in picks:
         S = int(w.seq_lens[b])
-        out = torch.zeros((S, 576), dtype=torch.bfloat16, device=cuda)
-        mla.check(mla.mla_debug_gather(cache, bt, bt.shape[1], seq, b, out))
-        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
-        ref = O.gather_rows(cpool, cbt[b], S)
-        assert np.array_equal(got, ref)
+        ref = _gather_expected(w, cpool, cbt, b, S)
+        for path in (0, 1):
+            out = torch.zeros((S, 576), dtype=torch.bfloat16, device=cuda)
+            mla.check(mla.mla_debug_gather(cache, bt, bt.shape[1], seq, b, path, out))
+            got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, ref), (b, path)
+    status, _ = mla.mla_read_device_status(None)
+    assert status == mla.MLA_OK
+
+
+def test_gather_out_of_pool_ids_read_zeros(mla, cuda):
+    """A block id outside [0, num_blocks) reads as zeros through the decode's maps; the
+    other pages, including a ragged last page, are untouched."""
+    import torch
+    from mla_latent_cache_gb300.runtime import pool_to_device
+    w = W.custom_workload(16, [700, 130], T=1, seed=19)
+    pool = pool_to_device(torch, w, cuda)
+    cache = mla.cache_from_pool(pool)
+    bt_np = w.block_table.copy()
+    bt_np[0, 2] = w.num_blocks + 7
+    bt_np[0, 5] = -3
+    bt = torch.from_numpy(bt_np).to(cuda)
+    seq = torch.from_numpy(w.seq_lens).to(cuda)
+    cpool, cbt = w.compact_view()
+    for b, bad in [(0, (2, 5)), (1, ())]:
+        S = int(w.seq_lens[b])
+        ref = _gather_expected(w, cpool, cbt, b, S, bad)
+        for path in (0, 1):
+            out = torch.full((S, 576), float("nan"), dtype=torch.bfloat16, device=cuda)
+            mla.check(mla.mla_debug_gather(cache, bt, bt.shape[1], seq, b, path, out))
+            got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+            assert np.array_equal(got, ref), (b, path)
 
 
 # ---------------------------------------------------------------------------
@@ -165,25 +226,59 @@ def test_decode_tiny_config(mla, cuda):
     _compare(st, w, name="tiny")
 
 
-def test_decode_v3_uniform_sampled(mla, cuda):
-    w = W.config_workload(2)
+@pytest.mark.parametrize("sharp", [False, True])
+def test_decode_v3_uniform_all(mla, cuda, sharp):
+    """Every one of the 64 sequences (one CTA pair each) compared element by element."""
+    w = W.config_workload(2, sharp=sharp)
     st = _run_decode(mla, w, cuda)
-    _compare(st, w, batches=[0, 17, 63], name="v3 uniform")
+    _compare(st, w, name=f"v3 uniform sharp={sharp}")
 
 
-def test_decode_v3_ragged_sampled(mla, cuda):
-    w = W.config_workload(3)
+@pytest.mark.parametrize("sharp", [False, True])
+def test_decode_v3_ragged_all(mla, cuda, sharp):
+    """Every one of the 128 sequences: balanced page ranges that cut sequences at
+    arbitrary pages, partial states merged by log-sum-exp."""
+    w = W.config_workload(3, sharp=sharp)
     st = _run_decode(mla, w, cuda)
-    lens = w.seq_lens
-    pick = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 5, 100})
-    _compare(st, w, batches=pick, name="v3 ragged")
+    hdr = st.plan_header()
+    assert hdr[mla.HDR["NUM_PARTIALS"]] > 0        # the plan does split sequences
+    _compare(st, w, name=f"v3 ragged sharp={sharp}")
 
 
-@pytest.mark.parametrize("override", [0, 64, 256])
-def test_decode_v3_long(mla, cuda, override):
-    w = W.config_workload(4)
+@pytest.mark.parametrize("sharp", [False, True])
+@pytest.mark.parametrize("override", [0, 64, 128, 256])
+def test_decode_v3_long(mla, cuda, override, sharp):
+    w = W.config_workload(4, sharp=sharp)
     st = _run_decode(mla, w, cuda, override=override)
-    _compare(st, w, name=f"v3 long N={override}")
+    _compare(st, w, name=f"v3 long N={override} sharp={sharp}")
+
+
+@pytest.mark.parametrize("override", [0, 64])
+def test_long_sharp_merge_negative_controls(mla, cuda, override):
+    """With peaked logits the partials' LSEs differ widely, so the tolerance separates
+    the exact merge from the wrong ones the pages warn about ("M5.8" 0x0C: averaging
+    per-split outputs is wrong; mlxcel Stage 2: weights are e^x of natural-log LSEs,
+    not 2^x).  The wrong merges are built from the oracle's own partials for the
+    device plan's segments (planted on the CPU); the device result, merged by the
+    same plan, must pass where they fail."""
+    from mla_latent_cache_gb300.runtime import read_plan_tables
+    import torch
+    w = W.config_workload(4, sharp=True)
+    st = _run_decode(mla, w, cuda, override=override)
+    seg, _, _ = read_plan_tables(torch, st.workspace)
+    segments = [(int(r[2]), int(r[3])) for r in seg]
+    assert len(segments) > 1
+    po, pl = _oracle_partials(w, 0, segments)
+    ref_o, ref_l = O.merge_ref(po, pl)
+    parity(_to_np(st.o_lat)[0], ref_o, "device o_lat")
+    parity(_to_np(st.lse)[0], ref_l, "device lse")
+    avg = po.mean(axis=0)
+    m = pl.max(axis=0)
+    w2 = np.exp2(pl - m)
+    log2_o = (w2[..., None] * po).sum(axis=0) / w2.sum(axis=0)[..., None]
+    for name, bad in [("average", avg), ("2^x weights", log2_o)]:
+        with pytest.raises(AssertionError):
+            parity(bad, ref_o, name)
 
 
 @pytest.mark.parametrize("T", [1, 16, 64, 170, 512])
@@ -205,11 +300,23 @@ def test_decode_page_boundaries(mla, cuda, H, T, causal):
         _compare(st, w, name=f"edges H={H} T={T} slots={slots} ov={ov}")
 
 
-@pytest.mark.parametrize("cfg", [1, 2])
-def test_decode_sharp_softmax(mla, cuda, cfg):
-    w = W.config_workload(cfg, sharp=True)
+def test_decode_sharp_softmax_tiny(mla, cuda):
+    w = W.config_workload(1, sharp=True)
     st = _run_decode(mla, w, cuda)
-    _compare(st, w, batches=None if cfg == 1 else [0, 31], name="sharp")
+    _compare(st, w, name="sharp tiny")
+
+
+@pytest.mark.parametrize("H", [1, 2, 4, 8, 32, 64])
+@pytest.mark.parametrize("T,causal", [(1, False), (3, True)])
+def test_decode_head_counts(mla, cuda, H, T, causal):
+    """Every head count the boundary accepts (128 % H == 0) besides 16 and 128: a
+    128-row group then spans 128 / H tokens, or a token's rows split across groups."""
+    lens = [1, 64, 65, 300, 1000, 3]
+    lens = [s for s in lens if s >= T]
+    w = W.custom_workload(H, lens, T=T, causal=causal, seed=41 + H + T, sharp=(H % 2 == 0))
+    for slots, ov in [(0, 0), (3, 0), (0, 4)]:
+        st = _run_decode(mla, w, cuda, num_slots=slots, override=ov)
+        _compare(st, w, name=f"H={H} T={T} slots={slots} ov={ov}")
 
 
 def test_decode_split_cache_layout(mla, cuda):
