@@ -99,6 +99,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 static_assert(kTmemQ + 32 * kQTmemBoxes <= kTmemCols, "tensor memory");
 static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
 static_assert(kSmemRing % 1024 == 0 && kSmemP % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle atoms");
+static_assert(kSlotBytes == 4096 && kQBoxBytes == 8192 && kQTmemBoxes == 6 && kBoxes == 9,
+              "the immediate operand offsets of qk_page_e and pv_page_e");
 
 enum {
   BAR_FULL = 0,                        // kStages: this CTA's half-page landed (TMA); at CTA 0 also CTA 1's (relayed)
@@ -255,6 +257,98 @@ __device__ __forceinline__ int page_block(const FastArgs& a, int b, int p, int* 
   return blk;
 }
 
+// One page of Q K^T as a single issue sequence from one elected lane (36 pair
+// MMAs, K = 576 in steps of 16): issuing the 36 MMAs from one asm block, with the
+// operand addresses advanced by immediate offsets, was measured to raise the
+// page rate over one elect.sync per MMA.  A operand: query boxes 0..5 in tensor
+// memory (32 columns per box, 8 per K step), boxes 6..8 in shared memory
+// (8 KB apart, 32 bytes per K step); B operand: the stage's nine 4 KB slots
+// (descriptor units of 16 bytes: 256 per slot, 2 per K step).  The first MMA
+// overwrites the score tile.
+#define QK_TS(AOFF, BOFF)                                                  \
+  "add.u32 aq, %1, " #AOFF ";\n\tadd.u64 bq, %2, " #BOFF ";\n\t"        \
+  "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [aq], bq, %3, t;\n\t"
+#define QK_SS(AOFF, BOFF)                                                  \
+  "add.u64 as, %4, " #AOFF ";\n\tadd.u64 bq, %2, " #BOFF ";\n\t"        \
+  "@e tcgen05.mma.cta_group::2.kind::f16 [%0], as, bq, %3, t;\n\t"
+__device__ __forceinline__ void qk_page_e(uint32_t d_tmem, uint32_t q_tmem, uint64_t b_desc0, uint32_t idesc,
+                                          uint64_t q_smem_desc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t.reg .b64 bq, as;\n\t.reg .b32 aq;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.eq.b32 p, 1, 0;\n\t"
+      "setp.eq.b32 t, 1, 1;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      QK_TS(8, 2)
+      QK_TS(16, 4)
+      QK_TS(24, 6)
+      QK_TS(32, 256)
+      QK_TS(40, 258)
+      QK_TS(48, 260)
+      QK_TS(56, 262)
+      QK_TS(64, 512)
+      QK_TS(72, 514)
+      QK_TS(80, 516)
+      QK_TS(88, 518)
+      QK_TS(96, 768)
+      QK_TS(104, 770)
+      QK_TS(112, 772)
+      QK_TS(120, 774)
+      QK_TS(128, 1024)
+      QK_TS(136, 1026)
+      QK_TS(144, 1028)
+      QK_TS(152, 1030)
+      QK_TS(160, 1280)
+      QK_TS(168, 1282)
+      QK_TS(176, 1284)
+      QK_TS(184, 1286)
+      QK_SS(0, 1536)
+      QK_SS(2, 1538)
+      QK_SS(4, 1540)
+      QK_SS(6, 1542)
+      QK_SS(512, 1792)
+      QK_SS(514, 1794)
+      QK_SS(516, 1796)
+      QK_SS(518, 1798)
+      QK_SS(1024, 2048)
+      QK_SS(1026, 2050)
+      QK_SS(1028, 2052)
+      QK_SS(1030, 2054)
+      "}" ::"r"(d_tmem), "r"(q_tmem), "l"(b_desc0), "r"(idesc), "l"(q_smem_desc0)
+      : "memory");
+}
+#undef QK_TS
+#undef QK_SS
+
+// One page of P V the same way (8 pair MMAs, N = 256: two 256-column halves of
+// the accumulator, K = 64 page rows in steps of 16).  A: P (K-major, 32 bytes
+// per K step); B: V, N-major, latent column block pairs {4m, 4m+1} for rows
+// 0..31 (steps 0, 1: 2 KB apart) and {4m+2, 4m+3} for rows 32..63.  The first
+// MMA of each half accumulates only when `accumulate` != 0.
+#define PV_SS(D, AOFF, BOFF, PRED)                                          \
+  "add.u64 ap, %1, " #AOFF ";\n\tadd.u64 bv, %2, " #BOFF ";\n\t"         \
+  "@e tcgen05.mma.cta_group::2.kind::f16 [" #D "], ap, bv, %3, " #PRED ";\n\t"
+__device__ __forceinline__ void pv_page_e(uint32_t o_tmem, uint64_t p_desc0, uint64_t v_desc0, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t.reg .b64 ap, bv;\n\t.reg .b32 d1;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 1, 1;\n\t"
+      "add.u32 d1, %0, 128;\n\t"
+      PV_SS(%0, 0, 0, p)
+      PV_SS(%0, 2, 128, t)
+      PV_SS(%0, 4, 512, t)
+      PV_SS(%0, 6, 640, t)
+      PV_SS(d1, 0, 1024, p)
+      PV_SS(d1, 2, 1152, t)
+      PV_SS(d1, 4, 1536, t)
+      PV_SS(d1, 6, 1664, t)
+      "}" ::"r"(o_tmem), "l"(p_desc0), "l"(v_desc0), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+#undef PV_SS
+
 // Q K^T issuer (CTA 0, one converged warp): page t goes to score tile t % 2
 // once both CTAs' halves of the page have landed (CTA 0's load barrier also
 // counts CTA 1's, relayed) and both softmaxes have read the tile's previous
@@ -262,9 +356,7 @@ __device__ __forceinline__ int page_block(const FastArgs& a, int b, int p, int* 
 __device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hdr, volatile int* abort_flag,
                                         const int* seg, SegWalk walk) {
   const uint32_t id_qk = idesc_bf16_f32(128, 64, 0);
-  uint64_t qdesc[kQSmemBoxes];
-#pragma unroll
-  for (int bx = 0; bx < kQSmemBoxes; ++bx) qdesc[bx] = kmajor_desc(sh.q(kQTmemBoxes + bx));
+  const uint64_t qdesc0 = kmajor_desc(sh.q(kQTmemBoxes));
   int gt = 0, sc = 0;
   bool ok = true;
   for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
@@ -280,17 +372,7 @@ __device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hd
         ok = false; break;
       }
       tc_fence_after();
-      const uint32_t d = tmem + kTmemS + 32 * sb;
-#pragma unroll
-      for (int bx = 0; bx < kBoxes; ++bx) {
-        const uint64_t bd = kmajor_desc(sh.slot(st, bx));
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t acc = (bx || kk) ? 1u : 0u;
-          if (bx < kQTmemBoxes) mma2_ts_e(d, tmem + kTmemQ + 32 * bx + 8 * kk, bd + 2 * kk, id_qk, acc);
-          else mma2_ss_e(d, qdesc[bx - kQTmemBoxes] + 2 * kk, bd + 2 * kk, id_qk, acc);
-        }
-      }
+      qk_page_e(tmem + kTmemS + 32 * sb, tmem + kTmemQ, kmajor_desc(sh.slot(st, 0)), id_qk, qdesc0);
       commit2_both_e(sh.bar(BAR_S_FULL + sb));
       commit2_both_e(sh.bar(BAR_QK_DONE + st));
       if (i == n_tiles - 1) commit2_both_e(sh.bar(BAR_Q_FREE));
@@ -325,15 +407,7 @@ __device__ __forceinline__ void pv_role(const Shared& sh, uint32_t tmem, int* hd
         ok = false; break;
       }
       tc_fence_after();
-      const uint64_t pdesc = kmajor_desc(sh.p(pb));
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t vaddr = sh.slot(st, 4 * m + 2 * (kk >> 1)) + (kk & 1) * 2048;
-          mma2_ss_e(tmem + kTmemO + 128 * m, pdesc + 2 * kk, vdesc(vaddr), id_pv, (i == 0 && kk == 0) ? 0u : 1u);
-        }
-      }
+      pv_page_e(tmem + kTmemO, kmajor_desc(sh.p(pb)), vdesc(sh.slot(st, 0)), id_pv, i == 0 ? 0u : 1u);
       commit2_both_e(sh.bar(BAR_PV_DONE + st));
     }
     ++sc;
@@ -360,6 +434,38 @@ __device__ __forceinline__ void relay_role(const Shared& sh, int* hdr, volatile 
       }
       asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(dst0 + 8 * st) : "memory");
     }
+  }
+}
+
+// Reloads of the other half's rows (one thread): once Q K^T is done with a page,
+// the slots that held this CTA's Q K^T-only latent boxes receive the other page
+// half's rows of the boxes this CTA accumulates (two 2-block boxes, L2 hits:
+// the partner CTA fetched them from HBM).
+__device__ __forceinline__ void reload_role(const Shared& sh, const CUtensorMap* tm_pair, const FastArgs& a, int* hdr,
+                                            volatile int* abort_flag, const int* seg, SegWalk walk, int rank) {
+  int gt = 0;
+  bool ok = true;
+  for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
+    const int* rec = seg + (size_t)si * kSegWords;
+    const int b = rec[0];
+    for (int p = rec[2]; ok && p < rec[3]; ++p, ++gt) {
+      const int blk = page_block(a, b, p, hdr, false);
+      const int st = gt % kStages;
+      if (!mbar_wait_sleep(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
+        fail(hdr, abort_flag, 13); ok = false; break;
+      }
+      // Two 2-block boxes: latent boxes {2r, 2r+1} and {4+2r, 5+2r} of the other half.
+      mbar_arrive_expect_tx(sh.bar(BAR_RELOAD + st), 4 * kSlotBytes);
+      for (int i = 0; i < 4; i += 2)
+        load_pair_box(sh.slot(st, reload_slot(rank, i)), tm_pair, sh.bar(BAR_RELOAD + st), 1 - rank,
+                      own_pv_box(rank, i), blk);
+    }
+  }
+  // Drain: every reload issued must have landed before the CTA may exit.
+  const int first = gt > kStages ? gt - kStages : 0;
+  for (int g = first; g < gt; ++g) {
+    volatile int never = 0;
+    mbar_wait(sh.bar(BAR_RELOAD + g % kStages), (g / kStages) & 1, &never);
   }
 }
 
@@ -494,6 +600,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         volatile int never = 0;
         mbar_wait(sh.bar(BAR_Q_TMA), (sc - 1) & 1, &never);
       }
+    } else if (lane == 1) {
+      // ------------------------------------------------------------ reloads of the other half's rows
+      reload_role(sh, &tm_pair, a, hdr, abort_flag, seg, walk0, rank);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -507,33 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     else if (lane == 0) relay_role(sh, hdr, abort_flag, seg, walk0, BAR_FULL, BAR_FULL, 12);
     __syncwarp();
   } else if (warp == 3) {
-    // ------------------------------------------------------------ reloads of the other half's rows
-    if (lane == 0) {
-      SegWalk walk = walk0;
-      int gt = 0;
-      bool ok = true;
-      for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
-        const int* rec = seg + (size_t)si * kSegWords;
-        const int b = rec[0];
-        for (int p = rec[2]; ok && p < rec[3]; ++p, ++gt) {
-          const int blk = page_block(a, b, p, hdr, false);
-          const int st = gt % kStages;
-          if (!mbar_wait_sleep(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
-            fail(hdr, abort_flag, 13); ok = false; break;
-          }
-          // Two 2-block boxes: latent boxes {2r, 2r+1} and {4+2r, 5+2r} of the other half.
-          mbar_arrive_expect_tx(sh.bar(BAR_RELOAD + st), 4 * kSlotBytes);
-          for (int i = 0; i < 4; i += 2)
-            load_pair_box(sh.slot(st, reload_slot(rank, i)), &tm_pair, sh.bar(BAR_RELOAD + st), 1 - rank,
-                          own_pv_box(rank, i), blk);
-        }
-      }
-      const int first = gt > kStages ? gt - kStages : 0;
-      for (int g = first; g < gt; ++g) {
-        volatile int never = 0;
-        mbar_wait(sh.bar(BAR_RELOAD + g % kStages), (g / kStages) & 1, &never);
-      }
-    }
+    // idle: a warp issuing next to two softmax warps slows them (measured)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue (warps 4..11)
