@@ -1,8 +1,8 @@
 """Benchmark: absorbed MLA decode at V3 geometry (H=128, B=64, S=4096, T=1).
 
 One step = one pass of the whole hot path through libmla.so: split plan,
-absorption (q_nope @ W_UK), split-KV latent attention (+ LSE merge when the
-plan splits), un-absorption (o_lat @ W_UV).  The step is captured into one
+absorption (q_nope @ W_UK), split-KV latent attention (with the LSE merge of
+split groups in the same kernel), un-absorption (o_lat @ W_UV).  The step is captured into one
 CUDA graph so that host launch cost does not pace the GPU; the dominant
 kernel is timed separately: a decode-only graph (four chained decode launches,
 one when the L2 is flushed between launches) bracketed by CUDA events on the
@@ -292,7 +292,7 @@ def run_ours(args):
     with torch.cuda.graph(g_dec, stream=stream):
         for _ in range(dec_per_graph):
             st.decode(stream)
-    launches_per_step = 5  # plan, absorb, decode, merge, un-absorb
+    launches_per_step = 4  # plan, absorb, decode (its merge runs in the same kernel), un-absorb
 
     def barrier():
         if world > 1:

@@ -135,8 +135,12 @@ enum {
   MLA_HDR_WORDS = 64
 };
 #define MLA_PLAN_MAGIC 0x4d4c4131 /* "MLA1" */
-/* segment record: int32[8] = {b, rb, page_begin, page_end, range, slot (-1 = final), 0, 0}
- * merge record:   int32[4] = {b, rb, slot_begin, count} (count 0 = empty group)
+/* range pointers: int32 [cap_ranges + 1]; the segments of range r are
+ *   rptr[r] .. rptr[r+1]-1; entries past num_ranges equal the segment count
+ * segment record: int32[8] = {b, rb, page_begin, page_end, range, slot (-1 = final),
+ *   merge record of its group (-1 = final), 0}
+ * merge record:   int32[4] = {b, rb, slot_begin, count} (count 0 = empty group), and two
+ *   int32 counters per record (partial rows stored, rows merged; zero between decodes)
  * part_lse float32 [cap_partials, 128]; part_o float32 [cap_partials, 128, 512] (normalised) */
 
 /* Bytes of workspace needed for this geometry and batch shape. 0 on invalid arguments. */

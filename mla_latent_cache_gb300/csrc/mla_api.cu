@@ -66,6 +66,7 @@ bool compute_layout(const mla_geom* g, const mla_batch* b, WsLayout* L) {
   L->off_segments = off;   off = align_up(off + (size_t)cap_segments * kSegWords * sizeof(int));
   L->off_range_ptr = off;  off = align_up(off + (size_t)(cap_ranges + 1) * sizeof(int));
   L->off_merge = off;      off = align_up(off + (size_t)groups * kMergeWords * sizeof(int));
+  L->off_merge_sync = off; off = align_up(off + (size_t)groups * 2 * sizeof(int));
   L->off_part_lse = off;   off = align_up(off + (size_t)cap_partials * kRowsPerBlock * sizeof(float));
   L->off_part_o = off;     off = align_up(off + (size_t)cap_partials * kRowsPerBlock * kDLat * sizeof(float));
   L->total = off;
@@ -209,12 +210,11 @@ mla_status mla_decode(const mla_geom* geom, const mla_batch* batch, const void* 
   if (!compute_layout(geom, batch, &L)) return MLA_ERR_SHAPE;
   if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = launch_decode_sm103(geom, batch, L, static_cast<const __nv_bfloat16*>(q_lat),
-                                       static_cast<const __nv_bfloat16*>(q_pe), cv, block_table, bt_stride, seq_lens,
-                                       checked, static_cast<__nv_bfloat16*>(o_lat), lse, workspace, st);
-  if (e != cudaSuccess) return MLA_ERR_CUDA;
-  e = launch_plan_merge(geom, batch, L, static_cast<__nv_bfloat16*>(o_lat), lse, workspace, st);
-  return cuda_status(e);
+  // One kernel: the split-KV decode, and (when the plan has merge records) the
+  // LSE merge of the partial states by the same CTAs after a grid-wide barrier.
+  return cuda_status(launch_decode_sm103(geom, batch, L, static_cast<const __nv_bfloat16*>(q_lat),
+                                         static_cast<const __nv_bfloat16*>(q_pe), cv, block_table, bt_stride,
+                                         seq_lens, checked, static_cast<__nv_bfloat16*>(o_lat), lse, workspace, st));
 }
 
 mla_status mla_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M, int rows, int D,

@@ -63,6 +63,7 @@
 #include <atomic>
 
 #include "mla_internal.cuh"
+#include "mla_plan_merge.cuh"
 #include "sm103_ptx.cuh"
 
 namespace mla {
@@ -70,7 +71,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 384;   // a multiple of 128 (the merge's thread groups)
 constexpr int kSoftmaxThreads = 256;
 constexpr int kCtaRows = 64;                   // query rows per CTA
 constexpr int kHalfRows = 32;                  // page rows loaded by each CTA
@@ -82,6 +83,9 @@ constexpr int kQTmemBoxes = 6;                 // query boxes 0..5 in TMEM
 constexpr int kQSmemBoxes = kBoxes - kQTmemBoxes;
 constexpr int kQBoxBytes = kCtaRows * 128;     // 8 KB
 constexpr int kPBufs = 2;
+// The first segment's query boxes 0..5 land in ring stages 3 and 4 (before their
+// first page) and are copied from there into tensor memory.
+constexpr int kQStageFirst = 3;
 constexpr int kPBytes = kCtaRows * 128;        // 8 KB: 64 rows x 64 page rows bf16
 constexpr int kSmemQ = 0;
 constexpr int kSmemP = kSmemQ + kQSmemBoxes * kQBoxBytes;
@@ -97,6 +101,7 @@ constexpr uint32_t kTmemQ = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 static_assert(kTmemQ + 32 * kQTmemBoxes <= kTmemCols, "tensor memory");
+static_assert(kQStageFirst + 2 == kStages && kQTmemBoxes * 8192 <= 2 * kBoxes * 4096, "query staging in the ring");
 static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
 static_assert(kSmemRing % 1024 == 0 && kSmemP % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzle atoms");
 static_assert(kSlotBytes == 4096 && kQBoxBytes == 8192 && kQTmemBoxes == 6 && kBoxes == 9,
@@ -112,14 +117,15 @@ enum {
   BAR_P_FULL = BAR_S_FREE + 2,         // kPBufs: (CTA 0) both CTAs wrote P (16 warp arrivals)
   BAR_Q_TMA = BAR_P_FULL + kPBufs,     // query boxes in shared memory landed (TMA)
   BAR_Q_READY = BAR_Q_TMA + 1,         // (CTA 0) both CTAs staged the query (16 warp arrivals)
-  BAR_Q_FREE = BAR_Q_READY + 1,        // Q K^T of the segment done with the query (both CTAs)
+  BAR_Q_COPIED = BAR_Q_READY + 1,      // the first query's boxes 0..5 left ring stages 3, 4 (8 local warp arrivals)
+  BAR_Q_FREE = BAR_Q_COPIED + 1,        // Q K^T of the segment done with the query (both CTAs)
   BAR_O_FREE = BAR_Q_FREE + 1,         // (CTA 0) both CTAs' epilogues read the accumulator (16 warp arrivals)
   BAR_XCH = BAR_O_FREE + 1,            // 2: the four softmax warps sharing a row range (4 warp arrivals)
   BAR_FINAL_QK = BAR_XCH + 2,
   BAR_FINAL_PV,
   kNumBars = BAR_FINAL_PV + 1
 };
-static_assert(kNumBars * 8 + 8 <= 512, "barrier area");
+static_assert(kNumBars * 8 + 16 <= 512, "barrier area");
 
 // Slots: box b of a page half is slot b.  CTA r accumulates latent boxes
 // {2r, 2r+1, 4+2r, 5+2r}; after Q K^T the slots of the other four latent boxes
@@ -164,6 +170,8 @@ struct FastArgs {
 struct Shared {
   uint32_t base;
   __device__ uint32_t q(int box) const { return base + kSmemQ + (box - kQTmemBoxes) * kQBoxBytes; }
+  // Where the first segment's query box 0..5 lands (inside ring stages 3, 4).
+  __device__ uint32_t q_first(int box) const { return base + kSmemRing + kQStageFirst * kStageBytes + box * kQBoxBytes; }
   __device__ uint32_t p(int buf) const { return base + kSmemP + buf * kPBytes; }
   __device__ uint32_t stage(int st) const { return base + kSmemRing + st * kStageBytes; }
   __device__ uint32_t slot(int st, int s) const { return stage(st) + s * kSlotBytes; }
@@ -229,7 +237,7 @@ __device__ __forceinline__ uint64_t vdesc(uint32_t saddr) { return sw128_desc(sa
 
 // What a softmax thread needs to know about one segment.
 struct SegRows {
-  int b, p0, p1, slot_out, S, fr, limit;
+  int b, p0, p1, slot_out, merge_rec, S, fr, limit;
   bool row_valid;
 };
 
@@ -239,6 +247,7 @@ __device__ __forceinline__ SegRows seg_rows(const int* rec, const FastArgs& a, i
   s.p0 = rec[2];
   s.p1 = rec[3];
   s.slot_out = rec[5];
+  s.merge_rec = rec[6];
   int S = a.seq_lens[s.b];
   s.S = S < 0 ? 0 : min(S, a.max_pages * kPage);
   s.fr = rec[1] * kRowsPerBlock + row;
@@ -488,6 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Shared sh{smem_addr(smem)};
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(smem + kSmemBar + kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemBar + kNumBars * 8 + 4);
+  volatile int* s_num_merge = reinterpret_cast<volatile int*>(smem + kSmemBar + kNumBars * 8 + 8);
+  volatile int* s_merge_ok = reinterpret_cast<volatile int*>(smem + kSmemBar + kNumBars * 8 + 12);
 
   const int* seg = reinterpret_cast<const int*>(ws + a.L.off_segments);
   const int* rptr = reinterpret_cast<const int*>(ws + a.L.off_range_ptr);
@@ -515,6 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kPBufs; ++i) mbar_init(sh.bar(BAR_P_FULL + i), 16);
     mbar_init(sh.bar(BAR_Q_TMA), 1);
+    mbar_init(sh.bar(BAR_Q_COPIED), 8);
     mbar_init(sh.bar(BAR_Q_READY), 16);
     mbar_init(sh.bar(BAR_Q_FREE), 1);
     mbar_init(sh.bar(BAR_O_FREE), 16);
@@ -542,8 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (shared memory), so they take idle SMs and those this grid frees, and wait
   // there for this grid to finish instead of paying their launch after it.
   pdl_trigger();
-  const int num_ranges = hdr[MLA_HDR_NUM_RANGES];
-  const SegWalk walk0(rptr, pair, num_pairs, num_ranges);
+  if (tid == 0) *s_num_merge = hdr[MLA_HDR_NUM_MERGE];
+  // The planner fills the range pointers up to the capacity (empty ranges past the
+  // last), so the walk needs no range count from the header.
+  const SegWalk walk0(rptr, pair, num_pairs, a.L.cap_ranges);
 
   if (a.checked && blockIdx.x == 0 && tid == 0) {
     if (hdr[MLA_HDR_MAGIC] != MLA_PLAN_MAGIC || hdr[MLA_HDR_B] != a.B || hdr[MLA_HDR_T] != a.T ||
@@ -574,7 +588,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3];
         if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_FREE), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
         const int row0 = b * R + rb * kRowsPerBlock + kCtaRows * rank;
-        mbar_arrive_expect_tx(sh.bar(BAR_Q_TMA), kQSmemBoxes * kQBoxBytes);
+        // The first segment's whole query comes by TMA ahead of the pages (boxes 0..5
+        // into ring stages 3, 4, copied to tensor memory by the softmax warps); later
+        // segments' boxes 0..5 are read by those warps while the ring is in use.
+        mbar_arrive_expect_tx(sh.bar(BAR_Q_TMA), (sc == 0 ? kBoxes : kQSmemBoxes) * kQBoxBytes);
+        if (sc == 0)
+          for (int box = 0; box < kQTmemBoxes; ++box)
+            tma_load_2d(sh.q_first(box), &tm_qlat, sh.bar(BAR_Q_TMA), 64 * box, row0);
         for (int box = kQTmemBoxes; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_TMA), 64 * box, row0);
         tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_TMA), 0, row0);
         q_in_flight = true;
@@ -583,6 +603,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = gt % kStages;
           if (gt >= kStages && !mbar_wait_sleep(sh.bar(BAR_PV_DONE + st), ((gt / kStages) - 1) & 1, abort_flag)) {
             fail(hdr, abort_flag, 11); ok = false; break;
+          }
+          if (gt >= kQStageFirst && gt < kStages && !mbar_wait_sleep(sh.bar(BAR_Q_COPIED), 0, abort_flag)) {
+            fail(hdr, abort_flag, 15); ok = false; break;
           }
           // One 4-D box per page half: 32 rows x all column blocks, landing as the nine
           // 32-row x 64-column slots (streams ~8 % faster than nine 3-D boxes).
@@ -657,11 +680,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool w_ok = sc_of == 0 || mbar_wait(sh.bar(BAR_Q_FREE), (sc_of - 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, w_ok)) return false;
       tc_fence_after();
-      const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)s.b * R + (s.row_valid ? s.fr : 0)) * kDLat) +
-                         8 * 3 * cw;
       uint4 v[24];
+      if (sc_of == 0) {
+        // From the TMA copy in ring stages 3, 4: row hr of box k, 16-byte chunk c
+        // at k * 8 KB + 128 hr + 16 (c ^ (hr % 8)) (128-byte swizzle).
+        const bool t_ok = mbar_wait(sh.bar(BAR_Q_TMA), 0, abort_flag);
+        if (!__all_sync(0xffffffffu, t_ok)) return false;
 #pragma unroll
-      for (int e = 0; e < 24; ++e) v[e] = s.row_valid ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
+        for (int bb = 0; bb < 3; ++bb) {
+          const unsigned char* box = smem + kSmemRing + kQStageFirst * kStageBytes + (3 * cw + bb) * kQBoxBytes + hr * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) v[8 * bb + c] = *reinterpret_cast<const uint4*>(box + 16 * (c ^ (hr & 7)));
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(a.q_lat + ((size_t)s.b * R + (s.row_valid ? s.fr : 0)) * kDLat) +
+                           8 * 3 * cw;
+#pragma unroll
+        for (int e = 0; e < 24; ++e) v[e] = s.row_valid ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
       for (int bb = 0; bb < 3; ++bb) {
         uint32_t q[32];
@@ -673,6 +709,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(t_lane + kTmemQ + 32 * (3 * cw + bb), q);
       }
       tmem_wait_st();
+      if (sc_of == 0) {
+        // the staging area goes back to the page ring (its reads precede the page loads' writes)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sh.bar(BAR_Q_COPIED));
+      }
       const bool t_ok = mbar_wait(sh.bar(BAR_Q_TMA), sc_of & 1, abort_flag);
       if (!__all_sync(0xffffffffu, t_ok)) return false;
       tc_fence_before();
@@ -859,6 +901,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (slot_out < 0) a.lse[(size_t)b * R + fr] = lse_v;
         else part_lse[(size_t)slot_out * kRowsPerBlock + row] = lse_v;
       }
+      if (slot_out >= 0) {
+        // this warp's partial rows of the group are stored: count them into its merge record
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          atomicAdd(reinterpret_cast<int*>(ws + a.L.off_merge_sync) + 2 * cur.merge_rec, 1);
+        }
+      }
       tc_fence_before();
       warp_arrive_leader(sh.bar(BAR_O_FREE), rank);
       ++sc;
@@ -872,6 +922,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
+
+  // The plan's merge records (split groups and empty groups): each CTA merges a
+  // contiguous share of their rows, each record once all its partial rows are
+  // stored (by any CTA of the grid).
+  const int num_merge = *s_num_merge;
+  if (num_merge > 0) {
+    const merge::Out out{a.T, a.H, a.o_lat, a.lse};
+    merge::merge_plan_share<kThreads / 128>(out, ws, a.L, num_merge, blockIdx.x, gridDim.x,
+                                            reinterpret_cast<float*>(smem + kSmemRing), s_merge_ok);
+  }
 }
 
 // Test export of the decode kernel's gather: page p of sequence b is fetched by

@@ -23,7 +23,7 @@ constexpr int kGroupWords = 8;
 
 // Workspace layout, computed on the host from (geometry, batch shape, slots).
 struct WsLayout {
-  size_t off_groups, off_segments, off_range_ptr, off_merge, off_part_lse, off_part_o, total;
+  size_t off_groups, off_segments, off_range_ptr, off_merge, off_merge_sync, off_part_lse, off_part_o, total;
   int cap_groups, cap_segments, cap_ranges, cap_partials;
   int num_slots;
 };
@@ -102,8 +102,6 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
                                 const int32_t* block_table, int bt_stride, const int32_t* seq_lens, int checked,
                                 __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st);
 int decode_sm103_pairs_per_device();
-cudaError_t launch_plan_merge(const mla_geom* g, const mla_batch* b, const WsLayout& L,
-                              __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st);
 cudaError_t launch_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M,
                                int rows, int D, __nv_bfloat16* o, float* lse, cudaStream_t st);
 cudaError_t launch_absorb_sm103(const __nv_bfloat16* q_nope, const __nv_bfloat16* w_uk, __nv_bfloat16* q_lat,

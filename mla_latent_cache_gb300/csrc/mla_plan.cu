@@ -104,7 +104,7 @@ struct PlanArgs {
 // segment sb, in the given mode; writes the record and, for a segment that
 // opens a work range, the range pointer.
 __device__ __forceinline__ void write_segment(int* seg, int* rptr, int mode, int q, int b, int rb, int n, int off,
-                                              int k, int sb, int pb, int s) {
+                                              int k, int sb, int pb, int mi, int s) {
   int p0, p1, r;
   if (mode == 2) {
     p0 = (int)(((long long)s * n) / k);
@@ -119,7 +119,7 @@ __device__ __forceinline__ void write_segment(int* seg, int* rptr, int mode, int
   }
   int* rec = seg + (size_t)(sb + s) * kSegWords;
   rec[0] = b; rec[1] = rb; rec[2] = p0; rec[3] = p1; rec[4] = r;
-  rec[5] = (k > 1) ? pb + s : -1; rec[6] = 0; rec[7] = 0;
+  rec[5] = (k > 1) ? pb + s : -1; rec[6] = (k > 1) ? mi : -1; rec[7] = 0;
   // Every range starts with the segment holding its first page.
   if (mode != 1 || (off + p0) % q == 0) rptr[r] = sb + s;
 }
@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
   int* seg = reinterpret_cast<int*>(ws + a.L.off_segments);
   int* rptr = reinterpret_cast<int*>(ws + a.L.off_range_ptr);
   int* mrg = reinterpret_cast<int*>(ws + a.L.off_merge);
+  int* msync = reinterpret_cast<int*>(ws + a.L.off_merge_sync);
   __shared__ int sh[128];
   __shared__ int s_sb[kSmemGroups];
   __shared__ int s_q, s_mode;
@@ -210,6 +211,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
       grp[g * kGroupWords + 4] = pb;
       grp[g * kGroupWords + 5] = mflag ? cmrg + v[2] : -1;
       if (g < kSmemGroups) s_sb[g] = sb;
+      msync[2 * g] = 0;       // merge record g's stored-partial count and merged-row count
+      msync[2 * g + 1] = 0;
       if (mflag) {
         int* m = mrg + (size_t)(cmrg + v[2]) * kMergeWords;
         m[0] = g / a.RB; m[1] = g % a.RB; m[2] = (k > 1) ? pb : 0; m[3] = (k > 1) ? k : 0;
@@ -233,16 +236,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
       }
       const int g = lo;
       const int* gr = grp + g * kGroupWords;
-      write_segment(seg, rptr, mode, q, g / a.RB, g % a.RB, gr[0], gr[1], gr[2], gr[3], gr[4], i - gr[3]);
+      write_segment(seg, rptr, mode, q, g / a.RB, g % a.RB, gr[0], gr[1], gr[2], gr[3], gr[4], gr[5], i - gr[3]);
     }
   } else {
     for (int g = tid; g < a.num_groups; g += blockDim.x) {
       const int* gr = grp + g * kGroupWords;
       const int k = gr[2];
       for (int s = 0; s < k; ++s)
-        write_segment(seg, rptr, mode, q, g / a.RB, g % a.RB, gr[0], gr[1], k, gr[3], gr[4], s);
+        write_segment(seg, rptr, mode, q, g / a.RB, g % a.RB, gr[0], gr[1], k, gr[3], gr[4], gr[5], s);
     }
   }
+  // Range pointers past the last range repeat the segment count, up to the
+  // table's capacity: a decode CTA pair then reads its ranges' pointers
+  // directly, without first reading the range count.
+  for (int r = num_ranges + 1 + tid; r <= a.L.cap_ranges; r += blockDim.x) rptr[r] = total_seg;
   if (tid == 0) {
     rptr[num_ranges] = total_seg;
     hdr[MLA_HDR_B] = a.B; hdr[MLA_HDR_T] = a.T; hdr[MLA_HDR_H] = a.H; hdr[MLA_HDR_CAUSAL] = a.causal;
