@@ -64,7 +64,7 @@ def _peaks():
 
 PROFILE = os.path.join(ROOT, "profiles", "decode_sm103_v3_uniform_b64_s4096.md")
 DECODE_SOURCES = ["mla_latent_cache_gb300/csrc/mla_decode_sm103.cu", "mla_latent_cache_gb300/csrc/sm103_ptx.cuh",
-                  "mla_latent_cache_gb300/csrc/mla_internal.cuh"]
+                  "mla_latent_cache_gb300/csrc/mla_internal.cuh", "mla_latent_cache_gb300/csrc/mla_plan_merge.cuh"]
 
 
 def profiled_traffic():
