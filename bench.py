@@ -120,14 +120,15 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
+        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}_{id(self)}.csv")
 
     def __enter__(self):
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.5)   # let it start sampling before the timed region begins
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -141,10 +142,21 @@ class ClockSampler:
                 self.proc.kill()
             self.fh.close()
 
-    def summary(self) -> dict:
-        if self.proc is None or not os.path.exists(self.path):
+    def summary(self, *others: "ClockSampler") -> dict:
+        """Median SM clock, maximum clock and throttle reasons over this sampler's
+        samples and those of `others` (further timed regions of the same run)."""
+        sm, smax, reasons, ok = [], [], set(), False
+        for smp in (self,) + others:
+            if smp._collect(sm, smax, reasons):
+                ok = True
+        if not ok:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        sm, smax, reasons = [], [], set()
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+    def _collect(self, sm, smax, reasons) -> bool:
+        if self.proc is None or not os.path.exists(self.path):
+            return False
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
@@ -163,8 +175,7 @@ class ClockSampler:
             os.remove(self.path)
         except OSError:
             pass
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return True
 
 
 def cpu_oracle_sample(w, budget_s: float = 15.0):
@@ -217,6 +228,16 @@ def _emit(line: dict):
     print(json.dumps(line), flush=True)
 
 
+def workload_config(w, args, world: int) -> dict:
+    """The workload keys both arms print (the reference arm runs a bounded sample of it)."""
+    pool_bytes = w.num_blocks * 64 * 576 * 2
+    return {"workload": w.name, "H": w.H, "B": w.B, "T": w.T, "S": int(w.seq_lens[0]),
+            "S_total": int(np.asarray(w.seq_lens, dtype=np.int64).sum()), "page": 64, "pool_blocks": w.num_blocks,
+            "parallelism": f"replicas{world}", "splits": args.splits or "auto",
+            "l2": ("L2 flushed between steps (256 MB write, outside the timed events)" if pool_bytes < 2 * L2_BYTES
+                   else f"inputs larger than L2: {pool_bytes / 1e6:.0f} MB latent pool vs 129 MB L2")}
+
+
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
@@ -234,14 +255,19 @@ def run_reference(args):
         samples.append((tps, done, dt, cores))
     tps = sum(s[1] for s in samples) * w.T / sum(per_step)
     cores = samples[-1][3]
-    ms = 1000.0 * w.B * w.T / tps
+    seqs = [s[1] for s in samples]
+    # ms_per_step is the time each timed step actually took: one bounded sample of
+    # the workload (its first sequences, whole), not the full batch
+    ms = 1000.0 * sum(per_step) / len(per_step)
     _emit({"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": w.name, "H": w.H, "B": w.B, "T": w.T, "S": int(w.seq_lens[0]), "page": 64},
+           "config": workload_config(w, args, world),
+           "step": f"one bounded sample of the workload per step: its first sequences, whole "
+                   f"({min(seqs)}-{max(seqs)} of B={w.B}), absorb + attention + un-absorb in float64",
            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                            "sample": f"whole sequences of the workload, {samples[-1][1]} per step "
-                                      f"(~{budget:.1f} s budget); ms_per_step extrapolates to B={w.B}"},
+                            "sample": f"{min(seqs)}-{max(seqs)} whole sequences of the workload per step "
+                                      f"(~{budget:.1f} s budget per step)"},
            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
     return 0
 
@@ -350,35 +376,61 @@ def run_ours(args):
     if status != L.MLA_OK:
         raise RuntimeError(f"device status after timing: {L.mla_status_string(status)} ({info})")
 
-    # end to end through the C ABI with host buffers: per step, copy the step's inputs
+    # end to end through the C ABI with host buffers: every step copies its inputs
     # (q_nope, q_pe, seq_lens, block table: one pinned host buffer mirroring the
-    # device buffer they live in) to the device, run, read o back; the copies and
-    # the step are one graph.
+    # device buffer they live in) to the device and reads its o back.  Two input
+    # buffers and two outputs alternate, so that the upload of the next step and
+    # the read-back of the previous one run on side streams under the current
+    # step's kernels; one graph holds two steps (buffer sets A and B).
+    io_a = st.io_set()
+    io_b = st.new_io_set()
     h_in = torch.empty_like(st.inputs, device="cpu").pin_memory(); h_in.copy_(st.inputs)
-    h_o = torch.empty_like(st.o, device="cpu").pin_memory()
+    h_o = [torch.empty_like(st.o, device="cpu").pin_memory() for _ in range(2)]
     h2d = h_in.numel() * h_in.element_size()
-    d2h = h_o.numel() * h_o.element_size()
-    e_steps = max(3, min(args.steps, 200))
+    d2h = h_o[0].numel() * h_o[0].element_size()
+    e_pairs = max(2, min(args.steps, 200) // 2)
+    s_up, s_down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     g_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_e2e, stream=stream):
-        st.inputs.copy_(h_in, non_blocking=True)
-        st.step(stream)
-        h_o.copy_(st.o, non_blocking=True)
 
+    def half(io_run, io_next, h_out_prev, o_prev):
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        up, down = torch.cuda.Event(), torch.cuda.Event()
+        s_up.wait_event(fork)
+        with torch.cuda.stream(s_up):
+            io_next["inputs"].copy_(h_in, non_blocking=True)      # the next step's inputs
+            up.record(s_up)
+        s_down.wait_event(fork)
+        with torch.cuda.stream(s_down):
+            h_out_prev.copy_(o_prev, non_blocking=True)           # the previous step's output
+            down.record(s_down)
+        st.bind(io_run)
+        st.step(stream)
+        stream.wait_event(up)
+        stream.wait_event(down)
+
+    with torch.cuda.graph(g_e2e, stream=stream):
+        half(io_a, io_b, h_o[1], io_b["o"])
+        half(io_b, io_a, h_o[0], io_a["o"])
+    st.bind(io_a)
     with torch.cuda.stream(stream):
         for _ in range(3):
             g_e2e.replay()
     stream.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e_steps):
-            g_e2e.replay()
-        e1.record(stream)
-    stream.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
+    with ClockSampler(local) as clocks_e2e:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(e_pairs):
+                g_e2e.replay()
+            e1.record(stream)
+        stream.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / (2 * e_pairs), dev)
     e2e_value = replica_throughput(w.B * w.T, world, e2e_ms)
+    # (each step's output lands on the host one step later: o of the last step of
+    # a replay is read back in the next replay's first half)
+    e2e_check = bool(torch.equal(h_o[0].to(dev), io_a["o"]) and torch.equal(h_o[1].to(dev), io_b["o"]))
 
     achieved = ab["decode"] / (dec_ms / 1000.0) / 1e9
     tflops = fl["decode"] / (dec_ms / 1000.0) / 1e12
@@ -392,25 +444,22 @@ def run_ours(args):
                 "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "traffic": profiled_traffic() if WORKLOADS[args.workload] == WORKLOAD_INDEX else None,
                 "algorithmic_bytes": ab["decode"], "decode_ms": dec_ms, "decode_tflops": tflops}
-    l2_note = ("L2 flushed between steps (256 MB write, outside the timed events)" if flush is not None else
-               f"inputs larger than L2: {pool_bytes / 1e6:.0f} MB latent pool vs 129 MB L2")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "H": w.H, "B": w.B, "T": w.T, "S": int(w.seq_lens[0]),
-                   "S_total": int(np.asarray(w.seq_lens, dtype=np.int64).sum()), "page": 64,
-                   "pool_blocks": w.num_blocks, "parallelism": f"replicas{world}", "splits": args.splits or "auto",
-                   "l2": l2_note,
-                   "step": "plan, absorb, decode(+merge), unabsorb; one CUDA graph per step, kernels chained with "
-                           "programmatic dependent launch; decode timed alone in its own graph (dec_per_graph "
-                           "chained launches per replay)", "dec_per_graph": dec_per_graph},
+        "config": workload_config(w, args, world),
+        "step": "plan, absorb, decode (the split plan's merge in the same kernel), unabsorb; one CUDA graph per "
+                "step, kernels chained with programmatic dependent launch; the decode timed alone in its own "
+                f"graph ({dec_per_graph} chained launches per replay)",
         "roofline": roof,
         "step_hbm_gbs": ab["step"] / (ms / 1000.0) / 1e9,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms, "overlap": "uploads and read-backs on side streams under the other "
+                                                  "buffer set's step (two input buffers, two outputs)",
+                "readback_matches_device": e2e_check},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clocks.summary(clocks_e2e),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, done, dt, cores = cpu_oracle_sample(w, budget_s=args.ref_budget)

@@ -64,6 +64,7 @@ class DecodeStep:
             view = self.inputs[o: o + src.numel() * src.element_size()].view(src.dtype).view(src.shape)
             view.copy_(src)
             setattr(self, n, view)
+        self._input_parts = list(zip(parts, offs))
         self.o_lat = torch.empty((w.B, w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((w.B, w.T, w.H), dtype=torch.float32, device=dev)
         self.ws_bytes = L.mla_workspace_size(self.geom, self.batch)
@@ -74,6 +75,29 @@ class DecodeStep:
     @property
     def BT(self) -> int:
         return self.w.B * self.w.T
+
+    def io_set(self) -> dict:
+        """The per-step input buffer (with its views) and output o of this step."""
+        return {"inputs": self.inputs, "o": getattr(self, "o", None),
+                **{n: getattr(self, n) for n, _ in self._input_parts}}
+
+    def new_io_set(self) -> dict:
+        """A second input buffer (same contents) and output, for double-buffered steps."""
+        torch = self.torch
+        inputs = self.inputs.clone()
+        io = {"inputs": inputs, "o": torch.empty_like(self.o) if hasattr(self, "o") else None}
+        for n, off in self._input_parts:
+            src = getattr(self, n)
+            io[n] = inputs[off: off + src.numel() * src.element_size()].view(src.dtype).view(src.shape)
+        return io
+
+    def bind(self, io: dict):
+        """Point the step at an input/output set (the next calls use its buffers)."""
+        self.inputs = io["inputs"]
+        if io.get("o") is not None:
+            self.o = io["o"]
+        for n, _ in self._input_parts:
+            setattr(self, n, io[n])
 
     def plan(self, stream=None):
         L.check(L.mla_plan(self.geom, self.batch, self.seq_lens, self.workspace, self.ws_bytes, stream), "mla_plan")
