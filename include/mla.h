@@ -193,6 +193,37 @@ mla_status mla_decode(const mla_geom* geom, const mla_batch* batch, const void* 
                       void* workspace, size_t ws_bytes, mla_stream_t stream);
 
 /*
+ * Index-driven (sparse) decode ("M5.8" 0x0B "FP8 Cache Format And Sparse
+ * Selection", the sparse-indices passage: indices [B, S_q, topk] of physical
+ * rows, block * 64 + offset, with topk_length [B] bounding each list's valid
+ * prefix; "MLA in full detail", the DeepSeek-V3.2 passage: an indexer picks the rows
+ * of the latent cache the absorbed decode attends to).  Same arithmetic as
+ * mla_decode, but token t of sequence b attends to exactly the rows
+ * indices[b, t, 0 .. topk_length[b]) (repeats count once per listing), in any
+ * order, instead of a block-table prefix; no causal mask.
+ *   batch: B, T (= S_q), num_slots and num_splits_override as for mla_decode;
+ *     causal must be 0; max_pages is ignored (taken as ceil(topk / 64)).
+ *   q_lat [B,T,H,512], q_pe [B,T,H,64] bf16; o_lat [B,T,H,512] bf16, lse
+ *     [B,T,H] float32 (-inf, o = 0 for an empty list); indices int32 [B,T,topk]
+ *     and topk_length int32 [B] on the device, 16-byte aligned; a length above
+ *     topk counts as topk, a negative one as 0, and either is reported in the
+ *     workspace status word (MLA_ERR_DEVICE_CHECK, info = b * S_q + t of the
+ *     first token affected), checked or not.
+ *   cache: its blocks must be evenly spaced (block stride = 64 x row stride, for
+ *     both parts), so that the pool is one array of num_blocks * 64 rows.
+ *   checked != 0 reports, in the same word, a listed row outside
+ *     [0, num_blocks * 64) (MLA_ERR_DEVICE_CHECK); without it such a row reads
+ *     as zeros (it still takes part in the softmax, with score 0).
+ * Plans and decodes in one call (no separate mla_plan): the workspace needs
+ * mla_sparse_workspace_size(geom, batch, topk) bytes (0 on invalid arguments).
+ */
+size_t mla_sparse_workspace_size(const mla_geom* geom, const mla_batch* batch, int topk);
+mla_status mla_decode_sparse(const mla_geom* geom, const mla_batch* batch, const void* q_lat, const void* q_pe,
+                             const mla_cache* cache, const int32_t* indices, int topk, const int32_t* topk_length,
+                             int checked, void* o_lat, float* lse, void* workspace, size_t ws_bytes,
+                             mla_stream_t stream);
+
+/*
  * Exact merge of split partial states ("M5.8" 0x0C; "mlxcel" Stage-2
  * contract, here with natural-log LSE):
  * part_o float32 [N, rows, D] (each normalised by its own denominator),

@@ -72,6 +72,8 @@ def _load() -> ctypes.CDLL:
         "mla_unabsorb_o": (I, [G, P, P, P, I, P]),
         "mla_decode": (I, [G, Bt, P, P, C, P, I, P, I, P, P, P, ctypes.c_size_t, P]),
         "mla_decode_noalloc": (I, [G, Bt, P, P, C, P, I, P, P, P, P]),
+        "mla_sparse_workspace_size": (ctypes.c_size_t, [G, Bt, I]),
+        "mla_decode_sparse": (I, [G, Bt, P, P, C, P, I, P, I, P, P, P, ctypes.c_size_t, P]),
         "mla_split_merge": (I, [P, P, P, I, I, I, P, P, P]),
         "mla_debug_gather": (I, [C, P, I, P, I, I, P, P]),
         "mla_fp8_pack_cache": (I, [C, P, P]),
@@ -92,6 +94,7 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 EXPORTED = ("mla_workspace_size", "mla_plan", "mla_absorb_q", "mla_unabsorb_o", "mla_decode", "mla_decode_noalloc",
+            "mla_sparse_workspace_size", "mla_decode_sparse",
             "mla_split_merge", "mla_normal_rows_per_seq", "mla_normal_expanded_bytes", "mla_normal_expand",
             "mla_normal_attention",
             "mla_fp8_pack_cache", "mla_debug_gather", "mla_read_device_status", "mla_status_string",
@@ -192,6 +195,18 @@ def mla_decode_noalloc(geom, batch, q_lat, q_pe, cache: mla_cache, block_table, 
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def mla_sparse_workspace_size(geom, batch, topk: int) -> int:
+    return _lib.mla_sparse_workspace_size(ctypes.byref(geom), ctypes.byref(batch), int(topk))
+
+
+def mla_decode_sparse(geom, batch, q_lat, q_pe, cache: mla_cache, indices, topk: int, topk_length, checked: int,
+                      o_lat, lse, workspace, ws_bytes: int, stream=None) -> int:
+    """Plan + decode over listed physical rows indices [B, S_q, topk] (lengths topk_length [B])."""
+    return _lib.mla_decode_sparse(ctypes.byref(geom), ctypes.byref(batch), _ptr(q_lat), _ptr(q_pe),
+                                  ctypes.byref(cache), _ptr(indices), int(topk), _ptr(topk_length), int(checked),
+                                  _ptr(o_lat), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream))
 
 
 def mla_split_merge(part_o, part_lse, indptr, M: int, rows: int, D: int, o, lse, stream=None) -> int:

@@ -211,10 +211,59 @@ mla_status mla_decode(const mla_geom* geom, const mla_batch* batch, const void* 
   if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
   // One kernel: the split-KV decode, and (when the plan has merge records) the
-  // LSE merge of the partial states by the same CTAs after a grid-wide barrier.
+  // LSE merge of each split group by the CTAs that finish its partial states last.
   return cuda_status(launch_decode_sm103(geom, batch, L, static_cast<const __nv_bfloat16*>(q_lat),
                                          static_cast<const __nv_bfloat16*>(q_pe), cv, block_table, bt_stride,
                                          seq_lens, checked, static_cast<__nv_bfloat16*>(o_lat), lse, workspace, st));
+}
+
+// The sparse decode as a dense one over B * S_q one-token sequences of up to topk
+// listed rows (non-causal), lengths topk_length[b] shared by sequence b's tokens.
+static bool sparse_batch(const mla_batch* batch, int topk, mla_batch* vb) {
+  if (!batch || topk < 1 || batch->B < 0 || batch->T < 1 || batch->causal) return false;
+  if ((long long)batch->B * batch->T > (1LL << 26)) return false;
+  *vb = *batch;
+  vb->B = batch->B * batch->T;
+  vb->T = 1;
+  vb->causal = 0;
+  vb->max_pages = (topk + kPage - 1) / kPage;
+  return true;
+}
+
+size_t mla_sparse_workspace_size(const mla_geom* geom, const mla_batch* batch, int topk) {
+  mla_batch vb;
+  if (!sparse_batch(batch, topk, &vb)) return 0;
+  return mla_workspace_size(geom, &vb);
+}
+
+mla_status mla_decode_sparse(const mla_geom* geom, const mla_batch* batch, const void* q_lat, const void* q_pe,
+                             const mla_cache* cache, const int32_t* indices, int topk, const int32_t* topk_length,
+                             int checked, void* o_lat, float* lse, void* workspace, size_t ws_bytes,
+                             mla_stream_t stream) {
+  mla_status s = check_geom(geom);
+  if (s != MLA_OK) return s;
+  mla_batch vb;
+  if (!sparse_batch(batch, topk, &vb)) return MLA_ERR_ARG;
+  if ((s = check_batch(&vb)) != MLA_OK) return s;
+  if (vb.B == 0) return MLA_OK;
+  if (!q_lat || !q_pe || !indices || !topk_length || !o_lat || !lse || !workspace) return MLA_ERR_ARG;
+  if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned16(indices) || !aligned16(topk_length) || !aligned32(o_lat) ||
+      !aligned16(lse) || !aligned32(workspace))
+    return MLA_ERR_ALIGN;
+  CacheView cv;
+  if ((s = check_cache(cache, &cv)) != MLA_OK) return s;
+  // The pool's rows must be evenly spaced across blocks (one 2-D array of rows).
+  if (cv.ckv_block != (int64_t)kPage * cv.ckv_row || cv.kpe_block != (int64_t)kPage * cv.kpe_row) return MLA_ERR_ARG;
+  if ((long long)cv.num_blocks * kPage >= (1LL << 31)) return MLA_ERR_SHAPE;
+  WsLayout L;
+  if (!compute_layout(geom, &vb, &L)) return MLA_ERR_SHAPE;
+  if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (launch_plan(topk_length, geom, &vb, L, workspace, st, batch->T, topk) != cudaSuccess) return MLA_ERR_CUDA;
+  const SparseList list{indices, topk, batch->T};
+  return cuda_status(launch_decode_sm103(geom, &vb, L, static_cast<const __nv_bfloat16*>(q_lat),
+                                         static_cast<const __nv_bfloat16*>(q_pe), cv, nullptr, 0, topk_length,
+                                         checked, static_cast<__nv_bfloat16*>(o_lat), lse, workspace, st, &list));
 }
 
 mla_status mla_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M, int rows, int D,

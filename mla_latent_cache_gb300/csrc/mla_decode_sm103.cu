@@ -158,8 +158,12 @@ struct FastArgs {
   const __nv_bfloat16* q_lat;
   const int32_t* block_table;
   int bt_stride;
-  const int32_t* seq_lens;
+  const int32_t* seq_lens;   // length of sequence b: seq_lens[b / seq_div]
+  int seq_div;
   int B, T, H, causal, checked, max_pages, num_blocks;
+  int max_rows;              // longest length: max_pages * 64, or the sparse decode's topk
+  const int32_t* indices;    // sparse decode: physical cache rows [B, topk] (B = sequences x query tokens)
+  int topk;
   int kpe_separate;          // RoPE values not at latent + 512 in the same rows: loaded by their own box
   float scale_log2;          // softmax scale times log2(e)
   __nv_bfloat16* o_lat;
@@ -248,8 +252,8 @@ __device__ __forceinline__ SegRows seg_rows(const int* rec, const FastArgs& a, i
   s.p1 = rec[3];
   s.slot_out = rec[5];
   s.merge_rec = rec[6];
-  int S = a.seq_lens[s.b];
-  s.S = S < 0 ? 0 : min(S, a.max_pages * kPage);
+  int S = a.seq_lens[s.b / a.seq_div];
+  s.S = S < 0 ? 0 : min(S, a.max_rows);
   s.fr = rec[1] * kRowsPerBlock + row;
   s.row_valid = s.fr < R;
   s.limit = s.row_valid ? visible_limit(s.S, a.T, s.fr / a.H, a.causal) : 0;
@@ -358,6 +362,62 @@ __device__ __forceinline__ void pv_page_e(uint32_t o_tmem, uint64_t p_desc0, uin
 }
 #undef PV_SS
 
+// ---------------------------------------------------------------- sparse (index-driven) loads
+// "M5.8" 0x0B: sparse indices are physical cache rows (block * 64 + offset).  A
+// sparse decode's "page" p of a (sequence, query token) is listed rows
+// 64 p .. 64 p + 63; its half for CTA r is rows 64 p + 32 r .. + 31, fetched four
+// rows at a time with tile::gather4 loads of the pool seen as one 2-D array of
+// rows, into the same 128-byte-swizzled slots as a page half.  List entries at or
+// past the list's length read as zeros (coordinate -1), and are masked and
+// zeroed like the rows past a sequence's end.
+
+// The 32 physical rows of listed rows j0 .. j0 + 31 of (virtual) sequence b whose
+// list holds S valid entries; an entry outside the pool reads as zeros (and is
+// reported in checked mode).
+__device__ __forceinline__ void sparse_rows32(const FastArgs& a, int b, int j0, int S, int* hdr, bool report,
+                                              int (&r)[32]) {
+  const int* src = a.indices + (size_t)b * a.topk;
+  const int nrows = a.num_blocks * kPage;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const int j = j0 + k;
+    int v = j < S ? __ldg(src + j) : -1;
+    if (j < S && (v < 0 || v >= nrows)) {
+      if (report && a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | (j & 0xFFFF));
+      v = -1;
+    }
+    r[k] = v;
+  }
+}
+
+// Listed rows r[0..31] into the nine slots of a stage (all 576 columns).
+__device__ __forceinline__ void sparse_page_half(uint32_t stage, const CUtensorMap* tm_rows, const CUtensorMap* tm_kpe,
+                                                 uint32_t bar, const int (&r)[32], int kpe_separate) {
+  mbar_arrive_expect_tx(bar, kStageBytes);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int r0 = r[4 * q], r1 = r[4 * q + 1], r2 = r[4 * q + 2], r3 = r[4 * q + 3];
+    for (int s = 0; s < (kpe_separate ? 8 : kBoxes); ++s)
+      tma_gather4(stage + s * kSlotBytes + 512 * q, tm_rows, bar, 64 * s, r0, r1, r2, r3);
+    if (kpe_separate) tma_gather4(stage + 8 * kSlotBytes + 512 * q, tm_kpe, bar, 0, r0, r1, r2, r3);
+  }
+}
+
+// The reload of a sparse page: listed rows r[0..31] (the other half's) of this
+// CTA's four P V latent boxes into the slots its Q K^T-only boxes held.
+__device__ __forceinline__ void sparse_reload(uint32_t stage, const CUtensorMap* tm_rows, uint32_t bar,
+                                              const int (&r)[32], int rank) {
+  mbar_arrive_expect_tx(bar, 4 * kSlotBytes);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int r0 = r[4 * q], r1 = r[4 * q + 1], r2 = r[4 * q + 2], r3 = r[4 * q + 3];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      tma_gather4(stage + reload_slot(rank, i) * kSlotBytes + 512 * q, tm_rows, bar, 64 * own_pv_box(rank, i), r0, r1,
+                  r2, r3);
+  }
+}
+
 // Q K^T issuer (CTA 0, one converged warp): page t goes to score tile t % 2
 // once both CTAs' halves of the page have landed (CTA 0's load barrier also
 // counts CTA 1's, relayed) and both softmaxes have read the tile's previous
@@ -450,6 +510,8 @@ __device__ __forceinline__ void relay_role(const Shared& sh, int* hdr, volatile 
 // the slots that held this CTA's Q K^T-only latent boxes receive the other page
 // half's rows of the boxes this CTA accumulates (two 2-block boxes, L2 hits:
 // the partner CTA fetched them from HBM).
+// (Sparse decode: tm_pair is the 2-D row map, and the rows come by gather4.)
+template <bool kSparse>
 __device__ __forceinline__ void reload_role(const Shared& sh, const CUtensorMap* tm_pair, const FastArgs& a, int* hdr,
                                             volatile int* abort_flag, const int* seg, SegWalk walk, int rank) {
   int gt = 0;
@@ -457,17 +519,31 @@ __device__ __forceinline__ void reload_role(const Shared& sh, const CUtensorMap*
   for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
     const int* rec = seg + (size_t)si * kSegWords;
     const int b = rec[0];
+    int S = 0;
+    if constexpr (kSparse) {
+      S = a.seq_lens[b / a.seq_div];
+      S = S < 0 ? 0 : min(S, a.max_rows);
+    }
     for (int p = rec[2]; ok && p < rec[3]; ++p, ++gt) {
-      const int blk = page_block(a, b, p, hdr, false);
       const int st = gt % kStages;
-      if (!mbar_wait_sleep(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
-        fail(hdr, abort_flag, 13); ok = false; break;
+      if constexpr (kSparse) {
+        int r[32];
+        sparse_rows32(a, b, p * kPage + kHalfRows * (1 - rank), S, hdr, false, r);
+        if (!mbar_wait_sleep(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
+          fail(hdr, abort_flag, 13); ok = false; break;
+        }
+        sparse_reload(sh.stage(st), tm_pair, sh.bar(BAR_RELOAD + st), r, rank);
+      } else {
+        const int blk = page_block(a, b, p, hdr, false);
+        if (!mbar_wait_sleep(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
+          fail(hdr, abort_flag, 13); ok = false; break;
+        }
+        // Two 2-block boxes: latent boxes {2r, 2r+1} and {4+2r, 5+2r} of the other half.
+        mbar_arrive_expect_tx(sh.bar(BAR_RELOAD + st), 4 * kSlotBytes);
+        for (int i = 0; i < 4; i += 2)
+          load_pair_box(sh.slot(st, reload_slot(rank, i)), tm_pair, sh.bar(BAR_RELOAD + st), 1 - rank,
+                        own_pv_box(rank, i), blk);
       }
-      // Two 2-block boxes: latent boxes {2r, 2r+1} and {4+2r, 5+2r} of the other half.
-      mbar_arrive_expect_tx(sh.bar(BAR_RELOAD + st), 4 * kSlotBytes);
-      for (int i = 0; i < 4; i += 2)
-        load_pair_box(sh.slot(st, reload_slot(rank, i)), tm_pair, sh.bar(BAR_RELOAD + st), 1 - rank,
-                      own_pv_box(rank, i), blk);
     }
   }
   // Drain: every reload issued must have landed before the CTA may exit.
@@ -478,6 +554,10 @@ __device__ __forceinline__ void reload_role(const Shared& sh, const CUtensorMap*
   }
 }
 
+// kSparse: the sparse (index-driven) decode; tm_page is then the pool as a 2-D
+// array of rows (the latent part when the RoPE values are separate, tm_kpe the
+// RoPE part), tm_pair unused.
+template <bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_sm103_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_constant__ CUtensorMap tm_qpe,
                         const __grid_constant__ CUtensorMap tm_page, const __grid_constant__ CUtensorMap tm_pair,
@@ -566,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       unsigned h = 0;
       for (int b = 0; b < a.B; ++b) {
-        unsigned S = (unsigned)a.seq_lens[b];
+        unsigned S = (unsigned)a.seq_lens[b / a.seq_div];
         unsigned x = (unsigned)b + 0x632BE5ABu;
         x ^= x >> 16; x *= 0x7feb352dU; x ^= x >> 15; x *= 0x846ca68bU; x ^= x >> 16;
         unsigned y = S * 0x9E3779B1u + x;
@@ -598,8 +678,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int box = kQTmemBoxes; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_TMA), 64 * box, row0);
         tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_TMA), 0, row0);
         q_in_flight = true;
+        int S_sparse = 0;
+        if constexpr (kSparse) {
+          S_sparse = a.seq_lens[b / a.seq_div];
+          S_sparse = S_sparse < 0 ? 0 : min(S_sparse, a.max_rows);
+        }
         for (int p = p0; ok && p < p1; ++p, ++gt) {
-          const int blk = page_block(a, b, p, hdr, true);
+          int blk = 0;
+          int rows[32];
+          if constexpr (kSparse) sparse_rows32(a, b, p * kPage + kHalfRows * rank, S_sparse, hdr, true, rows);
+          else blk = page_block(a, b, p, hdr, true);
           const int st = gt % kStages;
           if (gt >= kStages && !mbar_wait_sleep(sh.bar(BAR_PV_DONE + st), ((gt / kStages) - 1) & 1, abort_flag)) {
             fail(hdr, abort_flag, 11); ok = false; break;
@@ -609,7 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // One 4-D box per page half: 32 rows x all column blocks, landing as the nine
           // 32-row x 64-column slots (streams ~8 % faster than nine 3-D boxes).
-          load_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rank, blk, a.kpe_separate);
+          if constexpr (kSparse) sparse_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rows, a.kpe_separate);
+          else load_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rank, blk, a.kpe_separate);
         }
         ++sc;
       }
@@ -625,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (lane == 1) {
       // ------------------------------------------------------------ reloads of the other half's rows
-      reload_role(sh, &tm_pair, a, hdr, abort_flag, seg, walk0, rank);
+      reload_role<kSparse>(sh, kSparse ? &tm_page : &tm_pair, a, hdr, abort_flag, seg, walk0, rank);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -1061,8 +1150,10 @@ bool set_kernel_attributes() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (!done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(decode_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(decode_sm103_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(decode_sm103_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+            cudaSuccess)
       return false;
     done[dev].store(true, std::memory_order_release);
   }
@@ -1103,7 +1194,7 @@ int decode_sm103_pairs_per_device() {
       cudaLaunchConfig_t cfg;
       cudaLaunchAttribute attr[2];
       cluster_launch_config(&cfg, attr, 256, 0, false);
-      if (cudaOccupancyMaxActiveClusters(&n, decode_sm103_kernel, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, decode_sm103_kernel<false>, &cfg) != cudaSuccess) n = 0;
     }
     if (n <= 0) {
       const int sms = mla_device_sm_count();
@@ -1118,7 +1209,7 @@ int decode_sm103_pairs_per_device() {
 cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsLayout& L,
                                 const __nv_bfloat16* q_lat, const __nv_bfloat16* q_pe, const CacheView& cv,
                                 const int32_t* block_table, int bt_stride, const int32_t* seq_lens, int checked,
-                                __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st) {
+                                __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st, const SparseList* sparse) {
   const long long rows_total = (long long)b->B * b->T * g->H;
   CUtensorMap m_qlat, m_qpe, m_page, m_pair, m_kpe;
   {
@@ -1134,12 +1225,35 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
     if (!make_map(&m_qpe, q_pe, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   bool combined = false;
-  if (!make_cache_maps(cv, &m_page, &m_pair, &m_kpe, &combined)) return cudaErrorInvalidValue;
+  if (sparse == nullptr) {
+    if (!make_cache_maps(cv, &m_page, &m_pair, &m_kpe, &combined)) return cudaErrorInvalidValue;
+  } else {
+    // The pool as one 2-D array of rows (block * 64 + offset), boxes one row high
+    // (tile::gather4): the combined 576-wide row, or the latent and RoPE parts.
+    combined = cv.kpe == cv.ckv + kDLat && cv.kpe_row == cv.ckv_row && cv.kpe_block == cv.ckv_block;
+    const cuuint64_t rows = (cuuint64_t)cv.num_blocks * kPage;
+    const cuuint32_t box[2] = {64, 1};
+    {
+      const cuuint64_t dims[2] = {(cuuint64_t)(combined ? kDK : kDLat), rows};
+      const cuuint64_t str[1] = {(cuuint64_t)cv.ckv_row * 2};
+      if (!make_map(&m_page, cv.ckv, 2, dims, str, box)) return cudaErrorInvalidValue;
+      m_pair = m_page;
+    }
+    {
+      const cuuint64_t dims[2] = {(cuuint64_t)kDRope, rows};
+      const cuuint64_t str[1] = {(cuuint64_t)cv.kpe_row * 2};
+      if (!make_map(&m_kpe, cv.kpe, 2, dims, str, box)) return cudaErrorInvalidValue;
+    }
+  }
   FastArgs a;
   a.q_lat = q_lat;
   a.block_table = block_table; a.bt_stride = bt_stride; a.seq_lens = seq_lens;
+  a.seq_div = sparse ? sparse->seq_div : 1;
   a.B = b->B; a.T = b->T; a.H = g->H; a.causal = b->causal ? 1 : 0; a.checked = checked;
   a.max_pages = b->max_pages; a.num_blocks = cv.num_blocks;
+  a.max_rows = sparse ? sparse->topk : b->max_pages * kPage;
+  a.indices = sparse ? sparse->indices : nullptr;
+  a.topk = sparse ? sparse->topk : 0;
   a.kpe_separate = combined ? 0 : 1;
   a.scale_log2 = g->softmax_scale * 1.4426950408889634f;
   a.o_lat = o_lat; a.lse = lse; a.L = L;
@@ -1151,7 +1265,10 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
   cluster_launch_config(&cfg, attr, pairs, st, true);
-  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel, m_qlat, m_qpe, m_page, m_pair, m_kpe, a,
+  if (sparse)
+    return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<true>, m_qlat, m_qpe, m_page, m_pair, m_kpe, a,
+                              reinterpret_cast<char*>(ws));
+  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<false>, m_qlat, m_qpe, m_page, m_pair, m_kpe, a,
                             reinterpret_cast<char*>(ws));
 }
 

@@ -96,11 +96,18 @@ __host__ __device__ __forceinline__ int visible_limit(int S, int T, int t, int c
 
 // Launchers (one per translation unit); all return cudaError_t of the launch.
 cudaError_t launch_plan(const int32_t* seq_lens, const mla_geom* g, const mla_batch* b,
-                        const WsLayout& L, void* ws, cudaStream_t st);
+                        const WsLayout& L, void* ws, cudaStream_t st, int seq_div = 1, int max_rows = 0);
+// The sparse decode's index lists: physical rows indices [B', topk] for the
+// B' = B * seq_div (sequence, query token) pairs, lengths seq_lens[b' / seq_div].
+struct SparseList {
+  const int32_t* indices;
+  int topk, seq_div;
+};
 cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsLayout& L,
                                 const __nv_bfloat16* q_lat, const __nv_bfloat16* q_pe, const CacheView& cv,
                                 const int32_t* block_table, int bt_stride, const int32_t* seq_lens, int checked,
-                                __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st);
+                                __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st,
+                                const SparseList* sparse = nullptr);
 int decode_sm103_pairs_per_device();
 cudaError_t launch_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M,
                                int rows, int D, __nv_bfloat16* o, float* lse, cudaStream_t st);

@@ -94,8 +94,10 @@ __device__ __forceinline__ uint32_t mix32(uint32_t x) {
 }
 
 struct PlanArgs {
-  const int32_t* seq_lens;
+  const int32_t* seq_lens;   // length of sequence b is seq_lens[b / seq_div]
+  int seq_div;               // 1; the sparse decode's S_q (one length per sequence, shared by its tokens)
   int B, T, H, causal, G, N, max_pages;
+  int max_rows;              // longest allowed length: max_pages * 64, or the sparse decode's topk
   int RB, num_groups;
   WsLayout L;
 };
@@ -143,9 +145,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
   unsigned hsum = 0;
   int errb = INT_MAX;
   for (int b = tid; b < a.B; b += blockDim.x) {
-    const int S = a.seq_lens[b];
+    const int S = a.seq_lens[b / a.seq_div];
     hsum += mix32((uint32_t)S * 0x9E3779B1u + mix32((uint32_t)b + 0x632BE5ABu));
-    if (S < 0 || S > a.max_pages * kPage || (S > 0 && S < a.T)) errb = min(errb, b);
+    if (S < 0 || S > a.max_rows || (S > 0 && S < a.T)) errb = min(errb, b);
   }
 
   // Pass A: pages per group and their exclusive prefix.
@@ -156,8 +158,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
     int n = 0;
     if (g < a.num_groups) {
       const int b = g / a.RB, rb = g % a.RB;
-      int S = a.seq_lens[b];
-      S = S < 0 ? 0 : (S > a.max_pages * kPage ? a.max_pages * kPage : S);
+      int S = a.seq_lens[b / a.seq_div];
+      S = S < 0 ? 0 : (S > a.max_rows ? a.max_rows : S);
       const int r_last = min(R, (rb + 1) * kRowsPerBlock) - 1;
       const int vis = visible_limit(S, a.T, r_last / a.H, a.causal);
       n = (vis + kPage - 1) / kPage;
@@ -282,11 +284,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
 }  // namespace
 
 cudaError_t launch_plan(const int32_t* seq_lens, const mla_geom* g, const mla_batch* b, const WsLayout& L,
-                        void* ws, cudaStream_t st) {
+                        void* ws, cudaStream_t st, int seq_div, int max_rows) {
   PlanArgs a;
   a.seq_lens = seq_lens;
+  a.seq_div = seq_div;
   a.B = b->B; a.T = b->T; a.H = g->H; a.causal = b->causal ? 1 : 0;
   a.G = L.num_slots; a.N = b->num_splits_override; a.max_pages = b->max_pages;
+  a.max_rows = max_rows > 0 ? max_rows : b->max_pages * kPage;
   a.RB = (b->T * g->H + kRowsPerBlock - 1) / kRowsPerBlock;
   a.num_groups = b->B * a.RB;
   a.L = L;

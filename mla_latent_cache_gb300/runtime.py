@@ -148,6 +148,38 @@ def read_plan_tables(torch, workspace):
     return seg, rp, mg
 
 
+class SparseStep:
+    """The index-driven decode (mla_decode_sparse) on one SparseWorkload: the
+    absorbed query attends to the listed physical rows of the pool."""
+
+    def __init__(self, sw, device="cuda", num_slots: int = 0, num_splits_override: int = 0, checked: bool = False):
+        import torch
+        self.torch = torch
+        self.sw = sw
+        w = sw.ctx
+        dev = self.device = torch.device(device)
+        self.geom = L.make_geom(w.H)
+        self.batch = L.make_batch(w.B, w.T, False, 1, num_slots, num_splits_override)
+        self.checked = 1 if checked else 0
+        self.pool = pool_to_device(torch, w, dev)
+        self.cache = L.cache_from_pool(self.pool)
+        self.q_lat = _u16_to_bf16(torch, w.q_lat, dev)
+        self.q_pe = _u16_to_bf16(torch, w.q_pe, dev)
+        self.indices = torch.from_numpy(np.ascontiguousarray(sw.indices)).to(dev)
+        self.topk_length = torch.from_numpy(np.ascontiguousarray(sw.topk_length)).to(dev)
+        self.o_lat = torch.empty((w.B, w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.B, w.T, w.H), dtype=torch.float32, device=dev)
+        self.ws_bytes = L.mla_sparse_workspace_size(self.geom, self.batch, sw.topk)
+        if self.ws_bytes == 0:
+            raise L.MlaError(L.MLA_ERR_ARG, "mla_sparse_workspace_size")
+        self.workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
+
+    def decode(self, stream=None):
+        L.check(L.mla_decode_sparse(self.geom, self.batch, self.q_lat, self.q_pe, self.cache, self.indices,
+                                    self.sw.topk, self.topk_length, self.checked, self.o_lat, self.lse,
+                                    self.workspace, self.ws_bytes, stream), "mla_decode_sparse")
+
+
 class NormalStep:
     """The Normal (decompressed) arm on one workload: expand the latent cache into
     per-head keys and values (mla_normal_expand), then causal MHA over them

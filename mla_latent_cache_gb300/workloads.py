@@ -40,7 +40,7 @@ PAGE = 64
 BF16_NAN = np.uint16(0x7FC0)
 
 # Per-tensor generator streams.
-_S_LAYOUT, _S_CACHE, _S_QNOPE, _S_QPE, _S_WUK, _S_WUV, _S_QLAT = range(7)
+_S_LAYOUT, _S_CACHE, _S_QNOPE, _S_QPE, _S_WUK, _S_WUV, _S_QLAT, _S_SPARSE = range(8)
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -239,3 +239,64 @@ def custom_workload(H: int, seq_lens, T: int = 1, causal: bool = False, seed: in
         num_blocks = max(1, pages + 3)
     qs, ql = (0.1, 0.05) if not sharp else (0.1 * SHARP_Q, 0.05 * SHARP_Q)
     return _build(name, seed, H, T, list(seq_lens), num_blocks, causal, qs, ql)
+
+
+@dataclass
+class SparseWorkload:
+    """Input of the index-driven decode: a context workload ``ctx`` (its T is the
+    S_q query tokens per sequence, its block table places each sequence's rows)
+    and, per query token, a list of physical rows (block * 64 + offset) of that
+    sequence's context, as an indexer's top-k would give.
+
+    indices int32 [B, S_q, topk]; topk_length int32 [B] (entries at or past a
+    sequence's length point at a NaN row of an unreferenced block, or are -1 when
+    the pool has none: a kernel that reads them poisons its output).
+    """
+
+    ctx: Workload
+    topk: int
+    indices: np.ndarray
+    topk_length: np.ndarray
+    name: str = "sparse"
+
+    @property
+    def B(self) -> int:
+        return self.ctx.B
+
+    @property
+    def S_q(self) -> int:
+        return self.ctx.T
+
+    @property
+    def H(self) -> int:
+        return self.ctx.H
+
+
+def sparse_workload(H: int, ctx_lens, S_q: int, topk: int, lengths=None, replace: bool = False, seed: int = 11,
+                    num_blocks: int | None = None, sharp: bool = False, in_order: bool = False,
+                    name: str = "sparse") -> SparseWorkload:
+    """Per token, ``lengths[b]`` (default min(topk, context length)) positions of
+    sequence b's context drawn uniformly (distinct unless ``replace``; all of them
+    in order when ``in_order``), mapped through the block table to physical rows,
+    in the drawn order."""
+    w = custom_workload(H, ctx_lens, T=S_q, causal=False, seed=seed, num_blocks=num_blocks, sharp=sharp, name=name)
+    B = w.B
+    if lengths is None:
+        lengths = [min(topk, int(s)) for s in w.seq_lens]
+    lengths = np.asarray(lengths, dtype=np.int32)
+    free = np.setdiff1d(np.arange(w.num_blocks), w.pool_ids)
+    poison = int(free[0]) * PAGE if len(free) else -1
+    g = _rng(seed, _S_SPARSE)
+    idx = np.full((B, S_q, topk), poison, dtype=np.int32)
+    for b in range(B):
+        S = int(w.seq_lens[b])
+        n = min(int(lengths[b]), topk)
+        if n <= 0:
+            continue
+        for t in range(S_q):
+            if in_order:
+                pos = np.arange(n)
+            else:
+                pos = g.choice(S, size=n, replace=replace)
+            idx[b, t, :n] = w.block_table[b, pos // PAGE].astype(np.int64) * PAGE + pos % PAGE
+    return SparseWorkload(ctx=w, topk=topk, indices=idx, topk_length=lengths, name=name)

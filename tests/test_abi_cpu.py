@@ -87,6 +87,39 @@ def test_host_validation_rejects_before_launch(mla):
     assert mla.mla_fp8_pack_cache(empty, 0x3000, 0) == mla.MLA_ERR_ARG
 
 
+def test_sparse_decode_host_side(mla):
+    g = mla.make_geom(128)
+    b = mla.make_batch(4, 2, False, 1, num_slots=8)
+    # the workspace is that of a dense decode over B * S_q one-token sequences of ceil(topk / 64) pages
+    vb = mla.make_batch(8, 1, False, 32, num_slots=8)
+    assert mla.mla_sparse_workspace_size(g, b, 2048) == mla.mla_workspace_size(g, vb)
+    assert mla.mla_sparse_workspace_size(g, b, 2047) == mla.mla_workspace_size(g, vb)
+    assert mla.mla_sparse_workspace_size(g, b, 0) == 0
+    assert mla.mla_sparse_workspace_size(g, mla.make_batch(4, 2, True, 1, num_slots=8), 64) == 0  # causal refused
+    cache = mla.mla_cache(0x1000, 0x1400, 576, 64 * 576, 576, 64 * 576, 8)
+    ws = mla.mla_sparse_workspace_size(g, b, 2048)
+    ok = dict(q_lat=0x10000, q_pe=0x20000, indices=0x30000, topk_length=0x40000, o_lat=0x50000, lse=0x60000,
+              workspace=0x70000)
+
+    def call(cache=cache, batch=b, topk=2048, ws_bytes=ws, **kw):
+        a = {**ok, **kw}
+        return mla.mla_decode_sparse(g, batch, a["q_lat"], a["q_pe"], cache, a["indices"], topk, a["topk_length"], 0,
+                                     a["o_lat"], a["lse"], a["workspace"], ws_bytes, 0)
+
+    assert call(indices=None) == mla.MLA_ERR_ARG
+    assert call(topk_length=None) == mla.MLA_ERR_ARG
+    assert call(topk=0) == mla.MLA_ERR_ARG
+    assert call(batch=mla.make_batch(4, 2, True, 1, num_slots=8)) == mla.MLA_ERR_ARG
+    assert call(indices=0x30004) == mla.MLA_ERR_ALIGN
+    assert call(o_lat=0x50010) == mla.MLA_ERR_ALIGN
+    assert call(ws_bytes=ws - 1) == mla.MLA_ERR_WORKSPACE
+    # blocks that are not evenly spaced rows cannot be indexed as one row array
+    gapped = mla.mla_cache(0x1000, 0x1400, 576, 64 * 576 + 8, 576, 64 * 576 + 8, 8)
+    assert call(cache=gapped) == mla.MLA_ERR_ARG
+    assert call(cache=mla.mla_cache(0x1000, 0x1402, 576, 64 * 576, 576, 64 * 576, 8)) == mla.MLA_ERR_ALIGN
+    assert call(batch=mla.make_batch(0, 2, False, 1, num_slots=8)) == mla.MLA_OK  # nothing to do
+
+
 def test_normal_arm_host_side(mla):
     g = mla.make_geom(128)
     assert mla.mla_normal_rows_per_seq(1) == 128 and mla.mla_normal_rows_per_seq(2) == 128
