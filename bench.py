@@ -9,7 +9,7 @@ one when the L2 is flushed between launches) bracketed by CUDA events on the
 launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload uniform|tiny|ragged|long|extend] [--T T] [--splits N]
+                  [--workload uniform|tiny|ragged|long|extend|sparse] [--T T] [--splits N]
                   [--arm absorb|normal]
 
 The default workload is the uniform V3 batch; the others (the tiny V2-Lite
@@ -17,8 +17,11 @@ case, the ragged batch, the single 131072-row sequence with --splits N, the
 causal extend batch with --T new rows) print the same JSON line for that
 workload.  ``--arm normal`` times the decompressed comparison arm (expansion
 of the latent cache into per-head keys and values, then causal MHA) on the
-same workload instead.  A workload whose cache fits in L2 is timed with an L2 flush (a
-256 MB write) between steps, outside the timed events.
+same workload instead.  ``--workload sparse`` times the index-driven decode
+(mla_decode_sparse) on its own: 64 sequences of 8192 cached rows, one query
+token each, top-2048 lists of distinct rows in random order.  A workload whose
+cache fits in L2 is timed with an L2 flush (a 256 MB write) between steps,
+outside the timed events.
 
 Multi-GPU runs are replicas: each rank runs the same independent batch (the
 path shards by request and needs no collective); ``value`` is the tokens of
@@ -41,7 +44,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD_INDEX = 2
-WORKLOADS = {"tiny": 1, "uniform": 2, "ragged": 3, "long": 4, "extend": 5}
+WORKLOADS = {"tiny": 1, "uniform": 2, "ragged": 3, "long": 4, "extend": 5, "sparse": 6}
+SPARSE = {"H": 128, "B": 64, "S_q": 1, "topk": 2048, "ctx": 8192, "seed": 1206}
 METRIC = "MLA decode tokens/s and achieved HBM GB/s (% of roofline) at V3 geometry"
 L2_BYTES = 129 * 2**20
 
@@ -559,6 +563,111 @@ def run_normal(args):
     return 0
 
 
+def sparse_bytes(sw) -> int:
+    """Algorithmic bytes of one sparse decode: the listed rows (1152 B each, read once per
+    token that lists them), the lists, the query and the outputs."""
+    n = int(sum(min(int(sw.topk_length[b]), sw.topk) for b in range(sw.B))) * sw.S_q
+    BT = sw.B * sw.S_q
+    return n * 1152 + n * 4 + BT * sw.H * (576 * 2 + 512 * 2 + 4) + sw.B * 4
+
+
+def run_sparse(args):
+    """The index-driven decode alone: device-resident inputs (L2 flushed between launches),
+    and end to end with the step's query, lists and lengths copied in and o_lat, lse read back."""
+    import torch
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from mla_latent_cache_gb300 import binding as L
+    from mla_latent_cache_gb300 import workloads as W
+    from mla_latent_cache_gb300.runtime import SparseStep
+    c = SPARSE
+    sw = W.sparse_workload(c["H"], [c["ctx"]] * c["B"], c["S_q"], c["topk"], seed=c["seed"],
+                           name=f"v32_sparse_b{c['B']}_sq{c['S_q']}_topk{c['topk']}_ctx{c['ctx']}")
+    st = SparseStep(sw, device=dev, num_splits_override=args.splits)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    hbm_peak, tc_peak, peak_kind = _peaks()
+    nbytes = sparse_bytes(sw)
+    with torch.cuda.stream(stream):
+        st.decode(stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        st.decode(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+    stream.synchronize()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    evs = [(ev(), ev()) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.fill_(i & 0xff)              # the listed rows of the previous launch leave the L2
+                evs[i][0].record(stream)
+                g.replay()
+                evs[i][1].record(stream)
+        stream.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    status, info = L.mla_read_device_status(st.workspace, stream)
+    if status != L.MLA_OK:
+        raise RuntimeError(f"device status after timing: {L.mla_status_string(status)} ({info})")
+    # end to end: pinned host copies of q_lat, q_pe, indices, lengths in; o_lat, lse out
+    ins = [st.q_lat, st.q_pe, st.indices, st.topk_length]
+    h_in = [torch.empty_like(t, device="cpu").pin_memory() for t in ins]
+    for h, t in zip(h_in, ins):
+        h.copy_(t)
+    outs = [st.o_lat, st.lse]
+    h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        for t, h in zip(ins, h_in):
+            t.copy_(h, non_blocking=True)
+        st.decode(stream)
+        for h, t in zip(h_out, outs):
+            h.copy_(t, non_blocking=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g_e2e.replay()
+    stream.synchronize()
+    e_steps = max(3, min(args.steps, 200))
+    e0, e1 = ev(), ev()
+    with ClockSampler(local) as clocks_e2e:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(e_steps):
+                g_e2e.replay()
+            e1.record(stream)
+        stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    tokens = sw.B * sw.S_q
+    achieved = nbytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": tokens / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": sw.name, "H": sw.H, "B": sw.B, "S_q": sw.S_q, "topk": sw.topk, "ctx": c["ctx"],
+                   "page": 64, "pool_blocks": sw.ctx.num_blocks, "parallelism": "replicas1",
+                   "splits": args.splits or "auto",
+                   "l2": "L2 flushed between launches (256 MB write, outside the timed events)"},
+        "step": "mla_decode_sparse (plan + index-driven decode with the in-kernel merge), one CUDA graph",
+        "roofline": {"bound": "hbm", "kernel": "mla_decode_sparse", "achieved": achieved, "peak": hbm_peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+                     "algorithmic_bytes": nbytes, "decode_ms": ms},
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in h_in),
+                "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in h_out), "ms_per_step": e2e_ms},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(clocks_e2e),
+    }
+    _emit(line)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -577,6 +686,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "sparse":
+        return run_sparse(args)
     if args.arm == "normal":
         return run_normal(args)
     return run_ours(args)

@@ -43,11 +43,24 @@ BF16_NAN = np.uint16(0x7FC0)
 _S_LAYOUT, _S_CACHE, _S_QNOPE, _S_QPE, _S_WUK, _S_WUV, _S_QLAT, _S_SPARSE = range(8)
 
 
-def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to bf16 (nearest, ties to even); return uint16 bits."""
-    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    rounded = b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))
-    return (rounded >> np.uint32(16)).astype(np.uint16)
+def f32_to_bf16_bits(x: np.ndarray, scale: float | None = None) -> np.ndarray:
+    """Round float32 values (times ``scale`` in float32, when given) to bf16
+    (nearest, ties to even); return uint16 bits.  Works in cache-sized chunks."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    flat = x.reshape(-1)
+    out = np.empty(flat.size, dtype=np.uint16)
+    step = 1 << 22
+    for i in range(0, flat.size, step):
+        c = flat[i:i + step]
+        if scale is not None:
+            c = c * np.float32(scale)
+        b = c.view(np.uint32)
+        r = (b >> np.uint32(16)) & np.uint32(1)
+        r += np.uint32(0x7FFF)
+        r += b
+        r >>= np.uint32(16)
+        out[i:i + step] = r
+    return out.reshape(x.shape)
 
 
 def bf16_bits_to_f32(u: np.ndarray) -> np.ndarray:
@@ -66,8 +79,8 @@ def _rng(seed: int, stream: int) -> np.random.Generator:
 
 def _normal_bf16(seed: int, stream: int, shape, scale: float) -> np.ndarray:
     g = _rng(seed, stream)
-    x = g.standard_normal(size=int(np.prod(shape)), dtype=np.float32) * np.float32(scale)
-    return f32_to_bf16_bits(x).reshape(shape)
+    x = g.standard_normal(size=int(np.prod(shape)), dtype=np.float32)
+    return f32_to_bf16_bits(x, scale).reshape(shape)
 
 
 @dataclass
