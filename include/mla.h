@@ -266,6 +266,19 @@ mla_status mla_debug_gather(const mla_cache* cache, const int32_t* block_table, 
                             const int32_t* seq_lens, int b, int path, void* out, mla_stream_t stream);
 
 /*
+ * Test export of the failure detector: sets, on the current device, the limit in
+ * clock cycles of the decode kernel's pipeline waits (a page to land, scores to
+ * be written, a merge record to fill); cycles <= 0 restores the default (about
+ * one second).  A wait that runs past the limit abandons the launch: the kernel
+ * records MLA_ERR_TIMEOUT in the workspace status word (mla_read_device_status),
+ * lets every copy and MMA it issued land (those waits keep the full limit),
+ * frees its tensor memory and returns, leaving the context usable; the next
+ * mla_plan + mla_decode on the workspace run normally.  Synchronous; affects
+ * every later decode launch on the device, from any thread, until reset.
+ */
+mla_status mla_debug_set_wait_limit(long long cycles);
+
+/*
  * Decode for callers that cannot allocate device memory (no counterpart on the
  * source pages; this is a deployment convenience).  Code running inside an
  * allocator or memory-pool callback, or a serving loop that must keep device

@@ -76,6 +76,7 @@ def _load() -> ctypes.CDLL:
         "mla_decode_sparse": (I, [G, Bt, P, P, C, P, I, P, I, P, P, P, ctypes.c_size_t, P]),
         "mla_split_merge": (I, [P, P, P, I, I, I, P, P, P]),
         "mla_debug_gather": (I, [C, P, I, P, I, I, P, P]),
+        "mla_debug_set_wait_limit": (I, [ctypes.c_longlong]),
         "mla_fp8_pack_cache": (I, [C, P, P]),
         "mla_normal_rows_per_seq": (ctypes.c_int64, [I]),
         "mla_normal_expanded_bytes": (ctypes.c_size_t, [G, I, I]),
@@ -97,7 +98,8 @@ EXPORTED = ("mla_workspace_size", "mla_plan", "mla_absorb_q", "mla_unabsorb_o", 
             "mla_sparse_workspace_size", "mla_decode_sparse",
             "mla_split_merge", "mla_normal_rows_per_seq", "mla_normal_expanded_bytes", "mla_normal_expand",
             "mla_normal_attention",
-            "mla_fp8_pack_cache", "mla_debug_gather", "mla_read_device_status", "mla_status_string",
+            "mla_fp8_pack_cache", "mla_debug_gather", "mla_debug_set_wait_limit", "mla_read_device_status",
+            "mla_status_string",
             "mla_device_sm_count")
 
 
@@ -224,6 +226,11 @@ def mla_debug_gather(cache: mla_cache, block_table, bt_stride: int, seq_lens, b:
     (path 0: page-half boxes; path 1: latent columns through the reload boxes)."""
     return _lib.mla_debug_gather(ctypes.byref(cache), _ptr(block_table), bt_stride, _ptr(seq_lens), b, int(path),
                                  _ptr(out), _stream(stream))
+
+
+def mla_debug_set_wait_limit(cycles: int) -> int:
+    """Limit of the decode kernel's pipeline waits on the current device (<= 0: the default)."""
+    return _lib.mla_debug_set_wait_limit(int(cycles))
 
 
 def mla_normal_rows_per_seq(max_pages: int) -> int:

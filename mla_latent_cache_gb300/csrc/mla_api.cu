@@ -298,6 +298,10 @@ mla_status mla_debug_gather(const mla_cache* cache, const int32_t* block_table, 
                                          static_cast<__nv_bfloat16*>(out), (cudaStream_t)stream));
 }
 
+mla_status mla_debug_set_wait_limit(long long cycles) {
+  return cuda_status(set_pipeline_wait_limit(cycles));
+}
+
 int64_t mla_normal_rows_per_seq(int max_pages) { return max_pages < 1 ? 0 : normal_rows_per_seq(max_pages); }
 
 size_t mla_normal_expanded_bytes(const mla_geom* geom, int B, int max_pages) {

@@ -62,6 +62,15 @@
 
 #include <atomic>
 
+// The decode's pipeline waits read their limit from here (a test can shorten it
+// through mla_debug_set_wait_limit; the drains keep the full limit).
+namespace mla {
+namespace wait_override {
+__constant__ long long c_pipeline_wait_limit = 2000000000LL;
+}
+}  // namespace mla
+#define MLA_PIPELINE_WAIT_LIMIT (::mla::wait_override::c_pipeline_wait_limit)
+
 #include "mla_internal.cuh"
 #include "mla_plan_merge.cuh"
 #include "sm103_ptx.cuh"
@@ -450,8 +459,7 @@ __device__ __forceinline__ void qk_role(const Shared& sh, uint32_t tmem, int* hd
   }
   // Every MMA issued by this warp must be complete before the CTAs may leave.
   commit2_both_e(sh.bar(BAR_FINAL_QK));
-  volatile int never = 0;
-  mbar_wait(sh.bar(BAR_FINAL_QK), 0, &never);
+  mbar_wait_drain(sh.bar(BAR_FINAL_QK), 0);
   __syncwarp();
 }
 
@@ -482,8 +490,7 @@ __device__ __forceinline__ void pv_role(const Shared& sh, uint32_t tmem, int* hd
     ++sc;
   }
   commit2_both_e(sh.bar(BAR_FINAL_PV));
-  volatile int never = 0;
-  mbar_wait(sh.bar(BAR_FINAL_PV), 0, &never);
+  mbar_wait_drain(sh.bar(BAR_FINAL_PV), 0);
   __syncwarp();
 }
 
@@ -549,8 +556,7 @@ __device__ __forceinline__ void reload_role(const Shared& sh, const CUtensorMap*
   // Drain: every reload issued must have landed before the CTA may exit.
   const int first = gt > kStages ? gt - kStages : 0;
   for (int g = first; g < gt; ++g) {
-    volatile int never = 0;
-    mbar_wait(sh.bar(BAR_RELOAD + g % kStages), (g / kStages) & 1, &never);
+    mbar_wait_drain(sh.bar(BAR_RELOAD + g % kStages), (g / kStages) & 1);
   }
 }
 
@@ -705,12 +711,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Drain: every load issued must have landed before the CTA may exit.
       const int first = gt > kStages ? gt - kStages : 0;
       for (int g = first; g < gt; ++g) {
-        volatile int never = 0;
-        mbar_wait(sh.bar(BAR_FULL + g % kStages), (g / kStages) & 1, &never);
+        mbar_wait_drain(sh.bar(BAR_FULL + g % kStages), (g / kStages) & 1);
       }
       if (q_in_flight) {
-        volatile int never = 0;
-        mbar_wait(sh.bar(BAR_Q_TMA), (sc - 1) & 1, &never);
+        mbar_wait_drain(sh.bar(BAR_Q_TMA), (sc - 1) & 1);
       }
     } else if (lane == 1) {
       // ------------------------------------------------------------ reloads of the other half's rows
@@ -1054,7 +1058,6 @@ __global__ void __launch_bounds__(kGatherThreads)
     s_ok = 1;
   }
   __syncthreads();
-  volatile int never = 0;
   uint32_t phase = 0;
   for (int half = 0; half < 2; ++half) {
     for (int pass = 0; pass < (path == 0 ? 1 : 2); ++pass) {
@@ -1065,7 +1068,7 @@ __global__ void __launch_bounds__(kGatherThreads)
           mbar_arrive_expect_tx(bar, 8 * kSlotBytes);
           for (int box = 0; box < 8; box += 2) load_pair_box(stage + box * kSlotBytes, &tm_pair, bar, half, box, blk);
         }
-        if (!mbar_wait(bar, phase, &never)) {
+        if (!mbar_wait_drain(bar, phase)) {
           s_ok = 0;
           atomicCAS(status, 0, MLA_ERR_TIMEOUT);
         }
@@ -1270,6 +1273,11 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
                               reinterpret_cast<char*>(ws));
   return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<false>, m_qlat, m_qpe, m_page, m_pair, m_kpe, a,
                             reinterpret_cast<char*>(ws));
+}
+
+cudaError_t set_pipeline_wait_limit(long long cycles) {
+  const long long v = cycles > 0 ? cycles : ptx::kWaitLimitCycles;
+  return cudaMemcpyToSymbol(wait_override::c_pipeline_wait_limit, &v, sizeof(v));
 }
 
 cudaError_t launch_debug_gather(const CacheView& cv, const int32_t* block_table, int bt_stride,

@@ -126,5 +126,7 @@ cudaError_t launch_normal_attention(const mla_geom* g, const mla_batch* b, const
                                     __nv_bfloat16* o, float* lse, cudaStream_t st);
 cudaError_t launch_debug_gather(const CacheView& cv, const int32_t* block_table, int bt_stride,
                                 const int32_t* seq_lens, int b, int path, __nv_bfloat16* out, cudaStream_t st);
+// Limit (clock cycles) of the decode kernel's pipeline waits on the current device; <= 0: the default.
+cudaError_t set_pipeline_wait_limit(long long cycles);
 
 }  // namespace mla

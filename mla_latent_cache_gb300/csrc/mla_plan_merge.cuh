@@ -153,7 +153,7 @@ __device__ __forceinline__ bool wait_record(int* hdr, int* stored, int need, vol
       int v;
       asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(stored) : "memory");
       if (v >= need) break;
-      if (clock64() - t0 > ptx::kWaitLimitCycles) { ok = false; record_error(hdr, MLA_ERR_TIMEOUT, 60); break; }
+      if (clock64() - t0 > MLA_PIPELINE_WAIT_LIMIT) { ok = false; record_error(hdr, MLA_ERR_TIMEOUT, 60); break; }
       __nanosleep(64);
     }
     *flag = ok ? 1 : 0;

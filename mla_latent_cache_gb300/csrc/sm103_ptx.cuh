@@ -13,6 +13,15 @@ namespace ptx {
 // is treated as a hang, recorded, and abandoned.
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
+// The limit of the pipeline waits below (mbar_wait and its variants).  A
+// translation unit may define MLA_PIPELINE_WAIT_LIMIT, before it includes this
+// header, as an expression read at run time (a test override of the limit);
+// mbar_wait_drain, for the copies and MMAs a CTA must see land before it
+// leaves, always keeps kWaitLimitCycles.
+#ifndef MLA_PIPELINE_WAIT_LIMIT
+#define MLA_PIPELINE_WAIT_LIMIT ::mla::ptx::kWaitLimitCycles
+#endif
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -54,13 +63,24 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with the given parity to complete.  Returns false if the
-// wait ran past kWaitLimitCycles or another role raised *abort.
+// wait ran past MLA_PIPELINE_WAIT_LIMIT or another role raised *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
   if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
+    if (clock64() - t0 > MLA_PIPELINE_WAIT_LIMIT) return false;
+  }
+}
+
+// Wait for async work this CTA issued (TMA copies, MMA commits) before it may
+// leave: the full limit whatever the pipeline limit is, and no abort.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
     if (clock64() - t0 > kWaitLimitCycles) return false;
   }
 }
@@ -86,7 +106,7 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, v
   while (true) {
     if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > MLA_PIPELINE_WAIT_LIMIT) return false;
   }
 }
 
@@ -99,7 +119,7 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
     __nanosleep(64);
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > MLA_PIPELINE_WAIT_LIMIT) return false;
   }
 }
 
@@ -145,7 +165,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   while (true) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > MLA_PIPELINE_WAIT_LIMIT) return false;
   }
 }
 
