@@ -348,6 +348,30 @@ mla_status mla_normal_attention(const mla_geom* geom, const mla_batch* batch, co
                                 const int32_t* seq_lens, const void* kv_exp, void* o, float* lse,
                                 mla_stream_t stream);
 
+/*
+ * Chunked-prefix Normal path (zdszero "MLA", "路径选择" (path choice), the
+ * MHA_CHUNKED_KV variant: the prefix is read, expanded and attended one chunk
+ * at a time and the chunks' states are merged by LSE, so the expanded prefix
+ * held at once is one chunk): the same o and lse as mla_normal_expand +
+ * mla_normal_attention, with the expanded rows bounded by chunk_rows rows per
+ * sequence.  Window c covers cache rows [c * chunk_rows, (c + 1) * chunk_rows)
+ * for c < ceil(max_pages * 64 / chunk_rows); per window the call expands the
+ * window's rows into kv_chunk (bf16 [H][B * chunk_rows][256], layout as
+ * kv_exp), attends to the window's visible keys, and merges the window's
+ * state into a running one ("M5.8" 0x0C merge: m = max lse, weights
+ * e^{lse - m}); the last window writes o bf16 [B,T,H,128] and lse fp32 [B,T,H].
+ * chunk_rows: a positive multiple of 128.  kv_chunk: mla_normal_chunk_bytes
+ * bytes; state: mla_normal_chunk_state_bytes bytes (fp32 running o and lse,
+ * overwritten); both 32-byte aligned, owned by the caller.  Two launches per
+ * window on the stream; validation and errors as for mla_normal_attention.
+ */
+size_t mla_normal_chunk_bytes(const mla_geom* geom, int B, int chunk_rows);
+size_t mla_normal_chunk_state_bytes(const mla_geom* geom, const mla_batch* batch);
+mla_status mla_normal_chunked(const mla_geom* geom, const mla_batch* batch, const void* q_nope, const void* q_pe,
+                              const mla_cache* cache, const int32_t* block_table, int bt_stride,
+                              const int32_t* seq_lens, const void* w_uk, const void* w_uv, int chunk_rows,
+                              void* kv_chunk, void* state, void* o, float* lse, mla_stream_t stream);
+
 /* Synchronise `stream`, then return the status word a kernel recorded in the
  * workspace (MLA_OK if none) and, if info != NULL, its detail word.  The
  * workspace-free kernels (absorption, un-absorption, the Normal arm, the gather

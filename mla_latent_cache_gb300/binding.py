@@ -82,6 +82,9 @@ def _load() -> ctypes.CDLL:
         "mla_normal_expanded_bytes": (ctypes.c_size_t, [G, I, I]),
         "mla_normal_expand": (I, [G, C, P, I, P, I, I, P, P, P, P]),
         "mla_normal_attention": (I, [G, Bt, P, P, C, P, I, P, P, P, P, P]),
+        "mla_normal_chunk_bytes": (ctypes.c_size_t, [G, I, I]),
+        "mla_normal_chunk_state_bytes": (ctypes.c_size_t, [G, Bt]),
+        "mla_normal_chunked": (I, [G, Bt, P, P, C, P, I, P, P, P, I, P, P, P, P, P]),
         "mla_read_device_status": (I, [P, ctypes.POINTER(ctypes.c_int), P]),
         "mla_status_string": (ctypes.c_char_p, [I]),
         "mla_device_sm_count": (I, []),
@@ -97,7 +100,7 @@ _lib = _load()
 EXPORTED = ("mla_workspace_size", "mla_plan", "mla_absorb_q", "mla_unabsorb_o", "mla_decode", "mla_decode_noalloc",
             "mla_sparse_workspace_size", "mla_decode_sparse",
             "mla_split_merge", "mla_normal_rows_per_seq", "mla_normal_expanded_bytes", "mla_normal_expand",
-            "mla_normal_attention",
+            "mla_normal_attention", "mla_normal_chunk_bytes", "mla_normal_chunk_state_bytes", "mla_normal_chunked",
             "mla_fp8_pack_cache", "mla_debug_gather", "mla_debug_set_wait_limit", "mla_read_device_status",
             "mla_status_string",
             "mla_device_sm_count")
@@ -252,6 +255,23 @@ def mla_normal_attention(geom, batch, q_nope, q_pe, cache: mla_cache, block_tabl
     return _lib.mla_normal_attention(ctypes.byref(geom), ctypes.byref(batch), _ptr(q_nope), _ptr(q_pe),
                                      ctypes.byref(cache), _ptr(block_table), bt_stride, _ptr(seq_lens), _ptr(kv_exp),
                                      _ptr(o), _ptr(lse), _stream(stream))
+
+
+def mla_normal_chunk_bytes(geom, B: int, chunk_rows: int) -> int:
+    return _lib.mla_normal_chunk_bytes(ctypes.byref(geom), B, chunk_rows)
+
+
+def mla_normal_chunk_state_bytes(geom, batch) -> int:
+    return _lib.mla_normal_chunk_state_bytes(ctypes.byref(geom), ctypes.byref(batch))
+
+
+def mla_normal_chunked(geom, batch, q_nope, q_pe, cache: mla_cache, block_table, bt_stride: int, seq_lens, w_uk,
+                       w_uv, chunk_rows: int, kv_chunk, state, o, lse, stream=None) -> int:
+    """The Normal path with the prefix expanded and attended chunk_rows rows at a time (LSE-merged)."""
+    return _lib.mla_normal_chunked(ctypes.byref(geom), ctypes.byref(batch), _ptr(q_nope), _ptr(q_pe),
+                                   ctypes.byref(cache), _ptr(block_table), bt_stride, _ptr(seq_lens), _ptr(w_uk),
+                                   _ptr(w_uv), int(chunk_rows), _ptr(kv_chunk), _ptr(state), _ptr(o), _ptr(lse),
+                                   _stream(stream))
 
 
 def mla_read_device_status(workspace, stream=None) -> tuple[int, int]:

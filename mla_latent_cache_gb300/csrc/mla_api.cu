@@ -352,6 +352,48 @@ mla_status mla_normal_attention(const mla_geom* geom, const mla_batch* batch, co
                                              static_cast<__nv_bfloat16*>(o), lse, (cudaStream_t)stream));
 }
 
+size_t mla_normal_chunk_bytes(const mla_geom* geom, int B, int chunk_rows) {
+  if (check_geom(geom) != MLA_OK || B < 0 || chunk_rows < 128 || chunk_rows % 128 != 0) return 0;
+  return (size_t)geom->H * (size_t)B * (size_t)chunk_rows * 256 * 2;
+}
+
+size_t mla_normal_chunk_state_bytes(const mla_geom* geom, const mla_batch* batch) {
+  if (check_geom(geom) != MLA_OK || check_batch(batch) != MLA_OK) return 0;
+  const size_t rows = (size_t)batch->B * batch->T * geom->H;
+  return align_up(rows * kDV * 4) + align_up(rows * 4);
+}
+
+mla_status mla_normal_chunked(const mla_geom* geom, const mla_batch* batch, const void* q_nope, const void* q_pe,
+                              const mla_cache* cache, const int32_t* block_table, int bt_stride,
+                              const int32_t* seq_lens, const void* w_uk, const void* w_uv, int chunk_rows,
+                              void* kv_chunk, void* state, void* o, float* lse, mla_stream_t stream) {
+  mla_status s = check_geom(geom);
+  if (s != MLA_OK) return s;
+  if ((s = check_batch(batch)) != MLA_OK) return s;
+  if (chunk_rows < 128 || chunk_rows % 128 != 0) return MLA_ERR_ARG;
+  if (batch->B == 0) return MLA_OK;
+  if (!q_nope || !q_pe || !block_table || !seq_lens || !w_uk || !w_uv || !kv_chunk || !state || !o || !lse)
+    return MLA_ERR_ARG;
+  if (bt_stride < batch->max_pages) return MLA_ERR_ARG;
+  if ((long long)batch->B * chunk_rows >= (1LL << 31) || batch->B > 65535 || (batch->T + 127) / 128 > 65535)
+    return MLA_ERR_SHAPE;
+  if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(block_table) || !aligned16(seq_lens) ||
+      !aligned16(w_uk) || !aligned16(w_uv) || !aligned32(kv_chunk) || !aligned32(state) || !aligned32(o) ||
+      !aligned16(lse))
+    return MLA_ERR_ALIGN;
+  CacheView cv;
+  if ((s = check_cache(cache, &cv)) != MLA_OK) return s;
+  const size_t rows = (size_t)batch->B * batch->T * geom->H;
+  float* st_o = static_cast<float*>(state);
+  float* st_lse = reinterpret_cast<float*>(static_cast<char*>(state) + align_up(rows * kDV * 4));
+  return cuda_status(launch_normal_chunked(geom, batch, static_cast<const __nv_bfloat16*>(q_nope),
+                                           static_cast<const __nv_bfloat16*>(q_pe), cv, block_table, bt_stride,
+                                           seq_lens, static_cast<const __nv_bfloat16*>(w_uk),
+                                           static_cast<const __nv_bfloat16*>(w_uv), chunk_rows,
+                                           static_cast<__nv_bfloat16*>(kv_chunk), st_o, st_lse,
+                                           static_cast<__nv_bfloat16*>(o), lse, (cudaStream_t)stream));
+}
+
 mla_status mla_read_device_status(const void* workspace, int* info, mla_stream_t stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MLA_ERR_CUDA;
   if (info) *info = 0;

@@ -124,6 +124,14 @@ cudaError_t launch_normal_attention(const mla_geom* g, const mla_batch* b, const
                                     const __nv_bfloat16* q_pe, const CacheView& cv, const int32_t* block_table,
                                     int bt_stride, const int32_t* seq_lens, const __nv_bfloat16* kv_exp,
                                     __nv_bfloat16* o, float* lse, cudaStream_t st);
+// The chunked-prefix Normal path over windows of chunk_rows (a multiple of 128)
+// cache rows; kv_chunk holds one window ([H][B * chunk_rows][256]), st_o / st_lse
+// the running state (fp32 [B,T,H,128] and [B,T,H]).
+cudaError_t launch_normal_chunked(const mla_geom* g, const mla_batch* bt, const __nv_bfloat16* q_nope,
+                                  const __nv_bfloat16* q_pe, const CacheView& cv, const int32_t* block_table,
+                                  int bt_stride, const int32_t* seq_lens, const __nv_bfloat16* w_uk,
+                                  const __nv_bfloat16* w_uv, int chunk_rows, __nv_bfloat16* kv_chunk, float* st_o,
+                                  float* st_lse, __nv_bfloat16* o, float* lse, cudaStream_t st);
 cudaError_t launch_debug_gather(const CacheView& cv, const int32_t* block_table, int bt_stride,
                                 const int32_t* seq_lens, int b, int path, __nv_bfloat16* out, cudaStream_t st);
 // Limit (clock cycles) of the decode kernel's pipeline waits on the current device; <= 0: the default.

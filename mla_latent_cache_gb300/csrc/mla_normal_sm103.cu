@@ -31,6 +31,7 @@
 // Every wait is bounded; a wait that runs out records MLA_ERR_TIMEOUT in the
 // status word of the workspace-free kernels, the CTA drains what it issued,
 // frees TMEM and exits.
+#include <limits.h>
 #include <math.h>
 
 #include "mla_internal.cuh"
@@ -70,7 +71,8 @@ struct ExpArgs {
   int bt_stride;
   const int32_t* seq_lens;
   int B, H, max_pages, num_blocks;
-  int rows_per_seq, tiles_per_seq;
+  int row_begin;                    // first cache row expanded (a multiple of 128)
+  int rows_per_seq, tiles_per_seq;  // expanded rows held per sequence (from row_begin), in 128-row tiles
   __nv_bfloat16* kv_exp;
   int* status;
 };
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(kExpThreads, 1)
   const int b = blockIdx.x / a.tiles_per_seq, tile = blockIdx.x % a.tiles_per_seq;
   int S = a.seq_lens[b];
   S = S < 0 ? 0 : min(S, a.max_pages * kPage);
-  const int r0 = tile * 128;
+  const int r0 = a.row_begin + tile * 128;
   if (r0 >= S) return;  // nothing of this sequence lives in the tile (uniform over the CTA)
   const int valid = min(128, S - r0);
   const int h0 = blockIdx.y * kExpHeads;
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(kExpThreads, 1)
       // The tile's two pages: all eight 64-column boxes of each present page.
       int blk[2], bytes = 0;
       for (int pg = 0; pg < 2; ++pg) {
-        const int p = 2 * tile + pg;
+        const int p = r0 / kPage + pg;
         blk[pg] = -1;
         if (p * kPage < S) {
           const int id = a.block_table[(size_t)b * a.bt_stride + p];
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(kExpThreads, 1)
     fence_proxy_async_smem();
     mbar_arrive(bar(EB_A_READY));
     const size_t rows_cap = (size_t)a.B * a.rows_per_seq;
-    const size_t grow = (size_t)b * a.rows_per_seq + r0 + row;
+    const size_t grow = (size_t)b * a.rows_per_seq + (r0 - a.row_begin) + row;
     for (int i = 0; ok && i < nh; ++i) {
       const int acc = i & 1;
       const bool w_ok = mbar_wait(bar(EB_ACC_FULL + acc), (i >> 1) & 1, abort_flag);
@@ -288,6 +290,15 @@ struct AttArgs {
   int bt_stride;
   const int32_t* seq_lens;
   int B, T, H, causal, max_pages, num_blocks, rows_per_seq;
+  // Key window [key_begin, key_end): the expanded rows of a sequence start at
+  // key_begin (a multiple of 128); keys outside the window are not attended.
+  int key_begin, key_end;
+  // Chunked prefix: merge this window's state with the running one (st_o fp32
+  // [B,T,H,128] normalised, st_lse [B,T,H]) when has_prev; write the final bf16
+  // o and lse when final_out, else the merged running state.
+  int has_prev, final_out;
+  float* st_o;
+  float* st_lse;
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
@@ -304,8 +315,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   int S = a.seq_lens[b];
   S = S < 0 ? 0 : min(S, a.max_pages * kPage);
   const int t_last = min(a.T, t0 + 128) - 1;
-  const int lim_max = visible_limit(S, a.T, t_last, a.causal);
-  const int n_tiles = (lim_max + 127) / 128;
+  const int lim_max = min(visible_limit(S, a.T, t_last, a.causal), a.key_end);
+  const int n_tiles = lim_max > a.key_begin ? (lim_max - a.key_begin + 127) / 128 : 0;
   const int n_pages = (S + kPage - 1) / kPage;
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -365,7 +376,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         if (!mbar_wait(bar(AB_EMPTY_K + st), par, abort_flag)) { fail_status(a.status, abort_flag); break; }
         int blk[2], bytes = 2 * kAttBox;
         for (int pg = 0; pg < 2; ++pg) {
-          const int p = 2 * kt + pg;
+          const int p = a.key_begin / kPage + 2 * kt + pg;
           blk[pg] = -1;
           if (p < n_pages) {
             const int id = a.block_table[(size_t)b * a.bt_stride + p];
@@ -454,7 +465,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
     const int t = t0 + row;
     const bool row_valid = t < a.T;
-    const int limit = row_valid ? visible_limit(S, a.T, t, a.causal) : 0;
+    const int limit = row_valid ? min(visible_limit(S, a.T, t, a.causal), a.key_end) : 0;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int kt = 0; kt < n_tiles; ++kt) {
@@ -467,7 +478,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(t_lane + s_col + 32 * c, s[c]);
       tmem_wait_ld();
-      const int jbase = 128 * kt;
+      const int jbase = a.key_begin + 128 * kt;
       const bool full = jbase + 128 <= limit;
       float tmax = -INFINITY;
 #pragma unroll
@@ -531,9 +542,24 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       tc_fence_after();
     }
     if (ok) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      __nv_bfloat16* dst = a.o + (((size_t)b * a.T + (row_valid ? t : 0)) * a.H + h) * kDV;
+      const size_t ri = ((size_t)b * a.T + (row_valid ? t : 0)) * a.H + h;   // output row (t, h) of sequence b
+      // This window's state (o_w = O / l, natural-log lse_w), merged with the running
+      // one: m = max(lse_p, lse_w), weights e^{lse - m} normalised to sum 1.
+      float lse_out = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      float w_cur = l > 0.f ? 1.f / l : 0.f, w_prev = 0.f;
+      if (a.has_prev && row_valid) {
+        const float lp = a.st_lse[ri];
+        const float m = fmaxf(lp, lse_out);
+        if (m == -INFINITY) {
+          w_cur = 0.f;
+        } else {
+          const float ep = expf(lp - m), ec = expf(lse_out - m), sum = ep + ec;
+          w_prev = ep / sum;
+          w_cur *= ec / sum;
+          lse_out = m + logf(sum);
+        }
+      }
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
@@ -544,18 +570,45 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
-        if (row_valid) {
+        if (!row_valid) continue;
+        if (w_prev != 0.f) {
+          const float4* prev = reinterpret_cast<const float4*>(a.st_o + ri * kDV + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 p = prev[e];
+            o[4 * e] = __float_as_uint(fmaf(__uint_as_float(o[4 * e]), w_cur, p.x * w_prev));
+            o[4 * e + 1] = __float_as_uint(fmaf(__uint_as_float(o[4 * e + 1]), w_cur, p.y * w_prev));
+            o[4 * e + 2] = __float_as_uint(fmaf(__uint_as_float(o[4 * e + 2]), w_cur, p.z * w_prev));
+            o[4 * e + 3] = __float_as_uint(fmaf(__uint_as_float(o[4 * e + 3]), w_cur, p.w * w_prev));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * w_cur);
+        }
+        if (a.final_out) {
+          __nv_bfloat16* dst = a.o + ri * kDV + 32 * c;
 #pragma unroll
           for (int e = 0; e < 32; e += 16) {
             uint32_t w[8];
-            pack_bf16x8(o + e, inv, w);
-            pack_bf16x8(o + e + 8, inv, w + 4);
-            st_global_v8(dst + 32 * c + e, w);
+            pack_bf16x8(o + e, 1.f, w);
+            pack_bf16x8(o + e + 8, 1.f, w + 4);
+            st_global_v8(dst + e, w);
+          }
+        } else {
+          float* dst = a.st_o + ri * kDV + 32 * c;
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = o[e + k];
+            st_global_v8(dst + e, w);
           }
         }
       }
-      if (row_valid)
-        a.lse[((size_t)b * a.T + t) * a.H + h] = l > 0.f ? (m_use + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (row_valid) {
+        if (a.final_out) a.lse[ri] = lse_out;
+        else a.st_lse[ri] = lse_out;
+      }
     }
   }
   tc_fence_before();
@@ -591,9 +644,10 @@ bool make_map_n(CUtensorMap* m, const void* base, int rank, const cuuint64_t* di
 
 int64_t normal_rows_per_seq(int max_pages) { return (int64_t)((max_pages + 1) / 2) * 128; }
 
-cudaError_t launch_normal_expand(const mla_geom* g, const CacheView& cv, const int32_t* block_table, int bt_stride,
-                                 const int32_t* seq_lens, int B, int max_pages, const __nv_bfloat16* w_uk,
-                                 const __nv_bfloat16* w_uv, __nv_bfloat16* kv_exp, cudaStream_t st) {
+cudaError_t launch_normal_expand_rows(const mla_geom* g, const CacheView& cv, const int32_t* block_table,
+                                      int bt_stride, const int32_t* seq_lens, int B, int max_pages, int row_begin,
+                                      int rows_per_seq, const __nv_bfloat16* w_uk, const __nv_bfloat16* w_uv,
+                                      __nv_bfloat16* kv_exp, cudaStream_t st) {
   int* status = bmm_status_ptr();
   if (!status) return cudaErrorInvalidValue;
   CUtensorMap m_ckv, m_wuk, m_wuv;
@@ -620,22 +674,31 @@ cudaError_t launch_normal_expand(const mla_geom* g, const CacheView& cv, const i
   ExpArgs a;
   a.block_table = block_table; a.bt_stride = bt_stride; a.seq_lens = seq_lens;
   a.B = B; a.H = g->H; a.max_pages = max_pages; a.num_blocks = cv.num_blocks;
-  a.rows_per_seq = (int)normal_rows_per_seq(max_pages);
-  a.tiles_per_seq = a.rows_per_seq / 128;
+  a.row_begin = row_begin;
+  a.rows_per_seq = rows_per_seq;
+  a.tiles_per_seq = rows_per_seq / 128;
   a.kv_exp = kv_exp;
   a.status = status;
   const dim3 grid((unsigned)(B * a.tiles_per_seq), (unsigned)((g->H + kExpHeads - 1) / kExpHeads));
   return launch_pdl(normal_expand_kernel, grid, dim3(kExpThreads), kExpSmemAlloc, st, m_ckv, m_wuk, m_wuv, a);
 }
 
-cudaError_t launch_normal_attention(const mla_geom* g, const mla_batch* bt, const __nv_bfloat16* q_nope,
-                                    const __nv_bfloat16* q_pe, const CacheView& cv, const int32_t* block_table,
-                                    int bt_stride, const int32_t* seq_lens, const __nv_bfloat16* kv_exp,
-                                    __nv_bfloat16* o, float* lse, cudaStream_t st) {
+cudaError_t launch_normal_expand(const mla_geom* g, const CacheView& cv, const int32_t* block_table, int bt_stride,
+                                 const int32_t* seq_lens, int B, int max_pages, const __nv_bfloat16* w_uk,
+                                 const __nv_bfloat16* w_uv, __nv_bfloat16* kv_exp, cudaStream_t st) {
+  return launch_normal_expand_rows(g, cv, block_table, bt_stride, seq_lens, B, max_pages, 0,
+                                   (int)normal_rows_per_seq(max_pages), w_uk, w_uv, kv_exp, st);
+}
+
+cudaError_t launch_normal_attention_window(const mla_geom* g, const mla_batch* bt, const __nv_bfloat16* q_nope,
+                                           const __nv_bfloat16* q_pe, const CacheView& cv, const int32_t* block_table,
+                                           int bt_stride, const int32_t* seq_lens, const __nv_bfloat16* kv_exp,
+                                           int64_t rows_per_seq, int key_begin, int key_end, int has_prev,
+                                           int final_out, float* st_o, float* st_lse, __nv_bfloat16* o, float* lse,
+                                           cudaStream_t st) {
   int* status = bmm_status_ptr();
   if (!status) return cudaErrorInvalidValue;
   const int B = bt->B, T = bt->T, H = g->H;
-  const int64_t rows_per_seq = normal_rows_per_seq(bt->max_pages);
   CUtensorMap m_qn, m_qp, m_kv, m_kpe;
   {
     const cuuint64_t dims[4] = {(cuuint64_t)kDNope, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
@@ -673,10 +736,44 @@ cudaError_t launch_normal_attention(const mla_geom* g, const mla_batch* bt, cons
   a.block_table = block_table; a.bt_stride = bt_stride; a.seq_lens = seq_lens;
   a.B = B; a.T = T; a.H = H; a.causal = bt->causal ? 1 : 0; a.max_pages = bt->max_pages;
   a.num_blocks = cv.num_blocks; a.rows_per_seq = (int)rows_per_seq;
+  a.key_begin = key_begin; a.key_end = key_end;
+  a.has_prev = has_prev; a.final_out = final_out; a.st_o = st_o; a.st_lse = st_lse;
   a.scale_log2 = g->softmax_scale * 1.4426950408889634f;
   a.o = o; a.lse = lse; a.status = status;
   const dim3 grid((unsigned)((T + 127) / 128), (unsigned)H, (unsigned)B);
   return launch_pdl(normal_attention_kernel, grid, dim3(kAttThreads), kAttSmemAlloc, st, m_qn, m_qp, m_kv, m_kpe, a);
+}
+
+cudaError_t launch_normal_attention(const mla_geom* g, const mla_batch* bt, const __nv_bfloat16* q_nope,
+                                    const __nv_bfloat16* q_pe, const CacheView& cv, const int32_t* block_table,
+                                    int bt_stride, const int32_t* seq_lens, const __nv_bfloat16* kv_exp,
+                                    __nv_bfloat16* o, float* lse, cudaStream_t st) {
+  return launch_normal_attention_window(g, bt, q_nope, q_pe, cv, block_table, bt_stride, seq_lens, kv_exp,
+                                        normal_rows_per_seq(bt->max_pages), 0, INT_MAX, 0, 1, nullptr, nullptr, o,
+                                        lse, st);
+}
+
+// The chunked-prefix Normal path: per window of chunk_rows cache rows, expand the
+// window's latents (into kv_chunk, chunk_rows rows per sequence), then attend to
+// the window's keys, merging into the running state; the last window writes o, lse.
+cudaError_t launch_normal_chunked(const mla_geom* g, const mla_batch* bt, const __nv_bfloat16* q_nope,
+                                  const __nv_bfloat16* q_pe, const CacheView& cv, const int32_t* block_table,
+                                  int bt_stride, const int32_t* seq_lens, const __nv_bfloat16* w_uk,
+                                  const __nv_bfloat16* w_uv, int chunk_rows, __nv_bfloat16* kv_chunk, float* st_o,
+                                  float* st_lse, __nv_bfloat16* o, float* lse, cudaStream_t st) {
+  const int64_t total = (int64_t)bt->max_pages * kPage;
+  const int n_chunks = (int)((total + chunk_rows - 1) / chunk_rows);
+  for (int c = 0; c < n_chunks; ++c) {
+    const int j0 = c * chunk_rows;
+    cudaError_t e = launch_normal_expand_rows(g, cv, block_table, bt_stride, seq_lens, bt->B, bt->max_pages, j0,
+                                              chunk_rows, w_uk, w_uv, kv_chunk, st);
+    if (e != cudaSuccess) return e;
+    e = launch_normal_attention_window(g, bt, q_nope, q_pe, cv, block_table, bt_stride, seq_lens, kv_chunk,
+                                       chunk_rows, j0, j0 + chunk_rows, c > 0 ? 1 : 0, c == n_chunks - 1 ? 1 : 0,
+                                       st_o, st_lse, o, lse, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace mla

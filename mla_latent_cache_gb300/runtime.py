@@ -185,12 +185,13 @@ class NormalStep:
     per-head keys and values (mla_normal_expand), then causal MHA over them
     (mla_normal_attention).  Inputs are q_nope / q_pe directly; no absorption."""
 
-    def __init__(self, w: Workload, device="cuda"):
+    def __init__(self, w: Workload, device="cuda", chunk_rows: int = 0):
         import torch
         self.torch = torch
         self.w = w
         self.device = torch.device(device)
         dev = self.device
+        self.chunk_rows = int(chunk_rows)
         self.geom = L.make_geom(w.H)
         self.batch = L.make_batch(w.B, w.T, w.causal, w.max_pages)
         self.pool = pool_to_device(torch, w, dev)
@@ -201,10 +202,19 @@ class NormalStep:
         self.q_pe = _u16_to_bf16(torch, w.q_pe, dev)
         self.w_uk = _u16_to_bf16(torch, w.w_uk, dev)
         self.w_uv = _u16_to_bf16(torch, w.w_uv, dev)
-        self.rows_per_seq = L.mla_normal_rows_per_seq(w.max_pages)
-        nbytes = L.mla_normal_expanded_bytes(self.geom, w.B, w.max_pages)
-        if nbytes == 0 and w.B > 0:
-            raise L.MlaError(L.MLA_ERR_ARG, "mla_normal_expanded_bytes")
+        if self.chunk_rows > 0:
+            # chunked prefix: one window of expanded rows plus the running fp32 state
+            self.rows_per_seq = self.chunk_rows
+            nbytes = L.mla_normal_chunk_bytes(self.geom, w.B, self.chunk_rows)
+            sbytes = L.mla_normal_chunk_state_bytes(self.geom, self.batch)
+            if nbytes == 0 or sbytes == 0:
+                raise L.MlaError(L.MLA_ERR_ARG, "mla_normal_chunk_bytes")
+            self.state = torch.empty(sbytes, dtype=torch.uint8, device=dev)
+        else:
+            self.rows_per_seq = L.mla_normal_rows_per_seq(w.max_pages)
+            nbytes = L.mla_normal_expanded_bytes(self.geom, w.B, w.max_pages)
+            if nbytes == 0 and w.B > 0:
+                raise L.MlaError(L.MLA_ERR_ARG, "mla_normal_expanded_bytes")
         self.kv_exp = torch.empty(max(1, nbytes // 2), dtype=torch.bfloat16, device=dev)
         self.o = torch.empty((w.B, w.T, w.H, 128), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((w.B, w.T, w.H), dtype=torch.float32, device=dev)
@@ -219,7 +229,15 @@ class NormalStep:
                                        self.block_table.shape[1], self.seq_lens, self.kv_exp, self.o, self.lse,
                                        stream), "mla_normal_attention")
 
+    def chunked(self, stream=None):
+        L.check(L.mla_normal_chunked(self.geom, self.batch, self.q_nope, self.q_pe, self.cache, self.block_table,
+                                     self.block_table.shape[1], self.seq_lens, self.w_uk, self.w_uv, self.chunk_rows,
+                                     self.kv_exp, self.state, self.o, self.lse, stream), "mla_normal_chunked")
+
     def step(self, stream=None):
+        if self.chunk_rows > 0:
+            self.chunked(stream)
+            return
         self.expand(stream)
         self.attention(stream)
 

@@ -138,3 +138,29 @@ def test_normal_arm_host_side(mla):
                                     0) == mla.MLA_ERR_ALIGN
     assert mla.mla_normal_attention(mla.make_geom(24), b, 0x1000, 0x2000, cache, 0x3000, 8, 0x4000, 0x5000, 0x6000,
                                     0x7000, 0) == mla.MLA_ERR_SHAPE
+
+
+def test_normal_chunked_host_side(mla):
+    g = mla.make_geom(128)
+    # one window of expanded rows per sequence, and the fp32 running state
+    assert mla.mla_normal_chunk_bytes(g, 8, 2048) == 128 * 8 * 2048 * 256 * 2
+    assert mla.mla_normal_chunk_bytes(g, 8, 200) == 0 and mla.mla_normal_chunk_bytes(g, 8, 0) == 0
+    b = mla.make_batch(2, 16, True, 8)
+    assert mla.mla_normal_chunk_state_bytes(g, b) >= 2 * 16 * 128 * (128 + 1) * 4
+    cache = mla.mla_cache(0x1000, 0x1400, 576, 64 * 576, 576, 64 * 576, 8)
+    ok = [0x10000, 0x20000, cache, 0x30000, 8, 0x40000, 0x50000, 0x60000, 256, 0x70000, 0x80000, 0x90000, 0xA0000]
+
+    def call(i=None, v=None, batch=b):
+        a = list(ok)
+        if i is not None:
+            a[i] = v
+        return mla.mla_normal_chunked(g, batch, *a, 0)
+
+    assert call(8, 200) == mla.MLA_ERR_ARG     # window not a multiple of 128
+    assert call(8, 0) == mla.MLA_ERR_ARG
+    assert call(0, None) == mla.MLA_ERR_ARG
+    assert call(10, None) == mla.MLA_ERR_ARG   # no state buffer
+    assert call(4, 4) == mla.MLA_ERR_ARG       # block-table row narrower than max_pages
+    assert call(10, 0x80010) == mla.MLA_ERR_ALIGN
+    assert call(9, 0x70010) == mla.MLA_ERR_ALIGN
+    assert call(batch=mla.make_batch(0, 16, True, 8)) == mla.MLA_OK

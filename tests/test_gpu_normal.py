@@ -115,3 +115,62 @@ def test_normal_extend_full_size_sampled_heads(mla, cuda, T):
     lse_got = st.lse.cpu().numpy()[:, :, heads]
     parity(o_got[bs], o_ref[bs], "o (sampled heads)")
     parity(lse_got[bs], lse_ref[bs], "lse (sampled heads)")
+
+
+def _oracle_chunked(w, chunk, batches=None, heads=None):
+    pool, bt = w.compact_view()
+    qn, qp, wuk, wuv = _f64(w.q_nope), _f64(w.q_pe), _f64(w.w_uk), _f64(w.w_uv)
+    if heads is not None:
+        qn, qp, wuk, wuv = qn[:, :, heads], qp[:, :, heads], wuk[heads], wuv[heads]
+    return O.normal_chunked_ref(qn, qp, _f64(pool), bt, w.seq_lens, wuk, wuv, w.causal, chunk, batches=batches)
+
+
+@pytest.mark.parametrize("H,seq_lens,T,causal,chunk", [
+    (16, [700, 1500, 0, 64], 3, True, 256),    # several windows, a ragged last window, an empty sequence
+    (128, [1000, 300], 16, True, 128),         # the smallest window; the new rows span two windows
+    (16, [600], 170, True, 512),               # two query tiles; the new rows span both windows
+    (128, [257], 1, False, 1024),              # one window longer than the sequence
+    (16, [4000, 130], 1, False, 384),          # a window not a power of two
+])
+def test_normal_chunked(mla, cuda, H, seq_lens, T, causal, chunk):
+    """The chunked-prefix Normal path against the oracle's chunked restatement (and,
+    through it, the one-shot Normal path)."""
+    import torch
+    from mla_latent_cache_gb300.runtime import NormalStep
+    w = W.custom_workload(H, seq_lens, T=T, causal=causal, seed=43)
+    st = NormalStep(w, device=cuda, chunk_rows=chunk)
+    st.o.fill_(float("nan"))
+    st.lse.fill_(float("nan"))
+    st.step()
+    torch.cuda.synchronize()
+    status, _ = mla.mla_read_device_status(None)
+    assert status == mla.MLA_OK, mla.mla_status_string(status)
+    o_ref, lse_ref = _oracle_chunked(w, chunk)
+    parity(_np(st.o), o_ref, f"chunked o (chunk {chunk})")
+    parity(st.lse.cpu().numpy(), lse_ref, f"chunked lse (chunk {chunk})")
+    one = NormalStep(w, device=cuda)
+    one.step()
+    torch.cuda.synchronize()
+    parity(_np(st.o), _np(one.o), "chunked vs one-shot o")
+
+
+@pytest.mark.parametrize("T", [16, 512])
+def test_normal_chunked_extend_full_size_sampled_heads(mla, cuda, T):
+    """The extend workload at full size through 2048-row windows (the expanded rows held
+    at once drop from the whole prefix to one window), checked on sampled heads."""
+    import torch
+    from mla_latent_cache_gb300.runtime import NormalStep
+    w = W.config_workload(5, T=T)
+    st = NormalStep(w, device=cuda, chunk_rows=2048)
+    assert st.kv_exp.numel() * 2 == w.H * w.B * 2048 * 512
+    st.step()
+    torch.cuda.synchronize()
+    status, _ = mla.mla_read_device_status(None)
+    assert status == mla.MLA_OK, mla.mla_status_string(status)
+    heads = [3, 64]
+    bs = [0, 5]
+    o_ref, lse_ref = _oracle_chunked(w, 2048, batches=bs, heads=heads)
+    o_got = _np(st.o)[:, :, heads]
+    lse_got = st.lse.cpu().numpy()[:, :, heads]
+    parity(o_got[bs], o_ref[bs], "chunked o (sampled heads)")
+    parity(lse_got[bs], lse_ref[bs], "chunked lse (sampled heads)")
