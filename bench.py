@@ -90,12 +90,13 @@ def profiled_traffic():
     return int(m_bytes.group(1)) if h.hexdigest()[:16] == m_sha.group(1) else None
 
 
-def algorithmic_bytes(w) -> dict:
-    """Bytes each kernel of the step must move at minimum (inputs read once, outputs written once)."""
+def algorithmic_bytes(w, row_bytes: int = 1152) -> dict:
+    """Bytes each kernel of the step must move at minimum (inputs read once, outputs written once);
+    row_bytes: one cached row (1152 bf16, 656 in the FP8 format)."""
     H, B, T = w.H, w.B, w.T
     rows = int(w.seq_lens.astype(np.int64).sum())
     BT = B * T
-    decode = rows * 1152 + BT * H * (512 + 64) * 2 + BT * H * 512 * 2 + BT * H * 4 + w.block_table.size * 4 + B * 4
+    decode = rows * row_bytes + BT * H * (512 + 64) * 2 + BT * H * 512 * 2 + BT * H * 4 + w.block_table.size * 4 + B * 4
     absorb = BT * H * 128 * 2 + H * 128 * 512 * 2 + BT * H * 512 * 2
     unabsorb = BT * H * 512 * 2 + H * 128 * 512 * 2 + BT * H * 128 * 2
     return {"decode": decode, "absorb": absorb, "unabsorb": unabsorb, "step": decode + absorb + unabsorb}
@@ -234,12 +235,15 @@ def _emit(line: dict):
 
 def workload_config(w, args, world: int) -> dict:
     """The workload keys both arms print (the reference arm runs a bounded sample of it)."""
-    pool_bytes = w.num_blocks * 64 * 576 * 2
-    return {"workload": w.name, "H": w.H, "B": w.B, "T": w.T, "S": int(w.seq_lens[0]),
+    fp8 = getattr(args, "cache", "bf16") == "fp8"
+    pool_bytes = w.num_blocks * 64 * (656 if fp8 else 1152)
+    extra = {"cache": "fp8 656-byte rows (E4M3 latent, 4 fp32 scales, bf16 RoPE)"} if fp8 else {}
+    return {**extra, "workload": w.name, "H": w.H, "B": w.B, "T": w.T, "S": int(w.seq_lens[0]),
             "S_total": int(np.asarray(w.seq_lens, dtype=np.int64).sum()), "page": 64, "pool_blocks": w.num_blocks,
             "parallelism": f"replicas{world}", "splits": args.splits or "auto",
             "l2": ("L2 flushed between steps (256 MB write, outside the timed events)" if pool_bytes < 2 * L2_BYTES
                    else f"inputs larger than L2: {pool_bytes / 1e6:.0f} MB latent pool vs 129 MB L2")}
+
 
 
 def run_reference(args):
@@ -295,12 +299,13 @@ def run_ours(args):
     from mla_latent_cache_gb300.runtime import DecodeStep
 
     w = W.config_workload(WORKLOADS[args.workload], T=args.T if args.workload == "extend" else None)
-    st = DecodeStep(w, device=dev, num_splits_override=args.splits)
+    st = DecodeStep(w, device=dev, num_splits_override=args.splits, cache_format=args.cache)
     stream = torch.cuda.Stream(device=dev)
-    pool_bytes = w.num_blocks * 64 * 576 * 2
+    row_bytes = 656 if args.cache == "fp8" else 1152
+    pool_bytes = w.num_blocks * 64 * row_bytes
     flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev) if pool_bytes < 2 * L2_BYTES else None
     hbm_peak, tc_peak, peak_kind = _peaks()
-    ab = algorithmic_bytes(w)
+    ab = algorithmic_bytes(w, row_bytes)
     fl = algorithmic_flops(w)
 
     # warm up eagerly once (sets kernel attributes), then capture
@@ -446,7 +451,8 @@ def run_ours(args):
     else:
         roof = {"bound": "hbm", "kernel": "mla_decode (split-KV decode + merge)", "achieved": achieved,
                 "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": profiled_traffic() if WORKLOADS[args.workload] == WORKLOAD_INDEX else None,
+                "traffic": (profiled_traffic() if WORKLOADS[args.workload] == WORKLOAD_INDEX and args.cache == "bf16"
+                            else None),
                 "algorithmic_bytes": ab["decode"], "decode_ms": dec_ms, "decode_tflops": tflops}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -727,6 +733,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS, key=WORKLOADS.get), default="uniform")
     ap.add_argument("--T", type=int, default=1, help="new rows per sequence (extend workload)")
     ap.add_argument("--splits", type=int, default=0, help="split count override (0 = the automatic plan)")
+    ap.add_argument("--cache", choices=["bf16", "fp8"], default="bf16",
+                    help="cache row format of the absorbed decode (fp8: 656-byte rows, mla_decode_fp8)")
     ap.add_argument("--chunk", type=int, default=0,
                     help="normal arm: chunked-prefix windows of this many cache rows (multiple of 128; 0 = one shot)")
     ap.add_argument("--arm", choices=["absorb", "normal"], default="absorb",

@@ -193,6 +193,22 @@ mla_status mla_decode(const mla_geom* geom, const mla_batch* batch, const void* 
                       void* workspace, size_t ws_bytes, mla_stream_t stream);
 
 /*
+ * Absorbed decode over FP8 cache rows ("M5.8" 0x0B "Exact 656-byte FP8 row";
+ * the row as mla_fp8_pack_cache writes it: 512 E4M3 latent codes, 4 fp32
+ * scales, 64 bf16 RoPE values).  The same computation and plan as mla_decode
+ * (mla_plan on the same workspace first), with cache row j's latent value c
+ * = E4M3(code_c) * scale_{c / 128}, rounded to bf16 as the tensor-core operand,
+ * and its RoPE values as stored.  cache_fp8: uint8 [num_blocks, 64, 656]
+ * (contiguous, 16-byte aligned, device); every other argument as for
+ * mla_decode.  The page's raw rows are read from HBM once (656 bytes per row,
+ * 0.57 of the bf16 row) and converted to bf16 in shared memory.
+ */
+mla_status mla_decode_fp8(const mla_geom* geom, const mla_batch* batch, const void* q_lat, const void* q_pe,
+                          const void* cache_fp8, int num_blocks, const int32_t* block_table, int bt_stride,
+                          const int32_t* seq_lens, int checked, void* o_lat, float* lse, void* workspace,
+                          size_t ws_bytes, mla_stream_t stream);
+
+/*
  * Index-driven (sparse) decode ("M5.8" 0x0B "FP8 Cache Format And Sparse
  * Selection", the sparse-indices passage: indices [B, S_q, topk] of physical
  * rows, block * 64 + offset, with topk_length [B] bounding each list's valid

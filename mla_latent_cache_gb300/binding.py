@@ -73,6 +73,7 @@ def _load() -> ctypes.CDLL:
         "mla_decode": (I, [G, Bt, P, P, C, P, I, P, I, P, P, P, ctypes.c_size_t, P]),
         "mla_decode_noalloc": (I, [G, Bt, P, P, C, P, I, P, P, P, P]),
         "mla_sparse_workspace_size": (ctypes.c_size_t, [G, Bt, I]),
+        "mla_decode_fp8": (I, [G, Bt, P, P, P, I, P, I, P, I, P, P, P, ctypes.c_size_t, P]),
         "mla_decode_sparse": (I, [G, Bt, P, P, C, P, I, P, I, P, P, P, ctypes.c_size_t, P]),
         "mla_split_merge": (I, [P, P, P, I, I, I, P, P, P]),
         "mla_debug_gather": (I, [C, P, I, P, I, I, P, P]),
@@ -98,7 +99,7 @@ def _load() -> ctypes.CDLL:
 
 _lib = _load()
 EXPORTED = ("mla_workspace_size", "mla_plan", "mla_absorb_q", "mla_unabsorb_o", "mla_decode", "mla_decode_noalloc",
-            "mla_sparse_workspace_size", "mla_decode_sparse",
+            "mla_sparse_workspace_size", "mla_decode_sparse", "mla_decode_fp8",
             "mla_split_merge", "mla_normal_rows_per_seq", "mla_normal_expanded_bytes", "mla_normal_expand",
             "mla_normal_attention", "mla_normal_chunk_bytes", "mla_normal_chunk_state_bytes", "mla_normal_chunked",
             "mla_fp8_pack_cache", "mla_debug_gather", "mla_debug_set_wait_limit", "mla_read_device_status",
@@ -200,6 +201,14 @@ def mla_decode_noalloc(geom, batch, q_lat, q_pe, cache: mla_cache, block_table, 
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def mla_decode_fp8(geom, batch, q_lat, q_pe, cache_fp8, num_blocks: int, block_table, bt_stride: int, seq_lens,
+                   checked: int, o_lat, lse, workspace, ws_bytes: int, stream=None) -> int:
+    """Decode over the FP8 cache rows (uint8 [num_blocks, 64, 656]); plan with mla_plan first."""
+    return _lib.mla_decode_fp8(ctypes.byref(geom), ctypes.byref(batch), _ptr(q_lat), _ptr(q_pe), _ptr(cache_fp8),
+                               int(num_blocks), _ptr(block_table), bt_stride, _ptr(seq_lens), int(checked),
+                               _ptr(o_lat), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream))
 
 
 def mla_sparse_workspace_size(geom, batch, topk: int) -> int:

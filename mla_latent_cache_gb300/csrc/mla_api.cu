@@ -217,6 +217,32 @@ mla_status mla_decode(const mla_geom* geom, const mla_batch* batch, const void* 
                                          seq_lens, checked, static_cast<__nv_bfloat16*>(o_lat), lse, workspace, st));
 }
 
+mla_status mla_decode_fp8(const mla_geom* geom, const mla_batch* batch, const void* q_lat, const void* q_pe,
+                          const void* cache_fp8, int num_blocks, const int32_t* block_table, int bt_stride,
+                          const int32_t* seq_lens, int checked, void* o_lat, float* lse, void* workspace,
+                          size_t ws_bytes, mla_stream_t stream) {
+  mla_status s = check_geom(geom);
+  if (s != MLA_OK) return s;
+  if ((s = check_batch(batch)) != MLA_OK) return s;
+  if (batch->B == 0) return MLA_OK;
+  if (!q_lat || !q_pe || !cache_fp8 || !block_table || !seq_lens || !o_lat || !lse || !workspace) return MLA_ERR_ARG;
+  if (num_blocks < 1 || bt_stride < batch->max_pages) return MLA_ERR_ARG;
+  if ((long long)num_blocks * kPage >= (1LL << 31)) return MLA_ERR_SHAPE;
+  if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned16(cache_fp8) || !aligned16(block_table) ||
+      !aligned16(seq_lens) || !aligned32(o_lat) || !aligned16(lse) || !aligned32(workspace))
+    return MLA_ERR_ALIGN;
+  WsLayout L;
+  if (!compute_layout(geom, batch, &L)) return MLA_ERR_SHAPE;
+  if (ws_bytes < L.total) return MLA_ERR_WORKSPACE;
+  CacheView cv{};
+  cv.num_blocks = num_blocks;
+  const Fp8Pool pool{static_cast<const unsigned char*>(cache_fp8), num_blocks};
+  return cuda_status(launch_decode_sm103(geom, batch, L, static_cast<const __nv_bfloat16*>(q_lat),
+                                         static_cast<const __nv_bfloat16*>(q_pe), cv, block_table, bt_stride,
+                                         seq_lens, checked, static_cast<__nv_bfloat16*>(o_lat), lse, workspace,
+                                         (cudaStream_t)stream, nullptr, &pool));
+}
+
 // The sparse decode as a dense one over B * S_q one-token sequences of up to topk
 // listed rows (non-causal), lengths topk_length[b] shared by sequence b's tokens.
 static bool sparse_batch(const mla_batch* batch, int topk, mla_batch* vb) {

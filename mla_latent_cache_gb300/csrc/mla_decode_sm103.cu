@@ -80,7 +80,13 @@ namespace {
 
 using namespace ptx;
 
+// Load modes of the decode kernel: bf16 pages through the block table, listed
+// rows (the sparse decode), or 656-byte FP8 rows through the block table.
+constexpr int kModeDense = 0, kModeSparse = 1, kModeFp8 = 2;
 constexpr int kThreads = 384;   // a multiple of 128 (the merge's thread groups)
+constexpr int kFp8Threads = 512;  // plus four converter warps (12..15) in the FP8 mode
+template <int kMode>
+__host__ __device__ constexpr int threads_of() { return kMode == kModeFp8 ? kFp8Threads : kThreads; }
 constexpr int kSoftmaxThreads = 256;
 constexpr int kCtaRows = 64;                   // query rows per CTA
 constexpr int kHalfRows = 32;                  // page rows loaded by each CTA
@@ -132,7 +138,12 @@ enum {
   BAR_XCH = BAR_O_FREE + 1,            // 2: the four softmax warps sharing a row range (4 warp arrivals)
   BAR_FINAL_QK = BAR_XCH + 2,
   BAR_FINAL_PV,
-  kNumBars = BAR_FINAL_PV + 1
+  // FP8 mode: the raw rows landed (TMA), for the converter warps; then BAR_FULL and
+  // BAR_RELOAD count the converters' four warp arrivals (at CTA 0 also CTA 1's, relayed).
+  BAR_RAW,                             // kStages: the page half's raw rows
+  BAR_RLRAW = BAR_RAW + kStages,       // kStages: the other half's raw codes and scales of this CTA's P V boxes
+  BAR_CONV = BAR_RLRAW + kStages,      // the four converter warps read a raw region (4 warp arrivals)
+  kNumBars = BAR_CONV + 1
 };
 static_assert(kNumBars * 8 + 16 <= 512, "barrier area");
 
@@ -427,6 +438,181 @@ __device__ __forceinline__ void sparse_reload(uint32_t stage, const CUtensorMap*
   }
 }
 
+// ---------------------------------------------------------------- FP8 656-byte rows
+// "M5.8" 0x0B "Exact 656-byte FP8 row": a cached row is 512 E4M3 latent codes,
+// 4 fp32 scales (scale t for latent values [128 t, 128 t + 128)) and 64 bf16
+// RoPE values; value = E4M3(code) * scale.  The pool is one 2-D byte array of
+// rows (block * 64 + offset, 656 bytes each).  A page half's raw rows land in
+// the upper part of a stage as three row-major regions (codes 0..255, codes
+// 256..511, scales + RoPE: 144 bytes per row); the converter warps read them
+// and rewrite the stage as the nine bf16 slots a bf16 page half fills (the
+// dequantised value rounded to bf16, the MMA operand type).  After Q K^T the
+// other half's codes of this CTA's P V boxes (two 128-byte-wide boxes) and the
+// rows' scales land in the Q K^T-only slots and are converted in place the same
+// way.  Every region of a raw stage is read by all converter threads before any
+// of them writes (an mbarrier of the four warps, bounded).
+constexpr int kFp8Row = 656;
+constexpr int kRawA = kStageBytes - kHalfRows * kFp8Row;   // codes 0..255 of the 32 rows
+constexpr int kRawB = kRawA + kHalfRows * 256;              // codes 256..511
+constexpr int kRawC = kRawB + kHalfRows * 256;              // scales (16 bytes) + RoPE (128 bytes)
+static_assert(kRawC + kHalfRows * 144 == kStageBytes && kRawA % 128 == 0 && kRawB % 128 == 0 && kRawC % 128 == 0,
+              "raw FP8 regions of a stage");
+constexpr int kRawReloadBytes = 2 * kHalfRows * 128 + kHalfRows * 16;
+
+// Rows [y, y + 32) of the FP8 pool (y < 0: a block outside the pool, read as
+// zeros) into the raw regions of a stage.
+__device__ __forceinline__ void fp8_load_half(uint32_t stage, const CUtensorMap* tm256, const CUtensorMap* tm144,
+                                              uint32_t bar, int y) {
+  mbar_arrive_expect_tx(bar, kHalfRows * kFp8Row);
+  tma_load_2d(stage + kRawA, tm256, bar, 0, y);
+  tma_load_2d(stage + kRawB, tm256, bar, 256, y);
+  tma_load_2d(stage + kRawC, tm144, bar, 512, y);
+}
+// The other half's rows [y, y + 32): codes of this CTA's P V latent columns
+// [256 m + 128 rank, +128) into Q K^T-only slot reload_slot(rank, 2 m), the 16
+// scale bytes into slot reload_slot(rank, 1).
+__device__ __forceinline__ void fp8_load_reload(uint32_t stage, const CUtensorMap* tm128, const CUtensorMap* tm16,
+                                                uint32_t bar, int y, int rank) {
+  mbar_arrive_expect_tx(bar, kRawReloadBytes);
+  for (int m = 0; m < 2; ++m)
+    tma_load_2d(stage + reload_slot(rank, 2 * m) * kSlotBytes, tm128, bar, 256 * m + 128 * rank, y);
+  tma_load_2d(stage + reload_slot(rank, 1) * kSlotBytes, tm16, bar, 512, y);
+}
+
+// Two E4M3 codes (the low byte first) to fp32, exactly: f16 holds every E4M3 value.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 c, l, u;\n\t.reg .b32 h;\n\t"
+      "cvt.u16.u32 c, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h, c;\n\t"
+      "mov.b32 {l, u}, h;\n\t"
+      "cvt.f32.f16 %0, l;\n\t"
+      "cvt.f32.f16 %1, u;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(two));
+  return make_float2(lo, hi);
+}
+// Eight codes (one 16-byte chunk's worth: words w0, w1) times `scale`, as four bf16 pairs.
+__device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, float scale) {
+  const float2 a = e4m3x2_to_float2(w0 & 0xFFFFu), b = e4m3x2_to_float2(w0 >> 16);
+  const float2 c = e4m3x2_to_float2(w1 & 0xFFFFu), d = e4m3x2_to_float2(w1 >> 16);
+  uint4 r;
+  __nv_bfloat162 h;
+  h = __floats2bfloat162_rn(a.x * scale, a.y * scale); r.x = *reinterpret_cast<uint32_t*>(&h);
+  h = __floats2bfloat162_rn(b.x * scale, b.y * scale); r.y = *reinterpret_cast<uint32_t*>(&h);
+  h = __floats2bfloat162_rn(c.x * scale, c.y * scale); r.z = *reinterpret_cast<uint32_t*>(&h);
+  h = __floats2bfloat162_rn(d.x * scale, d.y * scale); r.w = *reinterpret_cast<uint32_t*>(&h);
+  return r;
+}
+__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Converter warps (FP8 mode, warps 12..15; ctid 0..127).  Page g's own half is
+// converted as soon as its raw rows land; the reload of page g - 1 after that.
+struct Fp8Conv {
+  const Shared& sh;
+  int* hdr;
+  volatile int* abort_flag;
+  int rank, ctid, lane, nconv;
+  // All four warps have read the raw region (bounded: a warp that gave up never arrives).
+  __device__ bool regions_read() {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sh.bar(BAR_CONV));
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(sh.bar(BAR_CONV), nconv & 1, abort_flag));
+    ++nconv;
+    return ok;
+  }
+  // Own half of page g: thread (row rho, scale tile tau) writes latent columns
+  // [128 tau, +128) of row rho (slots 2 tau, 2 tau + 1) and RoPE columns [16 tau, +16).
+  __device__ bool own(int g) {
+    const int st = g % kStages;
+    if (!__all_sync(0xffffffffu, mbar_wait(sh.bar(BAR_RAW + st), (g / kStages) & 1, abort_flag))) return false;
+    const int rho = ctid >> 2, tau = ctid & 3;
+    const uint32_t stage = sh.stage(st);
+    const uint32_t src = stage + (tau < 2 ? kRawA : kRawB) + rho * 256 + 128 * (tau & 1);
+    uint4 code[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) code[c] = ld_shared_u4(src + 16 * c);
+    const float scale = ld_shared_f32(stage + kRawC + rho * 144 + 4 * tau);
+    const uint4 rope0 = ld_shared_u4(stage + kRawC + rho * 144 + 16 + 32 * tau);
+    const uint4 rope1 = ld_shared_u4(stage + kRawC + rho * 144 + 32 + 32 * tau);
+    if (!regions_read()) return false;
+    const int sw = rho & 7;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t dst = stage + (2 * tau + h) * kSlotBytes + rho * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        // chunk (8 latent values) 2c and 2c + 1 of this slot row: codes 64 h + 16 c .. + 15
+        const uint4 v = code[4 * h + c];
+        st_shared_u4(dst + 16 * ((2 * c) ^ sw), dequant8(v.x, v.y, scale));
+        st_shared_u4(dst + 16 * ((2 * c + 1) ^ sw), dequant8(v.z, v.w, scale));
+      }
+    }
+    const uint32_t rdst = stage + 8 * kSlotBytes + rho * 128;
+    st_shared_u4(rdst + 16 * ((2 * tau) ^ sw), rope0);
+    st_shared_u4(rdst + 16 * ((2 * tau + 1) ^ sw), rope1);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sh.bar(BAR_FULL + st));
+    return true;
+  }
+  // The reload of page g: thread (row rho, k) writes slot reload_slot(rank, k) row
+  // rho: latent box own_pv_box(rank, k) of the other half's row rho.
+  __device__ bool reload(int g) {
+    const int st = g % kStages;
+    if (!__all_sync(0xffffffffu, mbar_wait(sh.bar(BAR_RLRAW + st), (g / kStages) & 1, abort_flag))) return false;
+    const int rho = ctid >> 2, k = ctid & 3;
+    const int m = k >> 1, tile = own_pv_box(rank, k) >> 1;
+    const uint32_t stage = sh.stage(st);
+    const uint32_t src = stage + reload_slot(rank, 2 * m) * kSlotBytes + rho * 128 + 64 * (k & 1);
+    uint4 code[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) code[c] = ld_shared_u4(src + 16 * c);
+    const float scale = ld_shared_f32(stage + reload_slot(rank, 1) * kSlotBytes + rho * 16 + 4 * tile);
+    if (!regions_read()) return false;
+    const int sw = rho & 7;
+    const uint32_t dst = stage + reload_slot(rank, k) * kSlotBytes + rho * 128;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      st_shared_u4(dst + 16 * ((2 * c) ^ sw), dequant8(code[c].x, code[c].y, scale));
+      st_shared_u4(dst + 16 * ((2 * c + 1) ^ sw), dequant8(code[c].z, code[c].w, scale));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sh.bar(BAR_RELOAD + st));
+    return true;
+  }
+};
+
+__device__ __forceinline__ void fp8_convert_role(const Shared& sh, int* hdr, volatile int* abort_flag, const int* seg,
+                                                 SegWalk walk, int rank, int ctid) {
+  Fp8Conv cv{sh, hdr, abort_flag, rank, ctid, (int)(threadIdx.x & 31), 0};
+  int g = 0;
+  bool ok = true;
+  for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
+    const int* rec = seg + (size_t)si * kSegWords;
+    for (int p = rec[2]; p < rec[3]; ++p, ++g) {
+      if (!cv.own(g) || (g > 0 && !cv.reload(g - 1))) { ok = false; break; }
+    }
+  }
+  if (ok && g > 0 && !cv.reload(g - 1)) ok = false;
+  if (!ok && cv.lane == 0) fail(hdr, abort_flag, 40);
+}
+
 // Q K^T issuer (CTA 0, one converged warp): page t goes to score tile t % 2
 // once both CTAs' halves of the page have landed (CTA 0's load barrier also
 // counts CTA 1's, relayed) and both softmaxes have read the tile's previous
@@ -517,10 +703,14 @@ __device__ __forceinline__ void relay_role(const Shared& sh, int* hdr, volatile 
 // the slots that held this CTA's Q K^T-only latent boxes receive the other page
 // half's rows of the boxes this CTA accumulates (two 2-block boxes, L2 hits:
 // the partner CTA fetched them from HBM).
-// (Sparse decode: tm_pair is the 2-D row map, and the rows come by gather4.)
-template <bool kSparse>
-__device__ __forceinline__ void reload_role(const Shared& sh, const CUtensorMap* tm_pair, const FastArgs& a, int* hdr,
-                                            volatile int* abort_flag, const int* seg, SegWalk walk, int rank) {
+// (Sparse decode: tm_pair is the 2-D row map, and the rows come by gather4.  FP8
+// rows: the raw codes and scales, by tm_pair and tm_aux, for the converter warps.)
+template <int kMode>
+__device__ __forceinline__ void reload_role(const Shared& sh, const CUtensorMap* tm_pair, const CUtensorMap* tm_aux,
+                                            const FastArgs& a, int* hdr, volatile int* abort_flag, const int* seg,
+                                            SegWalk walk, int rank) {
+  constexpr bool kSparse = kMode == kModeSparse;
+  const int landed = kMode == kModeFp8 ? BAR_RLRAW : BAR_RELOAD;
   int gt = 0;
   bool ok = true;
   for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
@@ -540,6 +730,13 @@ __device__ __forceinline__ void reload_role(const Shared& sh, const CUtensorMap*
           fail(hdr, abort_flag, 13); ok = false; break;
         }
         sparse_reload(sh.stage(st), tm_pair, sh.bar(BAR_RELOAD + st), r, rank);
+      } else if constexpr (kMode == kModeFp8) {
+        const int blk = page_block(a, b, p, hdr, false);
+        if (!mbar_wait_sleep(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
+          fail(hdr, abort_flag, 13); ok = false; break;
+        }
+        fp8_load_reload(sh.stage(st), tm_pair, tm_aux, sh.bar(BAR_RLRAW + st),
+                        blk >= 0 ? blk * kPage + kHalfRows * (1 - rank) : -kPage, rank);
       } else {
         const int blk = page_block(a, b, p, hdr, false);
         if (!mbar_wait_sleep(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
@@ -556,19 +753,24 @@ __device__ __forceinline__ void reload_role(const Shared& sh, const CUtensorMap*
   // Drain: every reload issued must have landed before the CTA may exit.
   const int first = gt > kStages ? gt - kStages : 0;
   for (int g = first; g < gt; ++g) {
-    mbar_wait_drain(sh.bar(BAR_RELOAD + g % kStages), (g / kStages) & 1);
+    mbar_wait_drain(sh.bar(landed + g % kStages), (g / kStages) & 1);
   }
 }
 
-// kSparse: the sparse (index-driven) decode; tm_page is then the pool as a 2-D
-// array of rows (the latent part when the RoPE values are separate, tm_kpe the
-// RoPE part), tm_pair unused.
-template <bool kSparse>
-__global__ void __launch_bounds__(kThreads, 1)
+// kMode == kModeSparse: the sparse (index-driven) decode; tm_page is then the
+// pool as a 2-D array of rows (the latent part when the RoPE values are
+// separate, tm_kpe the RoPE part), tm_pair unused.  kMode == kModeFp8: the FP8
+// pool as a 2-D byte array of 656-byte rows, through boxes 256 (tm_page), 128
+// (tm_pair), 144 (tm_kpe) and 16 (tm_aux) bytes wide, 32 rows high.  tm_aux is
+// unused by the other modes.
+template <int kMode>
+__global__ void __launch_bounds__(threads_of<kMode>(), 1)
     decode_sm103_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_constant__ CUtensorMap tm_qpe,
                         const __grid_constant__ CUtensorMap tm_page, const __grid_constant__ CUtensorMap tm_pair,
-                        const __grid_constant__ CUtensorMap tm_kpe,
+                        const __grid_constant__ CUtensorMap tm_kpe, const __grid_constant__ CUtensorMap tm_aux,
                         FastArgs a, char* ws) {
+  constexpr bool kSparse = kMode == kModeSparse;
+  constexpr bool kFp8 = kMode == kModeFp8;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   int* hdr = reinterpret_cast<int*>(ws);
@@ -599,9 +801,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      // CTA 0's load barriers also count the arrival relayed from CTA 1.
-      mbar_init(sh.bar(BAR_FULL + i), rank == 0 ? 2 : 1);
-      mbar_init(sh.bar(BAR_RELOAD + i), rank == 0 ? 2 : 1);
+      // CTA 0's load barriers also count the arrival relayed from CTA 1; in the FP8
+      // mode the local arrivals are the converter warps' (one each).
+      const int local = kFp8 ? 4 : 1;
+      mbar_init(sh.bar(BAR_FULL + i), local + (rank == 0 ? 1 : 0));
+      mbar_init(sh.bar(BAR_RELOAD + i), local + (rank == 0 ? 1 : 0));
+      mbar_init(sh.bar(BAR_RAW + i), 1);
+      mbar_init(sh.bar(BAR_RLRAW + i), 1);
       mbar_init(sh.bar(BAR_QK_DONE + i), 1);
       mbar_init(sh.bar(BAR_PV_DONE + i), 1);
     }
@@ -618,13 +824,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sh.bar(BAR_O_FREE), 16);
     mbar_init(sh.bar(BAR_FINAL_QK), 1);
     mbar_init(sh.bar(BAR_FINAL_PV), 1);
+    mbar_init(sh.bar(BAR_CONV), 4);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_qlat);
     prefetch_tmap(&tm_qpe);
     prefetch_tmap(&tm_page);
     prefetch_tmap(&tm_pair);
-    if (a.kpe_separate) prefetch_tmap(&tm_kpe);
+    if (a.kpe_separate || kFp8) prefetch_tmap(&tm_kpe);
+    if (kFp8) prefetch_tmap(&tm_aux);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_addr(tmem_base_slot), kTmemCols);
@@ -704,6 +912,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // One 4-D box per page half: 32 rows x all column blocks, landing as the nine
           // 32-row x 64-column slots (streams ~8 % faster than nine 3-D boxes).
           if constexpr (kSparse) sparse_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rows, a.kpe_separate);
+          else if constexpr (kFp8)
+            fp8_load_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_RAW + st),
+                          blk >= 0 ? blk * kPage + kHalfRows * rank : -kPage);
           else load_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rank, blk, a.kpe_separate);
         }
         ++sc;
@@ -711,14 +922,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Drain: every load issued must have landed before the CTA may exit.
       const int first = gt > kStages ? gt - kStages : 0;
       for (int g = first; g < gt; ++g) {
-        mbar_wait_drain(sh.bar(BAR_FULL + g % kStages), (g / kStages) & 1);
+        mbar_wait_drain(sh.bar((kFp8 ? BAR_RAW : BAR_FULL) + g % kStages), (g / kStages) & 1);
       }
       if (q_in_flight) {
         mbar_wait_drain(sh.bar(BAR_Q_TMA), (sc - 1) & 1);
       }
     } else if (lane == 1) {
       // ------------------------------------------------------------ reloads of the other half's rows
-      reload_role<kSparse>(sh, kSparse ? &tm_page : &tm_pair, a, hdr, abort_flag, seg, walk0, rank);
+      reload_role<kMode>(sh, kSparse ? &tm_page : &tm_pair, &tm_aux, a, hdr, abort_flag, seg, walk0, rank);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -734,6 +945,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 3) {
     // idle: a warp issuing next to two softmax warps slows them (measured)
     __syncwarp();
+  } else if (kFp8 && warp >= 12) {
+    // ------------------------------------------------------------ FP8 row conversion (warps 12..15)
+    fp8_convert_role(sh, hdr, abort_flag, seg, walk0, rank, tid - 384);
   } else {
     // ------------------------------------------------------------ softmax + epilogue (warps 4..11)
     // TMEM lane ln holds query row hr = ln % 64 of this CTA and page half kh = ln / 64;
@@ -1022,7 +1236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_merge = *s_num_merge;
   if (num_merge > 0) {
     const merge::Out out{a.T, a.H, a.o_lat, a.lse};
-    merge::merge_plan_share<kThreads / 128>(out, ws, a.L, num_merge, blockIdx.x, gridDim.x,
+    merge::merge_plan_share<threads_of<kMode>() / 128>(out, ws, a.L, num_merge, blockIdx.x, gridDim.x,
                                             reinterpret_cast<float*>(smem + kSmemRing), s_merge_ok);
   }
 }
@@ -1121,6 +1335,20 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
+// A 2-D byte tensor map over the FP8 pool's rows (656 bytes each): boxes
+// box_w bytes wide and 32 rows high, no swizzle (the converters read them as rows).
+bool make_fp8_map(CUtensorMap* m, const void* base, long long rows, uint32_t box_w) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kFp8Row, (cuuint64_t)rows};
+  const cuuint64_t str[1] = {(cuuint64_t)kFp8Row};
+  const cuuint32_t box[2] = {box_w, (cuuint32_t)kHalfRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, str, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Tensor maps of the paged cache.  Page halves are 4-D boxes (64 columns, 32
 // rows, column blocks, 1 block): with the RoPE values at latent + 512 of the same
 // rows (the combined 576-wide row) the nine column blocks are one box; otherwise
@@ -1153,10 +1381,12 @@ bool set_kernel_attributes() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (!done[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(decode_sm103_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(decode_sm103_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(decode_sm103_kernel<kModeDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAlloc) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_sm103_kernel<kModeSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAlloc) != cudaSuccess ||
+        cudaFuncSetAttribute(decode_sm103_kernel<kModeFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAlloc) != cudaSuccess)
       return false;
     done[dev].store(true, std::memory_order_release);
   }
@@ -1166,10 +1396,10 @@ bool set_kernel_attributes() {
 // Launch configuration: clusters of two CTAs; with `pdl`, also programmatic
 // stream serialisation (the kernel waits for its predecessor in pdl_wait).
 void cluster_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pairs, cudaStream_t st,
-                           bool pdl) {
+                           bool pdl, int threads = kThreads) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = dim3(2 * pairs, 1, 1);
-  cfg->blockDim = dim3(kThreads, 1, 1);
+  cfg->blockDim = dim3(threads, 1, 1);
   cfg->dynamicSmemBytes = kSmemAlloc;
   cfg->stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1197,7 +1427,7 @@ int decode_sm103_pairs_per_device() {
       cudaLaunchConfig_t cfg;
       cudaLaunchAttribute attr[2];
       cluster_launch_config(&cfg, attr, 256, 0, false);
-      if (cudaOccupancyMaxActiveClusters(&n, decode_sm103_kernel<false>, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, decode_sm103_kernel<kModeDense>, &cfg) != cudaSuccess) n = 0;
     }
     if (n <= 0) {
       const int sms = mla_device_sm_count();
@@ -1212,9 +1442,10 @@ int decode_sm103_pairs_per_device() {
 cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsLayout& L,
                                 const __nv_bfloat16* q_lat, const __nv_bfloat16* q_pe, const CacheView& cv,
                                 const int32_t* block_table, int bt_stride, const int32_t* seq_lens, int checked,
-                                __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st, const SparseList* sparse) {
+                                __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st, const SparseList* sparse,
+                                const Fp8Pool* fp8) {
   const long long rows_total = (long long)b->B * b->T * g->H;
-  CUtensorMap m_qlat, m_qpe, m_page, m_pair, m_kpe;
+  CUtensorMap m_qlat, m_qpe, m_page, m_pair, m_kpe, m_aux;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)kDLat, (cuuint64_t)rows_total};
     const cuuint64_t str[1] = {(cuuint64_t)kDLat * 2};
@@ -1228,8 +1459,17 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
     if (!make_map(&m_qpe, q_pe, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   bool combined = false;
-  if (sparse == nullptr) {
+  int num_blocks = cv.num_blocks;
+  if (fp8 != nullptr) {
+    const long long rows = (long long)fp8->num_blocks * kPage;
+    num_blocks = fp8->num_blocks;
+    combined = true;
+    if (!make_fp8_map(&m_page, fp8->rows, rows, 256) || !make_fp8_map(&m_pair, fp8->rows, rows, 128) ||
+        !make_fp8_map(&m_kpe, fp8->rows, rows, 144) || !make_fp8_map(&m_aux, fp8->rows, rows, 16))
+      return cudaErrorInvalidValue;
+  } else if (sparse == nullptr) {
     if (!make_cache_maps(cv, &m_page, &m_pair, &m_kpe, &combined)) return cudaErrorInvalidValue;
+    m_aux = m_pair;
   } else {
     // The pool as one 2-D array of rows (block * 64 + offset), boxes one row high
     // (tile::gather4): the combined 576-wide row, or the latent and RoPE parts.
@@ -1247,13 +1487,14 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
       const cuuint64_t str[1] = {(cuuint64_t)cv.kpe_row * 2};
       if (!make_map(&m_kpe, cv.kpe, 2, dims, str, box)) return cudaErrorInvalidValue;
     }
+    m_aux = m_pair;
   }
   FastArgs a;
   a.q_lat = q_lat;
   a.block_table = block_table; a.bt_stride = bt_stride; a.seq_lens = seq_lens;
   a.seq_div = sparse ? sparse->seq_div : 1;
   a.B = b->B; a.T = b->T; a.H = g->H; a.causal = b->causal ? 1 : 0; a.checked = checked;
-  a.max_pages = b->max_pages; a.num_blocks = cv.num_blocks;
+  a.max_pages = b->max_pages; a.num_blocks = num_blocks;
   a.max_rows = sparse ? sparse->topk : b->max_pages * kPage;
   a.indices = sparse ? sparse->indices : nullptr;
   a.topk = sparse ? sparse->topk : 0;
@@ -1267,12 +1508,14 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
   if (pairs <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  cluster_launch_config(&cfg, attr, pairs, st, true);
+  cluster_launch_config(&cfg, attr, pairs, st, true, fp8 ? kFp8Threads : kThreads);
+  char* w = reinterpret_cast<char*>(ws);
+  if (fp8)
+    return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<kModeFp8>, m_qlat, m_qpe, m_page, m_pair, m_kpe, m_aux, a, w);
   if (sparse)
-    return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<true>, m_qlat, m_qpe, m_page, m_pair, m_kpe, a,
-                              reinterpret_cast<char*>(ws));
-  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<false>, m_qlat, m_qpe, m_page, m_pair, m_kpe, a,
-                            reinterpret_cast<char*>(ws));
+    return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<kModeSparse>, m_qlat, m_qpe, m_page, m_pair, m_kpe, m_aux, a,
+                              w);
+  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<kModeDense>, m_qlat, m_qpe, m_page, m_pair, m_kpe, m_aux, a, w);
 }
 
 cudaError_t set_pipeline_wait_limit(long long cycles) {

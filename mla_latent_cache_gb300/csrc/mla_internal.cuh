@@ -103,11 +103,16 @@ struct SparseList {
   const int32_t* indices;
   int topk, seq_div;
 };
+// The FP8 decode's cache: num_blocks x 64 rows of 656 bytes, contiguous.
+struct Fp8Pool {
+  const unsigned char* rows;
+  int num_blocks;
+};
 cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsLayout& L,
                                 const __nv_bfloat16* q_lat, const __nv_bfloat16* q_pe, const CacheView& cv,
                                 const int32_t* block_table, int bt_stride, const int32_t* seq_lens, int checked,
                                 __nv_bfloat16* o_lat, float* lse, void* ws, cudaStream_t st,
-                                const SparseList* sparse = nullptr);
+                                const SparseList* sparse = nullptr, const Fp8Pool* fp8 = nullptr);
 int decode_sm103_pairs_per_device();
 cudaError_t launch_split_merge(const float* part_o, const float* part_lse, const int32_t* indptr, int M,
                                int rows, int D, __nv_bfloat16* o, float* lse, cudaStream_t st);

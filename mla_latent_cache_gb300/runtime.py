@@ -27,8 +27,11 @@ def pool_to_device(torch, w: Workload, device):
 
 
 class DecodeStep:
+    """cache_format "fp8": the bf16 pool is packed once into 656-byte FP8 rows
+    (mla_fp8_pack_cache) and the decode reads those (mla_decode_fp8)."""
+
     def __init__(self, w: Workload, device="cuda", num_slots: int = 0, num_splits_override: int = 0,
-                 checked: bool = False, with_absorb: bool = True):
+                 checked: bool = False, with_absorb: bool = True, cache_format: str = "bf16"):
         import torch
         self.torch = torch
         self.w = w
@@ -39,6 +42,12 @@ class DecodeStep:
         dev = self.device
         self.pool = pool_to_device(torch, w, dev)
         self.cache = L.cache_from_pool(self.pool)
+        self.cache_format = cache_format
+        if cache_format == "fp8":
+            self.pool_fp8 = torch.empty((w.num_blocks, 64, 656), dtype=torch.uint8, device=dev)
+            L.check(L.mla_fp8_pack_cache(self.cache, self.pool_fp8), "mla_fp8_pack_cache")
+        elif cache_format != "bf16":
+            raise ValueError(f"cache_format {cache_format!r}")
         self.block_table = torch.from_numpy(w.block_table).to(dev)
         self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
         self.q_pe = _u16_to_bf16(torch, w.q_pe, dev)
@@ -106,6 +115,11 @@ class DecodeStep:
         L.check(L.mla_absorb_q(self.geom, self.q_nope, self.w_uk, self.q_lat, self.BT, stream), "mla_absorb_q")
 
     def decode(self, stream=None):
+        if self.cache_format == "fp8":
+            L.check(L.mla_decode_fp8(self.geom, self.batch, self.q_lat, self.q_pe, self.pool_fp8, self.w.num_blocks,
+                                     self.block_table, self.block_table.shape[1], self.seq_lens, self.checked,
+                                     self.o_lat, self.lse, self.workspace, self.ws_bytes, stream), "mla_decode_fp8")
+            return
         L.check(L.mla_decode(self.geom, self.batch, self.q_lat, self.q_pe, self.cache, self.block_table,
                              self.block_table.shape[1], self.seq_lens, self.checked, self.o_lat, self.lse,
                              self.workspace, self.ws_bytes, stream), "mla_decode")

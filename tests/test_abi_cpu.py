@@ -87,6 +87,27 @@ def test_host_validation_rejects_before_launch(mla):
     assert mla.mla_fp8_pack_cache(empty, 0x3000, 0) == mla.MLA_ERR_ARG
 
 
+def test_fp8_decode_host_side(mla):
+    g = mla.make_geom(128)
+    b = mla.make_batch(2, 1, False, 8, num_slots=4)
+    ws = mla.mla_workspace_size(g, b)
+    ok = [0x10000, 0x20000, 0x30000, 16, 0x40000, 8, 0x50000, 0, 0x60000, 0x70000, 0x80000, ws]
+
+    def call(i=None, v=None, batch=b):
+        a = list(ok)
+        if i is not None:
+            a[i] = v
+        return mla.mla_decode_fp8(g, batch, *a, 0)
+
+    assert call(2, None) == mla.MLA_ERR_ARG          # no FP8 cache
+    assert call(3, 0) == mla.MLA_ERR_ARG             # no blocks
+    assert call(5, 4) == mla.MLA_ERR_ARG             # block-table row narrower than max_pages
+    assert call(2, 0x30008) == mla.MLA_ERR_ALIGN     # the cache rows are read by TMA
+    assert call(8, 0x60010) == mla.MLA_ERR_ALIGN     # o_lat is written with 32-byte stores
+    assert call(11, ws - 1) == mla.MLA_ERR_WORKSPACE
+    assert call(batch=mla.make_batch(0, 1, False, 8, num_slots=4)) == mla.MLA_OK
+
+
 def test_sparse_decode_host_side(mla):
     g = mla.make_geom(128)
     b = mla.make_batch(4, 2, False, 1, num_slots=8)
