@@ -107,7 +107,8 @@ constexpr int kSmemP = kSmemQ + kQSmemBoxes * kQBoxBytes;
 constexpr int kSmemRing = kSmemP + kPBufs * kPBytes;
 constexpr int kSmemBar = kSmemRing + kStages * kStageBytes;
 constexpr int kSmemXchg = kSmemBar + 512;                     // float [2 buffers][4 quarters][64 rows]
-constexpr int kSmemBytes = kSmemXchg + 2048;
+constexpr int kSmemScales = kSmemXchg + 2048;                 // FP8 mode: a stage's 32 rows x 4 fp32 scales
+constexpr int kSmemBytes = kSmemScales + kStages * 512;
 constexpr int kSmemAlloc = kSmemBytes + 1024;                 // slack to align the base to 1024 B (checked)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
@@ -139,11 +140,10 @@ enum {
   BAR_FINAL_QK = BAR_XCH + 2,
   BAR_FINAL_PV,
   // FP8 mode: the raw rows landed (TMA), for the converter warps; then BAR_FULL and
-  // BAR_RELOAD count the converters' four warp arrivals (at CTA 0 also CTA 1's, relayed).
+  // BAR_RELOAD count the four converter warps' arrivals (at CTA 0 also CTA 1's, relayed).
   BAR_RAW,                             // kStages: the page half's raw rows
   BAR_RLRAW = BAR_RAW + kStages,       // kStages: the other half's raw codes and scales of this CTA's P V boxes
-  BAR_CONV = BAR_RLRAW + kStages,      // the four converter warps read a raw region (4 warp arrivals)
-  kNumBars = BAR_CONV + 1
+  kNumBars = BAR_RLRAW + kStages
 };
 static_assert(kNumBars * 8 + 16 <= 512, "barrier area");
 
@@ -442,66 +442,63 @@ __device__ __forceinline__ void sparse_reload(uint32_t stage, const CUtensorMap*
 // "M5.8" 0x0B "Exact 656-byte FP8 row": a cached row is 512 E4M3 latent codes,
 // 4 fp32 scales (scale t for latent values [128 t, 128 t + 128)) and 64 bf16
 // RoPE values; value = E4M3(code) * scale.  The pool is one 2-D byte array of
-// rows (block * 64 + offset, 656 bytes each).  A page half's raw rows land in
-// the upper part of a stage as three row-major regions (codes 0..255, codes
-// 256..511, scales + RoPE: 144 bytes per row); the converter warps read them
-// and rewrite the stage as the nine bf16 slots a bf16 page half fills (the
-// dequantised value rounded to bf16, the MMA operand type).  After Q K^T the
-// other half's codes of this CTA's P V boxes (two 128-byte-wide boxes) and the
-// rows' scales land in the Q K^T-only slots and are converted in place the same
-// way.  Every region of a raw stage is read by all converter threads before any
-// of them writes (an mbarrier of the four warps, bounded).
+// rows (block * 64 + offset, 656 bytes each).  A page half lands by TMA as:
+// codes [128 t, 128 t + 128) of the 32 rows (128 bytes per row) in slot 2 t + 1;
+// the RoPE values straight into slot 8 (a bf16 map over the rows' last 128
+// bytes, 128-byte swizzled like a bf16 page); the scales into a small ring of
+// their own.  Converter thread (row rho, tile t) reads its 128 codes from row
+// rho of slot 2 t + 1 and writes them as bf16 (the dequantised value rounded
+// to nearest, the MMA operand type) to row rho of slots 2 t and 2 t + 1: no
+// thread overwrites another's input, so no barrier is needed between them.
+// After Q K^T the other half's codes of this CTA's P V boxes land in Q K^T-only
+// slot reload_slot(rank, 2 m + 1) (m = 0, 1) and their scales in slot 8 (no
+// longer read), and are converted into reload_slot(rank, 2 m), +1 the same way.
 constexpr int kFp8Row = 656;
-constexpr int kRawA = kStageBytes - kHalfRows * kFp8Row;   // codes 0..255 of the 32 rows
-constexpr int kRawB = kRawA + kHalfRows * 256;              // codes 256..511
-constexpr int kRawC = kRawB + kHalfRows * 256;              // scales (16 bytes) + RoPE (128 bytes)
-static_assert(kRawC + kHalfRows * 144 == kStageBytes && kRawA % 128 == 0 && kRawB % 128 == 0 && kRawC % 128 == 0,
-              "raw FP8 regions of a stage");
-constexpr int kRawReloadBytes = 2 * kHalfRows * 128 + kHalfRows * 16;
+constexpr int kRawHalfBytes = kHalfRows * kFp8Row;                         // 20992
+constexpr int kRawReloadBytes = 2 * kHalfRows * 128 + kHalfRows * 16;    // 8704
+// A page is converted this many pages after its Q K^T-only slots are freed, so
+// that the reload's L2 round trip is off the converters' path.
+constexpr int kReloadLag = 2;
 
 // Rows [y, y + 32) of the FP8 pool (y < 0: a block outside the pool, read as
-// zeros) into the raw regions of a stage.
-__device__ __forceinline__ void fp8_load_half(uint32_t stage, const CUtensorMap* tm256, const CUtensorMap* tm144,
-                                              uint32_t bar, int y) {
-  mbar_arrive_expect_tx(bar, kHalfRows * kFp8Row);
-  tma_load_2d(stage + kRawA, tm256, bar, 0, y);
-  tma_load_2d(stage + kRawB, tm256, bar, 256, y);
-  tma_load_2d(stage + kRawC, tm144, bar, 512, y);
+// zeros) into a stage and its scale entry.
+__device__ __forceinline__ void fp8_load_half(uint32_t stage, uint32_t scales, const CUtensorMap* tm128,
+                                              const CUtensorMap* tm_rope, const CUtensorMap* tm16, uint32_t bar,
+                                              int y) {
+  mbar_arrive_expect_tx(bar, kRawHalfBytes);
+  for (int t = 0; t < 4; ++t) tma_load_2d(stage + (2 * t + 1) * kSlotBytes, tm128, bar, 128 * t, y);
+  tma_load_2d(stage + 8 * kSlotBytes, tm_rope, bar, 0, y);
+  tma_load_2d(scales, tm16, bar, 512, y);
 }
 // The other half's rows [y, y + 32): codes of this CTA's P V latent columns
-// [256 m + 128 rank, +128) into Q K^T-only slot reload_slot(rank, 2 m), the 16
-// scale bytes into slot reload_slot(rank, 1).
+// [256 m + 128 rank, +128) into slot reload_slot(rank, 2 m + 1), scales into slot 8.
 __device__ __forceinline__ void fp8_load_reload(uint32_t stage, const CUtensorMap* tm128, const CUtensorMap* tm16,
                                                 uint32_t bar, int y, int rank) {
   mbar_arrive_expect_tx(bar, kRawReloadBytes);
   for (int m = 0; m < 2; ++m)
-    tma_load_2d(stage + reload_slot(rank, 2 * m) * kSlotBytes, tm128, bar, 256 * m + 128 * rank, y);
-  tma_load_2d(stage + reload_slot(rank, 1) * kSlotBytes, tm16, bar, 512, y);
+    tma_load_2d(stage + reload_slot(rank, 2 * m + 1) * kSlotBytes, tm128, bar, 256 * m + 128 * rank, y);
+  tma_load_2d(stage + 8 * kSlotBytes, tm16, bar, 512, y);
 }
 
-// Two E4M3 codes (the low byte first) to fp32, exactly: f16 holds every E4M3 value.
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
-  float lo, hi;
-  asm("{\n\t.reg .b16 c, l, u;\n\t.reg .b32 h;\n\t"
-      "cvt.u16.u32 c, %2;\n\t"
+// Two E4M3 codes (the low byte first) times the tile's scale, as a bf16 pair:
+// each code is widened exactly (to f16 by the E4M3 conversion, to fp32 by a
+// mixed-precision multiply-add with 1), multiplied by the fp32 scale, and the
+// products rounded to bf16 (measured faster than building the fp32 bits with
+// integer operations).
+__device__ __forceinline__ uint32_t dequant2(uint32_t two, float scale) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c, l, u, one;\n\t.reg .b32 h;\n\t.reg .f32 a, b;\n\t"
+      "mov.b16 one, 0x3C00;\n\t"
+      "cvt.u16.u32 c, %1;\n\t"
       "cvt.rn.f16x2.e4m3x2 h, c;\n\t"
       "mov.b32 {l, u}, h;\n\t"
-      "cvt.f32.f16 %0, l;\n\t"
-      "cvt.f32.f16 %1, u;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(two));
-  return make_float2(lo, hi);
-}
-// Eight codes (one 16-byte chunk's worth: words w0, w1) times `scale`, as four bf16 pairs.
-__device__ __forceinline__ uint4 dequant8(uint32_t w0, uint32_t w1, float scale) {
-  const float2 a = e4m3x2_to_float2(w0 & 0xFFFFu), b = e4m3x2_to_float2(w0 >> 16);
-  const float2 c = e4m3x2_to_float2(w1 & 0xFFFFu), d = e4m3x2_to_float2(w1 >> 16);
-  uint4 r;
-  __nv_bfloat162 h;
-  h = __floats2bfloat162_rn(a.x * scale, a.y * scale); r.x = *reinterpret_cast<uint32_t*>(&h);
-  h = __floats2bfloat162_rn(b.x * scale, b.y * scale); r.y = *reinterpret_cast<uint32_t*>(&h);
-  h = __floats2bfloat162_rn(c.x * scale, c.y * scale); r.z = *reinterpret_cast<uint32_t*>(&h);
-  h = __floats2bfloat162_rn(d.x * scale, d.y * scale); r.w = *reinterpret_cast<uint32_t*>(&h);
+      "fma.rn.f32.f16 a, l, one, 0f00000000;\n\t"
+      "fma.rn.f32.f16 b, u, one, 0f00000000;\n\t"
+      "mul.rn.f32 a, a, %2;\n\t"
+      "mul.rn.f32 b, b, %2;\n\t"
+      "cvt.rn.bf16x2.f32 %0, b, a;\n\t}"
+      : "=r"(r)
+      : "r"(two), "f"(scale));
   return r;
 }
 __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
@@ -519,98 +516,78 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
+// 16 codes times the tile's scale, as bf16: output chunks oc and oc + 1 (8 values
+// each; oc even) of the 128-byte-swizzled slot row at row_base (row `row`).
+__device__ __forceinline__ void dequant_store16(uint4 code, float scale, uint32_t row_base, int oc, int row) {
+  const int sw = row & 7;
+  st_shared_u4(row_base + 16 * (oc ^ sw),
+               make_uint4(dequant2(code.x & 0xFFFFu, scale), dequant2(code.x >> 16, scale),
+                          dequant2(code.y & 0xFFFFu, scale), dequant2(code.y >> 16, scale)));
+  st_shared_u4(row_base + 16 * ((oc + 1) ^ sw),
+               make_uint4(dequant2(code.z & 0xFFFFu, scale), dequant2(code.z >> 16, scale),
+                          dequant2(code.w & 0xFFFFu, scale), dequant2(code.w >> 16, scale)));
+}
 
-// Converter warps (FP8 mode, warps 12..15; ctid 0..127).  Page g's own half is
-// converted as soon as its raw rows land; the reload of page g - 1 after that.
-struct Fp8Conv {
-  const Shared& sh;
-  int* hdr;
-  volatile int* abort_flag;
-  int rank, ctid, lane, nconv;
-  // All four warps have read the raw region (bounded: a warp that gave up never arrives).
-  __device__ bool regions_read() {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sh.bar(BAR_CONV));
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(sh.bar(BAR_CONV), nconv & 1, abort_flag));
-    ++nconv;
-    return ok;
-  }
-  // Own half of page g: thread (row rho, scale tile tau) writes latent columns
-  // [128 tau, +128) of row rho (slots 2 tau, 2 tau + 1) and RoPE columns [16 tau, +16).
-  __device__ bool own(int g) {
+// Converter warps (warps 12..15; t = 0..127): page g's own half as soon as its raw
+// rows land, then the reload of page g - kReloadLag.
+__device__ __forceinline__ void fp8_convert_role(const Shared& sh, int* hdr, volatile int* abort_flag, const int* seg,
+                                                 SegWalk walk, int rank, int t) {
+  const int lane = t & 31, rho = t >> 2, q = t & 3;
+  // own half: thread (rho, tile q); reload: thread (rho, m = q >> 1, half h = q & 1)
+  const int m = q >> 1, h = q & 1;
+  const int tile_rl = own_pv_box(rank, 2 * m) >> 1;
+  // Shared-memory access order: lane L takes its 16-byte chunks in a rotated order
+  // (own: chunk c ^ (L % 8); reload: (c + rot) % 4), so that any eight consecutive
+  // lanes touch eight different 16-byte bank groups in every load and store.
+  const int own_k = lane & 7;
+  const int rl_rot = (m + 2 * h + 2 * (rho & 1)) & 3;
+  auto own = [&](int g) -> bool {
     const int st = g % kStages;
     if (!__all_sync(0xffffffffu, mbar_wait(sh.bar(BAR_RAW + st), (g / kStages) & 1, abort_flag))) return false;
-    const int rho = ctid >> 2, tau = ctid & 3;
     const uint32_t stage = sh.stage(st);
-    const uint32_t src = stage + (tau < 2 ? kRawA : kRawB) + rho * 256 + 128 * (tau & 1);
+    const uint32_t src = stage + (2 * q + 1) * kSlotBytes + rho * 128;
     uint4 code[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) code[c] = ld_shared_u4(src + 16 * c);
-    const float scale = ld_shared_f32(stage + kRawC + rho * 144 + 4 * tau);
-    const uint4 rope0 = ld_shared_u4(stage + kRawC + rho * 144 + 16 + 32 * tau);
-    const uint4 rope1 = ld_shared_u4(stage + kRawC + rho * 144 + 32 + 32 * tau);
-    if (!regions_read()) return false;
-    const int sw = rho & 7;
+    for (int c = 0; c < 8; ++c) code[c] = ld_shared_u4(src + 16 * (c ^ own_k));
+    const float ts = ld_shared_f32(sh.base + kSmemScales + st * 512 + rho * 16 + 4 * q);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t dst = stage + (2 * tau + h) * kSlotBytes + rho * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        // chunk (8 latent values) 2c and 2c + 1 of this slot row: codes 64 h + 16 c .. + 15
-        const uint4 v = code[4 * h + c];
-        st_shared_u4(dst + 16 * ((2 * c) ^ sw), dequant8(v.x, v.y, scale));
-        st_shared_u4(dst + 16 * ((2 * c + 1) ^ sw), dequant8(v.z, v.w, scale));
-      }
+    for (int c = 0; c < 8; ++c) {
+      const int ci = c ^ own_k;   // codes [16 ci, 16 ci + 16) of the tile: slot 2 q + ci / 4, chunks 2 ci % 8, +1
+      dequant_store16(code[c], ts, stage + (2 * q + (ci >> 2)) * kSlotBytes + rho * 128, (2 * ci) & 7, rho);
     }
-    const uint32_t rdst = stage + 8 * kSlotBytes + rho * 128;
-    st_shared_u4(rdst + 16 * ((2 * tau) ^ sw), rope0);
-    st_shared_u4(rdst + 16 * ((2 * tau + 1) ^ sw), rope1);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(sh.bar(BAR_FULL + st));
     return true;
-  }
-  // The reload of page g: thread (row rho, k) writes slot reload_slot(rank, k) row
-  // rho: latent box own_pv_box(rank, k) of the other half's row rho.
-  __device__ bool reload(int g) {
+  };
+  auto reload = [&](int g) -> bool {
     const int st = g % kStages;
     if (!__all_sync(0xffffffffu, mbar_wait(sh.bar(BAR_RLRAW + st), (g / kStages) & 1, abort_flag))) return false;
-    const int rho = ctid >> 2, k = ctid & 3;
-    const int m = k >> 1, tile = own_pv_box(rank, k) >> 1;
     const uint32_t stage = sh.stage(st);
-    const uint32_t src = stage + reload_slot(rank, 2 * m) * kSlotBytes + rho * 128 + 64 * (k & 1);
+    const uint32_t src = stage + reload_slot(rank, 2 * m + 1) * kSlotBytes + rho * 128 + 64 * h;
     uint4 code[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) code[c] = ld_shared_u4(src + 16 * c);
-    const float scale = ld_shared_f32(stage + reload_slot(rank, 1) * kSlotBytes + rho * 16 + 4 * tile);
-    if (!regions_read()) return false;
-    const int sw = rho & 7;
-    const uint32_t dst = stage + reload_slot(rank, k) * kSlotBytes + rho * 128;
+    for (int c = 0; c < 4; ++c) code[c] = ld_shared_u4(src + 16 * ((c + rl_rot) & 3));
+    const float ts = ld_shared_f32(stage + 8 * kSlotBytes + rho * 16 + 4 * tile_rl);
+    __syncwarp();   // the lane of half 1 overwrites the raw row its half-0 neighbour reads
+    const uint32_t dst = stage + reload_slot(rank, 2 * m + h) * kSlotBytes + rho * 128;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      st_shared_u4(dst + 16 * ((2 * c) ^ sw), dequant8(code[c].x, code[c].y, scale));
-      st_shared_u4(dst + 16 * ((2 * c + 1) ^ sw), dequant8(code[c].z, code[c].w, scale));
-    }
+    for (int c = 0; c < 4; ++c) dequant_store16(code[c], ts, dst, 2 * ((c + rl_rot) & 3), rho);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(sh.bar(BAR_RELOAD + st));
     return true;
-  }
-};
-
-__device__ __forceinline__ void fp8_convert_role(const Shared& sh, int* hdr, volatile int* abort_flag, const int* seg,
-                                                 SegWalk walk, int rank, int ctid) {
-  Fp8Conv cv{sh, hdr, abort_flag, rank, ctid, (int)(threadIdx.x & 31), 0};
+  };
   int g = 0;
   bool ok = true;
   for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
     const int* rec = seg + (size_t)si * kSegWords;
     for (int p = rec[2]; p < rec[3]; ++p, ++g) {
-      if (!cv.own(g) || (g > 0 && !cv.reload(g - 1))) { ok = false; break; }
+      if (!own(g) || (g >= kReloadLag && !reload(g - kReloadLag))) { ok = false; break; }
     }
   }
-  if (ok && g > 0 && !cv.reload(g - 1)) ok = false;
-  if (!ok && cv.lane == 0) fail(hdr, abort_flag, 40);
+  for (int r = g > kReloadLag ? g - kReloadLag : 0; ok && r < g; ++r) ok = reload(r);
+  if (!ok && lane == 0) fail(hdr, abort_flag, 40);
 }
 
 // Q K^T issuer (CTA 0, one converged warp): page t goes to score tile t % 2
@@ -760,9 +737,10 @@ __device__ __forceinline__ void reload_role(const Shared& sh, const CUtensorMap*
 // kMode == kModeSparse: the sparse (index-driven) decode; tm_page is then the
 // pool as a 2-D array of rows (the latent part when the RoPE values are
 // separate, tm_kpe the RoPE part), tm_pair unused.  kMode == kModeFp8: the FP8
-// pool as a 2-D byte array of 656-byte rows, through boxes 256 (tm_page), 128
-// (tm_pair), 144 (tm_kpe) and 16 (tm_aux) bytes wide, 32 rows high.  tm_aux is
-// unused by the other modes.
+// pool as a 2-D byte array of 656-byte rows, through boxes 128 (tm_pair) and 16
+// (tm_aux) bytes wide, 32 rows high, and tm_kpe the rows' RoPE values as bf16
+// (64 x 32 boxes, 128-byte swizzled); tm_page unused.  tm_aux is unused by the
+// other modes.
 template <int kMode>
 __global__ void __launch_bounds__(threads_of<kMode>(), 1)
     decode_sm103_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_constant__ CUtensorMap tm_qpe,
@@ -824,7 +802,6 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
     mbar_init(sh.bar(BAR_O_FREE), 16);
     mbar_init(sh.bar(BAR_FINAL_QK), 1);
     mbar_init(sh.bar(BAR_FINAL_PV), 1);
-    mbar_init(sh.bar(BAR_CONV), 4);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_qlat);
@@ -913,8 +890,8 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
           // 32-row x 64-column slots (streams ~8 % faster than nine 3-D boxes).
           if constexpr (kSparse) sparse_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rows, a.kpe_separate);
           else if constexpr (kFp8)
-            fp8_load_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_RAW + st),
-                          blk >= 0 ? blk * kPage + kHalfRows * rank : -kPage);
+            fp8_load_half(sh.stage(st), sh.base + kSmemScales + st * 512, &tm_pair, &tm_kpe, &tm_aux,
+                          sh.bar(BAR_RAW + st), blk >= 0 ? blk * kPage + kHalfRows * rank : -kPage);
           else load_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rank, blk, a.kpe_separate);
         }
         ++sc;
@@ -1464,9 +1441,14 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
     const long long rows = (long long)fp8->num_blocks * kPage;
     num_blocks = fp8->num_blocks;
     combined = true;
-    if (!make_fp8_map(&m_page, fp8->rows, rows, 256) || !make_fp8_map(&m_pair, fp8->rows, rows, 128) ||
-        !make_fp8_map(&m_kpe, fp8->rows, rows, 144) || !make_fp8_map(&m_aux, fp8->rows, rows, 16))
+    if (!make_fp8_map(&m_pair, fp8->rows, rows, 128) || !make_fp8_map(&m_aux, fp8->rows, rows, 16))
       return cudaErrorInvalidValue;
+    m_page = m_pair;
+    // the RoPE values: bytes 528..655 of every row, as 64 bf16 (16-byte aligned: 528 = 33 x 16)
+    const cuuint64_t dims[2] = {(cuuint64_t)kDRope, (cuuint64_t)rows};
+    const cuuint64_t str[1] = {(cuuint64_t)kFp8Row};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kHalfRows};
+    if (!make_map(&m_kpe, fp8->rows + 528, 2, dims, str, box)) return cudaErrorInvalidValue;
   } else if (sparse == nullptr) {
     if (!make_cache_maps(cv, &m_page, &m_pair, &m_kpe, &combined)) return cudaErrorInvalidValue;
     m_aux = m_pair;
