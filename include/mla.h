@@ -181,8 +181,8 @@ mla_status mla_unabsorb_o(const mla_geom* geom, const void* o_lat, const void* w
  * "attend against the latent directly"; "M5.8" 0x05 "Paged and ragged address
  * translation" for the pages; 0x0C and "mlxcel" Stage 2 for the merge of split
  * states), using the plan in the workspace: scores s = (q_lat . c_j + q_pe . k_pe_j) * scale, softmax over the
- * visible rows j, o_lat = sum_j p_j c_j, lse = log sum_j e^{s_j}.  Launches the
- * split-KV decode kernel and, when the plan has partial segments, the merge.
+ * visible rows j, o_lat = sum_j p_j c_j, lse = log sum_j e^{s_j}.  One kernel
+ * launch: the split-KV decode, whose CTAs also merge the plan's partial segments.
  * q_lat [B,T,H,512], q_pe [B,T,H,64] bf16; o_lat [B,T,H,512] bf16; lse [B,T,H] float32.
  * checked != 0 validates every block id read, the plan stamp and T <= S_b on the
  * device (errors go to the status word; invalid pages are skipped).

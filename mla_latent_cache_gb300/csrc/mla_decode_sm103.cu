@@ -42,8 +42,8 @@
 // 36 KB), the P tiles (64 rows x 64 page rows, bf16, K-major) and the shared
 // part of the query.
 //
-// Roles (384 threads per CTA): warp 0 issues the page loads and warp 3 the
-// reloads; in CTA 0 warp 1 issues the Q K^T MMAs and warp 2 the P V MMAs (two
+// Roles (384 threads per CTA): warp 0's lane 0 issues the page loads and its
+// lane 1 the reloads; in CTA 0 warp 1 issues the Q K^T MMAs and warp 2 the P V MMAs (two
 // issuers, so that Q K^T of the next pages keeps the tensor pipe busy while
 // P V waits for the softmax); in CTA 1 warps 2 and 1 forward the arrival of
 // its page halves and of its reloads to CTA 0; warps 4..11 run the online
@@ -53,6 +53,14 @@
 // reference; only rounding differs), with scores in log2 units.  Cache rows
 // past the sequence end (last page only) are zeroed in shared memory before
 // P V so stale or NaN contents never reach the accumulator.
+//
+// Segments that are splits of their group write normalised partial states;
+// after freeing tensor memory the CTAs merge the plan's records (exact LSE
+// merge), each record once its partial rows are counted in.
+//
+// Load modes (template kMode): bf16 pages through the block table; the sparse
+// decode's listed rows (tile::gather4); FP8 656-byte rows, converted to bf16
+// in shared memory by four more warps (512 threads).
 //
 // Every wait is bounded; a wait that runs out records MLA_ERR_TIMEOUT in the
 // workspace and raises a CTA-wide abort flag.  Loads and MMAs already issued
