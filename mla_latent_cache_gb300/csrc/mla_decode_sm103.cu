@@ -59,8 +59,8 @@
 // merge), each record once its partial rows are counted in.
 //
 // Load modes (template kMode): bf16 pages through the block table; the sparse
-// decode's listed rows (tile::gather4); FP8 656-byte rows, converted to bf16
-// in shared memory by four more warps (512 threads).
+// decode's listed rows (copied by whole warps with cp.async); FP8 656-byte
+// rows, converted to bf16 in shared memory by four more warps (512 threads).
 //
 // Every wait is bounded; a wait that runs out records MLA_ERR_TIMEOUT in the
 // workspace and raises a CTA-wide abort flag.  Loads and MMAs already issued
@@ -95,7 +95,6 @@ constexpr int kThreads = 384;   // a multiple of 128 (the merge's thread groups)
 constexpr int kFp8Threads = 512;  // plus four converter warps (12..15) in the FP8 mode
 template <int kMode>
 __host__ __device__ constexpr int threads_of() { return kMode == kModeFp8 ? kFp8Threads : kThreads; }
-constexpr int kSoftmaxThreads = 256;
 constexpr int kCtaRows = 64;                   // query rows per CTA
 constexpr int kHalfRows = 32;                  // page rows loaded by each CTA
 constexpr int kBoxes = 9;                      // 8 latent boxes + 1 RoPE box per cached row
@@ -192,6 +191,9 @@ struct FastArgs {
   int max_rows;              // longest length: max_pages * 64, or the sparse decode's topk
   const int32_t* indices;    // sparse decode: physical cache rows [B, topk] (B = sequences x query tokens)
   int topk;
+  const __nv_bfloat16* ckv;  // sparse decode: the pool's rows (latent part), row stride ckv_row elements
+  const __nv_bfloat16* kpe;  // and their RoPE values, row stride kpe_row
+  long long ckv_row, kpe_row;
   int kpe_separate;          // RoPE values not at latent + 512 in the same rows: loaded by their own box
   float scale_log2;          // softmax scale times log2(e)
   __nv_bfloat16* o_lat;
@@ -393,57 +395,153 @@ __device__ __forceinline__ void pv_page_e(uint32_t o_tmem, uint64_t p_desc0, uin
 // ---------------------------------------------------------------- sparse (index-driven) loads
 // "M5.8" 0x0B: sparse indices are physical cache rows (block * 64 + offset).  A
 // sparse decode's "page" p of a (sequence, query token) is listed rows
-// 64 p .. 64 p + 63; its half for CTA r is rows 64 p + 32 r .. + 31, fetched four
-// rows at a time with tile::gather4 loads of the pool seen as one 2-D array of
-// rows, into the same 128-byte-swizzled slots as a page half.  List entries at or
-// past the list's length read as zeros (coordinate -1), and are masked and
-// zeroed like the rows past a sequence's end.
+// 64 p .. 64 p + 63; its half for CTA r is rows 64 p + 32 r .. + 31.  A whole
+// warp copies them with cp.async, 16 bytes per lane per copy, straight into the
+// 128-byte-swizzled slots a page half fills (eight lanes cover one 128-byte
+// piece of a row, so every copy instruction reads four rows' contiguous
+// pieces); list entries at or past the list's length, and rows outside the
+// pool, are zero-filled (and masked like the rows past a sequence's end).  The
+// writing warp waits for its own copies, makes them visible to the tensor
+// cores (fence.proxy.async) and then arrives on the stage's barrier.
 
-// The 32 physical rows of listed rows j0 .. j0 + 31 of (virtual) sequence b whose
-// list holds S valid entries; an entry outside the pool reads as zeros (and is
-// reported in checked mode).
-__device__ __forceinline__ void sparse_rows32(const FastArgs& a, int b, int j0, int S, int* hdr, bool report,
-                                              int (&r)[32]) {
-  const int* src = a.indices + (size_t)b * a.topk;
-  const int nrows = a.num_blocks * kPage;
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory"); }
+
+// The physical row of list entry e of (virtual) sequence b whose list holds S
+// valid entries, or -1 (past the length, or outside the pool: reported in
+// checked mode when `report`).
+__device__ __forceinline__ int sparse_row(const FastArgs& a, int b, int e, int S, int* hdr, bool report) {
+  if (e >= S) return -1;
+  const int v = __ldg(a.indices + (size_t)b * a.topk + e);
+  if (v < 0 || v >= a.num_blocks * kPage) {
+    if (report && a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | (e & 0xFFFF));
+    return -1;
+  }
+  return v;
+}
+
+// Warp-wide: the 32 rows whose physical rows the lanes hold (lane i: row i of the
+// page half, v = -1 for a zero row), latent column block box[k] (8 = the RoPE
+// values) into slot slot[k] of the stage, k < kN.
+template <int kN>
+__device__ __forceinline__ void sparse_copy(uint32_t stage, const FastArgs& a, int v, int lane, const int (&box)[kN],
+                                            const int (&slot)[kN]) {
+  const int c = lane & 7;
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    const int j = j0 + k;
-    int v = j < S ? __ldg(src + j) : -1;
-    if (j < S && (v < 0 || v >= nrows)) {
-      if (report && a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | (j & 0xFFFF));
-      v = -1;
+  for (int q = 0; q < 8; ++q) {
+    const int r = (lane >> 3) + 4 * q;
+    const int rv = __shfl_sync(0xffffffffu, v, r);
+    const bool valid = rv >= 0;
+    const __nv_bfloat16* lat = a.ckv + (valid ? (long long)rv * a.ckv_row : 0);
+    const __nv_bfloat16* rope = a.kpe + (valid ? (long long)rv * a.kpe_row : 0);
+    const uint32_t dst_row = stage + r * 128 + 16 * (c ^ (r & 7));
+#pragma unroll
+    for (int k = 0; k < kN; ++k) {
+      const __nv_bfloat16* src = (box[k] < 8 ? lat + 64 * box[k] : rope) + 8 * c;
+      cp_async16(dst_row + slot[k] * kSlotBytes, src, valid);
     }
-    r[k] = v;
   }
 }
 
-// Listed rows r[0..31] into the nine slots of a stage (all 576 columns).
-__device__ __forceinline__ void sparse_page_half(uint32_t stage, const CUtensorMap* tm_rows, const CUtensorMap* tm_kpe,
-                                                 uint32_t bar, const int (&r)[32], int kpe_separate) {
-  mbar_arrive_expect_tx(bar, kStageBytes);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int r0 = r[4 * q], r1 = r[4 * q + 1], r2 = r[4 * q + 2], r3 = r[4 * q + 3];
-    for (int s = 0; s < (kpe_separate ? 8 : kBoxes); ++s)
-      tma_gather4(stage + s * kSlotBytes + 512 * q, tm_rows, bar, 64 * s, r0, r1, r2, r3);
-    if (kpe_separate) tma_gather4(stage + 8 * kSlotBytes + 512 * q, tm_kpe, bar, 0, r0, r1, r2, r3);
-  }
+// Completion of the oldest pages a warp copied: each lane waits for its copy
+// groups but the kKeep most recent, makes them visible to the async proxy, and
+// lane 0 arrives on the barriers of the pages that completed.
+template <int kKeep>
+__device__ __forceinline__ void sparse_complete(const Shared& sh, int bar0, int& done, int issued, int lane) {
+  if (issued - done <= kKeep) return;
+  if (kKeep == 0) cp_async_wait<0>();
+  else cp_async_wait<kKeep>();
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0)
+    for (int g = done; g < issued - kKeep; ++g) mbar_arrive(sh.bar(bar0 + g % kStages));
+  __syncwarp();
+  done = issued - kKeep;
 }
 
-// The reload of a sparse page: listed rows r[0..31] (the other half's) of this
-// CTA's four P V latent boxes into the slots its Q K^T-only boxes held.
-__device__ __forceinline__ void sparse_reload(uint32_t stage, const CUtensorMap* tm_rows, uint32_t bar,
-                                              const int (&r)[32], int rank) {
-  mbar_arrive_expect_tx(bar, 4 * kSlotBytes);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int r0 = r[4 * q], r1 = r[4 * q + 1], r2 = r[4 * q + 2], r3 = r[4 * q + 3];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      tma_gather4(stage + reload_slot(rank, i) * kSlotBytes + 512 * q, tm_rows, bar, 64 * own_pv_box(rank, i), r0, r1,
-                  r2, r3);
+// Sparse mode, warp 3: the query loads (lane 0) and the page halves (all lanes).
+// A page's barrier is signalled once two later pages are in flight; at a
+// segment's end every page is completed first (the next segment's query waits
+// for the last Q K^T of this one, which needs those pages).
+__device__ __forceinline__ void sparse_gather_role(const Shared& sh, const CUtensorMap* tm_qlat,
+                                                   const CUtensorMap* tm_qpe, const FastArgs& a, int* hdr,
+                                                   volatile int* abort_flag, const int* seg, SegWalk walk, int rank,
+                                                   int R, int lane) {
+  constexpr int kInFlight = 2;
+  const int box[9] = {0, 1, 2, 3, 4, 5, 6, 7, 8};
+  int gt = 0, done = 0, sc = 0;
+  bool ok = true, q_in_flight = false;
+  for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
+    const int* rec = seg + (size_t)si * kSegWords;
+    const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3];
+    sparse_complete<0>(sh, BAR_FULL, done, gt, lane);
+    if (sc > 0 && !warp_wait(sh.bar(BAR_Q_FREE), (sc - 1) & 1, abort_flag, hdr, 10)) { ok = false; break; }
+    if (lane == 0) {
+      const int row0 = b * R + rb * kRowsPerBlock + kCtaRows * rank;
+      mbar_arrive_expect_tx(sh.bar(BAR_Q_TMA), (sc == 0 ? kBoxes : kQSmemBoxes) * kQBoxBytes);
+      if (sc == 0)
+        for (int qb = 0; qb < kQTmemBoxes; ++qb) tma_load_2d(sh.q_first(qb), tm_qlat, sh.bar(BAR_Q_TMA), 64 * qb, row0);
+      for (int qb = kQTmemBoxes; qb < 8; ++qb) tma_load_2d(sh.q(qb), tm_qlat, sh.bar(BAR_Q_TMA), 64 * qb, row0);
+      tma_load_2d(sh.q(8), tm_qpe, sh.bar(BAR_Q_TMA), 0, row0);
+    }
+    __syncwarp();
+    q_in_flight = true;
+    int S = a.seq_lens[b / a.seq_div];
+    S = S < 0 ? 0 : min(S, a.max_rows);
+    for (int p = p0; ok && p < p1; ++p, ++gt) {
+      const int v = sparse_row(a, b, p * kPage + kHalfRows * rank + lane, S, hdr, true);
+      const int st = gt % kStages;
+      if (gt >= kStages && !warp_wait(sh.bar(BAR_PV_DONE + st), ((gt / kStages) - 1) & 1, abort_flag, hdr, 11)) {
+        ok = false; break;
+      }
+      if (gt >= kQStageFirst && gt < kStages && !warp_wait(sh.bar(BAR_Q_COPIED), 0, abort_flag, hdr, 15)) {
+        ok = false; break;
+      }
+      sparse_copy<9>(sh.stage(st), a, v, lane, box, box);
+      cp_async_commit();
+      sparse_complete<kInFlight>(sh, BAR_FULL, done, gt + 1, lane);
+    }
+    ++sc;
   }
+  // Drain: every copy must have landed before the CTA may exit (signalled too
+  // when nothing failed), and the last query load.
+  if (ok) sparse_complete<0>(sh, BAR_FULL, done, gt, lane);
+  else cp_async_wait<0>();
+  if (q_in_flight && lane == 0) mbar_wait_drain(sh.bar(BAR_Q_TMA), (sc - 1) & 1);
+  __syncwarp();
+}
+
+// Sparse mode, warp 0: the other half's rows of this CTA's P V boxes, once Q K^T
+// is done with the page; a page's reload is signalled once the next one is in
+// flight, and at a segment's end at once (the softmax waits for it there).
+__device__ __forceinline__ void sparse_reload_role(const Shared& sh, const FastArgs& a, int* hdr,
+                                                   volatile int* abort_flag, const int* seg, SegWalk walk, int rank,
+                                                   int lane) {
+  const int box[4] = {own_pv_box(rank, 0), own_pv_box(rank, 1), own_pv_box(rank, 2), own_pv_box(rank, 3)};
+  const int slot[4] = {reload_slot(rank, 0), reload_slot(rank, 1), reload_slot(rank, 2), reload_slot(rank, 3)};
+  int gt = 0, done = 0;
+  bool ok = true;
+  for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
+    const int* rec = seg + (size_t)si * kSegWords;
+    const int b = rec[0];
+    int S = a.seq_lens[b / a.seq_div];
+    S = S < 0 ? 0 : min(S, a.max_rows);
+    for (int p = rec[2]; ok && p < rec[3]; ++p, ++gt) {
+      const int v = sparse_row(a, b, p * kPage + kHalfRows * (1 - rank) + lane, S, hdr, false);
+      const int st = gt % kStages;
+      if (!warp_wait(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag, hdr, 13)) { ok = false; break; }
+      sparse_copy<4>(sh.stage(st), a, v, lane, box, slot);
+      cp_async_commit();
+      sparse_complete<1>(sh, BAR_RELOAD, done, gt + 1, lane);
+    }
+    if (ok) sparse_complete<0>(sh, BAR_RELOAD, done, gt, lane);
+  }
+  if (!ok) cp_async_wait<0>();
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------- FP8 656-byte rows
@@ -688,34 +786,21 @@ __device__ __forceinline__ void relay_role(const Shared& sh, int* hdr, volatile 
 // the slots that held this CTA's Q K^T-only latent boxes receive the other page
 // half's rows of the boxes this CTA accumulates (two 2-block boxes, L2 hits:
 // the partner CTA fetched them from HBM).
-// (Sparse decode: tm_pair is the 2-D row map, and the rows come by gather4.  FP8
-// rows: the raw codes and scales, by tm_pair and tm_aux, for the converter warps.)
+// (FP8 rows: the raw codes and scales, by tm_pair and tm_aux, for the converter
+// warps.  The sparse decode reloads with a whole warp: sparse_reload_role.)
 template <int kMode>
 __device__ __forceinline__ void reload_role(const Shared& sh, const CUtensorMap* tm_pair, const CUtensorMap* tm_aux,
                                             const FastArgs& a, int* hdr, volatile int* abort_flag, const int* seg,
                                             SegWalk walk, int rank) {
-  constexpr bool kSparse = kMode == kModeSparse;
   const int landed = kMode == kModeFp8 ? BAR_RLRAW : BAR_RELOAD;
   int gt = 0;
   bool ok = true;
   for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
     const int* rec = seg + (size_t)si * kSegWords;
     const int b = rec[0];
-    int S = 0;
-    if constexpr (kSparse) {
-      S = a.seq_lens[b / a.seq_div];
-      S = S < 0 ? 0 : min(S, a.max_rows);
-    }
     for (int p = rec[2]; ok && p < rec[3]; ++p, ++gt) {
       const int st = gt % kStages;
-      if constexpr (kSparse) {
-        int r[32];
-        sparse_rows32(a, b, p * kPage + kHalfRows * (1 - rank), S, hdr, false, r);
-        if (!mbar_wait_sleep(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
-          fail(hdr, abort_flag, 13); ok = false; break;
-        }
-        sparse_reload(sh.stage(st), tm_pair, sh.bar(BAR_RELOAD + st), r, rank);
-      } else if constexpr (kMode == kModeFp8) {
+      if constexpr (kMode == kModeFp8) {
         const int blk = page_block(a, b, p, hdr, false);
         if (!mbar_wait_sleep(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag)) {
           fail(hdr, abort_flag, 13); ok = false; break;
@@ -856,7 +941,13 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
     }
   }
 
-  if (warp == 0) {
+  if (kSparse && warp == 0) {
+    // ------------------------------------------------------------ sparse: the other half's rows (whole warp)
+    sparse_reload_role(sh, a, hdr, abort_flag, seg, walk0, rank, lane);
+  } else if (kSparse && warp == 3) {
+    // ------------------------------------------------------------ sparse: query and listed rows (whole warp)
+    sparse_gather_role(sh, &tm_qlat, &tm_qpe, a, hdr, abort_flag, seg, walk0, rank, R, lane);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ page-half and query loads
     if (lane == 0) {
       SegWalk walk = walk0;
@@ -877,16 +968,8 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
         for (int box = kQTmemBoxes; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_TMA), 64 * box, row0);
         tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_TMA), 0, row0);
         q_in_flight = true;
-        int S_sparse = 0;
-        if constexpr (kSparse) {
-          S_sparse = a.seq_lens[b / a.seq_div];
-          S_sparse = S_sparse < 0 ? 0 : min(S_sparse, a.max_rows);
-        }
         for (int p = p0; ok && p < p1; ++p, ++gt) {
-          int blk = 0;
-          int rows[32];
-          if constexpr (kSparse) sparse_rows32(a, b, p * kPage + kHalfRows * rank, S_sparse, hdr, true, rows);
-          else blk = page_block(a, b, p, hdr, true);
+          const int blk = page_block(a, b, p, hdr, true);
           const int st = gt % kStages;
           if (gt >= kStages && !mbar_wait_sleep(sh.bar(BAR_PV_DONE + st), ((gt / kStages) - 1) & 1, abort_flag)) {
             fail(hdr, abort_flag, 11); ok = false; break;
@@ -896,8 +979,7 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
           }
           // One 4-D box per page half: 32 rows x all column blocks, landing as the nine
           // 32-row x 64-column slots (streams ~8 % faster than nine 3-D boxes).
-          if constexpr (kSparse) sparse_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rows, a.kpe_separate);
-          else if constexpr (kFp8)
+          if constexpr (kFp8)
             fp8_load_half(sh.stage(st), sh.base + kSmemScales + st * 512, &tm_pair, &tm_kpe, &tm_aux,
                           sh.bar(BAR_RAW + st), blk >= 0 ? blk * kPage + kHalfRows * rank : -kPage);
           else load_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rank, blk, a.kpe_separate);
@@ -914,7 +996,7 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
       }
     } else if (lane == 1) {
       // ------------------------------------------------------------ reloads of the other half's rows
-      reload_role<kMode>(sh, kSparse ? &tm_page : &tm_pair, &tm_aux, a, hdr, abort_flag, seg, walk0, rank);
+      reload_role<kMode>(sh, &tm_pair, &tm_aux, a, hdr, abort_flag, seg, walk0, rank);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -1461,23 +1543,9 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
     if (!make_cache_maps(cv, &m_page, &m_pair, &m_kpe, &combined)) return cudaErrorInvalidValue;
     m_aux = m_pair;
   } else {
-    // The pool as one 2-D array of rows (block * 64 + offset), boxes one row high
-    // (tile::gather4): the combined 576-wide row, or the latent and RoPE parts.
-    combined = cv.kpe == cv.ckv + kDLat && cv.kpe_row == cv.ckv_row && cv.kpe_block == cv.ckv_block;
-    const cuuint64_t rows = (cuuint64_t)cv.num_blocks * kPage;
-    const cuuint32_t box[2] = {64, 1};
-    {
-      const cuuint64_t dims[2] = {(cuuint64_t)(combined ? kDK : kDLat), rows};
-      const cuuint64_t str[1] = {(cuuint64_t)cv.ckv_row * 2};
-      if (!make_map(&m_page, cv.ckv, 2, dims, str, box)) return cudaErrorInvalidValue;
-      m_pair = m_page;
-    }
-    {
-      const cuuint64_t dims[2] = {(cuuint64_t)kDRope, rows};
-      const cuuint64_t str[1] = {(cuuint64_t)cv.kpe_row * 2};
-      if (!make_map(&m_kpe, cv.kpe, 2, dims, str, box)) return cudaErrorInvalidValue;
-    }
-    m_aux = m_pair;
+    // The sparse decode copies the listed rows with plain (cp.async) copies: no
+    // cache maps (the kernel prefetches and never uses these).
+    m_page = m_pair = m_kpe = m_aux = m_qlat;
   }
   FastArgs a;
   a.q_lat = q_lat;
@@ -1489,6 +1557,7 @@ cudaError_t launch_decode_sm103(const mla_geom* g, const mla_batch* b, const WsL
   a.indices = sparse ? sparse->indices : nullptr;
   a.topk = sparse ? sparse->topk : 0;
   a.kpe_separate = combined ? 0 : 1;
+  a.ckv = cv.ckv; a.kpe = cv.kpe; a.ckv_row = cv.ckv_row; a.kpe_row = cv.kpe_row;
   a.scale_log2 = g->softmax_scale * 1.4426950408889634f;
   a.o_lat = o_lat; a.lse = lse; a.L = L;
   if (!set_kernel_attributes()) return cudaErrorInvalidValue;

@@ -195,18 +195,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
-// Four rows of a 2-D tensor map (row coordinates r0..r3, any order, out-of-range
-// rows read as zeros) at column x: the box is one row high, so four box rows of
-// 128 bytes land at dst, dst + 128, dst + 256, dst + 384 (128-byte swizzled by
-// their shared-memory address like any tile load).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int x, int r0, int r1,
-                                            int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
-      "%5, %6, %7}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-      : "memory");
-}
 // Prefetch a contiguous global range (multiple of 16 bytes) into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* gptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gptr)), "r"(bytes)
