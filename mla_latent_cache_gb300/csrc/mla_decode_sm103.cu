@@ -471,7 +471,12 @@ __device__ __forceinline__ void sparse_gather_role(const Shared& sh, const CUten
                                                    const CUtensorMap* tm_qpe, const FastArgs& a, int* hdr,
                                                    volatile int* abort_flag, const int* seg, SegWalk walk, int rank,
                                                    int R, int lane) {
+  // A page's barrier is signalled once kInFlight later pages are issued.  Issuing
+  // page g waits for P V of page g - kStages, which needs the reload of that page,
+  // which the reload warp signals after Q K^T of the next page, which needs page
+  // g - kStages + 1's barrier: so kInFlight <= kStages - 2.
   constexpr int kInFlight = 2;
+  static_assert(kInFlight <= kStages - 2, "the gather must signal a page before it waits for that page's P V");
   const int box[9] = {0, 1, 2, 3, 4, 5, 6, 7, 8};
   int gt = 0, done = 0, sc = 0;
   bool ok = true, q_in_flight = false;
@@ -492,8 +497,16 @@ __device__ __forceinline__ void sparse_gather_role(const Shared& sh, const CUten
     q_in_flight = true;
     int S = a.seq_lens[b / a.seq_div];
     S = S < 0 ? 0 : min(S, a.max_rows);
+    // the list entries of the next two pages are loaded ahead (a dependent load
+    // at the head of every page otherwise paces the warp)
+    int v_next[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      v_next[k] = p0 + k < p1 ? sparse_row(a, b, (p0 + k) * kPage + kHalfRows * rank + lane, S, hdr, true) : -1;
     for (int p = p0; ok && p < p1; ++p, ++gt) {
-      const int v = sparse_row(a, b, p * kPage + kHalfRows * rank + lane, S, hdr, true);
+      const int v = v_next[0];
+      v_next[0] = v_next[1];
+      v_next[1] = p + 2 < p1 ? sparse_row(a, b, (p + 2) * kPage + kHalfRows * rank + lane, S, hdr, true) : -1;
       const int st = gt % kStages;
       if (gt >= kStages && !warp_wait(sh.bar(BAR_PV_DONE + st), ((gt / kStages) - 1) & 1, abort_flag, hdr, 11)) {
         ok = false; break;
@@ -530,8 +543,11 @@ __device__ __forceinline__ void sparse_reload_role(const Shared& sh, const FastA
     const int b = rec[0];
     int S = a.seq_lens[b / a.seq_div];
     S = S < 0 ? 0 : min(S, a.max_rows);
-    for (int p = rec[2]; ok && p < rec[3]; ++p, ++gt) {
-      const int v = sparse_row(a, b, p * kPage + kHalfRows * (1 - rank) + lane, S, hdr, false);
+    const int p1 = rec[3];
+    int v_next = rec[2] < p1 ? sparse_row(a, b, rec[2] * kPage + kHalfRows * (1 - rank) + lane, S, hdr, false) : -1;
+    for (int p = rec[2]; ok && p < p1; ++p, ++gt) {
+      const int v = v_next;
+      v_next = p + 1 < p1 ? sparse_row(a, b, (p + 1) * kPage + kHalfRows * (1 - rank) + lane, S, hdr, false) : -1;
       const int st = gt % kStages;
       if (!warp_wait(sh.bar(BAR_QK_DONE + st), (gt / kStages) & 1, abort_flag, hdr, 13)) { ok = false; break; }
       sparse_copy<4>(sh.stage(st), a, v, lane, box, slot);
