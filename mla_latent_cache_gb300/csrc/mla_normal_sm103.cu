@@ -22,9 +22,11 @@
 // Attention kernel.  A CTA takes up to 128 query tokens of one (sequence,
 // head) and walks the visible keys 128 at a time: S = Q K^T (M=128 tokens,
 // N=128 keys, K=192: two k_nope boxes from kv_exp and the two pages' k_pe
-// from the cache), online softmax with one thread per token row (lazy
-// rescale of the TMEM accumulator when the row maximum grows by more than
-// 2^8), P written over the score tile in TMEM (bf16 pairs), then O += P V
+// from the cache), online softmax with two threads per token row (each half
+// of the tile's keys and of the value columns; the row maximum and sum combined
+// through shared memory), lazy rescale of the TMEM accumulator when the row
+// maximum grows by more than 2^8, P written over the score tile in TMEM (bf16
+// pairs), then O += P V
 // (M=128, N=128, K=128 keys, A from TMEM).  Score tiles are double-buffered
 // so Q K^T of the next key tile runs while the softmax reads the current one.
 //
@@ -257,14 +259,15 @@ __global__ void __launch_bounds__(kExpThreads, 1)
 }
 
 // ----------------------------------------------------------------------------- attention
-constexpr int kAttThreads = 256;       // warp 0 TMA, 1 Q K^T, 2 P V, 3 idle, 4..7 softmax
+constexpr int kAttThreads = 384;       // warp 0 TMA, 1 Q K^T, 2 P V, 3 idle, 4..11 softmax (two per row)
 constexpr int kAttBox = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16
 constexpr int kAttStageK = 3 * kAttBox;  // k_nope (2 boxes) + k_pe (2 pages)
 constexpr int kAttStage = kAttStageK + 2 * kAttBox;  // + v (2 boxes)
 constexpr int kAttSmemQ = 0;                         // q_nope (2 boxes) + q_pe
 constexpr int kAttSmemRing = 3 * kAttBox;            // 49152
 constexpr int kAttSmemBar = kAttSmemRing + 2 * kAttStage;  // 212992
-constexpr int kAttSmemBytes = kAttSmemBar + 256;
+constexpr int kAttSmemXch = kAttSmemBar + 256;            // float [2 buffers][2 halves][128 rows]
+constexpr int kAttSmemBytes = kAttSmemXch + 2048;
 constexpr int kAttSmemAlloc = kAttSmemBytes + 1024;
 static_assert(kAttSmemAlloc <= 232448, "shared memory per CTA");
 constexpr uint32_t kAttTmemO = 0;    // 128 columns
@@ -282,6 +285,7 @@ enum {
   AB_P_EMPTY = AB_P_FULL + 2,  // 2
   AB_FINAL = AB_P_EMPTY + 2,
   AB_FINAL_PV,
+  AB_XCH,                     // the softmax warps exchanged a row value (8 warp arrivals)
   kAttBars
 };
 
@@ -340,11 +344,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       mbar_init(bar(AB_FULL_V + i), 1);
       mbar_init(bar(AB_EMPTY_V + i), 1);
       mbar_init(bar(AB_S_FULL + i), 1);
-      mbar_init(bar(AB_P_FULL + i), 128);
+      mbar_init(bar(AB_P_FULL + i), 256);
       mbar_init(bar(AB_P_EMPTY + i), 1);
     }
     mbar_init(bar(AB_FINAL), 1);
     mbar_init(bar(AB_FINAL_PV), 1);
+    mbar_init(bar(AB_XCH), 8);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_qn);
@@ -459,13 +464,31 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // Softmax + epilogue: one query token per thread (TMEM lane).
-    const int q4 = warp & 3;
+    // Softmax + epilogue: two threads per query token (TMEM lane): warps w and w + 4
+    // share lanes 32 (w % 4) .. + 31; half hf takes key columns [64 hf, +64) of
+    // each score tile and value columns [64 hf, +64) of the accumulator.  The two
+    // halves of a row combine their maximum (per tile) and sum (at the end)
+    // through shared memory.
+    const int q4 = warp & 3, hf = (warp - 4) >> 2;
     const int row = 32 * q4 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(32 * q4) << 16);
     const int t = t0 + row;
     const bool row_valid = t < a.T;
     const int limit = row_valid ? min(visible_limit(S, a.T, t, a.causal), a.key_end) : 0;
+    float* xch = reinterpret_cast<float*>(smem + kAttSmemXch);
+    int xc = 0;
+    // Both halves' value of this row (double-buffered by phase parity: a half can
+    // refill a buffer only after the other passed the next exchange).
+    auto exchange = [&](float v, float* other) -> bool {
+      float* buf = xch + (xc & 1) * 256;
+      buf[hf * 128 + row] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(AB_XCH));
+      const bool w = mbar_wait(bar(AB_XCH), xc & 1, abort_flag);
+      *other = buf[(1 - hf) * 128 + row];
+      ++xc;
+      return __all_sync(0xffffffffu, w);
+    };
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int kt = 0; kt < n_tiles; ++kt) {
@@ -474,19 +497,24 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       bool w_ok = mbar_wait(bar(AB_S_FULL + st), (kt >> 1) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, w_ok)) { fail_status(a.status, abort_flag); ok = false; break; }
       tc_fence_after();
-      uint32_t s[4][32];
+      uint32_t s2[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(t_lane + s_col + 32 * c, s[c]);
+      for (int c = 0; c < 2; ++c) tmem_ld32(t_lane + s_col + 64 * hf + 32 * c, s2[c]);
       tmem_wait_ld();
-      const int jbase = a.key_begin + 128 * kt;
-      const bool full = jbase + 128 <= limit;
+      const int jbase = a.key_begin + 128 * kt + 64 * hf;
+      const bool full = jbase + 64 <= limit;
       float tmax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (full || jbase + 32 * c + j < limit) tmax = fmaxf(tmax, __uint_as_float(s[c][j]));
-      tmax *= a.scale_log2;
+          if (full || jbase + 32 * c + j < limit) tmax = fmaxf(tmax, __uint_as_float(s2[c][j]));
+      {
+        // (both halves have read their scores once this returns: P may overwrite them)
+        float other;
+        if (!exchange(tmax, &other)) { fail_status(a.status, abort_flag); ok = false; break; }
+        tmax = fmaxf(tmax, other) * a.scale_log2;
+      }
       const bool grow = tmax > m_ref + kAttRescale;
       const float new_ref = grow ? tmax : m_ref;
       const float factor = (grow && m_ref != -INFINITY) ? ex2(m_ref - new_ref) : 1.f;
@@ -497,13 +525,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         if (!__all_sync(0xffffffffu, w_ok)) { fail_status(a.status, abort_flag); ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          tmem_ld32(t_lane + kAttTmemO + 32 * c, o);
+          tmem_ld32(t_lane + kAttTmemO + 64 * hf + 32 * c, o);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-          tmem_st32(t_lane + kAttTmemO + 32 * c, o);
+          tmem_st32(t_lane + kAttTmemO + 64 * hf + 32 * c, o);
         }
         tmem_wait_st();
       }
@@ -512,13 +540,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       float psum = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t pw[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int j = jbase + 32 * c + 2 * e;
-          float x0 = ex2(fmaf(__uint_as_float(s[c][2 * e]), a.scale_log2, -m_use));
-          float x1 = ex2(fmaf(__uint_as_float(s[c][2 * e + 1]), a.scale_log2, -m_use));
+          float x0 = ex2(fmaf(__uint_as_float(s2[c][2 * e]), a.scale_log2, -m_use));
+          float x1 = ex2(fmaf(__uint_as_float(s2[c][2 * e + 1]), a.scale_log2, -m_use));
           if (!full) {
             x0 = j < limit ? x0 : 0.f;
             x1 = j + 1 < limit ? x1 : 0.f;
@@ -527,12 +555,18 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
           pw[e] = *reinterpret_cast<const uint32_t*>(&h2);
         }
-        tmem_st16(t_lane + s_col + 16 * c, pw);
+        // keys [64 hf + 32 c, +32) as bf16 pairs: columns 32 hf + 16 c .. of the tile
+        tmem_st16(t_lane + s_col + 32 * hf + 16 * c, pw);
       }
       l += psum;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(AB_P_FULL + st));
+    }
+    if (ok) {
+      float other;
+      if (!exchange(l, &other)) { fail_status(a.status, abort_flag); ok = false; }
+      l += other;
     }
     // Epilogue: o = O / l (bf16), lse = m + ln l (natural log).
     if (ok && n_tiles > 0) {
@@ -561,7 +595,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         }
       }
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
         uint32_t o[32];
         if (n_tiles > 0) {
           tmem_ld32(t_lane + kAttTmemO + 32 * c, o);
@@ -605,7 +639,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           }
         }
       }
-      if (row_valid) {
+      if (row_valid && hf == 0) {
         if (a.final_out) a.lse[ri] = lse_out;
         else a.st_lse[ri] = lse_out;
       }
