@@ -1257,11 +1257,18 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       const float lse_v = l_row > 0.f ? (m_use + __log2f(l_row)) * 0.69314718055994531f : -INFINITY;
       const int b = cur.b, fr = cur.fr, slot_out = cur.slot_out;
+      // Two 32-column chunks per tensor-memory wait (the stores of one pair overlap
+      // the loads of the next; measured ~0.5 us per launch on the uniform batch).
 #pragma unroll 1
-      for (int c = 4 * cw; c < 4 * cw + 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(t_lane + kTmemO + 32 * c, o);
+      for (int c2 = 4 * cw; c2 < 4 * cw + 4; c2 += 2) {
+        uint32_t o2[2][32];
+        tmem_ld32(t_lane + kTmemO + 32 * c2, o2[0]);
+        tmem_ld32(t_lane + kTmemO + 32 * c2 + 32, o2[1]);
         tmem_wait_ld();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+        const int c = c2 + hh;
+        const uint32_t* o = o2[hh];
         // TMEM column 128 m + cc of this lane = latent column 256 m + 128 kh + cc.
         const int col0 = 256 * (c >> 2) + 128 * kh + 32 * (c & 3);
         if (cur.row_valid) {
@@ -1285,6 +1292,7 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
               st_global_v8(dst + e, w);
             }
           }
+        }
         }
       }
       if (cur.row_valid && part == 0) {
