@@ -578,9 +578,10 @@ __device__ __forceinline__ void sparse_reload_role(const Shared& sh, const FastA
 constexpr int kFp8Row = 656;
 constexpr int kRawHalfBytes = kHalfRows * kFp8Row;                         // 20992
 constexpr int kRawReloadBytes = 2 * kHalfRows * 128 + kHalfRows * 16;    // 8704
-// A page is converted this many pages after its Q K^T-only slots are freed, so
-// that the reload's L2 round trip is off the converters' path.
-constexpr int kReloadLag = 2;
+// The reload of page g - kReloadLag is converted after page g's own rows: the
+// reload's L2 round trip then overlaps a page's conversion (1 measured faster
+// than 2 or 3; any lag up to kStages - 1 keeps the ring free of a wait cycle).
+constexpr int kReloadLag = 1;
 
 // Rows [y, y + 32) of the FP8 pool (y < 0: a block outside the pool, read as
 // zeros) into a stage and its scale entry.
