@@ -381,6 +381,23 @@ def test_absorb_unabsorb(mla, cuda, cfg):
     parity(_to_np(st.o), O.unabsorb_ref(_f64(w.q_lat), _f64(w.w_uv)), "o")
 
 
+@pytest.mark.parametrize("H,lens,T", [(1, [5, 200], 3), (2, [70], 1), (8, [300] * 3, 2), (32, [64] * 5, 1),
+                                      (64, [129, 1, 1000], 3)])
+def test_absorb_unabsorb_head_counts(mla, cuda, H, lens, T):
+    """Every head count the boundary accepts (128 % H == 0), with token counts that
+    leave the GEMMs' 128-token tiles ragged (B*T = 3 .. 15)."""
+    import torch
+    from mla_latent_cache_gb300.runtime import DecodeStep
+    w = W.custom_workload(H, lens, T=T, causal=True, seed=57 + H)
+    st = DecodeStep(w, device=cuda)
+    st.absorb()
+    st.o_lat.copy_(torch.from_numpy(w.q_lat.view(np.int16)).to(cuda).view(torch.bfloat16))
+    st.unabsorb()
+    torch.cuda.synchronize()
+    parity(_to_np(st.q_lat), O.absorb_ref(_f64(w.q_nope), _f64(w.w_uk)), f"q_lat H={H}")
+    parity(_to_np(st.o), O.unabsorb_ref(_f64(w.q_lat), _f64(w.w_uv)), f"o H={H}")
+
+
 @pytest.mark.parametrize("cfg", [1, 2])
 def test_full_chain(mla, cuda, cfg):
     import torch
