@@ -92,6 +92,16 @@ def test_fp8_decode_v3_uniform_sampled(mla, cuda):
     _check(st, w, [0, 17, 40, 63], "fp8 v3 uniform")
 
 
+def test_fp8_decode_v3_ragged_sampled(mla, cuda):
+    # the ragged V3 batch (B=128, S from 256 to 32768, balanced ranges merged in the
+    # kernel) at full size; sampled sequences include the shortest and the longest
+    w = W.config_workload(3)
+    st = _run(mla, w, cuda)
+    lens = w.seq_lens
+    bs = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 5, 100})
+    _check(st, w, bs, "fp8 v3 ragged")
+
+
 def test_fp8_decode_matches_bf16_within_quantisation(mla, cuda):
     # the FP8 rows change every latent value by at most half an E4M3 step of its
     # tile's scale: the outputs move accordingly, and nothing else differs
