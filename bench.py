@@ -4,7 +4,7 @@ One step = one pass of the whole hot path through libmla.so: split plan,
 absorption (q_nope @ W_UK), split-KV latent attention (with the LSE merge of
 split groups in the same kernel), un-absorption (o_lat @ W_UV).  The step is captured into one
 CUDA graph so that host launch cost does not pace the GPU; the dominant
-kernel is timed separately: a decode-only graph (four chained decode launches,
+kernel is timed separately: a decode-only graph (eight chained decode launches,
 one when the L2 is flushed between launches) bracketed by CUDA events on the
 launching stream.
 
@@ -319,11 +319,12 @@ def run_ours(args):
     g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
         st.step(stream)
-    # Decode launches per decode graph: several back to back (chained by
-    # programmatic launch, as inside a model), so that the graph's own launch
-    # latency is not charged to the kernel; one when the pool is small enough
-    # that the L2 has to be flushed between launches.
-    dec_per_graph = 1 if flush is not None else 4
+    # Decode launches per decode graph: eight back to back (chained by
+    # programmatic launch, as a model chains its layers' decodes), so that the
+    # graph's own launch latency is not charged to the kernel (measured: 67.6 us
+    # per launch with four, 67.1-67.3 with eight or sixteen); one when the pool is
+    # small enough that the L2 has to be flushed between launches.
+    dec_per_graph = 1 if flush is not None else 8
     with torch.cuda.graph(g_dec, stream=stream):
         for _ in range(dec_per_graph):
             st.decode(stream)
