@@ -20,8 +20,11 @@ of the latent cache into per-head keys and values, then causal MHA) on the
 same workload instead.  ``--workload sparse`` times the index-driven decode
 (mla_decode_sparse) on its own: 64 sequences of 8192 cached rows, one query
 token each, top-2048 lists of distinct rows in random order.  A workload whose
-cache fits in L2 is timed with an L2 flush (a 256 MB write) between steps,
-outside the timed events.
+cache fits in L2 is timed with an L2 flush between steps, outside the timed
+events: a 256 MB write, then a 256 MB read, so that the L2 holds none of the
+workload's lines and no dirty lines of the flush either (their write-back
+would otherwise take HBM bandwidth inside the timed region: measured 53.9
+against 49.2 us per launch on the long-context decode).
 
 Multi-GPU runs are replicas: each rank runs the same independent batch (the
 path shards by request and needs no collective); ``value`` is the tokens of
@@ -48,6 +51,23 @@ WORKLOADS = {"tiny": 1, "uniform": 2, "ragged": 3, "long": 4, "extend": 5, "spar
 SPARSE = {"H": 128, "B": 64, "S_q": 1, "topk": 2048, "ctx": 8192, "seed": 1206}
 METRIC = "MLA decode tokens/s and achieved HBM GB/s (% of roofline) at V3 geometry"
 L2_BYTES = 129 * 2**20
+
+
+class L2Flush:
+    """Evicts the L2 between timed launches: a 256 MB write (the workload's lines
+    leave the cache) followed by a 256 MB read (the flush's own dirty lines are
+    written back before the timed region, not during it)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(64 * 2**20, dtype=torch.float32, device=dev)
+        self.acc = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def __call__(self, i: int):
+        import torch
+        self.w.fill_(i & 0xff)
+        torch.sum(self.r, dim=0, out=self.acc)
 
 
 def _dist():
@@ -241,7 +261,7 @@ def workload_config(w, args, world: int) -> dict:
     return {**extra, "workload": w.name, "H": w.H, "B": w.B, "T": w.T, "S": int(w.seq_lens[0]),
             "S_total": int(np.asarray(w.seq_lens, dtype=np.int64).sum()), "page": 64, "pool_blocks": w.num_blocks,
             "parallelism": f"replicas{world}", "splits": args.splits or "auto",
-            "l2": ("L2 flushed between steps (256 MB write, outside the timed events)" if pool_bytes < 2 * L2_BYTES
+            "l2": ("L2 flushed between steps (256 MB write then 256 MB read, outside the timed events)" if pool_bytes < 2 * L2_BYTES
                    else f"inputs larger than L2: {pool_bytes / 1e6:.0f} MB latent pool vs 129 MB L2")}
 
 
@@ -303,7 +323,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev)
     row_bytes = 656 if args.cache == "fp8" else 1152
     pool_bytes = w.num_blocks * 64 * row_bytes
-    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev) if pool_bytes < 2 * L2_BYTES else None
+    flush = L2Flush(dev) if pool_bytes < 2 * L2_BYTES else None
     hbm_peak, tc_peak, peak_kind = _peaks()
     ab = algorithmic_bytes(w, row_bytes)
     fl = algorithmic_flops(w)
@@ -357,7 +377,7 @@ def run_ours(args):
         with torch.cuda.stream(stream):
             for i in range(dec_steps):
                 if flush is not None:
-                    flush.fill_(i & 0xff)
+                    flush(i)
                 evs[i][0].record(stream)
                 g_dec.replay()
                 evs[i][1].record(stream)
@@ -368,7 +388,7 @@ def run_ours(args):
             t_start.record(stream)
             for i in range(args.steps):
                 if flush is not None:
-                    flush.fill_(i & 0xff)          # evict the cache lines of the previous step
+                    flush(i)                       # evict the cache lines of the previous step
                     step_evs[i][0].record(stream)
                 g_step.replay()
                 if flush is not None:
@@ -598,7 +618,7 @@ def run_sparse(args):
                            name=f"v32_sparse_b{c['B']}_sq{c['S_q']}_topk{c['topk']}_ctx{c['ctx']}")
     st = SparseStep(sw, device=dev, num_splits_override=args.splits)
     stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     hbm_peak, tc_peak, peak_kind = _peaks()
     nbytes = sparse_bytes(sw)
     with torch.cuda.stream(stream):
@@ -619,7 +639,7 @@ def run_sparse(args):
     with ClockSampler(local) as clocks:
         with torch.cuda.stream(stream):
             for i in range(args.steps):
-                flush.fill_(i & 0xff)              # the listed rows of the previous launch leave the L2
+                flush(i)                           # the listed rows of the previous launch leave the L2
                 evs[i][0].record(stream)
                 g.replay()
                 evs[i][1].record(stream)
@@ -665,7 +685,7 @@ def run_sparse(args):
         "config": {"workload": sw.name, "H": sw.H, "B": sw.B, "S_q": sw.S_q, "topk": sw.topk, "ctx": c["ctx"],
                    "page": 64, "pool_blocks": sw.ctx.num_blocks, "parallelism": "replicas1",
                    "splits": args.splits or "auto",
-                   "l2": "L2 flushed between launches (256 MB write, outside the timed events)"},
+                   "l2": "L2 flushed between launches (256 MB write then 256 MB read, outside the timed events)"},
         "step": "mla_decode_sparse (plan + index-driven decode with the in-kernel merge), one CUDA graph",
         "roofline": {"bound": "hbm", "kernel": "mla_decode_sparse", "achieved": achieved, "peak": hbm_peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
