@@ -372,7 +372,7 @@ def run_ours(args):
         # configuration), before the long step loop: it is compared with the copy
         # peak measured as a burst, so it is timed as a kernel alone, not after
         # minutes of power-capped load.
-        dec_steps = 200          # replays of the decode-only graph (whatever --steps is: a stable kernel figure)
+        dec_steps = max(1, args.dec_steps)   # replays of the decode-only graph (whatever --steps is: a stable kernel figure)
         evs = [(ev(), ev()) for _ in range(dec_steps)]
         with torch.cuda.stream(stream):
             for i in range(dec_steps):
@@ -754,6 +754,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of CPU oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dec-steps", type=int, default=200,
+                    help="replays of the decode-only graph timed for the roofline (a small count keeps a profiler's launch list on the step)")
     ap.add_argument("--workload", choices=sorted(WORKLOADS, key=WORKLOADS.get), default="uniform")
     ap.add_argument("--T", type=int, default=1, help="new rows per sequence (extend workload)")
     ap.add_argument("--splits", type=int, default=0, help="split count override (0 = the automatic plan)")

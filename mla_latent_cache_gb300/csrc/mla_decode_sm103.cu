@@ -291,6 +291,14 @@ __device__ __forceinline__ SegRows seg_rows(const int* rec, const FastArgs& a, i
 }
 
 // Block id of page p of sequence b (-1 = outside the pool, reads as zeros).
+// Block id `blk` (read from the table by the caller) validated.
+__device__ __forceinline__ int checked_block(const FastArgs& a, int blk, int b, int p, int* hdr, bool report) {
+  if (blk < 0 || blk >= a.num_blocks) {
+    if (report && a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | p);
+    blk = -1;
+  }
+  return blk;
+}
 __device__ __forceinline__ int page_block(const FastArgs& a, int b, int p, int* hdr, bool report) {
   int blk = a.block_table[(size_t)b * a.bt_stride + p];
   if (blk < 0 || blk >= a.num_blocks) {
@@ -887,6 +895,16 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
   const int num_pairs = gridDim.x >> 1;
   const int R = a.T * a.H;
 
+  // The plan lines this pair reads first (its range pointers, the record of its
+  // first segment when that is segment `pair`, as in plans of one segment per
+  // range, and the header) go to the L2 while the previous grid finishes; after
+  // a long launch they are usually cold (measured: ~2 us for the first
+  // range-pointer load of the uniform decode).
+  if (tid == 96 && pair < a.L.cap_ranges) {
+    prefetch_l2_line(rptr + pair);
+    prefetch_l2_line(seg + (size_t)min(pair, a.L.cap_segments - 1) * kSegWords);
+    prefetch_l2_line(hdr);
+  }
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       // CTA 0's load barriers also count the arrival relayed from CTA 1; in the FP8
@@ -935,7 +953,10 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
   // (shared memory), so they take idle SMs and those this grid frees, and wait
   // there for this grid to finish instead of paying their launch after it.
   pdl_trigger();
-  if (tid == 0) *s_num_merge = hdr[MLA_HDR_NUM_MERGE];
+  // The merge count is needed only after the roles: thread 0 (a loader) keeps the
+  // load in flight and stores it at the end, off its first page's critical path.
+  int num_merge_ld = 0;
+  if (tid == 0) asm volatile("ld.global.b32 %0, [%1];" : "=r"(num_merge_ld) : "l"(hdr + MLA_HDR_NUM_MERGE) : "memory");
   // The planner fills the range pointers up to the capacity (empty ranges past the
   // last), so the walk needs no range count from the header.
   const SegWalk walk0(rptr, pair, num_pairs, a.L.cap_ranges);
@@ -975,6 +996,11 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
         const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3];
         if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_FREE), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
         const int row0 = b * R + rb * kRowsPerBlock + kCtaRows * rank;
+        // The first page's block id is requested before the query copies are issued
+        // (their issue covers its latency).
+        int blk_first = 0;
+        if (p0 < p1)
+          asm volatile("ld.global.b32 %0, [%1];" : "=r"(blk_first) : "l"(a.block_table + (size_t)b * a.bt_stride + p0) : "memory");
         // The first segment's whole query comes by TMA ahead of the pages (boxes 0..5
         // into ring stages 3, 4, copied to tensor memory by the softmax warps); later
         // segments' boxes 0..5 are read by those warps while the ring is in use.
@@ -986,7 +1012,7 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
         tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_TMA), 0, row0);
         q_in_flight = true;
         for (int p = p0; ok && p < p1; ++p, ++gt) {
-          const int blk = page_block(a, b, p, hdr, true);
+          const int blk = p == p0 ? checked_block(a, blk_first, b, p, hdr, true) : page_block(a, b, p, hdr, true);
           const int st = gt % kStages;
           if (gt >= kStages && !mbar_wait_sleep(sh.bar(BAR_PV_DONE + st), ((gt / kStages) - 1) & 1, abort_flag)) {
             fail(hdr, abort_flag, 11); ok = false; break;
@@ -1316,6 +1342,7 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
     }
   }
 
+  if (tid == 0) *s_num_merge = num_merge_ld;
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();
