@@ -290,8 +290,8 @@ __device__ __forceinline__ SegRows seg_rows(const int* rec, const FastArgs& a, i
   return s;
 }
 
-// Block id of page p of sequence b (-1 = outside the pool, reads as zeros).
-// Block id `blk` (read from the table by the caller) validated.
+// Block id `blk` of page p of sequence b (read from the table by the caller)
+// validated: -1 = outside the pool, reads as zeros.
 __device__ __forceinline__ int checked_block(const FastArgs& a, int blk, int b, int p, int* hdr, bool report) {
   if (blk < 0 || blk >= a.num_blocks) {
     if (report && a.checked) record_error(hdr, MLA_ERR_DEVICE_CHECK, (b << 16) | p);
@@ -299,6 +299,7 @@ __device__ __forceinline__ int checked_block(const FastArgs& a, int blk, int b, 
   }
   return blk;
 }
+// Block id of page p of sequence b (-1 = outside the pool, reads as zeros).
 __device__ __forceinline__ int page_block(const FastArgs& a, int b, int p, int* hdr, bool report) {
   int blk = a.block_table[(size_t)b * a.bt_stride + p];
   if (blk < 0 || blk >= a.num_blocks) {
@@ -897,9 +898,8 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
 
   // The plan lines this pair reads first (its range pointers, the record of its
   // first segment when that is segment `pair`, as in plans of one segment per
-  // range, and the header) go to the L2 while the previous grid finishes; after
-  // a long launch they are usually cold (measured: ~2 us for the first
-  // range-pointer load of the uniform decode).
+  // range, and the header) go to the L2 while the previous grid finishes: after
+  // a launch that streamed the cache through the L2 they are usually cold.
   if (tid == 96 && pair < a.L.cap_ranges) {
     prefetch_l2_line(rptr + pair);
     prefetch_l2_line(seg + (size_t)min(pair, a.L.cap_segments - 1) * kSegWords);

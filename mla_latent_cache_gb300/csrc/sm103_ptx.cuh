@@ -195,13 +195,13 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
-// Prefetch a contiguous global range (multiple of 16 bytes) into L2.
 // L2 prefetch of the 128-byte line holding gptr: a hint that returns no data, so
 // it may precede the programmatic-launch wait (the L2 is the point of coherence:
 // a line written later by the previous grid is simply updated there).
 __device__ __forceinline__ void prefetch_l2_line(const void* gptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(gptr)) : "memory");
 }
+// Prefetch a contiguous global range (multiple of 16 bytes) into L2.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* gptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gptr)), "r"(bytes)
                : "memory");
