@@ -614,23 +614,25 @@ __device__ __forceinline__ void fp8_load_reload(uint32_t stage, const CUtensorMa
 
 // Two E4M3 codes (the low byte first) times the tile's scale, as a bf16 pair:
 // each code is widened exactly (to f16 by the E4M3 conversion, to fp32 by a
-// mixed-precision multiply-add with 1), multiplied by the fp32 scale, and the
-// products rounded to bf16 (measured faster than building the fp32 bits with
-// integer operations).
-__device__ __forceinline__ uint32_t dequant2(uint32_t two, float scale) {
+// mixed-precision multiply-add with 1), the pair multiplied by the fp32 scale
+// in one packed multiply (each lane rounded to nearest, as two scalar
+// multiplies), and the products rounded to bf16 (measured faster than building
+// the fp32 bits with integer operations).  scale2: the scale in both halves.
+__device__ __forceinline__ uint32_t dequant2(uint32_t two, uint64_t scale2) {
   uint32_t r;
-  asm("{\n\t.reg .b16 c, l, u, one;\n\t.reg .b32 h;\n\t.reg .f32 a, b;\n\t"
+  asm("{\n\t.reg .b16 c, l, u, one;\n\t.reg .b32 h;\n\t.reg .f32 a, b;\n\t.reg .b64 ab;\n\t"
       "mov.b16 one, 0x3C00;\n\t"
       "cvt.u16.u32 c, %1;\n\t"
       "cvt.rn.f16x2.e4m3x2 h, c;\n\t"
       "mov.b32 {l, u}, h;\n\t"
       "fma.rn.f32.f16 a, l, one, 0f00000000;\n\t"
       "fma.rn.f32.f16 b, u, one, 0f00000000;\n\t"
-      "mul.rn.f32 a, a, %2;\n\t"
-      "mul.rn.f32 b, b, %2;\n\t"
+      "mov.b64 ab, {a, b};\n\t"
+      "mul.rn.f32x2 ab, ab, %2;\n\t"
+      "mov.b64 {a, b}, ab;\n\t"
       "cvt.rn.bf16x2.f32 %0, b, a;\n\t}"
       : "=r"(r)
-      : "r"(two), "f"(scale));
+      : "r"(two), "l"(scale2));
   return r;
 }
 __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
@@ -650,7 +652,8 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
 }
 // 16 codes times the tile's scale, as bf16: output chunks oc and oc + 1 (8 values
 // each; oc even) of the 128-byte-swizzled slot row at row_base (row `row`).
-__device__ __forceinline__ void dequant_store16(uint4 code, float scale, uint32_t row_base, int oc, int row) {
+__device__ __forceinline__ void dequant_store16(uint4 code, float scale_f, uint32_t row_base, int oc, int row) {
+  const uint64_t scale = ((uint64_t)__float_as_uint(scale_f) << 32) | __float_as_uint(scale_f);
   const int sw = row & 7;
   st_shared_u4(row_base + 16 * (oc ^ sw),
                make_uint4(dequant2(code.x & 0xFFFFu, scale), dequant2(code.x >> 16, scale),
