@@ -612,27 +612,37 @@ __device__ __forceinline__ void fp8_load_reload(uint32_t stage, const CUtensorMa
   tma_load_2d(stage + 8 * kSlotBytes, tm16, bar, 512, y);
 }
 
-// Two E4M3 codes (the low byte first) times the tile's scale, as a bf16 pair:
-// each code is widened exactly (to f16 by the E4M3 conversion, to fp32 by a
-// mixed-precision multiply-add with 1), the pair multiplied by the fp32 scale
-// in one packed multiply (each lane rounded to nearest, as two scalar
-// multiplies), and the products rounded to bf16 (measured faster than building
-// the fp32 bits with integer operations).  scale2: the scale in both halves.
-__device__ __forceinline__ uint32_t dequant2(uint32_t two, uint64_t scale2) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 c, l, u, one;\n\t.reg .b32 h;\n\t.reg .f32 a, b;\n\t.reg .b64 ab;\n\t"
+// Four E4M3 codes (the lowest byte first) times the tile's scale, as two bf16
+// pairs: each code is widened exactly (to f16 by the E4M3 conversion, two codes
+// per instruction, to fp32 by a mixed-precision multiply-add with 1), each pair
+// multiplied by the fp32 scale in one packed multiply (each lane rounded to
+// nearest, as two scalar multiplies), and the products rounded to bf16
+// (measured faster than building the fp32 bits with integer operations).
+// scale2: the scale in both halves.
+__device__ __forceinline__ uint2 dequant4(uint32_t four, uint64_t scale2) {
+  uint2 r;
+  asm("{\n\t.reg .b16 c0, c1, l0, u0, l1, u1, one;\n\t.reg .b32 h0, h1;\n\t.reg .f32 a0, b0, a1, b1;\n\t"
+      ".reg .b64 p0, p1;\n\t"
       "mov.b16 one, 0x3C00;\n\t"
-      "cvt.u16.u32 c, %1;\n\t"
-      "cvt.rn.f16x2.e4m3x2 h, c;\n\t"
-      "mov.b32 {l, u}, h;\n\t"
-      "fma.rn.f32.f16 a, l, one, 0f00000000;\n\t"
-      "fma.rn.f32.f16 b, u, one, 0f00000000;\n\t"
-      "mov.b64 ab, {a, b};\n\t"
-      "mul.rn.f32x2 ab, ab, %2;\n\t"
-      "mov.b64 {a, b}, ab;\n\t"
-      "cvt.rn.bf16x2.f32 %0, b, a;\n\t}"
-      : "=r"(r)
-      : "r"(two), "l"(scale2));
+      "mov.b32 {c0, c1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h0, c0;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h1, c1;\n\t"
+      "mov.b32 {l0, u0}, h0;\n\t"
+      "mov.b32 {l1, u1}, h1;\n\t"
+      "fma.rn.f32.f16 a0, l0, one, 0f00000000;\n\t"
+      "fma.rn.f32.f16 b0, u0, one, 0f00000000;\n\t"
+      "fma.rn.f32.f16 a1, l1, one, 0f00000000;\n\t"
+      "fma.rn.f32.f16 b1, u1, one, 0f00000000;\n\t"
+      "mov.b64 p0, {a0, b0};\n\t"
+      "mov.b64 p1, {a1, b1};\n\t"
+      "mul.rn.f32x2 p0, p0, %3;\n\t"
+      "mul.rn.f32x2 p1, p1, %3;\n\t"
+      "mov.b64 {a0, b0}, p0;\n\t"
+      "mov.b64 {a1, b1}, p1;\n\t"
+      "cvt.rn.bf16x2.f32 %0, b0, a0;\n\t"
+      "cvt.rn.bf16x2.f32 %1, b1, a1;\n\t}"
+      : "=r"(r.x), "=r"(r.y)
+      : "r"(four), "l"(scale2));
   return r;
 }
 __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
@@ -655,12 +665,10 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
 __device__ __forceinline__ void dequant_store16(uint4 code, float scale_f, uint32_t row_base, int oc, int row) {
   const uint64_t scale = ((uint64_t)__float_as_uint(scale_f) << 32) | __float_as_uint(scale_f);
   const int sw = row & 7;
-  st_shared_u4(row_base + 16 * (oc ^ sw),
-               make_uint4(dequant2(code.x & 0xFFFFu, scale), dequant2(code.x >> 16, scale),
-                          dequant2(code.y & 0xFFFFu, scale), dequant2(code.y >> 16, scale)));
-  st_shared_u4(row_base + 16 * ((oc + 1) ^ sw),
-               make_uint4(dequant2(code.z & 0xFFFFu, scale), dequant2(code.z >> 16, scale),
-                          dequant2(code.w & 0xFFFFu, scale), dequant2(code.w >> 16, scale)));
+  const uint2 x = dequant4(code.x, scale), y = dequant4(code.y, scale);
+  const uint2 z = dequant4(code.z, scale), w = dequant4(code.w, scale);
+  st_shared_u4(row_base + 16 * (oc ^ sw), make_uint4(x.x, x.y, y.x, y.y));
+  st_shared_u4(row_base + 16 * ((oc + 1) ^ sw), make_uint4(z.x, z.y, w.x, w.y));
 }
 
 // Converter warps (warps 12..15; t = 0..127): page g's own half as soon as its raw
