@@ -1002,16 +1002,52 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
       SegWalk walk = walk0;
       int gt = 0, sc = 0;
       bool ok = true, q_in_flight = false;
+      // Page p of sequence b (block id blk) into stage gt % kStages, once P V of the
+      // page that stage held is done.
+      auto load_page = [&](int b, int p, int blk) -> bool {
+        const int st = gt % kStages;
+        if (gt >= kStages && !mbar_wait_sleep(sh.bar(BAR_PV_DONE + st), ((gt / kStages) - 1) & 1, abort_flag)) {
+          fail(hdr, abort_flag, 11);
+          return false;
+        }
+        if (gt >= kQStageFirst && gt < kStages && !mbar_wait_sleep(sh.bar(BAR_Q_COPIED), 0, abort_flag)) {
+          fail(hdr, abort_flag, 15);
+          return false;
+        }
+        // One 4-D box per page half: 32 rows x all column blocks, landing as the nine
+        // 32-row x 64-column slots (streams ~8 % faster than nine 3-D boxes).
+        if constexpr (kFp8)
+          fp8_load_half(sh.stage(st), sh.base + kSmemScales + st * 512, &tm_pair, &tm_kpe, &tm_aux,
+                        sh.bar(BAR_RAW + st), blk >= 0 ? blk * kPage + kHalfRows * rank : -kPage);
+        else load_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rank, blk, a.kpe_separate);
+        ++gt;
+        return true;
+      };
       for (int si = walk.cur(); ok && si >= 0; walk.advance(), si = walk.cur()) {
         const int* rec = seg + (size_t)si * kSegWords;
         const int b = rec[0], rb = rec[1], p0 = rec[2], p1 = rec[3];
-        if (sc > 0 && !mbar_wait(sh.bar(BAR_Q_FREE), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
         const int row0 = b * R + rb * kRowsPerBlock + kCtaRows * rank;
         // The first page's block id is requested before the query copies are issued
         // (their issue covers its latency).
         int blk_first = 0;
         if (p0 < p1)
           asm volatile("ld.global.b32 %0, [%1];" : "=r"(blk_first) : "l"(a.block_table + (size_t)b * a.bt_stride + p0) : "memory");
+        int p = p0;
+        if (sc > 0) {
+          // A later segment's first pages are requested before its query, which has to
+          // wait until Q K^T is done with the previous one: at most kStages of them, so
+          // that every stage they reuse held a page of an earlier segment (whose P V
+          // does not wait for this segment's query).  Its query rows go to the L2 for
+          // the softmax warps' staging.  (Measured on the ragged batch: ~8 us per
+          // segment change when the pages waited for the query.)
+          const int rows_valid = min(kCtaRows, R - (rb * kRowsPerBlock + kCtaRows * rank));
+          if (rows_valid > 0) prefetch_l2_bulk(a.q_lat + (size_t)row0 * kDLat, (uint32_t)rows_valid * kDLat * 2);
+          const int early = min(p1 - p0, kStages);
+          for (; ok && p < p0 + early; ++p)
+            ok = load_page(b, p, p == p0 ? checked_block(a, blk_first, b, p, hdr, true) : page_block(a, b, p, hdr, true));
+          if (!ok) break;
+          if (!mbar_wait(sh.bar(BAR_Q_FREE), (sc - 1) & 1, abort_flag)) { fail(hdr, abort_flag, 10); ok = false; break; }
+        }
         // The first segment's whole query comes by TMA ahead of the pages (boxes 0..5
         // into ring stages 3, 4, copied to tensor memory by the softmax warps); later
         // segments' boxes 0..5 are read by those warps while the ring is in use.
@@ -1022,22 +1058,8 @@ __global__ void __launch_bounds__(threads_of<kMode>(), 1)
         for (int box = kQTmemBoxes; box < 8; ++box) tma_load_2d(sh.q(box), &tm_qlat, sh.bar(BAR_Q_TMA), 64 * box, row0);
         tma_load_2d(sh.q(8), &tm_qpe, sh.bar(BAR_Q_TMA), 0, row0);
         q_in_flight = true;
-        for (int p = p0; ok && p < p1; ++p, ++gt) {
-          const int blk = p == p0 ? checked_block(a, blk_first, b, p, hdr, true) : page_block(a, b, p, hdr, true);
-          const int st = gt % kStages;
-          if (gt >= kStages && !mbar_wait_sleep(sh.bar(BAR_PV_DONE + st), ((gt / kStages) - 1) & 1, abort_flag)) {
-            fail(hdr, abort_flag, 11); ok = false; break;
-          }
-          if (gt >= kQStageFirst && gt < kStages && !mbar_wait_sleep(sh.bar(BAR_Q_COPIED), 0, abort_flag)) {
-            fail(hdr, abort_flag, 15); ok = false; break;
-          }
-          // One 4-D box per page half: 32 rows x all column blocks, landing as the nine
-          // 32-row x 64-column slots (streams ~8 % faster than nine 3-D boxes).
-          if constexpr (kFp8)
-            fp8_load_half(sh.stage(st), sh.base + kSmemScales + st * 512, &tm_pair, &tm_kpe, &tm_aux,
-                          sh.bar(BAR_RAW + st), blk >= 0 ? blk * kPage + kHalfRows * rank : -kPage);
-          else load_page_half(sh.stage(st), &tm_page, &tm_kpe, sh.bar(BAR_FULL + st), rank, blk, a.kpe_separate);
-        }
+        for (; ok && p < p1; ++p)
+          ok = load_page(b, p, p == p0 ? checked_block(a, blk_first, b, p, hdr, true) : page_block(a, b, p, hdr, true));
         ++sc;
       }
       // Drain: every load issued must have landed before the CTA may exit.
