@@ -102,11 +102,19 @@ struct PlanArgs {
   WsLayout L;
 };
 
-// Segment s of a group with n pages starting at global page off, its first
-// segment sb, in the given mode; writes the record and, for a segment that
-// opens a work range, the range pointer.
-__device__ __forceinline__ void write_segment(int* seg, int* rptr, int mode, int q, int b, int rb, int n, int off,
-                                              int k, int sb, int pb, int mi, int s) {
+// Fixed cost of starting a group's work in a range, in pages (query staging and
+// an output write per segment: measured ~8 us per segment change on the ragged
+// V3 batch against ~0.8 us per page): the balanced ranges leave that many line
+// positions between consecutive non-empty groups.
+constexpr int kSegmentCostPages = 8;
+
+// Segment s of a group with n pages whose first page sits at line position u
+// (mode 1) and whose first segment is sb, in the given mode; writes the record
+// and the range pointer of every range whose first segment it is (in mode 1
+// also of the ranges inside the gap before it, which hold no segment).  ne:
+// non-empty groups before this one.
+__device__ __forceinline__ void write_segment(int* seg, int* rptr, int mode, int q, int b, int rb, int n, int u,
+                                              int k, int sb, int pb, int mi, int s, int ne) {
   int p0, p1, r;
   if (mode == 2) {
     p0 = (int)(((long long)s * n) / k);
@@ -115,15 +123,20 @@ __device__ __forceinline__ void write_segment(int* seg, int* rptr, int mode, int
   } else if (mode == 0) {
     p0 = 0; p1 = n; r = sb;
   } else {
-    r = off / q + s;
-    const int gs = max(off, r * q), ge = min(off + n, (r + 1) * q);
-    p0 = gs - off; p1 = ge - off;
+    r = u / q + s;
+    const int gs = max(u, r * q), ge = min(u + n, (r + 1) * q);
+    p0 = gs - u; p1 = ge - u;
   }
   int* rec = seg + (size_t)(sb + s) * kSegWords;
   rec[0] = b; rec[1] = rb; rec[2] = p0; rec[3] = p1; rec[4] = r;
   rec[5] = (k > 1) ? pb + s : -1; rec[6] = (k > 1) ? mi : -1; rec[7] = 0;
-  // Every range starts with the segment holding its first page.
-  if (mode != 1 || (off + p0) % q == 0) rptr[r] = sb + s;
+  if (mode != 1 || s > 0) {
+    rptr[r] = sb + s;     // a cut: the segment starts its range
+  } else {
+    // the previous non-empty group's last page sits just before this group's gap
+    const int r_prev = ne > 0 ? (u - kSegmentCostPages - 1) / q : -1;
+    for (int rr = r_prev + 1; rr <= r; ++rr) rptr[rr] = sb;
+  }
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws) {
@@ -135,7 +148,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
   int* msync = reinterpret_cast<int*>(ws + a.L.off_merge_sync);
   __shared__ int sh[128];
   __shared__ int s_sb[kSmemGroups];
-  __shared__ int s_q, s_mode;
+  __shared__ int s_q, s_mode, s_U;
   const int tid = threadIdx.x;
   pdl_wait();
   pdl_trigger();
@@ -151,7 +164,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
   }
 
   // Pass A: pages per group and their exclusive prefix.
-  int carry = 0, nonempty = 0, maxn = 0;
+  int carry = 0, nonempty = 0, maxn = 0, nonempty_carry = 0;
   const int R = a.T * a.H;
   for (int base = 0; base < a.num_groups; base += blockDim.x) {
     const int g = base + tid;
@@ -164,15 +177,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
       const int vis = visible_limit(S, a.T, r_last / a.H, a.causal);
       n = (vis + kPage - 1) / kPage;
     }
-    int v[3] = {n, 0, 0}, tot[3];
+    int v[3] = {n, n > 0 ? 1 : 0, 0}, tot[3];
     block_excl_scan3(v, tot, sh);
     if (g < a.num_groups) {
+      const int ne = nonempty_carry + v[1];     // non-empty groups before g
       grp[g * kGroupWords + 0] = n;
       grp[g * kGroupWords + 1] = carry + v[0];
+      grp[g * kGroupWords + 6] = carry + v[0] + kSegmentCostPages * ne;   // line position of its first page
+      grp[g * kGroupWords + 7] = ne;
       nonempty += n > 0;
       maxn = max(maxn, n);
     }
     carry += tot[0];
+    nonempty_carry += tot[1];
   }
   block_reduce(hsum, errb, nonempty, maxn, sh);
   const int W = carry;
@@ -183,6 +200,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
     if (a.N > 0) s_mode = 2;
     else if (nonempty <= a.G && maxn <= (5 * q + 3) / 4) s_mode = 0;
     else s_mode = 1;
+    if (s_mode == 1) {
+      // balanced ranges over the line of pages and gaps
+      const int U = W + kSegmentCostPages * (nonempty - 1);
+      const int qw = (U + a.G - 1) / a.G;
+      s_q = qw < kMinSplitPages ? kMinSplitPages : qw;
+      s_U = U;
+    }
   }
   __syncthreads();
   const int q = s_q, mode = s_mode;
@@ -191,14 +215,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
   int cseg = 0, cpart = 0, cmrg = 0;
   for (int base = 0; base < a.num_groups; base += blockDim.x) {
     const int g = base + tid;
-    int k = 0, n = 0, off = 0;
+    int k = 0, n = 0;
     if (g < a.num_groups) {
       n = grp[g * kGroupWords + 0];
-      off = grp[g * kGroupWords + 1];
+      const int u = grp[g * kGroupWords + 6];
       if (n > 0) {
         if (mode == 2) k = min(n, a.N);
         else if (mode == 0) k = 1;
-        else k = (off + n - 1) / q - off / q + 1;
+        else k = (u + n - 1) / q - u / q + 1;
       }
     }
     const int part = k > 1 ? k : 0;
@@ -224,7 +248,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
   }
   __syncthreads();
   const int total_seg = cseg;
-  const int num_ranges = (mode == 1) ? (W + q - 1) / q : total_seg;
+  const int num_ranges = (mode == 1) ? (s_U + q - 1) / q : total_seg;
 
   // Pass C: segment records and range pointers, one segment per thread (its
   // group found by binary search over the segment bases), or one group per
@@ -238,14 +262,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a, char* ws
       }
       const int g = lo;
       const int* gr = grp + g * kGroupWords;
-      write_segment(seg, rptr, mode, q, g / a.RB, g % a.RB, gr[0], gr[1], gr[2], gr[3], gr[4], gr[5], i - gr[3]);
+      write_segment(seg, rptr, mode, q, g / a.RB, g % a.RB, gr[0], gr[6], gr[2], gr[3], gr[4], gr[5], i - gr[3], gr[7]);
     }
   } else {
     for (int g = tid; g < a.num_groups; g += blockDim.x) {
       const int* gr = grp + g * kGroupWords;
       const int k = gr[2];
       for (int s = 0; s < k; ++s)
-        write_segment(seg, rptr, mode, q, g / a.RB, g % a.RB, gr[0], gr[1], k, gr[3], gr[4], gr[5], s);
+        write_segment(seg, rptr, mode, q, g / a.RB, g % a.RB, gr[0], gr[6], k, gr[3], gr[4], gr[5], s, gr[7]);
     }
   }
   // Range pointers past the last range repeat the segment count, up to the

@@ -48,6 +48,9 @@ D_K = D_C + D_R
 PAGE = 64
 ROWS_PER_BLOCK = 128   # flattened (t, h) query rows handled together
 MIN_SPLIT_PAGES = 4
+# Plan rule: the fixed cost of starting a group's work in a range, in pages (a query
+# staging and an output write per segment; the pages fix no split rule, see plan_ref).
+SEGMENT_COST_PAGES = 8
 
 SCALE = 1.0 / math.sqrt(D_N + D_R)   # 1/sqrt(192): [zdszero] decoupled-RoPE note; [MLA-in-depth] parity reference
 
@@ -367,9 +370,15 @@ def plan_ref(seq_lens, T: int, H: int, causal: bool, num_slots: int, num_splits_
          segment s = [floor(s n/k), floor((s+1) n/k)); each segment is its own range.
       3. auto: q = max(4, ceil(W/G)).  If the non-empty groups number at most G
          and none has more than ceil(5q/4) pages, every non-empty group is one
-         segment and one range.  Otherwise range r covers global pages
-         [r q, min(W,(r+1) q)) of the concatenated groups, and each group is cut
-         where the range boundaries fall.
+         segment and one range.  Otherwise the non-empty groups are laid out on
+         a line, in order, each after a gap of c = SEGMENT_COST_PAGES positions
+         from the previous one (none before the first): group g's pages occupy
+         [u_g, u_g + n_g) with u_g = (pages of the groups before g) + c x (non-empty
+         groups before g); with U = W + c x (non-empty groups - 1) and
+         q' = max(4, ceil(U/G)), range r covers positions [r q', (r+1) q') and
+         each group is cut where the range boundaries fall.  (A range's work is
+         then its pages plus c for every group that starts in it; a range that
+         lies inside a gap holds no segment.)
       4. a segment that covers its whole group is final (slot -1); the other
          segments get partial slots numbered in segment order.
     """
@@ -395,16 +404,25 @@ def plan_ref(seq_lens, T: int, H: int, causal: bool, num_slots: int, num_splits_
                 raw.append((b, rb, 0, n, n_ranges))
                 n_ranges += 1
         else:
-            off = 0
+            c = SEGMENT_COST_PAGES
+            U = W + c * (len(nonempty) - 1) if nonempty else 0
+            qw = max(MIN_SPLIT_PAGES, -(-U // G)) if U > 0 else MIN_SPLIT_PAGES
+            u = 0          # line position of the next group's first page
+            started = False
             for (b, rb, n) in groups:
+                if n == 0:
+                    continue
+                if started:
+                    u += c
+                started = True
                 p = 0
                 while p < n:
-                    r = (off + p) // q
-                    end_in_group = min(n, (r + 1) * q - off)
+                    r = (u + p) // qw
+                    end_in_group = min(n, (r + 1) * qw - u)
                     raw.append((b, rb, p, end_in_group, r))
                     p = end_in_group
-                off += n
-            n_ranges = -(-W // q) if W > 0 else 0
+                u += n
+            n_ranges = -(-U // qw) if U > 0 else 0
     n_of = {(b, rb): n for (b, rb, n) in groups}
     segments = []
     slot = 0

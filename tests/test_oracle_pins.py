@@ -360,11 +360,24 @@ def _check_plan(seq_lens, T, H, causal, G, N):
     else:
         W = sum(n for (_, _, n) in groups)
         q = max(O.MIN_SPLIT_PAGES, -(-W // G))
+        nonempty = [g for g in groups if g[2] > 0]
         loads = [0] * max(1, plan["num_ranges"])
+        starts = [0] * max(1, plan["num_ranges"])
         for s in segs:
             loads[s[4]] += s[3] - s[2]
-        assert max(loads) <= -(-5 * q // 4)
+            starts[s[4]] += s[2] == 0
         assert plan["num_ranges"] <= G
+        if len(nonempty) <= G and max((g[2] for g in nonempty), default=0) <= -(-5 * q // 4):
+            # one whole group per range
+            assert all(s[2] == 0 and s[5] == -1 for s in segs) and len(segs) == len(nonempty)
+        else:
+            # a range's work (pages + c per group starting in it, the first group's
+            # start free) fits in q' line positions plus the one gap it may begin with
+            c = O.SEGMENT_COST_PAGES
+            qw = max(O.MIN_SPLIT_PAGES, -(-(W + c * (len(nonempty) - 1)) // G))
+            for r in range(plan["num_ranges"]):
+                assert loads[r] <= qw
+                assert loads[r] + c * starts[r] <= qw + c
     return plan
 
 
@@ -382,9 +395,13 @@ def test_plan_properties_random():
 
 
 def test_plan_named_workloads():
-    # uniform V3 batch on 152 slots: 4096 pages -> q = 27, every sequence split
+    # uniform V3 batch on 152 slots: 4096 pages -> q = 27 (64 > ceil(5*27/4): split);
+    # with the 63 gaps of 8 between sequences, 4600 positions in ranges of q' = 31
     p = _check_plan([4096] * 64, 1, 128, False, 152, 0)
-    assert p["num_ranges"] == 152 and p["num_partials"] > 64
+    assert p["num_ranges"] == 149 and p["num_partials"] > 64
+    # one long sequence: no gap, 2048 pages in 76 ranges of 27 (the last 23)
+    p = _check_plan([131072], 1, 128, False, 76, 0)
+    assert p["num_ranges"] == 76 and [s[3] - s[2] for s in p["segments"]] == [27] * 75 + [23]
     # on 76 slots it fits without splitting (64 <= ceil(5*54/4))
     p = _check_plan([4096] * 64, 1, 128, False, 76, 0)
     assert p["num_partials"] == 0 and p["num_ranges"] == 64
