@@ -121,7 +121,11 @@ typedef struct {
  *   G = num_slots.  With an override N, each group is cut into min(n, N) even
  *   chunks, one range each.  Otherwise, if at most G groups are non-empty and
  *   none exceeds ceil(5q/4) pages, each group is one segment and one range;
- *   else range r covers global pages [r q, (r+1) q) of the concatenated groups.
+ *   else the non-empty groups' pages are laid out in order on a line with a gap
+ *   of c = 8 positions before each group but the first (a segment's fixed cost
+ *   in pages), U = W + c (non-empty groups - 1), q' = max(4, ceil(U/G)), and
+ *   range r covers line positions [r q', (r+1) q'), each group cut where the
+ *   range boundaries fall (a range inside a gap holds no segment).
  *   A segment covering its whole group writes final outputs; the others write
  *   partial state to numbered slots, merged afterwards.
  */
