@@ -91,7 +91,8 @@ def _compare(st, w, batches=None, tokens=None, name=""):
 # ---------------------------------------------------------------------------
 # planner and gather: bit-exact
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("case", ["c1", "c2", "c2_76", "c3", "c4_auto", "c4_64", "c4_256", "c5_16", "c5_170", "rand"])
+@pytest.mark.parametrize("case", ["c1", "c2", "c2_76", "c3", "c4_auto", "c4_64", "c4_256", "c5_16", "c5_170", "rand",
+                                  "gap", "gap5"])
 def test_plan_bit_exact(mla, cuda, case):
     import torch
     from mla_latent_cache_gb300.runtime import read_plan_header, read_plan_tables
@@ -104,6 +105,8 @@ def test_plan_bit_exact(mla, cuda, case):
         "c5_170": (W.config_workload(5, T=170), 0, 0),
         "rand": (W.custom_workload(16, list(rng.integers(0, 3000, size=37)) + [0, 1, 64, 65], T=2, causal=True),
                  13, 0),
+        # a work range inside a gap of the balanced rule (no segment), and one-page groups
+        "gap": (W.custom_workload(128, [64, 384]), 10, 0), "gap5": (W.custom_workload(128, [64] * 5), 4, 0),
     }[case]
     w, slots, ov = spec
     geom = mla.make_geom(w.H)
@@ -124,6 +127,14 @@ def test_plan_bit_exact(mla, cuda, case):
     hdr = read_plan_header(torch, ws)
     assert hdr[mla.HDR["NUM_PARTIALS"]] == ref["num_partials"]
     assert hdr[mla.HDR["ERROR"]] == 0 or case == "rand"
+
+
+def test_decode_plan_with_empty_range(mla, cuda):
+    """The balanced rule can leave a work range inside a gap (its CTA pair has no
+    segment): the decode over that plan against the oracle, sharp logits."""
+    w = W.custom_workload(128, [64, 384, 200, 3000], seed=31, sharp=True)
+    st = _run_decode(mla, w, cuda, num_slots=40)
+    _compare(st, w, name="plan with an empty range")
 
 
 @pytest.mark.parametrize("slots,ov", [(0, 0), (19, 0), (0, 5)])

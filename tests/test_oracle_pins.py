@@ -381,6 +381,29 @@ def _check_plan(seq_lens, T, H, causal, G, N):
     return plan
 
 
+def test_plan_gap_rule_worked_examples():
+    """The balanced rule's line of pages and gaps, worked by hand (T=1, H=128: one
+    group of ceil(S/64) pages per sequence; c = 8)."""
+    assert O.SEGMENT_COST_PAGES == 8
+    # pages [10, 2, 2, 10], G=3: W=24, q=8; 4 groups > 3 -> balanced.  U = 24 + 3*8 =
+    # 48, q' = 16.  Line: g0 [0,10) gap g1 [18,20) gap g2 [28,30) gap g3 [38,48);
+    # ranges [0,16) [16,32) [32,48) -> g0 | g1 g2 | g3, nothing cut (the old rule,
+    # ranges of 8 pages, cut g0 and g3 and put four groups in the middle range).
+    p = O.plan_ref([640, 128, 128, 640], 1, 128, False, 3)
+    assert p["segments"] == [(0, 0, 0, 10, 0, -1), (1, 0, 0, 2, 1, -1), (2, 0, 0, 2, 1, -1), (3, 0, 0, 10, 2, -1)]
+    assert p["range_ptr"] == [0, 1, 3, 4] and p["merge"] == []
+    # pages [1, 6], G=10: W=7, q=4, 6 > ceil(5*4/4)=5 -> balanced.  U = 7 + 8 = 15,
+    # q' = max(4, 2) = 4.  Line: g0 [0,1) gap [1,9) g1 [9,15); ranges [0,4) [4,8)
+    # [8,12) [12,16): g0 | (inside the gap: empty) | g1 pages 0-3 | g1 pages 3-6.
+    p = O.plan_ref([64, 384], 1, 128, False, 10)
+    assert p["segments"] == [(0, 0, 0, 1, 0, -1), (1, 0, 0, 3, 2, 0), (1, 0, 3, 6, 3, 1)]
+    assert p["num_ranges"] == 4 and p["range_ptr"] == [0, 1, 1, 2, 3] and p["merge"] == [(1, 0, 0, 2)]
+    # five one-page groups, G=4: W=5, 5 groups > 4 -> balanced.  U = 5 + 4*8 = 37,
+    # q' = 10.  Pages at 0, 9, 18, 27, 36 -> ranges g0 g1 | g2 | g3 | g4.
+    p = O.plan_ref([64] * 5, 1, 128, False, 4)
+    assert [s[4] for s in p["segments"]] == [0, 0, 1, 2, 3] and p["range_ptr"] == [0, 2, 3, 4, 5]
+
+
 def test_plan_properties_random():
     rng = np.random.default_rng(8)
     for trial in range(60):
